@@ -1,0 +1,272 @@
+"""CPU oracle for the DFlash MoE verify layer -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg (and its ``--impl reference`` arm) may import this package.  The product
+path (``moe_nvfp4_block_gb300``) never imports, links or executes it.
+
+The arithmetic lives in ``moe_oracle.c`` (plain C11, fp64, compiled with
+``-ffp-contract=off`` so that the fixed-order FP32 logits are evaluated exactly
+as written).  This module only builds it and marshals numpy arrays.
+
+Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
+against values and identities that do not come from the oracle itself
+(hand-worked format tables, closed forms, float64 library routines, brute
+force on tiny shapes).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+
+def build(force: bool = False, extra_flags=(), out: str | None = None) -> str:
+    """Compile the oracle with gcc; ``extra_flags``/``out`` build variants."""
+    out = out or _LIB
+    if force or extra_flags or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(_SRC):
+        base = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+                *extra_flags, _SRC, "-o", out + ".tmp", "-lm"]
+        try:
+            subprocess.run(base[:3] + ["-fopenmp"] + base[3:], check=True, capture_output=True)
+        except subprocess.CalledProcessError:
+            subprocess.run(base, check=True)
+        os.replace(out + ".tmp", out)
+    return out
+
+
+class Proj(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("tscale", ctypes.c_void_p)]
+
+
+class LayerC(ctypes.Structure):
+    _fields_ = [("H", ctypes.c_int), ("E", ctypes.c_int), ("top_k", ctypes.c_int), ("I", ctypes.c_int),
+                ("Is", ctypes.c_int), ("routed_scale", ctypes.c_double),
+                ("router_w", ctypes.c_void_p), ("router_b", ctypes.c_void_p),
+                ("gate", Proj), ("up", Proj), ("down", Proj),
+                ("sh_gate", Proj), ("sh_up", Proj), ("sh_down", Proj)]
+
+
+_lib = None
+
+
+def _bind(L):
+    vp, ci, cd = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
+    L.orc_e2m1.restype = cd
+    L.orc_e2m1.argtypes = [ci]
+    L.orc_e4m3.restype = cd
+    L.orc_e4m3.argtypes = [ci]
+    L.orc_bf16.restype = cd
+    L.orc_bf16.argtypes = [ctypes.c_uint16]
+    L.orc_round_bf16.restype = ctypes.c_uint16
+    L.orc_round_bf16.argtypes = [cd]
+    L.orc_nvfp4_matrix.argtypes = [vp, ci, ci, ci, vp]
+    L.orc_router_logits_f32.argtypes = [vp, vp, ci, vp]
+    L.orc_router_logits_f64.argtypes = [vp, vp, ci, vp]
+    L.orc_topk.argtypes = [vp, ci, ci, ci, vp, vp]
+    L.orc_group.argtypes = [vp, ci, ci, ci, vp]
+    L.orc_expert.argtypes = [vp, vp, vp, ci, ci, ci, vp, vp, vp]
+    L.orc_moe_layer.argtypes = [vp, vp, ci, vp, vp, vp, vp, vp, vp]
+    L.orc_rmsnorm.argtypes = [vp, ci, ci, cd, vp]
+    L.orc_linear_bf16.argtypes = [vp, vp, ci, ci, ci, vp]
+    L.orc_attention.argtypes = [vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, vp, vp, vp, cd, vp]
+    L.orc_lm_argmax.argtypes = [vp, vp, ci, ci, ci, vp, vp]
+    L.orc_accept_prefix.restype = ci
+    L.orc_accept_prefix.argtypes = [vp, vp, ci]
+    return L
+
+
+def lib(path: str | None = None):
+    """The oracle library (built on first use); ``path`` loads a variant."""
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    if _lib is None:
+        _lib = _bind(ctypes.CDLL(build()))
+    return _lib
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data
+
+
+def _c(a, dt):
+    return np.ascontiguousarray(a, dtype=dt)
+
+
+RMS_EPS = 1e-6
+
+
+class OracleLayer:
+    """Keeps numpy arrays alive and exposes the C struct."""
+
+    def __init__(self, layer, H, E, top_k, I, Is, routed_scale=1.0):
+        self.keep = []
+
+        def arr(a, dt):
+            a = _c(a, dt)
+            self.keep.append(a)
+            return a
+
+        def proj(p):
+            if p is None:
+                return Proj(None, None, None)
+            return Proj(_p(arr(p.codes, np.uint8)), _p(arr(p.scales, np.uint8)), _p(arr(p.tscale, np.float32)))
+
+        rb = None if layer.router_b is None else arr(layer.router_b, np.float32)
+        self.c = LayerC(H, E, top_k, I, Is, routed_scale, _p(arr(layer.router_w, np.uint16)), _p(rb),
+                        proj(layer.gate), proj(layer.up), proj(layer.down),
+                        proj(layer.sh_gate), proj(layer.sh_up), proj(layer.sh_down))
+        self.H, self.E, self.k, self.I, self.Is = H, E, top_k, I, Is
+
+    @classmethod
+    def from_workload(cls, w, layer, routed_scale=None):
+        return cls(layer, w.H, w.E, w.top_k, w.I, w.Is, w.routed_scale if routed_scale is None else routed_scale)
+
+    @property
+    def ref(self):
+        return ctypes.byref(self.c)
+
+
+def e2m1(code: int, L=None) -> float:
+    return (L or lib()).orc_e2m1(code)
+
+
+def e4m3(code: int, L=None) -> float:
+    return (L or lib()).orc_e4m3(code)
+
+
+def bf16_value(b: int, L=None) -> float:
+    return (L or lib()).orc_bf16(b)
+
+
+def round_bf16(v: float, L=None) -> int:
+    return int((L or lib()).orc_round_bf16(v))
+
+
+def nvfp4_matrix(p, e, rows, cols, L=None) -> np.ndarray:
+    """Dequantised expert e of a projection, float64 [rows, cols]."""
+    codes, scales, ts = _c(p.codes, np.uint8), _c(p.scales, np.uint8), _c(p.tscale, np.float32)
+    pr = Proj(_p(codes), _p(scales), _p(ts))
+    out = np.empty((rows, cols), np.float64)
+    (L or lib()).orc_nvfp4_matrix(ctypes.byref(pr), e, rows, cols, _p(out))
+    return out
+
+
+def router_logits_f32(ol: OracleLayer, x, L=None) -> np.ndarray:
+    x = _c(x, np.uint16)
+    out = np.empty((x.shape[0], ol.E), np.float32)
+    (L or lib()).orc_router_logits_f32(ol.ref, _p(x), x.shape[0], _p(out))
+    return out
+
+
+def router_logits_f64(ol: OracleLayer, x, L=None) -> np.ndarray:
+    x = _c(x, np.uint16)
+    out = np.empty((x.shape[0], ol.E), np.float64)
+    (L or lib()).orc_router_logits_f64(ol.ref, _p(x), x.shape[0], _p(out))
+    return out
+
+
+def topk(logits, k, L=None):
+    logits = _c(logits, np.float32)
+    K, E = logits.shape
+    idx = np.empty((K, k), np.int32)
+    w = np.empty((K, k), np.float32)
+    (L or lib()).orc_topk(_p(logits), K, E, k, _p(idx), _p(w))
+    return idx, w
+
+
+def group_size(K, E, k):
+    G = min(E, K * k)
+    return 2 + 2 * G + K * k
+
+
+def group(idx, E, L=None) -> np.ndarray:
+    idx = _c(idx, np.int32)
+    K, k = idx.shape
+    g = np.empty(group_size(K, E, k), np.int32)
+    (L or lib()).orc_group(_p(idx), K, E, k, _p(g))
+    return g
+
+
+def expert(gate, up, down, e, H, I, x_row, L=None):
+    """One expert on one bf16 row: (d[H] float64, h[I] float64)."""
+    keep = [(_c(p.codes, np.uint8), _c(p.scales, np.uint8), _c(p.tscale, np.float32)) for p in (gate, up, down)]
+    prs = [Proj(_p(a), _p(b), _p(c)) for a, b, c in keep]
+    x_row = _c(x_row, np.uint16)
+    d = np.empty(H, np.float64)
+    h = np.empty(I, np.float64)
+    (L or lib()).orc_expert(ctypes.byref(prs[0]), ctypes.byref(prs[1]), ctypes.byref(prs[2]), e, H, I,
+                            _p(x_row), _p(d), _p(h))
+    return d, h
+
+
+def moe_layer(ol: OracleLayer, x_norm, residual=None, L=None):
+    """Returns dict(y=bf16 uint16 [K,H], y_f64, idx, w, group)."""
+    x_norm = _c(x_norm, np.uint16)
+    K = x_norm.shape[0]
+    res = None if residual is None else _c(residual, np.uint16)
+    y = np.empty((K, ol.H), np.uint16)
+    yf = np.empty((K, ol.H), np.float64)
+    idx = np.empty((K, ol.k), np.int32)
+    w = np.empty((K, ol.k), np.float32)
+    g = np.empty(group_size(K, ol.E, ol.k), np.int32)
+    (L or lib()).orc_moe_layer(ol.ref, _p(x_norm), K, _p(res), _p(y), _p(idx), _p(w), _p(g), _p(yf))
+    return dict(y=y, y_f64=yf, idx=idx, w=w, group=g)
+
+
+def rmsnorm(x, eps=RMS_EPS, L=None):
+    x = _c(x, np.uint16)
+    out = np.empty_like(x)
+    (L or lib()).orc_rmsnorm(_p(x), x.shape[0], x.shape[1], eps, _p(out))
+    return out
+
+
+def linear_bf16(x, W, L=None):
+    x, W = _c(x, np.uint16), _c(W, np.uint16)
+    out = np.empty((x.shape[0], W.shape[0]), np.uint16)
+    (L or lib()).orc_linear_bf16(_p(x), _p(W), x.shape[0], x.shape[1], W.shape[0], _p(out))
+    return out
+
+
+def attention(x, Wq, Wk, Wv, Wo, kc, vc, nq, nkv, hd, eps=RMS_EPS, L=None):
+    x = _c(x, np.uint16)
+    K, H = x.shape
+    C = kc.shape[1]
+    arrs = [_c(a, np.uint16) for a in (Wq, Wk, Wv, Wo, kc, vc)]
+    out = np.empty_like(x)
+    (L or lib()).orc_attention(_p(x), K, H, nq, nkv, hd, C, *[_p(a) for a in arrs], eps, _p(out))
+    return out
+
+
+def lm_argmax(x_norm, W, L=None):
+    x_norm, W = _c(x_norm, np.uint16), _c(W, np.uint16)
+    K, H = x_norm.shape
+    tok = np.empty(K, np.int32)
+    best = np.empty(K, np.float32)
+    (L or lib()).orc_lm_argmax(_p(x_norm), _p(W), K, H, W.shape[0], _p(tok), _p(best))
+    return tok, best
+
+
+def accept_prefix(draft, target, L=None) -> int:
+    d, t = _c(draft, np.int32), _c(target, np.int32)
+    return int((L or lib()).orc_accept_prefix(_p(d), _p(t), d.shape[0]))
+
+
+def moe_stack(w, layers, x0, n_layers=None, L=None, collect=False):
+    """Free-running stack of MoE layers: x_{l+1} = moe_l(rmsnorm(x_l)) + x_l.
+    ``layers`` is a callable l -> synthgen.Layer.  Returns the final x and,
+    with ``collect``, the list of per-layer inputs x_l."""
+    x = _c(x0, np.uint16)
+    xs = []
+    for l in range(n_layers or w.layers):
+        if collect:
+            xs.append(x.copy())
+        ol = OracleLayer.from_workload(w, layers(l))
+        x = moe_layer(ol, rmsnorm(x, L=L), residual=x, L=L)["y"]
+    return (x, xs) if collect else x

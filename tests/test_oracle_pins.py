@@ -1,0 +1,464 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle.
+
+Each test fixes one oracle function to something independent of it: the
+hand-worked format tables in ``tests/golden``, the pages' printed byte
+figures, float64 library routines (torch/numpy), closed forms, invariants,
+and brute force on tiny inputs.  A dropped term, a wrong sign, a transposed
+operand or a swapped nibble in the oracle fails at least one of them.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthgen
+from conftest import read_golden
+
+torch.set_default_dtype(torch.float64)
+
+
+# ---------------------------------------------------------------- formats
+
+def _e2m1_golden():
+    return {int(a): float(b) for a, b in (r.split() for r in read_golden("e2m1_values.txt"))}
+
+
+def _e4m3_golden():
+    return {int(a, 16): float(b) for a, b in (r.split() for r in read_golden("e4m3_values.txt"))}
+
+
+def test_e2m1_matches_hand_worked_table():
+    g = _e2m1_golden()
+    assert len(g) == 16
+    for c, v in g.items():
+        o = oracle.e2m1(c)
+        assert o == v and math.copysign(1, o) == math.copysign(1, v), (c, o, v)
+
+
+def test_e4m3_matches_hand_worked_spots():
+    for c, v in _e4m3_golden().items():
+        o = oracle.e4m3(c)
+        if math.isnan(v):
+            assert math.isnan(o), c
+        else:
+            assert o == v and math.copysign(1, o) == math.copysign(1, v), (hex(c), o, v)
+
+
+def test_e4m3_structure_all_codes():
+    vals = [oracle.e4m3(c) for c in range(256)]
+    pos = vals[:0x7F]
+    # strictly increasing over the finite positive codes, sign symmetric,
+    # NaN exactly at S.1111.111, no infinities
+    assert all(b > a for a, b in zip(pos, pos[1:]))
+    for c in range(0x7F):
+        assert vals[c | 0x80] == -vals[c] or (c == 0 and vals[0x80] == 0.0)
+    assert [c for c in range(256) if math.isnan(vals[c])] == [0x7F, 0xFF]
+    assert not any(math.isinf(v) for v in vals)
+    # within each binade the 8 mantissa steps are evenly spaced; subnormal
+    # spacing equals the first normal binade's spacing (2^-9)
+    for e in range(16):
+        row = pos[8 * e: 8 * e + 8]
+        d = np.diff(row)
+        assert np.all(d == d[0])
+    assert pos[8] - pos[7] == pos[1] - pos[0] == 2.0 ** -9
+
+
+def test_e4m3_roundtrip_through_generator_encoder():
+    # the generator quantises drawn scales to E4M3 with its own encoder;
+    # encoding a representable value must give back its code
+    for c in range(1, 0x7F):
+        v = oracle.e4m3(c)
+        out = synthgen.scales(0, 0, 99, 0, 1, lo=v, hi=v)
+        assert out[0] == c, (hex(c), v, out[0])
+
+
+def test_generator_scale_codes_in_declared_range():
+    s = synthgen.scales(5, 3, synthgen.T_GATE_S, 0, 200000)
+    vals = np.array([oracle.e4m3(int(c)) for c in range(256)])[s]
+    assert s.min() == 0x02 and s.max() == 0x18
+    assert vals.min() >= 2.0 ** -8 and vals.max() <= 2.0 ** -4
+
+
+def test_bf16_rounding_matches_library_on_float_inputs():
+    rng = np.random.default_rng(0)
+    v = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.integers(-30, 30, 20000),
+                        [1.0, -2.5, 3.0e38, 1e-40, 0.0]]).astype(np.float32)
+    ref = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([oracle.round_bf16(float(a)) for a in v], np.uint16)
+    assert np.array_equal(got, ref)
+
+
+def test_bf16_rounding_hand_worked_midpoints():
+    # 1 + 2^-8 lies halfway between 1 and 1 + 2^-7: ties go to the even (1.0)
+    assert oracle.round_bf16(1.0 + 2.0 ** -8) == 0x3F80
+    # 1 + 3*2^-8 lies halfway between 1+2^-7 (odd) and 1+2^-6 (even)
+    assert oracle.round_bf16(1.0 + 3 * 2.0 ** -8) == 0x3F82
+    # slightly above the midpoint rounds up; double rounding through float
+    # would lose the 2^-40 and round down
+    assert oracle.round_bf16(1.0 + 2.0 ** -8 + 2.0 ** -40) == 0x3F81
+    assert oracle.round_bf16(-1.0) == 0xBF80
+    for b in (0x0001, 0x3F80, 0x7F7F, 0x8001, 0xC2F7):
+        assert oracle.round_bf16(oracle.bf16_value(b)) == b
+
+
+# ---------------------------------------------------------------- NVFP4 decode / byte model
+
+def _decode_with_table(p, e, rows, cols):
+    """Independent dequantisation from the golden tables (not the oracle)."""
+    t2 = np.array([v for _, v in sorted(_e2m1_golden().items())])
+    t8 = np.array([oracle.e4m3(c) for c in range(256)])  # pinned above
+    c = p.codes[e].astype(np.int64)
+    nib = np.empty((rows, cols), np.int64)
+    nib[:, 0::2] = c & 15
+    nib[:, 1::2] = c >> 4
+    sc = np.repeat(t8[p.scales[e]], 16, axis=1)
+    return t2[nib] * sc * float(p.tscale[e])
+
+
+def test_nvfp4_matrix_layout_against_table_decode():
+    w = synthgen.WORKLOADS["tiny"]
+    L = synthgen.make_layer(w, 0)
+    L.gate.tscale[:] = np.linspace(0.5, 2.0, w.E, dtype=np.float32)
+    for e in (0, 7, 15):
+        got = oracle.nvfp4_matrix(L.gate, e, w.I, w.H)
+        assert np.array_equal(got, _decode_with_table(L.gate, e, w.I, w.H))
+        got = oracle.nvfp4_matrix(L.down, e, w.H, w.I)
+        assert np.array_equal(got, _decode_with_table(L.down, e, w.H, w.I))
+
+
+def test_nvfp4_nibble_order_single_element():
+    # one nonzero element at an odd column must land in the high nibble
+    p = synthgen.Proj(np.zeros((1, 1, 8), np.uint8), np.full((1, 1, 1), 0x38, np.uint8), np.ones(1, np.float32))
+    p.codes[0, 0, 2] = 0x70  # column 5 = code 7 (6.0), column 4 = code 0
+    m = oracle.nvfp4_matrix(p, 0, 1, 16)
+    expect = np.zeros((1, 16))
+    expect[0, 5] = 6.0
+    assert np.array_equal(m, expect)
+
+
+def test_byte_model_matches_page_figures():
+    figs = {r.split()[0]: (float(r.split()[1]), float(r.split()[2])) for r in read_golden("page_byte_figures.txt")}
+    proj = synthgen.nvfp4_bytes(512, 2048) - 4  # the pages' figure has no tensor scale
+    assert proj == 589_824
+    k2 = 2 * 8 * 3 * proj * 39
+    k1 = 1 * 8 * 3 * proj * 39
+    tiles = 16 * proj
+    assert k2 == 1_104_150_528
+    for name, got in (("routed_bytes_k2", k2), ("routed_bytes_k1", k1), ("layer_16_tiles", tiles)):
+        v, tol = figs[name]
+        assert abs(got - v) / v <= tol, (name, got, v)
+
+
+# ---------------------------------------------------------------- router
+
+def _bf(x):
+    return torch.from_numpy(synthgen.bf16_to_f32(x).astype(np.float64))
+
+
+@pytest.fixture(scope="module")
+def k2layer():
+    w = synthgen.WORKLOADS["k2_layer"]
+    L = synthgen.make_layer(w, 0)
+    return w, L, oracle.OracleLayer.from_workload(w, L)
+
+
+def test_router_logits_f64_match_library_matmul(k2layer):
+    w, L, ol = k2layer
+    x = synthgen.make_x(w, 0)
+    ref = (_bf(x) @ _bf(L.router_w).T).numpy()
+    got = oracle.router_logits_f64(ol, x)
+    assert np.allclose(got, ref, rtol=0, atol=1e-12)
+
+
+def test_router_logits_f32_within_float_error_bound(k2layer):
+    w, L, ol = k2layer
+    x = synthgen.make_x(w, 1)
+    ref = (_bf(x) @ _bf(L.router_w).T).numpy()
+    bound = (_bf(x).abs() @ _bf(L.router_w).abs().T).numpy() * (w.H + 5) * 2.0 ** -24
+    got = oracle.router_logits_f32(ol, x).astype(np.float64)
+    assert np.all(np.abs(got - ref) <= bound)
+    # and it is not the double result rounded: the fixed order leaves
+    # float rounding visible
+    assert np.any(got != ref.astype(np.float32))
+
+
+def test_router_fixed_order_hand_worked():
+    # H=256: lane l holds k = 8l..8l+7.  x = 2^24 at k=0 (lane 0), 1 at k=8
+    # (lane 1) and 1 at k=24 (lane 3), w = 1 there.  The pairwise rounds add
+    # lanes 1 and 3 first (distance 2): 1 + 1 = 2, then lane 0 + lane 1
+    # (distance 1): 2^24 + 2, exact.  A left-to-right sum would lose both
+    # ones (2^24 + 1 rounds to 2^24 under ties-to-even).
+    H = 256
+    one = 0x3F80
+    x = np.zeros((1, H), np.uint16)
+    W = np.zeros((1, H), np.uint16)
+    for k, xv in ((0, 0x4B80), (8, one), (24, one)):
+        x[0, k] = xv
+        W[0, k] = one
+    lay = synthgen.Layer(router_w=W, router_b=None, gate=None, up=None, down=None)
+    ol = oracle.OracleLayer(lay, H, 1, 1, 16, 0)
+    assert oracle.router_logits_f32(ol, x)[0, 0] == 2.0 ** 24 + 2
+    # the same three terms inside one lane (k = 0, 1, 2) lose the ones
+    x2 = np.zeros((1, H), np.uint16)
+    W2 = np.zeros((1, H), np.uint16)
+    for k, xv in ((0, 0x4B80), (1, one), (2, one)):
+        x2[0, k] = xv
+        W2[0, k] = one
+    lay2 = synthgen.Layer(router_w=W2, router_b=None, gate=None, up=None, down=None)
+    ol2 = oracle.OracleLayer(lay2, H, 1, 1, 16, 0)
+    assert oracle.router_logits_f32(ol2, x2)[0, 0] == 2.0 ** 24
+
+
+def test_topk_against_library_and_invariants(k2layer):
+    w, L, ol = k2layer
+    x = synthgen.make_x(w, 2, K=16)
+    l32 = oracle.router_logits_f32(ol, x)
+    idx, wt = oracle.topk(l32, w.top_k)
+    l64 = torch.from_numpy(l32.astype(np.float64))
+    ref_vals, ref_idx = torch.topk(l64, w.top_k, dim=1)
+    assert np.array_equal(idx, ref_idx.numpy())  # no exact ties in this draw
+    p = torch.softmax(l64, dim=1)
+    sel = torch.gather(p, 1, ref_idx)
+    ref_w = (sel / sel.sum(1, keepdim=True)).numpy()
+    assert np.allclose(wt, ref_w, rtol=1e-6, atol=0)
+    assert np.allclose(wt.astype(np.float64).sum(1), 1.0, atol=1e-6)
+    for r in range(x.shape[0]):
+        assert len(set(idx[r])) == w.top_k
+        unsel = np.setdiff1d(np.arange(w.E), idx[r])
+        assert l32[r, idx[r]].min() >= l32[r, unsel].max()
+        assert np.all(np.diff(l32[r, idx[r]]) <= 0)
+
+
+def test_topk_exact_ties_go_to_lower_index():
+    logits = np.array([[1.0, 3.0, 3.0, 0.5, 3.0, 2.0]], np.float32)
+    idx, w = oracle.topk(logits, 3)
+    assert idx.tolist() == [[1, 2, 4]]
+    assert np.allclose(w, 1 / 3)
+    idx, _ = oracle.topk(logits, 6)
+    assert idx.tolist() == [[1, 2, 4, 5, 0, 3]]
+
+
+def test_softmax_closed_form_two_experts():
+    # w_0 = 1 / (1 + e^{l1 - l0}) for top-2 of 2
+    logits = np.array([[0.75, -0.5]], np.float32)
+    _, w = oracle.topk(logits, 2)
+    assert abs(w[0, 0] - 1 / (1 + math.exp(-1.25))) < 1e-7
+
+
+# ---------------------------------------------------------------- grouping
+
+def _group_brute(idx, E):
+    K, k = idx.shape
+    G = min(E, K * k)
+    experts = sorted(set(idx.ravel().tolist()))
+    pairs, offs = [], []
+    for e in experts:
+        offs.append(len(pairs))
+        pairs += [r * k + s for r in range(K) for s in range(k) if idx[r, s] == e]
+    n = len(experts)
+    out = [n] + experts + [-1] * (G - n) + offs + [K * k] * (G + 1 - n) + pairs
+    return np.array(out, np.int32)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_group_brute_force(seed):
+    rng = np.random.default_rng(seed)
+    K, E, k = [(1, 16, 2), (2, 256, 8), (16, 256, 8), (4, 8, 8), (16, 8, 3), (3, 5, 5)][seed]
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(K)]).astype(np.int32)
+    g = oracle.group(idx, E)
+    assert np.array_equal(g, _group_brute(idx, E))
+    n = g[0]
+    assert n <= min(E, K * k)
+    assert sorted(g[2 + 2 * min(E, K * k):].tolist()) == list(range(K * k))
+
+
+def test_group_degenerate_cases():
+    # K=1 gives n = k; identical rows give n = k; k = E gives n = E
+    idx = np.array([[3, 1]], np.int32)
+    assert oracle.group(idx, 16)[0] == 2
+    idx = np.tile(np.array([[5, 2, 9]], np.int32), (4, 1))
+    g = oracle.group(idx, 16)
+    assert g[0] == 3 and g[1:4].tolist() == [2, 5, 9]
+    idx = np.array([[2, 0, 1], [1, 2, 0]], np.int32)
+    assert oracle.group(idx, 3)[0] == 3
+
+
+# ---------------------------------------------------------------- experts and the layer
+
+def _bf16_round_t(t):
+    return t.to(torch.float32).to(torch.bfloat16).to(torch.float64)
+
+
+def _dense_expert_torch(L, e, x64, shared=False):
+    gp, up, dp = (L.sh_gate, L.sh_up, L.sh_down) if shared else (L.gate, L.up, L.down)
+    H = x64.shape[1]
+    I = gp.codes.shape[1]
+    G = torch.from_numpy(_decode_with_table(gp, e, I, H))
+    U = torch.from_numpy(_decode_with_table(up, e, I, H))
+    D = torch.from_numpy(_decode_with_table(dp, e, H, I))
+    h = _bf16_round_t(torch.nn.functional.silu(x64 @ G.T) * (x64 @ U.T))
+    return h @ D.T
+
+
+def test_expert_equals_dense_swiglu_mlp():
+    # E = k = 1 reduces the layer to a dense SwiGLU MLP
+    w = synthgen.Workload("e1", K=3, H=256, E=1, top_k=1, I=128, Is=0, layers=1, seed=11)
+    L = synthgen.make_layer(w, 0)
+    x = synthgen.make_x(w, 0)
+    ol = oracle.OracleLayer.from_workload(w, L)
+    r = oracle.moe_layer(ol, x)
+    ref = _dense_expert_torch(L, 0, _bf(x)).numpy()
+    assert np.all(r["idx"] == 0) and np.allclose(r["w"], 1.0)
+    assert np.allclose(r["y_f64"], ref, rtol=1e-9, atol=1e-9 * np.abs(ref).max())
+
+
+@pytest.mark.parametrize("with_shared", [False, True])
+def test_layer_against_brute_force_dense(with_shared):
+    w = synthgen.Workload("bf", K=5, H=256, E=16, top_k=4, I=128, Is=128 if with_shared else 0,
+                          layers=1, seed=12, routed_scale=2.5)
+    L = synthgen.make_layer(w, 0)
+    x = synthgen.make_x(w, 0)
+    res = synthgen.make_x(w, 7)
+    ol = oracle.OracleLayer.from_workload(w, L)
+    r = oracle.moe_layer(ol, x, residual=res)
+    x64 = _bf(x)
+    # every expert on every row, then the routing mask
+    dense = torch.stack([_dense_expert_torch(L, e, x64) for e in range(w.E)])  # [E, K, H]
+    l64 = x64 @ _bf(L.router_w).T
+    p = torch.softmax(l64, 1)
+    mask = torch.zeros(w.K, w.E)
+    for rr in range(w.K):
+        top = torch.topk(l64[rr], w.top_k).indices
+        mask[rr, top] = p[rr, top] / p[rr, top].sum()
+        assert sorted(top.tolist()) == sorted(r["idx"][rr].tolist())
+    y = 2.5 * torch.einsum("ke,ekh->kh", mask, dense)
+    if with_shared:
+        y = y + _dense_expert_torch(L, 0, x64, shared=True)
+    y = y + _bf(res)
+    assert np.allclose(r["y_f64"], y.numpy(), rtol=0, atol=1e-6 * float(y.abs().max()))
+    yb = synthgen.bf16_to_f32(r["y"]).astype(np.float64)
+    assert np.allclose(yb, y.numpy(), rtol=2.0 ** -8, atol=1e-6)
+
+
+def test_combine_linearity_routed_scale_and_residual():
+    w = synthgen.Workload("lin", K=2, H=256, E=16, top_k=2, I=128, Is=128, layers=1, seed=13)
+    L = synthgen.make_layer(w, 0)
+    L.sh_gate.codes[:] = 0  # zero shared weights isolate the routed part
+    x = synthgen.make_x(w, 0)
+    res = synthgen.make_x(w, 3)
+    a = oracle.moe_layer(oracle.OracleLayer.from_workload(w, L, routed_scale=1.0), x)["y_f64"]
+    b = oracle.moe_layer(oracle.OracleLayer.from_workload(w, L, routed_scale=2.5), x)["y_f64"]
+    c = oracle.moe_layer(oracle.OracleLayer.from_workload(w, L, routed_scale=1.0), x, residual=res)["y_f64"]
+    assert np.array_equal(b, 2.5 * a)
+    assert np.allclose(c - a, synthgen.bf16_to_f32(res), rtol=0, atol=1e-12 * np.abs(c).max())
+    assert np.abs(a).max() > 0
+
+
+# ---------------------------------------------------------------- rmsnorm, attention, lm_head, accept
+
+def test_rmsnorm_against_library():
+    x = synthgen.normal_bf16(1, 0, 5, 0, 4 * 2048, 0.3, 2.0).reshape(4, 2048)
+    got = synthgen.bf16_to_f32(oracle.rmsnorm(x)).astype(np.float64)
+    x64 = _bf(x)
+    ref = (x64 * torch.rsqrt(x64.pow(2).mean(1, keepdim=True) + 1e-6)).numpy()
+    assert np.allclose(got, ref, rtol=2.0 ** -8, atol=0)
+    assert np.allclose(np.sqrt((got ** 2).mean(1)), 1.0, atol=1e-2)
+
+
+def _att_inputs(K, H, nq, nkv, hd, C, seed):
+    g = lambda t, n, s: synthgen.normal_bf16(seed, 0, t, 0, n, 0.0, s)
+    Wq = g(30, nq * hd * H, 0.05).reshape(nq * hd, H)
+    Wk = g(31, nkv * hd * H, 0.05).reshape(nkv * hd, H)
+    Wv = g(32, nkv * hd * H, 0.05).reshape(nkv * hd, H)
+    Wo = g(33, H * nq * hd, 0.05).reshape(H, nq * hd)
+    kc = g(34, nkv * C * hd, 1.0).reshape(nkv, C, hd)
+    vc = g(35, nkv * C * hd, 1.0).reshape(nkv, C, hd)
+    x = g(36, K * H, 1.0).reshape(K, H)
+    return x, Wq, Wk, Wv, Wo, kc, vc
+
+
+def test_attention_against_library_sdpa():
+    K, H, nq, nkv, hd, C = 3, 256, 4, 2, 32, 37
+    x, Wq, Wk, Wv, Wo, kc, vc = _att_inputs(K, H, nq, nkv, hd, C, 21)
+    got = synthgen.bf16_to_f32(oracle.attention(x, Wq, Wk, Wv, Wo, kc, vc, nq, nkv, hd)).astype(np.float64)
+    xn = _bf(oracle.rmsnorm(x))
+    q = _bf16_round_t(xn @ _bf(Wq).T).view(K, nq, hd).transpose(0, 1)
+    kn = _bf16_round_t(xn @ _bf(Wk).T).view(K, nkv, hd).transpose(0, 1)
+    vn = _bf16_round_t(xn @ _bf(Wv).T).view(K, nkv, hd).transpose(0, 1)
+    kk = torch.cat([_bf(kc.reshape(-1, hd)).view(nkv, C, hd), kn], 1).repeat_interleave(nq // nkv, 0)
+    vv = torch.cat([_bf(vc.reshape(-1, hd)).view(nkv, C, hd), vn], 1).repeat_interleave(nq // nkv, 0)
+    mask = torch.ones(K, C + K, dtype=torch.bool)
+    for r in range(K):
+        mask[r, C + r + 1:] = False
+    o = torch.nn.functional.scaled_dot_product_attention(q, kk, vv, attn_mask=mask)
+    o = _bf16_round_t(o.transpose(0, 1).reshape(K, nq * hd))
+    ref = _bf(x) + o @ _bf(Wo).T
+    assert np.allclose(got, ref.numpy(), rtol=2.0 ** -7, atol=1e-3)
+
+
+def test_attention_single_key_returns_value():
+    # no cache, one row: the only visible key is the row's own -> o = v
+    K, H, nq, nkv, hd = 1, 256, 2, 1, 32
+    x, Wq, Wk, Wv, Wo, kc, vc = _att_inputs(K, H, nq, nkv, hd, 0, 22)
+    kc = np.zeros((nkv, 0, hd), np.uint16)
+    vc = np.zeros((nkv, 0, hd), np.uint16)
+    got = synthgen.bf16_to_f32(oracle.attention(x, Wq, Wk, Wv, Wo, kc, vc, nq, nkv, hd)).astype(np.float64)
+    xn = oracle.rmsnorm(x)
+    v = _bf(oracle.linear_bf16(xn, Wv))  # [1, hd]
+    o = torch.cat([v, v], 1)  # both q heads share kv head 0
+    ref = _bf(x) + o @ _bf(Wo).T
+    assert np.allclose(got, ref.numpy(), rtol=2.0 ** -7, atol=1e-3)
+
+
+def test_attention_uniform_scores_average_values():
+    # Wq = 0 -> all scores 0 -> o = mean of the visible values
+    K, H, nq, nkv, hd, C = 2, 256, 2, 1, 32, 5
+    x, Wq, Wk, Wv, Wo, kc, vc = _att_inputs(K, H, nq, nkv, hd, C, 23)
+    Wq = np.zeros_like(Wq)
+    got = synthgen.bf16_to_f32(oracle.attention(x, Wq, Wk, Wv, Wo, kc, vc, nq, nkv, hd)).astype(np.float64)
+    vn = _bf(oracle.linear_bf16(oracle.rmsnorm(x), Wv))
+    vall = torch.cat([_bf(vc.reshape(C, hd)), vn], 0)
+    for r in range(K):
+        o = _bf16_round_t(vall[: C + r + 1].mean(0))
+        ref = _bf(x[r:r + 1]) + torch.cat([o, o])[None] @ _bf(Wo).T
+        assert np.allclose(got[r], ref.numpy()[0], rtol=2.0 ** -7, atol=1e-3)
+
+
+def test_lm_argmax_against_library():
+    K, H, V = 4, 512, 3001
+    x = synthgen.normal_bf16(2, 0, 50, 0, K * H).reshape(K, H)
+    W = synthgen.normal_bf16(2, 0, 51, 0, V * H, 0.0, 0.02).reshape(V, H)
+    tok, best = oracle.lm_argmax(x, W)
+    l64 = _bf(x) @ _bf(W).T
+    top2 = torch.topk(l64, 2, dim=1)
+    for r in range(K):
+        margin = float(top2.values[r, 0] - top2.values[r, 1])
+        if margin > 1e-4:
+            assert tok[r] == int(top2.indices[r, 0])
+        assert abs(best[r] - float(l64[r, tok[r]])) < 1e-4
+
+
+def test_lm_argmax_exact_tie_lowest_index():
+    K, H, V = 1, 256, 10
+    x = synthgen.normal_bf16(3, 0, 52, 0, H).reshape(K, H)
+    W = synthgen.normal_bf16(3, 0, 53, 0, V * H, 0.0, 0.02).reshape(V, H)
+    l64 = (_bf(x) @ _bf(W).T)[0]
+    b = int(torch.argmax(l64))
+    W[7] = W[b]
+    W[2] = W[b]
+    tok, _ = oracle.lm_argmax(x, W)
+    assert tok[0] == min(2, b)
+
+
+def test_accept_prefix_golden_and_brute_force():
+    for row in read_golden("accept_cases.txt"):
+        d, t, n = row.split("|")
+        assert oracle.accept_prefix(np.array(d.split(), np.int32), np.array(t.split(), np.int32)) == int(n)
+    for K in range(1, 9):
+        for pattern in range(1 << K):
+            eq = np.array([(pattern >> i) & 1 for i in range(K)], bool)
+            t = np.arange(K, dtype=np.int32) + 100
+            d = np.where(eq, t, t + 1).astype(np.int32)
+            assert oracle.accept_prefix(d, t) == int(np.cumprod(eq).sum())
