@@ -1,0 +1,416 @@
+#!/usr/bin/env python
+"""Benchmark of the MoE verify layer on GB300 (one JSON line on stdout).
+
+Workload (default ``k2_layer``): DFlash K=2 verify through one MoE layer --
+hidden 2048, 256 routed experts, top-8, expert intermediate 512, a shared
+expert of intermediate 512, NVFP4 expert weights, bf16 router, 2 bf16 rows.
+A step is one layer call (router -> top-k -> dedup -> gate/up+SwiGLU ->
+down+combine) on one batch of K rows.  Steps cycle over a ring of distinct
+seeded layers whose touched bytes exceed L2 several times, so every step
+streams its experts from HBM.  The timed steps run as CUDA-graph replays.
+
+value     = algorithmic bytes / time (GB/s): router weights + the distinct
+            experts' NVFP4 bytes (codes + E4M3 scales + FP32 tensor scale,
+            each distinct expert once) + activations in/out.
+e2e       = the same metric through the C ABI from pinned host buffers, the
+            host->device copy of x and device->host copy of y inside the
+            timed region, one eager call per step.
+roofline  = the dominant kernel's algorithmic bytes per launch over its mean
+            CUDA-event duration (a profiling pass with events between the
+            three kernels), against the measured HBM copy bandwidth.
+cpu_baseline = the CPU oracle on a bounded sample of the same workload.
+
+``--impl reference`` times the CPU oracle alone on the same workload (the
+reference arm).  ``--gpus N`` under torchrun runs N independent replicas
+(the layer does not shard); value sums the ranks' bytes over the slowest
+rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE verify-layer HBM GB/s (% of peak) and verified tokens/s at K=1..16"
+FALLBACK_HBM_GBS = 6800.0
+RING = 24
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=48000)
+    p.add_argument("--warmup", type=int, default=48)
+    p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    p.add_argument("--workload", default="k2_layer")
+    p.add_argument("--ring", type=int, default=RING)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    return p.parse_args()
+
+
+# --------------------------------------------------------------------------- helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def nvfp4_bytes(rows, cols):
+    return rows * cols // 2 + rows * cols // 16 + 4
+
+
+def kernel_bytes(w, n_u, residual=False):
+    """Algorithmic bytes of one layer call, per kernel."""
+    act = w.K * w.H * 2
+    slots = n_u + (1 if w.Is else 0)
+    router = w.E * w.H * 2 + act + (w.E * 4 if w.zipf_s else 0)
+    gateup = slots * 2 * nvfp4_bytes(w.I, w.H) + act
+    down = slots * nvfp4_bytes(w.H, w.I) + act * (2 if residual else 1)
+    layer = router + gateup + down - act  # x is read by router and gate/up but counted once
+    return dict(router=router, gateup=gateup, down=down, layer=layer)
+
+
+class Clocks:
+    """Samples SM clocks and throttle reasons with nvidia-smi during a region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = tempfile.mktemp(prefix="clk", suffix=".csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dominant_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if the kernel
+    sources are unchanged since it was taken (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    for line in open(path):
+        if ":" in line and not line.startswith(" "):
+            k, v = line.split(":", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("source_sha256") != source_hash():
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def source_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "moe_nvfp4_block_gb300", "csrc")
+    for fn in sorted(os.listdir(d)):
+        if fn.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(d, fn), "rb").read())
+    return h.hexdigest()[:16]
+
+
+# --------------------------------------------------------------------------- CPU oracle timing
+
+def oracle_sample(w, seconds, first_layer=0):
+    """Times the CPU oracle on whole layers of the workload until ~seconds of
+    oracle time is spent; returns (bytes/s, layers, seconds, threads)."""
+    import oracle
+    import synthgen
+    oracle.build()
+    t_total, b_total, n = 0.0, 0, 0
+    while t_total < seconds or n == 0:
+        l = first_layer + n
+        full = synthgen.make_layer(w, l, experts=[])  # router + shared only
+        x = synthgen.make_x(w, l)
+        ol0 = oracle.OracleLayer.from_workload(w, full)
+        idx, _ = oracle.topk(oracle.router_logits_f32(ol0, x), w.top_k)
+        L = synthgen.make_layer(w, l, experts=sorted(set(idx.ravel().tolist())))
+        ol = oracle.OracleLayer.from_workload(w, L)
+        t0 = time.perf_counter()
+        r = oracle.moe_layer(ol, x)
+        t_total += time.perf_counter() - t0
+        b_total += kernel_bytes(w, int(r["group"][0]))["layer"]
+        n += 1
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return b_total / t_total, n, t_total, threads
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    import torch
+    import synthgen
+    import moe_nvfp4_block_gb300 as M
+    import __graft_entry__
+    __graft_entry__.build()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = synthgen.WORKLOADS[args.workload]
+    R = args.ring
+    t_gen = time.perf_counter()
+    layers, xs, ys = [], [], []
+    for l in range(R):
+        L = synthgen.make_layer(w, l)
+        t = lambda p: (p.codes, p.scales, p.tscale)
+        sh = None if L.sh_gate is None else (t(L.sh_gate), t(L.sh_up), t(L.sh_down))
+        bias = L.router_b if w.zipf_s else None
+        layers.append(M.layer_from_arrays(L.router_w, bias, t(L.gate), t(L.up), t(L.down), sh, top_k=w.top_k,
+                                          routed_scale=w.routed_scale, device=dev))
+        xs.append(torch.from_numpy(synthgen.make_x(w, 1000 + l)).view(torch.bfloat16).to(dev))
+        ys.append(torch.empty_like(xs[-1]))
+        del L
+    t_gen = time.perf_counter() - t_gen
+    cl = [lay.c() for lay in layers]
+    ws = M.workspace(layers[0], w.K, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+
+    # routing of each ring layer (deterministic) -> distinct experts -> bytes
+    n_u = []
+    with torch.cuda.stream(stream):
+        grp = torch.empty(M.moe_group_ints(w.K, w.E, w.top_k), dtype=torch.int32, device=dev)
+        for i in range(R):
+            M.moe_verify_layer(layers[i], xs[i], None, ys[i], ws, group_out=grp, stream=stream, c_layer=cl[i])
+            stream.synchronize()
+            n_u.append(int(grp[0].item()))
+    kb = [kernel_bytes(w, n) for n in n_u]
+
+    def call(i):
+        j = i % R
+        M.moe_verify_layer(layers[j], xs[j], None, ys[j], ws, stream=stream, c_layer=cl[j])
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            call(i)
+    stream.synchronize()
+    assert M.moe_workspace_error(ws, stream) == 0
+
+    # graphs: full passes over the ring + a remainder
+    steps = args.steps
+    full, rem = divmod(steps, R)
+    g_full = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_full, stream=stream):
+        for i in range(R):
+            call(i)
+    g_rem = None
+    if rem:
+        g_rem = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_rem, stream=stream):
+            for i in range(rem):
+                call(i)
+    with torch.cuda.stream(stream):
+        g_full.replay()
+    stream.synchronize()
+
+    clocks = Clocks(local)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(full):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        ev1.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if dist:
+        dist.barrier()
+    ms = ev0.elapsed_time(ev1)
+    assert M.moe_workspace_error(ws, stream) == 0
+    total_bytes = sum(kb[i % R]["layer"] for i in range(steps))
+    if dist:
+        t = torch.tensor([ms, total_bytes], dtype=torch.float64, device=dev)
+        tl = [torch.zeros_like(t) for _ in range(world)]
+        dist.all_gather(tl, t)
+        ms = max(float(x[0]) for x in tl)
+        total_bytes = sum(float(x[1]) for x in tl)
+    gbs = total_bytes / (ms * 1e-3) / 1e9
+    hbm, peak_src = peaks()
+
+    # per-kernel durations (events between kernels, no overlap)
+    n_prof = 4 * R
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_prof)]
+    with torch.cuda.stream(stream):
+        for i in range(n_prof):
+            j = i % R
+            M.moe_verify_layer_profiled(layers[j], xs[j], None, ys[j], ws, events=evs[i], stream=stream,
+                                        c_layer=cl[j])
+    stream.synchronize()
+    dur = {"router": [], "gateup": [], "down": []}
+    for e in evs:
+        dur["router"].append(e[0].elapsed_time(e[1]))
+        dur["gateup"].append(e[1].elapsed_time(e[2]))
+        dur["down"].append(e[2].elapsed_time(e[3]))
+    mean_ms = {k: float(np.mean(v)) for k, v in dur.items()}
+    dom = max(mean_ms, key=mean_ms.get)
+    dom_bytes = float(np.mean([kb[i % R][dom] for i in range(n_prof)]))
+    achieved = dom_bytes / (mean_ms[dom] * 1e-3) / 1e9
+    traffic = dominant_traffic(dom, args.workload)
+
+    # end to end from pinned host buffers
+    n_e2e = min(steps, 20 * R)
+    hx = [torch.empty(xs[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(R)]
+    hy = [torch.empty(xs[0].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(R)]
+    for i in range(R):
+        hx[i].copy_(xs[i].cpu())
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stream.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(n_e2e):
+            j = i % R
+            xs[j].copy_(hx[j], non_blocking=True)
+            M.moe_verify_layer(layers[j], xs[j], None, ys[j], ws, stream=stream, c_layer=cl[j])
+            hy[j].copy_(ys[j], non_blocking=True)
+        e1.record(stream)
+    stream.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    e2e_gbs = sum(kb[i % R]["layer"] for i in range(n_e2e)) / (e2e_ms * 1e-3) / 1e9
+    act = w.K * w.H * 2
+
+    out = {
+        "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": ms / steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp4(e2m1)*fp16 mma -> f32", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: DFlash K={w.K} verify, {w.layers} MoE layer (H={w.H}, E={w.E}, "
+                               f"top-{w.top_k}, I={w.I}, shared I={w.Is}, NVFP4 experts, bf16 router)",
+                   "K": w.K, "ring_layers": R,
+                   "l2": f"inputs larger than L2: steps cycle over {R} distinct layers "
+                         f"({R * 257 * 3 * nvfp4_bytes(w.I, w.H) / 1e9:.1f} GB resident)",
+                   "launch": "CUDA graph replay, PDL between the 3 kernels of a call",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "pct_of_peak": round(100 * gbs / hbm, 1),
+        "row_layers_per_s": round(w.K * steps / (ms * 1e-3) * world, 1),
+        "layers_per_s": round(steps / (ms * 1e-3) * world, 1),
+        "distinct_experts_mean": float(np.mean(n_u)),
+        "clocks": clk,
+        "e2e": {"value": round(e2e_gbs, 1), "unit": "GB/s", "h2d_bytes_per_step": act, "d2h_bytes_per_step": act,
+                "steps": n_e2e},
+        "gpu_launches": 3 * steps,
+        "kernel_ms": {k: round(v, 5) for k, v in mean_ms.items()},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm,
+                     "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / hbm, 3),
+                     "traffic": traffic, "algorithmic_bytes_per_launch": dom_bytes},
+        "setup_s": round(t_gen, 1),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        bps, n, secs, threads = oracle_sample(w, args.cpu_seconds)
+        out["cpu_baseline"] = {"value": round(bps / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                               "sample": f"{n} whole {args.workload} layers (K={w.K}) of the same workload, "
+                                         f"{secs:.1f} s of oracle time"}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+# --------------------------------------------------------------------------- reference arm (CPU oracle)
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import synthgen
+    w = synthgen.WORKLOADS[args.workload]
+    # warm-up, then timed oracle steps; a step is one whole layer of the
+    # workload; the number of timed steps is capped to keep the run short
+    budget_s = 90.0
+    bps_w, _, t_w, _ = oracle_sample(w, 0.0, first_layer=0) if args.warmup > 0 else (0, 0, 0, 0)
+    per_step = max(t_w, 1e-3)
+    n = max(1, min(args.steps, int(budget_s / per_step)))
+    t0 = time.perf_counter()
+    bytes_total, secs_total = 0.0, 0.0
+    for i in range(n):
+        bps, _, secs, threads = oracle_sample(w, 0.0, first_layer=1 + i)
+        bytes_total += bps * secs
+        secs_total += secs
+    wall = time.perf_counter() - t0
+    gbs = bytes_total / secs_total / 1e9
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    sample = (f"{n} of the requested {args.steps} steps (each one whole {args.workload} layer, K={w.K}); "
+              f"{secs_total:.1f} s oracle time, {wall:.1f} s wall incl. input generation")
+    out = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": args.gpus,
+           "steps": n, "warmup": args.warmup, "ms_per_step": secs_total / n * 1e3, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": f"{args.workload}: DFlash K={w.K} verify, {w.layers} MoE layer (H={w.H}, E={w.E}, "
+                                  f"top-{w.top_k}, I={w.I}, shared I={w.Is})", "K": w.K},
+           "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_gpu(a)

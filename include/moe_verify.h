@@ -1,0 +1,220 @@
+/*
+ * moe_verify.h -- C ABI of the GB300 (sm_103a) MoE verify-layer library.
+ *
+ * The layer is the target model's MoE block inside DFlash target-verified
+ * block speculative decoding: K draft rows are verified in one forward; each
+ * row is routed top-k over E experts; each selected expert's NVFP4
+ * gate/up/down projections and a shared expert are evaluated and combined
+ * ("Why this challenge exists", mlxfast Laguna XS 2.1 (DFlash) README:
+ * 256 routed experts plus one shared expert, 8 experts per token, MoE
+ * intermediate 512, routed/shared projections NVFP4 4-bit group-16, router
+ * bf16).  An expert chosen by several rows streams its weights once (PR #844,
+ * "8. What I looked at": the routed gather reads an expert once per
+ * (row, slot) and has no cross-row dedup).
+ *
+ * Conventions for every entry point
+ *  - All data pointers are DEVICE pointers owned by the caller, 16-byte
+ *    aligned.  bf16 tensors are passed as their 16-bit patterns (uint16_t).
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *    asynchronous: they enqueue work and return; nothing blocks the host
+ *    except moe_workspace_error().
+ *  - The library allocates no memory, reads no environment variables and
+ *    keeps no per-call state on the host.  Concurrent calls on different
+ *    streams need distinct workspaces.
+ *  - Argument errors are detected on the host before anything is enqueued
+ *    and returned as a negative moe_status.  A failed launch returns
+ *    MOE_ERR_CUDA.  A device-side wait that ran out of time is recorded in
+ *    the workspace and read back with moe_workspace_error().
+ *  - Results are deterministic: identical inputs give bit-identical outputs
+ *    (no floating-point atomics; every reduction has a fixed order).
+ */
+#ifndef MOE_VERIFY_H
+#define MOE_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,        /* null pointer, K/shape out of range */
+  MOE_ERR_UNSUPPORTED_SHAPE = -2,  /* shape outside the supported envelope */
+  MOE_ERR_WORKSPACE_TOO_SMALL = -3,
+  MOE_ERR_MISALIGNED = -4,         /* a pointer is not 16-byte aligned */
+  MOE_ERR_CUDA = -5,               /* a CUDA runtime/driver call failed */
+  MOE_ERR_DEVICE_TIMEOUT = -6      /* a bounded device-side wait expired */
+} moe_status;
+
+/*
+ * One NVFP4 projection over a stack of experts, [n_exp][rows][cols]
+ * (cols is the reduction dimension).  Element (e, r, c) has the value
+ *   e2m1(code) * e4m3(scale) * tensor_scale[e]
+ * where code is the low nibble of codes[e][r][c/2] for even c and the high
+ * nibble for odd c (E2M1: sign, 2 exponent bits with bias 1, 1 mantissa
+ * bit), scale = scales[e][r][c/16] (OCP E4M3FN), one scale per 16
+ * consecutive columns of a row.
+ */
+typedef struct {
+  const uint8_t* codes;         /* [n_exp][rows][cols/2] */
+  const uint8_t* scales;        /* [n_exp][rows][cols/16] */
+  const float* tensor_scale;    /* [n_exp] */
+} moe_nvfp4;
+
+/*
+ * One MoE layer.  gate/up: rows = inter, cols = hidden; down: rows = hidden,
+ * cols = inter; the sh_* projections hold one expert of intermediate
+ * shared_inter (0 = no shared expert, the sh_* fields are then ignored).
+ * Supported envelope: hidden in {256, 512, ..., 2048} (a multiple of 256);
+ * inter in {128, 256, 512}; shared_inter in {0, inter}; 1 <= top_k <= 32;
+ * top_k <= n_experts <= 1024.  Outside it: MOE_ERR_UNSUPPORTED_SHAPE.
+ */
+typedef struct {
+  int hidden, n_experts, top_k, inter, shared_inter;
+  float routed_scale;          /* multiplies the routed sum (1.0 = none) */
+  const uint16_t* router_w;    /* bf16 [n_experts][hidden] */
+  const float* router_bias;    /* [n_experts], added to the logits; NULL = 0 */
+  moe_nvfp4 gate, up, down;
+  moe_nvfp4 sh_gate, sh_up, sh_down;
+} moe_layer;
+
+/* Largest number of verify rows one call accepts. */
+#define MOE_MAX_ROWS 16
+
+/*
+ * Bytes of device workspace a layer call with K rows needs (0 on an invalid
+ * layer or K).  The workspace must be zero-filled once before its first use
+ * (e.g. cudaMemsetAsync); every call leaves it ready for the next call.
+ * After a call that returned MOE_ERR_DEVICE_TIMEOUT zero-fill it again.
+ */
+size_t moe_verify_layer_workspace_size(const moe_layer* layer, int K);
+
+/*
+ * Router: logits = x_norm . router_w^T + bias in one fixed FP32 order, a
+ * softmax over all experts, the top_k experts per row (larger logit first,
+ * lower expert index on an exact tie), and their probabilities renormalised
+ * over the selected set (PR #844, "4. What I ported": top-k selection and
+ * renormalisation of the router scores).
+ *   x_norm  bf16 [K][hidden] (already normalised)
+ *   idx     int32 [K][top_k] out, rank order;  w  float [K][top_k] out
+ *   group   int32 out (nullable): experts grouped for dedup,
+ *           with G = min(n_experts, K*top_k):
+ *             group[0]                 n = number of distinct experts
+ *             group[1 .. 1+G)          the distinct experts ascending, then -1
+ *             group[1+G .. 2+2G)       offsets; expert u owns pair slots
+ *                                      [off[u], off[u+1]); off[u] = K*top_k for u >= n
+ *             group[2+2G .. 2+2G+K*top_k)  pair ids r*top_k + s, rows ascending
+ *           (moe_group_ints(K, n_experts, top_k) ints)
+ *   ws      workspace of moe_verify_layer_workspace_size(layer, K) bytes
+ */
+moe_status moe_router_topk(const moe_layer* layer, const uint16_t* x_norm, int K, int32_t* idx,
+                           float* w, int32_t* group, void* ws, size_t ws_bytes, void* stream);
+
+/* Number of int32 entries of the group output. */
+size_t moe_group_ints(int K, int n_experts, int top_k);
+
+/*
+ * The MoE verify layer:
+ *   y_r = bf16( routed_scale * sum_{s<top_k} w_{r,s} * Down_e(h_{r,s})
+ *               + Down_sh(h_sh) + residual_r ),   e = idx[r][s]
+ *   h = bf16( silu(Gate_e x_r) * (Up_e x_r) )
+ * (PR #844, "4. What I ported" and "5. Numerical safety": silu(gate)*up,
+ * weighted expert sum, routed scaling, shared add and decoder residual add
+ * in that order).  Each distinct expert's weights are read once per call.
+ *   x_norm    bf16 [K][hidden], the normalised block input
+ *   residual  bf16 [K][hidden] or NULL
+ *   y         bf16 [K][hidden] out (may alias residual, not x_norm)
+ *   idx_out, w_out, group_out: optional copies of the routing (as in
+ *             moe_router_topk); NULL to skip
+ * Accumulation is FP32; activations enter the tensor cores as FP16 after an
+ * exact per-row power-of-two rescaling, so no bf16 value overflows.
+ */
+moe_status moe_verify_layer(const moe_layer* layer, const uint16_t* x_norm, int K,
+                            const uint16_t* residual, uint16_t* y, int32_t* idx_out, float* w_out,
+                            int32_t* group_out, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * A stack of MoE decoder blocks for the K verify rows, in place:
+ *   for l in 0 .. n_layers-1:  x <- x + MoE_l( rmsnorm(x) )
+ * (moe_rmsnorm with `eps`, then moe_verify_layer with residual = x and
+ * y = x), all enqueued on `stream` with programmatic overlap between
+ * kernels.  All layers share `hidden`.
+ *   layers   host array of n_layers layer descriptions (read during the call)
+ *   x        bf16 [K][hidden], the residual stream, updated in place
+ *   ws       moe_verify_stack_workspace_size(layers, n_layers, K) bytes,
+ *            zero-filled before first use
+ */
+size_t moe_verify_stack_workspace_size(const moe_layer* layers, int n_layers, int K);
+moe_status moe_verify_stack(const moe_layer* layers, int n_layers, uint16_t* x, int K, float eps, void* ws,
+                            size_t ws_bytes, void* stream);
+
+/*
+ * Profiling variant of moe_verify_layer for benchmarks: identical results,
+ * but the three kernels (router, gate/up, down) are launched without
+ * programmatic overlap and, when `events` is not NULL, the cudaEvent_t
+ * handles events[0..3] are recorded on `stream` before the router, after the
+ * router, after gate/up and after down, so each kernel can be timed.
+ */
+moe_status moe_verify_layer_profiled(const moe_layer* layer, const uint16_t* x_norm, int K,
+                                     const uint16_t* residual, uint16_t* y, void* ws, size_t ws_bytes,
+                                     void* stream, void* const* events);
+
+/*
+ * Accepted prefix of a drafted block: the first i with draft[i] != target[i],
+ * or K when all match (README, opening section: decode advances by the
+ * longest correct prefix).
+ *   draft, target  int32 [K] (may be NULL when K == 0);  n_accepted  int32 [1] out.
+ *   0 <= K <= 4096.
+ */
+moe_status verify_accept_prefix(const int32_t* draft, const int32_t* target, int K,
+                                int32_t* n_accepted, void* stream);
+
+/*
+ * RMSNorm with unit gain between blocks of the verify step:
+ *   out_r = bf16( x_r * 1/sqrt(mean(x_r^2) + eps) )
+ * in FP32 in the router's fixed order (its output decides the top-k):
+ * the sum of squares is the fixed-order dot product of the row with itself,
+ * then one correctly rounded FP32 operation per step.
+ *   x, out  bf16 [K][H]; 1 <= K <= 16; H a multiple of 256.
+ */
+moe_status moe_rmsnorm(const uint16_t* x, int K, int H, float eps, uint16_t* out, void* stream);
+
+/* Bytes of workspace moe_lm_head_argmax needs for K rows (zero-filled once
+ * before first use; calls leave it ready for the next call). */
+size_t moe_lm_head_workspace_size(int K);
+
+/*
+ * Greedy token of every verify row (PR #844, "5. Numerical safety": the
+ * verifier takes the argmax over every row):
+ *   tok_r = argmax_v  x_norm_r . W_v   (FP32, the router's fixed order;
+ *                                       an exact tie goes to the lower v)
+ *   x_norm bf16 [K][H]; W bf16 [V][H]; tok int32 [K] out;
+ *   best_logit float [K] out (nullable): the winning logit.
+ *   1 <= K <= 16; H a multiple of 256, at most 2048.
+ */
+moe_status moe_lm_head_argmax(const uint16_t* x_norm, int K, int H, const uint16_t* W, int V, int32_t* tok,
+                              float* best_logit, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Reads the device error word of a workspace (0 = none, else a negative
+ * moe_status) and clears it.  Synchronises `stream`.
+ */
+moe_status moe_workspace_error(void* ws, int* code, void* stream);
+
+/* A short English description of a status. */
+const char* moe_status_string(moe_status s);
+
+/*
+ * Test hook: upper bound, in nanoseconds, of every device-side wait in
+ * kernels launched after this call (default 2e9).  0 makes every wait give
+ * up at once, which exercises the timeout path without hanging a GPU.
+ */
+void moe_debug_set_wait_limit_ns(uint64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_VERIFY_H */

@@ -1,0 +1,166 @@
+// internal.h -- shapes, workspace layout and kernel argument blocks shared by
+// the C-ABI layer (capi.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe_verify.h"
+
+namespace moe {
+
+constexpr int kRouterWarps = 8;          // experts per router CTA
+constexpr int kGUWarps = 8;              // consumer warps, gate/up kernel
+constexpr int kDNWarps = 8;              // consumer warps, down kernel
+constexpr int kGURows = 16;              // intermediate rows per gate/up item
+constexpr int kDNRows = 64;              // hidden rows per down item
+constexpr int kGUStages = 4;
+constexpr int kDNStages = 6;
+
+// Byte offsets of the workspace regions (all 256-byte aligned).
+struct WsLayout {
+  size_t hdr;      // int32[64]: [0] error word, [1] router ticket
+  size_t logits;   // float [K][E]
+  size_t idx;      // int32 [K][k]
+  size_t w;        // float [K][k]
+  size_t group;    // int32 [2 + 2G + K*k]
+  size_t urow;     // uint32 [G+1]: rows routed to each distinct expert (bitmask)
+  size_t slotmap;  // int32 [G+1][K]: slot of the expert in row r's selection, -1 if none
+  size_t hamax;    // uint32 [G+1][K]: max |h| bits per (expert, row)
+  size_t tilecnt;  // uint32 [H/64]: completed down items per hidden tile
+  size_t h;        // bf16 [G+1][K][I]
+  size_t dpart;    // float [K][k+1][H]
+  size_t total;
+};
+
+inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+inline int group_cap(int K, int E, int k) { return E < K * k ? E : K * k; }
+
+inline WsLayout ws_layout(int K, int E, int k, int H, int I) {
+  WsLayout L{};
+  const int G = group_cap(K, E, k);
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t r = o;
+    o = align256(o + bytes);
+    return r;
+  };
+  L.hdr = take(256);
+  L.logits = take(sizeof(float) * K * E);
+  L.idx = take(sizeof(int32_t) * K * k);
+  L.w = take(sizeof(float) * K * k);
+  L.group = take(sizeof(int32_t) * (2 + 2 * G + K * k));
+  L.urow = take(sizeof(uint32_t) * (G + 1));
+  L.slotmap = take(sizeof(int32_t) * (G + 1) * K);
+  L.hamax = take(sizeof(uint32_t) * (G + 1) * K);
+  L.tilecnt = take(sizeof(uint32_t) * (H / kDNRows));
+  L.h = take(sizeof(uint16_t) * (size_t)(G + 1) * K * I);
+  L.dpart = take(sizeof(float) * (size_t)K * (k + 1) * H);
+  L.total = o;
+  return L;
+}
+
+// Pointers into one workspace.
+struct WsPtrs {
+  int* err;
+  unsigned* ticket;
+  float* logits;
+  int* idx;
+  float* w;
+  int* group;
+  unsigned* urow;
+  int* slotmap;
+  unsigned* hamax;
+  unsigned* tilecnt;
+  uint16_t* h;
+  float* dpart;
+};
+
+inline WsPtrs ws_ptrs(void* ws, const WsLayout& L) {
+  char* b = static_cast<char*>(ws);
+  WsPtrs p;
+  p.err = reinterpret_cast<int*>(b + L.hdr);
+  p.ticket = reinterpret_cast<unsigned*>(b + L.hdr + 4);
+  p.logits = reinterpret_cast<float*>(b + L.logits);
+  p.idx = reinterpret_cast<int*>(b + L.idx);
+  p.w = reinterpret_cast<float*>(b + L.w);
+  p.group = reinterpret_cast<int*>(b + L.group);
+  p.urow = reinterpret_cast<unsigned*>(b + L.urow);
+  p.slotmap = reinterpret_cast<int*>(b + L.slotmap);
+  p.hamax = reinterpret_cast<unsigned*>(b + L.hamax);
+  p.tilecnt = reinterpret_cast<unsigned*>(b + L.tilecnt);
+  p.h = reinterpret_cast<uint16_t*>(b + L.h);
+  p.dpart = reinterpret_cast<float*>(b + L.dpart);
+  return p;
+}
+
+struct RouterArgs {
+  const uint16_t* x;        // [K][H]
+  const uint16_t* router_w; // [E][H]
+  const float* bias;        // [E] or null
+  int K, H, E, k, G;
+  int has_shared;
+  int n_tiles;              // H / kDNRows
+  WsPtrs ws;
+  int32_t* idx_out;         // caller copies (nullable)
+  float* w_out;
+  int32_t* group_out;
+};
+
+// Per-projection pointers the expert kernels need besides the tensor maps.
+struct ProjPtrs {
+  const uint8_t* scales;
+  const float* tscale;
+};
+
+struct GateUpArgs {
+  const uint16_t* x;  // [K][H] bf16
+  int K, H, I, G;
+  int has_shared;
+  ProjPtrs gate, up, sh_gate, sh_up;
+  WsPtrs ws;
+  uint64_t wait_ns;
+};
+
+struct DownArgs {
+  const uint16_t* residual;  // [K][H] or null
+  uint16_t* y;               // [K][H]
+  int K, H, I, k, G;
+  int has_shared;
+  float routed_scale;
+  ProjPtrs down, sh_down;
+  WsPtrs ws;
+  uint64_t wait_ns;
+};
+
+struct LmHeadArgs {
+  const uint16_t* x;  // [K][H] normalised rows
+  const uint16_t* W;  // [V][H]
+  int K, H, V;
+  int32_t* tok;       // [K] out
+  float* best;        // [K] out (nullable)
+  float* part_v;      // [grid][K]
+  int* part_i;        // [grid][K]
+  unsigned* ticket;
+};
+
+constexpr int kLmMaxGrid = 1024;
+
+inline size_t lmhead_ws_bytes(int K) { return 256 + align256(sizeof(float) * kLmMaxGrid * K) + sizeof(int) * kLmMaxGrid * K; }
+
+// Launchers (return cudaGetLastError()).
+cudaError_t launch_rmsnorm(const uint16_t* x, int K, int H, float eps, uint16_t* out, cudaStream_t s, bool pdl);
+cudaError_t launch_lmhead(const LmHeadArgs& a, cudaStream_t s, bool pdl);
+cudaError_t launch_router(const RouterArgs& a, cudaStream_t s, bool pdl);
+cudaError_t launch_gateup(const GateUpArgs& a, const CUtensorMap& gate, const CUtensorMap& up,
+                          const CUtensorMap& sh_gate, const CUtensorMap& sh_up, cudaStream_t s, bool pdl);
+cudaError_t launch_down(const DownArgs& a, const CUtensorMap& down, const CUtensorMap& sh_down, cudaStream_t s,
+                        bool pdl);
+cudaError_t launch_accept(const int32_t* draft, const int32_t* target, int K, int32_t* out, cudaStream_t s);
+
+int num_sms();
+
+}  // namespace moe

@@ -369,13 +369,23 @@ void orc_moe_layer(const orc_layer* L, const uint16_t* x_norm, int K, const uint
 /* RMSNorm, attention, lm_head, acceptance                             */
 /* ------------------------------------------------------------------ */
 
-/* out = bf16( x / sqrt(mean(x^2) + eps) ), unit gain, per row. */
+/* RMSNorm with unit gain: out = bf16( x * 1/sqrt(mean(x^2) + eps) ).
+ * Its output feeds the router's top-k, an integer decision, so it is taken
+ * in FP32 in the fixed order of the router logits: the sum of squares is the
+ * fixed-order dot product of the row with itself, then mean = ss / H,
+ * inv = 1 / sqrt(mean + eps) and x * inv, each a correctly rounded FP32
+ * operation, and the product is rounded to bf16. */
 void orc_rmsnorm(const uint16_t* x, int K, int H, double eps, uint16_t* out) {
+  const float epsf = (float)eps;
   for (int r = 0; r < K; ++r) {
-    double ss = 0.0;
-    for (int c = 0; c < H; ++c) { double v = orc_bf16(x[(size_t)r * H + c]); ss += v * v; }
-    double inv = 1.0 / sqrt(ss / H + eps);
-    for (int c = 0; c < H; ++c) out[(size_t)r * H + c] = orc_round_bf16(orc_bf16(x[(size_t)r * H + c]) * inv);
+    const uint16_t* row = x + (size_t)r * H;
+    float ss = dot_fixed_order(row, row, H);
+    float mean = ss / (float)H;
+    float inv = 1.0f / sqrtf(mean + epsf);
+    for (int c = 0; c < H; ++c) {
+      float v = (float)orc_bf16(row[c]) * inv;
+      out[(size_t)r * H + c] = orc_round_bf16((double)v);
+    }
   }
 }
 
