@@ -4,8 +4,8 @@
 Workload (default ``k2_layer``): DFlash K=2 verify through one MoE layer --
 hidden 2048, 256 routed experts, top-8, expert intermediate 512, a shared
 expert of intermediate 512, NVFP4 expert weights, bf16 router, 2 bf16 rows.
-A step is one layer call (router -> top-k -> dedup -> gate/up+SwiGLU ->
-down+combine) on one batch of K rows.  Steps cycle over a ring of distinct
+A step is one layer call (router logits, then one persistent experts kernel:
+top-k -> dedup -> gate/up+SwiGLU -> down+combine) on one batch of K rows.  Steps cycle over a ring of distinct
 seeded layers whose touched bytes exceed L2 several times, so every step
 streams its experts from HBM.  The timed steps run as CUDA-graph replays.
 
@@ -16,8 +16,10 @@ e2e       = the same metric through the C ABI from pinned host buffers, the
             host->device copy of x and device->host copy of y inside the
             timed region, one eager call per step.
 roofline  = the dominant kernel's algorithmic bytes per launch over its mean
-            CUDA-event duration (a profiling pass with events between the
-            three kernels), against the measured HBM copy bandwidth.
+            CUDA-event duration (a graph-captured profiling pass with events
+            between the two kernels), against the measured HBM copy bandwidth.
+stack_sweep = 40-layer verify steps at K = 1, 2, 4, 8, 16 (and the Zipf-biased
+            K = 16 stack): verified tokens/s = K / step time.
 cpu_baseline = the CPU oracle on a bounded sample of the same workload.
 
 ``--impl reference`` times the CPU oracle alone on the same workload (the
@@ -57,6 +59,9 @@ def parse():
     p.add_argument("--ring", type=int, default=RING)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--no-sweep", action="store_true", help="skip the 40-layer stack sweep")
+    p.add_argument("--sweep-steps", type=int, default=100)
+    p.add_argument("--no-full-step", action="store_true", help="skip the full verify step (attention + MoE)")
     return p.parse_args()
 
 
@@ -76,15 +81,17 @@ def nvfp4_bytes(rows, cols):
     return rows * cols // 2 + rows * cols // 16 + 4
 
 
-def kernel_bytes(w, n_u, residual=False):
-    """Algorithmic bytes of one layer call, per kernel."""
-    act = w.K * w.H * 2
+def kernel_bytes(w, n_u, residual=False, K=None):
+    """Algorithmic bytes of one layer call, per kernel: the router reads its
+    weights and x; the experts kernel reads each distinct expert once (gate,
+    up, down, plus the shared expert), x, the residual, and writes y."""
+    K = w.K if K is None else K
+    act = K * w.H * 2
     slots = n_u + (1 if w.Is else 0)
     router = w.E * w.H * 2 + act + (w.E * 4 if w.zipf_s else 0)
-    gateup = slots * 2 * nvfp4_bytes(w.I, w.H) + act
-    down = slots * nvfp4_bytes(w.H, w.I) + act * (2 if residual else 1)
-    layer = router + gateup + down - act  # x is read by router and gate/up but counted once
-    return dict(router=router, gateup=gateup, down=down, layer=layer)
+    experts = slots * (2 * nvfp4_bytes(w.I, w.H) + nvfp4_bytes(w.H, w.I)) + act * (3 if residual else 2)
+    layer = router + experts - act  # x is read by both kernels but counted once
+    return dict(router=router, experts=experts, layer=layer)
 
 
 class Clocks:
@@ -295,20 +302,27 @@ def run_gpu(args):
     gbs = total_bytes / (ms * 1e-3) / 1e9
     hbm, peak_src = peaks()
 
-    # per-kernel durations (events between kernels, no overlap)
+    # per-kernel durations: the profiling variant (events between the two
+    # kernels, no overlap) captured in a graph, so host gaps do not count
     n_prof = 4 * R
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_prof)]
-    with torch.cuda.stream(stream):
+    for e4 in evs:
+        for e in e4:
+            e.record(stream)
+    stream.synchronize()
+    g_prof = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_prof, stream=stream):
         for i in range(n_prof):
             j = i % R
             M.moe_verify_layer_profiled(layers[j], xs[j], None, ys[j], ws, events=evs[i], stream=stream,
                                         c_layer=cl[j])
+    with torch.cuda.stream(stream):
+        g_prof.replay()
     stream.synchronize()
-    dur = {"router": [], "gateup": [], "down": []}
+    dur = {"router": [], "experts": []}
     for e in evs:
         dur["router"].append(e[0].elapsed_time(e[1]))
-        dur["gateup"].append(e[1].elapsed_time(e[2]))
-        dur["down"].append(e[2].elapsed_time(e[3]))
+        dur["experts"].append(e[1].elapsed_time(e[2]))
     mean_ms = {k: float(np.mean(v)) for k, v in dur.items()}
     dom = max(mean_ms, key=mean_ms.get)
     dom_bytes = float(np.mean([kb[i % R][dom] for i in range(n_prof)]))
@@ -345,7 +359,8 @@ def run_gpu(args):
                    "K": w.K, "ring_layers": R,
                    "l2": f"inputs larger than L2: steps cycle over {R} distinct layers "
                          f"({R * 257 * 3 * nvfp4_bytes(w.I, w.H) / 1e9:.1f} GB resident)",
-                   "launch": "CUDA graph replay, PDL between the 3 kernels of a call",
+                   "launch": "CUDA graph replay; per call a router kernel and one persistent experts kernel "
+                             "(programmatic dependent launch between them)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "pct_of_peak": round(100 * gbs / hbm, 1),
         "row_layers_per_s": round(w.K * steps / (ms * 1e-3) * world, 1),
@@ -354,13 +369,17 @@ def run_gpu(args):
         "clocks": clk,
         "e2e": {"value": round(e2e_gbs, 1), "unit": "GB/s", "h2d_bytes_per_step": act, "d2h_bytes_per_step": act,
                 "steps": n_e2e},
-        "gpu_launches": 3 * steps,
+        "gpu_launches": 2 * steps,
         "kernel_ms": {k: round(v, 5) for k, v in mean_ms.items()},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm,
                      "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / hbm, 3),
                      "traffic": traffic, "algorithmic_bytes_per_launch": dom_bytes},
         "setup_s": round(t_gen, 1),
     }
+    if not args.no_sweep:
+        out["stack_sweep"] = stack_sweep(M, torch, synthgen, dev, stream, hbm, args.sweep_steps)
+    if not args.no_full_step:
+        out["full_step"] = full_step(M, torch, synthgen, dev, stream, hbm, max(10, args.sweep_steps // 4))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         bps, n, secs, threads = oracle_sample(w, args.cpu_seconds)
         out["cpu_baseline"] = {"value": round(bps / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
@@ -370,6 +389,148 @@ def run_gpu(args):
         print(json.dumps(out), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+# --------------------------------------------------------------------------- 40-layer stacks
+
+def stack_sweep(M, torch, synthgen, dev, stream, hbm, steps):
+    """Verify steps through 40-layer MoE stacks (x <- x + MoE_l(rmsnorm(x))):
+    K = 1, 2, 4, 8, 16 on the k8_stack40 weights and K = 16 on the Zipf-biased
+    k16_zipf_stack40 weights.  A step is one pass of all 40 layers; verified
+    tokens/s = K / step time; GB/s = algorithmic bytes of the step / time."""
+    res = []
+    for wname, Ks in (("k8_stack40", (1, 2, 4, 8, 16)), ("k16_zipf_stack40", (16,))):
+        w = synthgen.WORKLOADS[wname]
+        t = lambda p: (p.codes, p.scales, p.tscale)
+        layers = []
+        for l in range(w.layers):
+            L = synthgen.make_layer(w, l)
+            sh = (t(L.sh_gate), t(L.sh_up), t(L.sh_down))
+            layers.append(M.layer_from_arrays(L.router_w, L.router_b if w.zipf_s else None, t(L.gate), t(L.up),
+                                              t(L.down), sh, top_k=w.top_k, device=dev))
+            del L
+        carr = M.layer_array(layers)
+        for K in Ks:
+            x0 = torch.from_numpy(synthgen.make_x(w, 900 + K, K=K)).view(torch.bfloat16).to(dev)
+            x = x0.clone()
+            ws = M.stack_workspace(carr, K, device=dev)
+            # distinct experts per layer along the stack (routing is deterministic)
+            wl = M.workspace(layers[0], K, device=dev)
+            xn = torch.empty_like(x)
+            grp = torch.empty(M.moe_group_ints(K, w.E, w.top_k), dtype=torch.int32, device=dev)
+            n_u = []
+            with torch.cuda.stream(stream):
+                for l in range(w.layers):
+                    M.moe_rmsnorm(x, xn, stream=stream)
+                    M.moe_verify_layer(layers[l], xn, x, x, wl, group_out=grp, stream=stream)
+                    stream.synchronize()
+                    n_u.append(int(grp[0].item()))
+            step_bytes = sum(kernel_bytes(w, n, residual=True, K=K)["layer"] + 2 * K * w.H * 2 for n in n_u)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                x.copy_(x0)
+                M.moe_verify_stack(carr, x, ws, stream=stream)
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    g.replay()
+            stream.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for _ in range(steps):
+                    g.replay()
+                e1.record(stream)
+            stream.synchronize()
+            assert M.moe_workspace_error(ws, stream) == 0
+            ms = e0.elapsed_time(e1) / steps
+            gbs = step_bytes / (ms * 1e-3) / 1e9
+            res.append({"workload": wname, "K": K, "layers": w.layers, "ms_per_step": round(ms, 4),
+                        "verified_tokens_per_s": round(K / (ms * 1e-3), 1), "GBps": round(gbs, 1),
+                        "pct_of_peak": round(100 * gbs / hbm, 1),
+                        "distinct_experts_mean": round(float(np.mean(n_u)), 2), "steps": steps,
+                        "gpu_launches_per_step": 3 * w.layers})
+        del layers, carr
+        torch.cuda.empty_cache()
+    return res
+
+
+def full_step(M, torch, synthgen, dev, stream, hbm, steps):
+    """The k4_full_step workload: 40 x (GQA attention over a 16,384-position
+    bf16 cache + MoE block), lm_head argmax over 151,936 rows, accepted
+    prefix; one native moe_verify_step per step, replayed from a CUDA graph."""
+    w = synthgen.WORKLOADS["k4_full_step"]
+    t = lambda p: (p.codes, p.scales, p.tscale)
+    d = lambda a: torch.from_numpy(a).view(torch.bfloat16).to(dev)
+    layers = []
+    for l in range(w.layers):
+        A = synthgen.make_attention(w, l)
+        L = synthgen.make_layer(w, l)
+        sh = (t(L.sh_gate), t(L.sh_up), t(L.sh_down))
+        moe = M.layer_from_arrays(L.router_w, None, t(L.gate), t(L.up), t(L.down), sh, top_k=w.top_k, device=dev)
+        layers.append(M.DecoderLayer(d(A["Wq"]), d(A["Wk"]), d(A["Wv"]), d(A["Wo"]), d(A["kc"]), d(A["vc"]), moe))
+        del A, L
+    model = M.VerifyModel(layers, d(synthgen.make_lm_head(w)), w.n_q_heads, w.n_kv_heads)
+    K = w.K
+    x0 = d(synthgen.make_x(w, 11))
+    x = x0.clone()
+    ws = model.workspace(K, device=dev)
+    tgt = torch.empty(K, dtype=torch.int32, device=dev)
+    n = torch.empty(1, dtype=torch.int32, device=dev)
+    draft = torch.zeros(K, dtype=torch.int32, device=dev)
+    with torch.cuda.stream(stream):  # one eager step: targets -> drafts with a known accepted length
+        M.moe_verify_step(model, x, draft, tgt, n, ws, stream=stream)
+    stream.synchronize()
+    dr, j = synthgen.make_drafts(w, tgt.cpu().numpy())
+    draft.copy_(torch.from_numpy(dr))
+    # distinct experts per layer (one teacher pass with the MoE routing outputs)
+    wl = M.workspace(layers[0].moe, K, device=dev)
+    aws = M.attention_workspace(K, w.H, w.n_q_heads, w.n_kv_heads, device=dev)
+    xn = torch.empty_like(x)
+    grp = torch.empty(M.moe_group_ints(K, w.E, w.top_k), dtype=torch.int32, device=dev)
+    x.copy_(x0)
+    n_u = []
+    with torch.cuda.stream(stream):
+        for l in range(w.layers):
+            dl = layers[l]
+            M.moe_attention_block(x, dl.Wq, dl.Wk, dl.Wv, dl.Wo, dl.kcache, dl.vcache, x, aws, w.n_q_heads,
+                                  w.n_kv_heads, stream=stream)
+            M.moe_rmsnorm(x, xn, stream=stream)
+            M.moe_verify_layer(dl.moe, xn, x, x, wl, group_out=grp, stream=stream)
+            stream.synchronize()
+            n_u.append(int(grp[0].item()))
+    act = K * w.H * 2
+    att_bytes = 2 * (w.n_q_heads + 2 * w.n_kv_heads) * 128 * w.H + 2 * w.H * w.n_q_heads * 128 + \
+        2 * 2 * w.n_kv_heads * w.ctx * 128 + 2 * act
+    step_bytes = sum(att_bytes + kernel_bytes(w, nu, residual=True, K=K)["layer"] + 2 * act for nu in n_u) + \
+        w.vocab * w.H * 2 + 2 * act
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        x.copy_(x0)
+        M.moe_verify_step(model, x, draft, tgt, n, ws, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g.replay()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    assert M.moe_workspace_error(ws, stream) == 0
+    ms = e0.elapsed_time(e1) / steps
+    acc = int(n.item())
+    gbs = step_bytes / (ms * 1e-3) / 1e9
+    res = {"workload": "k4_full_step", "K": K, "layers": w.layers, "ctx": w.ctx, "vocab": w.vocab,
+           "ms_per_step": round(ms, 4), "verified_tokens_per_s": round(K / (ms * 1e-3), 1),
+           "accepted": acc, "accepted_expected": j,
+           "emitted_tokens_per_s": round((acc + 1 if acc < K else K) / (ms * 1e-3), 1),
+           "GBps": round(gbs, 1), "pct_of_peak": round(100 * gbs / hbm, 1),
+           "step_bytes": step_bytes, "distinct_experts_mean": round(float(np.mean(n_u)), 2), "steps": steps}
+    del layers, model
+    torch.cuda.empty_cache()
+    return res
 
 
 # --------------------------------------------------------------------------- reference arm (CPU oracle)

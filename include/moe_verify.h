@@ -152,10 +152,11 @@ moe_status moe_verify_stack(const moe_layer* layers, int n_layers, uint16_t* x, 
 
 /*
  * Profiling variant of moe_verify_layer for benchmarks: identical results,
- * but the three kernels (router, gate/up, down) are launched without
- * programmatic overlap and, when `events` is not NULL, the cudaEvent_t
- * handles events[0..3] are recorded on `stream` before the router, after the
- * router, after gate/up and after down, so each kernel can be timed.
+ * but the two kernels (router, experts) are launched without programmatic
+ * overlap and, when `events` is not NULL, the cudaEvent_t handles
+ * events[0..3] are recorded on `stream` before the router, after the router,
+ * and (twice) after the experts kernel, so each kernel can be timed.  Inside
+ * a stream capture the events are recorded as external event nodes.
  */
 moe_status moe_verify_layer_profiled(const moe_layer* layer, const uint16_t* x_norm, int K,
                                      const uint16_t* residual, uint16_t* y, void* ws, size_t ws_bytes,
@@ -198,6 +199,62 @@ moe_status moe_lm_head_argmax(const uint16_t* x_norm, int K, int H, const uint16
                               float* best_logit, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * GQA attention block of the verify step (README, "Why this challenge
+ * exists": GQA with 8 KV heads at head_dim 128; the verify forward runs all
+ * K drafted rows at once):
+ *   xn = rmsnorm(x)  (as moe_rmsnorm)
+ *   q = bf16(xn . Wq^T), k_new = bf16(xn . Wk^T), v_new = bf16(xn . Wv^T)
+ *   o[r, h] = bf16( softmax_p( q[r,h] . key_p / sqrt(128) ) . value_p )
+ *             over the C cached positions of KV head h / (nq/nkv) and the
+ *             new positions 0..r (block-causal)
+ *   x_out = bf16( x + o . Wo^T )
+ *   x, x_out bf16 [K][H] (x_out may alias x); Wq [nq*128][H], Wk, Wv
+ *   [nkv*128][H], Wo [H][nq*128]; kcache, vcache [nkv][C][128];
+ *   k_new_out, v_new_out: optional [K][nkv*128] copies of the new keys and
+ *   values (to append to the cache once rows are accepted).
+ * Envelope: head_dim 128, nq even, nq % nkv == 0, K * nq/nkv <= 16, H a
+ * multiple of 256 up to 4096, nq*128 <= 4096, C a multiple of 16.
+ */
+size_t moe_attention_workspace_size(int K, int H, int nq, int nkv, int head_dim);
+moe_status moe_attention_block(const uint16_t* x, int K, int H, int nq, int nkv, int head_dim, int C,
+                               const uint16_t* Wq, const uint16_t* Wk, const uint16_t* Wv, const uint16_t* Wo,
+                               const uint16_t* kcache, const uint16_t* vcache, float eps, uint16_t* x_out,
+                               uint16_t* k_new_out, uint16_t* v_new_out, void* ws, size_t ws_bytes,
+                               void* stream);
+
+/*
+ * The full verify step of a decoder with GQA attention and MoE blocks:
+ *   for each layer l:  x <- attention_block_l(x)          (moe_attention_block)
+ *                      x <- x + MoE_l(rmsnorm(x))          (moe_verify_stack)
+ *   target_r = argmax_v rmsnorm(x)_r . lm_head_v           (moe_lm_head_argmax)
+ *   n_accepted = first r with draft_r != target_r, else K (verify_accept_prefix)
+ * i.e. one target forward over the K drafted rows, its greedy token per row,
+ * and how far decode advances (README, opening section and "Why this
+ * challenge exists"; PR #844, "5. Numerical safety": argmax over every row).
+ */
+typedef struct {
+  const uint16_t *Wq, *Wk, *Wv, *Wo;  /* bf16 attention projections (see moe_attention_block) */
+  const uint16_t *kcache, *vcache;    /* bf16 [nkv][ctx][128] */
+  moe_layer moe;                      /* the MoE block of the layer */
+} moe_decoder_layer;
+
+typedef struct {
+  int n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ctx, vocab;
+  float eps;                          /* RMSNorm epsilon */
+  const moe_decoder_layer* layers;    /* host array of n_layers (read during the call) */
+  const uint16_t* lm_head;            /* bf16 [vocab][hidden] */
+} moe_verify_model;
+
+size_t moe_verify_step_workspace_size(const moe_verify_model* model, int K);
+
+/*   x          bf16 [K][hidden]: the rows' input to layer 0; overwritten with
+ *              the final residual stream
+ *   draft      int32 [K] drafted tokens;  target int32 [K] out;  n_accepted int32 [1] out
+ *   ws         moe_verify_step_workspace_size bytes, zero-filled before first use */
+moe_status moe_verify_step(const moe_verify_model* model, uint16_t* x, int K, const int32_t* draft,
+                           int32_t* target, int32_t* n_accepted, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Reads the device error word of a workspace (0 = none, else a negative
  * moe_status) and clears it.  Synchronises `stream`.
  */
@@ -212,6 +269,13 @@ const char* moe_status_string(moe_status s);
  * up at once, which exercises the timeout path without hanging a GPU.
  */
 void moe_debug_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Profiling hook: when `buf` (device memory, one row of 16 uint64 per SM)
+ * is not NULL, experts kernels launched afterwards record %globaltimer
+ * stamps of their milestones in it (NULL turns it off).
+ */
+void moe_debug_set_trace(void* buf);
 
 #ifdef __cplusplus
 }

@@ -30,7 +30,10 @@ MOE_MAX_ROWS = 16
 # Every symbol the header declares (checked by the tests).
 EXPORTS = ("moe_verify_layer_workspace_size", "moe_router_topk", "moe_group_ints", "moe_verify_layer",
            "moe_verify_layer_profiled", "verify_accept_prefix", "moe_rmsnorm", "moe_lm_head_workspace_size",
-           "moe_lm_head_argmax", "moe_verify_stack_workspace_size", "moe_verify_stack", "moe_workspace_error", "moe_status_string", "moe_debug_set_wait_limit_ns")
+           "moe_lm_head_argmax", "moe_verify_stack_workspace_size", "moe_verify_stack",
+           "moe_attention_workspace_size", "moe_attention_block",
+           "moe_verify_step_workspace_size", "moe_verify_step", "moe_workspace_error", "moe_status_string", "moe_debug_set_wait_limit_ns",
+           "moe_debug_set_trace")
 
 
 class MoeError(RuntimeError):
@@ -49,6 +52,18 @@ class moe_layer(ctypes.Structure):
                 ("router_w", ctypes.c_void_p), ("router_bias", ctypes.c_void_p),
                 ("gate", moe_nvfp4), ("up", moe_nvfp4), ("down", moe_nvfp4),
                 ("sh_gate", moe_nvfp4), ("sh_up", moe_nvfp4), ("sh_down", moe_nvfp4)]
+
+
+class moe_decoder_layer(ctypes.Structure):
+    _fields_ = [("Wq", ctypes.c_void_p), ("Wk", ctypes.c_void_p), ("Wv", ctypes.c_void_p), ("Wo", ctypes.c_void_p),
+                ("kcache", ctypes.c_void_p), ("vcache", ctypes.c_void_p), ("moe", moe_layer)]
+
+
+class moe_verify_model(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int), ("hidden", ctypes.c_int), ("n_q_heads", ctypes.c_int),
+                ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("ctx", ctypes.c_int),
+                ("vocab", ctypes.c_int), ("eps", ctypes.c_float), ("layers", ctypes.c_void_p),
+                ("lm_head", ctypes.c_void_p)]
 
 
 def _load():
@@ -74,6 +89,16 @@ def _load():
     L.moe_verify_stack_workspace_size.argtypes = [lp, ci, ci]
     L.moe_verify_stack.restype = ci
     L.moe_verify_stack.argtypes = [lp, ci, vp, ci, ctypes.c_float, vp, sz, vp]
+    L.moe_attention_workspace_size.restype = sz
+    L.moe_attention_workspace_size.argtypes = [ci, ci, ci, ci, ci]
+    L.moe_attention_block.restype = ci
+    L.moe_attention_block.argtypes = [vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp,
+                                      vp, vp, sz, vp]
+    mp = ctypes.POINTER(moe_verify_model)
+    L.moe_verify_step_workspace_size.restype = sz
+    L.moe_verify_step_workspace_size.argtypes = [mp, ci]
+    L.moe_verify_step.restype = ci
+    L.moe_verify_step.argtypes = [mp, vp, ci, vp, vp, vp, vp, sz, vp]
     L.moe_rmsnorm.restype = ci
     L.moe_rmsnorm.argtypes = [vp, ci, ci, ctypes.c_float, vp, vp]
     L.moe_lm_head_workspace_size.restype = sz
@@ -86,6 +111,8 @@ def _load():
     L.moe_status_string.argtypes = [ci]
     L.moe_debug_set_wait_limit_ns.restype = None
     L.moe_debug_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    L.moe_debug_set_trace.restype = None
+    L.moe_debug_set_trace.argtypes = [vp]
     return L
 
 
@@ -223,6 +250,63 @@ def moe_verify_stack(c_layers, x, ws, eps=1e-6, stream=None):
                                 _stream(stream)), "moe_verify_stack")
 
 
+def attention_workspace(K, H, nq, nkv, head_dim=128, device="cuda") -> torch.Tensor:
+    n = int(lib.moe_attention_workspace_size(K, H, nq, nkv, head_dim))
+    if n == 0:
+        raise MoeError(MOE_ERR_INVALID_ARG, "attention workspace size")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def moe_attention_block(x, Wq, Wk, Wv, Wo, kcache, vcache, x_out, ws, nq, nkv, eps=1e-6, k_new=None, v_new=None,
+                        stream=None):
+    K, H = x.shape
+    C = kcache.shape[1]
+    _check(lib.moe_attention_block(_ptr(x), K, H, nq, nkv, 128, C, _ptr(Wq), _ptr(Wk), _ptr(Wv), _ptr(Wo),
+                                   _ptr(kcache) if C else None, _ptr(vcache) if C else None, float(eps),
+                                   _ptr(x_out), _ptr(k_new), _ptr(v_new), _ptr(ws), ws.numel(), _stream(stream)),
+           "moe_attention_block")
+
+
+@dataclass
+class DecoderLayer:
+    """Device tensors of one decoder layer: attention weights, KV cache, MoE."""
+    Wq: torch.Tensor
+    Wk: torch.Tensor
+    Wv: torch.Tensor
+    Wo: torch.Tensor
+    kcache: torch.Tensor
+    vcache: torch.Tensor
+    moe: Layer
+
+
+class VerifyModel:
+    """Holds the C description (``moe_verify_model``) of a stack of decoder
+    layers plus the lm_head; keeps the ctypes arrays alive."""
+
+    def __init__(self, layers, lm_head, n_q_heads, n_kv_heads, eps=1e-6):
+        self.layers = layers
+        self.lm_head = lm_head
+        p = lambda t: t.data_ptr()
+        self.c_layers = (moe_decoder_layer * len(layers))(*[
+            moe_decoder_layer(p(d.Wq), p(d.Wk), p(d.Wv), p(d.Wo), p(d.kcache), p(d.vcache), d.moe.c())
+            for d in layers])
+        d0 = layers[0]
+        self.c = moe_verify_model(len(layers), d0.moe.hidden, n_q_heads, n_kv_heads, 128, d0.kcache.shape[1],
+                                  lm_head.shape[0], eps, ctypes.cast(self.c_layers, ctypes.c_void_p),
+                                  lm_head.data_ptr())
+
+    def workspace(self, K, device=None):
+        n = int(lib.moe_verify_step_workspace_size(ctypes.byref(self.c), K))
+        if n == 0:
+            raise MoeError(MOE_ERR_INVALID_ARG, "verify step workspace size")
+        return torch.zeros(n, dtype=torch.uint8, device=device or self.lm_head.device)
+
+
+def moe_verify_step(model: VerifyModel, x, draft, target, n_accepted, ws, stream=None):
+    _check(lib.moe_verify_step(ctypes.byref(model.c), _ptr(x), x.shape[0], _ptr(draft), _ptr(target),
+                               _ptr(n_accepted), _ptr(ws), ws.numel(), _stream(stream)), "moe_verify_step")
+
+
 def moe_rmsnorm(x, out, eps=1e-6, stream=None):
     _check(lib.moe_rmsnorm(_ptr(x), x.shape[0], x.shape[1], float(eps), _ptr(out), _stream(stream)), "moe_rmsnorm")
 
@@ -248,6 +332,11 @@ def moe_workspace_error(ws, stream=None) -> int:
 
 def moe_debug_set_wait_limit_ns(ns: int):
     lib.moe_debug_set_wait_limit_ns(int(ns))
+
+
+def moe_debug_set_trace(buf):
+    """Device uint64 tensor [n_sms, 16] for milestone stamps, or None."""
+    lib.moe_debug_set_trace(None if buf is None else ctypes.c_void_p(buf.data_ptr()))
 
 
 def _dev(a, device, dtype=None):

@@ -1,0 +1,384 @@
+// attention.cu -- the GQA attention block of the full verify step.
+//
+// K verify rows attend over a cache of C positions plus their own K new
+// positions (row r sees new positions 0..r), grouped-query with `group` query
+// heads per KV head, head dim 128 (README, "Why this challenge exists": all
+// layers are GQA with 8 KV heads at head_dim 128).  The block is
+//   x_out = bf16( x + bf16(softmax(q k^T / sqrt(128)) v) . Wo^T ),
+//   q, k_new, v_new = bf16( rmsnorm(x) . W{q,k,v}^T ).
+//
+// Kernels:
+//  * k_gemv_bf16   -- bf16 GEMV for up to three weight matrices sharing x
+//                     (one warp per output row, 16-byte loads, FP32 accumulate,
+//                     optional residual add, bf16 output).
+//  * k_attn_split  -- flash-decode over the cache: CTA (split, kv head) walks
+//                     16-position sub-chunks with tensor-core mma.sync (bf16 in,
+//                     FP32 accumulate) for q k^T and p v, online softmax in the
+//                     log2 domain, and writes its unnormalised partial
+//                     (m, l, o).  The K rows x `group` heads of a KV head form
+//                     the 16 query rows of one m16 tile.  Fragments come
+//                     straight from global memory with 16-byte loads: the
+//                     reduction index (head dim for q k^T, position for p v)
+//                     and the output dims are permuted so that each thread's
+//                     elements are contiguous in memory.
+//  * k_attn_combine-- merges the splits in fixed order with the block-causal
+//                     new positions and normalises.
+#include <cfloat>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+__device__ __forceinline__ uint4 ldg_v4(const void* p) { return *reinterpret_cast<const uint4*>(p); }
+
+}  // namespace
+
+// ------------------------------------------------------------------ bf16 GEMV
+template <int KR, int NJ>
+__global__ void __launch_bounds__(256) k_gemv_bf16(GemvArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int K = a.K, D = a.D, nj = D / 256;
+  pdl_wait();
+  pdl_launch_dependents();
+  uint4* xs = reinterpret_cast<uint4*>(smem);
+  for (int i = threadIdx.x; i < K * D / 8; i += blockDim.x) xs[i] = reinterpret_cast<const uint4*>(a.x)[i];
+  __syncthreads();
+  const int nw = gridDim.x * (blockDim.x >> 5);
+  for (int n = blockIdx.x * (blockDim.x >> 5) + warp; n < a.n_total; n += nw) {
+    int sg = 0, nl = n;
+    while (sg + 1 < a.nseg && nl >= a.seg[sg].N) {
+      nl -= a.seg[sg].N;
+      ++sg;
+    }
+    const GemvSeg& S = a.seg[sg];
+    const uint4* wrow = reinterpret_cast<const uint4*>(S.W + (size_t)nl * D);
+    uint4 wv[NJ];
+#pragma unroll
+    for (int j = 0; j < NJ; ++j)
+      if (j < nj) wv[j] = ldg_nc_v4(wrow + j * 32 + lane);
+    float acc[KR];
+#pragma unroll
+    for (int r = 0; r < KR; ++r) acc[r] = 0.f;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      if (j >= nj) break;
+      const uint32_t wq[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
+#pragma unroll
+      for (int r = 0; r < KR; ++r) {
+        if (r < K) {
+          const uint4 xv = xs[r * (D / 8) + j * 32 + lane];
+          const uint32_t xq[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc[r] = __fmaf_rn(bf_lo(xq[i]), bf_lo(wq[i]), acc[r]);
+            acc[r] = __fmaf_rn(bf_hi(xq[i]), bf_hi(wq[i]), acc[r]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < KR; ++r) {
+#pragma unroll
+      for (int d = 16; d >= 1; d >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], d);
+    }
+#pragma unroll
+    for (int r = 0; r < KR; ++r) {
+      if (r < K && lane == r) {
+        float v = acc[r];
+        if (S.res) v += bf_lo(S.res[(size_t)r * S.N + nl]);
+        S.out[(size_t)r * S.N + nl] = float_to_bf16_bits(v);
+      }
+    }
+  }
+}
+
+cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t s, bool pdl) {
+  const size_t sm = sizeof(uint16_t) * a.K * a.D;
+  auto run = [&](auto kern) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * num_sms());
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = sm;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+  };
+  if (a.D <= 2048) return a.K <= 4 ? run(k_gemv_bf16<4, 8>) : (a.K <= 8 ? run(k_gemv_bf16<8, 8>) : run(k_gemv_bf16<16, 8>));
+  return a.K <= 4 ? run(k_gemv_bf16<4, 16>) : (a.K <= 8 ? run(k_gemv_bf16<8, 16>) : run(k_gemv_bf16<16, 16>));
+}
+
+// ------------------------------------------------------------------ split-KV attention
+// Query row i of the m16 tile = r * group + hh (r < K, hh < group); rows
+// past K * group are zero.  Physical layout of a 16-position sub-chunk as
+// seen by the fragments: logical position 2t+b <-> physical 4t+b and
+// 2t+8+b <-> 4t+2+b (b = 0, 1), so each thread's four positions of the
+// p v step are consecutive; logical output dim (n-block nb, column c) <->
+// physical dim 16*c + nb, so each thread's V columns are 16 consecutive dims.
+constexpr int kAttnWarps = 4;
+
+__global__ void __launch_bounds__(kAttnWarps * 32) k_attn_split(AttnArgs a) {
+  __shared__ float s_m[kAttnWarps][16], s_l[kAttnWarps][16];
+  __shared__ float s_o[kAttnWarps][16][129];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int kvh = blockIdx.y, split = blockIdx.x;
+  const int HD = 128;
+  pdl_wait();
+  pdl_launch_dependents();
+
+  // Q fragments: thread t holds head dims [32t, 32t+32) of rows g and g+8
+  uint32_t qa[8][4];
+  {
+    const int nrow = a.K * a.group;
+    uint4 rg[4], rh[4];
+#pragma unroll
+    for (int hrow = 0; hrow < 2; ++hrow) {
+      const int i = g + 8 * hrow;
+      uint4* dst = hrow ? rh : rg;
+      if (i < nrow) {
+        const int r = i / a.group, hh = i % a.group;
+        const uint16_t* src = a.q + (size_t)r * a.nq * HD + (size_t)(kvh * a.group + hh) * HD + 32 * t;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) dst[u] = ldg_v4(src + 8 * u);
+      } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) dst[u] = make_uint4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint32_t* wg = reinterpret_cast<const uint32_t*>(&rg[ks >> 1]);
+      const uint32_t* wh = reinterpret_cast<const uint32_t*>(&rh[ks >> 1]);
+      const int w0 = (ks & 1) * 2;
+      qa[ks][0] = wg[w0];
+      qa[ks][1] = wh[w0];
+      qa[ks][2] = wg[w0 + 1];
+      qa[ks][3] = wh[w0 + 1];
+    }
+  }
+
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+  float o[16][4];
+#pragma unroll
+  for (int nb = 0; nb < 16; ++nb)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) o[nb][c] = 0.f;
+
+  const int n16 = a.C / 16;
+  const int c0 = (int)(((long long)split * n16) / gridDim.x);
+  const int c1 = (int)(((long long)(split + 1) * n16) / gridDim.x);
+  const uint16_t* kbase = a.kc + (size_t)kvh * a.C * HD;
+  const uint16_t* vbase = a.vc + (size_t)kvh * a.C * HD;
+  const int pk0 = 4 * (g >> 1) + (g & 1);  // physical row of logical column g (n-block 0); +2 for n-block 1
+
+  for (int sc = c0 + warp; sc < c1; sc += kAttnWarps) {
+    const uint16_t* kb = kbase + (size_t)sc * 16 * HD;
+    const uint16_t* vb = vbase + (size_t)sc * 16 * HD;
+    uint4 kr[2][4], vr[4][2];
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) kr[nb][u] = ldg_nc_v4(kb + (size_t)(pk0 + 2 * nb) * HD + 32 * t + 8 * u);
+#pragma unroll
+    for (int p = 0; p < 4; ++p)
+#pragma unroll
+      for (int u = 0; u < 2; ++u) vr[p][u] = ldg_nc_v4(vb + (size_t)(4 * t + p) * HD + 16 * g + 8 * u);
+
+    float s[2][4];
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) s[nb][c] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(&kr[nb][ks >> 1]);
+        const int w0 = (ks & 1) * 2;
+        mma_bf16(s[nb], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], w[w0], w[w0 + 1]);
+      }
+    }
+    // online softmax (log2 domain); row 0 = query g, row 1 = query g+8
+    float mx[2];
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      float v = -INFINITY;
+#pragma unroll
+      for (int nb = 0; nb < 2; ++nb) {
+        s[nb][2 * hr] *= a.scale_log2;
+        s[nb][2 * hr + 1] *= a.scale_log2;
+        v = fmaxf(v, fmaxf(s[nb][2 * hr], s[nb][2 * hr + 1]));
+      }
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+      mx[hr] = fmaxf(m[hr], v);
+      const float alpha = exp2f(m[hr] - mx[hr]);
+      m[hr] = mx[hr];
+      l[hr] *= alpha;
+#pragma unroll
+      for (int nb = 0; nb < 16; ++nb) {
+        o[nb][2 * hr] *= alpha;
+        o[nb][2 * hr + 1] *= alpha;
+      }
+#pragma unroll
+      for (int nb = 0; nb < 2; ++nb) {
+        s[nb][2 * hr] = exp2f(s[nb][2 * hr] - mx[hr]);
+        s[nb][2 * hr + 1] = exp2f(s[nb][2 * hr + 1] - mx[hr]);
+        l[hr] += s[nb][2 * hr] + s[nb][2 * hr + 1];
+      }
+    }
+    // P as the A operand (k = 16 logical positions)
+    const uint32_t pa0 = pack_bf16x2(s[0][0], s[0][1]);
+    const uint32_t pa1 = pack_bf16x2(s[0][2], s[0][3]);
+    const uint32_t pa2 = pack_bf16x2(s[1][0], s[1][1]);
+    const uint32_t pa3 = pack_bf16x2(s[1][2], s[1][3]);
+    // V as B: k = logical positions (2t, 2t+1 | 2t+8, 2t+9) = physical rows
+    // 4t, 4t+1 | 4t+2, 4t+3; n = logical dim (nb, g) = physical dim 16g + nb
+    const uint32_t* v0 = reinterpret_cast<const uint32_t*>(vr[0]);
+    const uint32_t* v1 = reinterpret_cast<const uint32_t*>(vr[1]);
+    const uint32_t* v2 = reinterpret_cast<const uint32_t*>(vr[2]);
+    const uint32_t* v3 = reinterpret_cast<const uint32_t*>(vr[3]);
+#pragma unroll
+    for (int nb = 0; nb < 16; ++nb) {
+      const int wi = nb >> 1;
+      const uint32_t sel = (nb & 1) ? 0x7632u : 0x5410u;  // high or low halves
+      const uint32_t b0 = __byte_perm(v0[wi], v1[wi], sel);
+      const uint32_t b1 = __byte_perm(v2[wi], v3[wi], sel);
+      mma_bf16(o[nb], pa0, pa1, pa2, pa3, b0, b1);
+    }
+  }
+
+  // per-warp row sums, then merge the warps in fixed order
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    l[hr] += __shfl_xor_sync(0xffffffffu, l[hr], 1);
+    l[hr] += __shfl_xor_sync(0xffffffffu, l[hr], 2);
+  }
+  if (t == 0) {
+    s_m[warp][g] = m[0];
+    s_m[warp][g + 8] = m[1];
+    s_l[warp][g] = l[0];
+    s_l[warp][g + 8] = l[1];
+  }
+#pragma unroll
+  for (int nb = 0; nb < 16; ++nb) {
+    s_o[warp][g][16 * (2 * t) + nb] = o[nb][0];
+    s_o[warp][g][16 * (2 * t + 1) + nb] = o[nb][1];
+    s_o[warp][g + 8][16 * (2 * t) + nb] = o[nb][2];
+    s_o[warp][g + 8][16 * (2 * t + 1) + nb] = o[nb][3];
+  }
+  __syncthreads();
+  const int d = threadIdx.x;  // 128 threads = head dims
+  float* po = a.part_o + ((size_t)(kvh * gridDim.x + split) * 16) * HD;
+  float* pml = a.part_ml + (size_t)(kvh * gridDim.x + split) * 32;
+  for (int i = 0; i < 16; ++i) {
+    float M = -INFINITY;
+    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, s_m[w][i]);
+    float L = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+      for (int w = 0; w < kAttnWarps; ++w) {
+        const float f = exp2f(s_m[w][i] - M);
+        L += s_l[w][i] * f;
+        O += s_o[w][i][d] * f;
+      }
+    }
+    po[i * HD + d] = O;
+    if (d == 0) {
+      pml[2 * i] = M;
+      pml[2 * i + 1] = L;
+    }
+  }
+}
+
+// One CTA per (query head h, row r); 128 threads = head dims.  Merges the
+// splits of KV head h/group in split order with the row's visible new
+// positions 0..r and writes o = bf16(O / L).
+__global__ void __launch_bounds__(128) k_attn_combine(AttnArgs a, int splits) {
+  __shared__ float s_red[4];
+  __shared__ float s_sc[16];
+  const int h = blockIdx.x, r = blockIdx.y, d = threadIdx.x;
+  const int HD = 128, kvh = h / a.group, hh = h % a.group;
+  const int i = r * a.group + hh;
+  pdl_wait();
+  pdl_launch_dependents();
+  const float qd = bf_lo(a.q[(size_t)r * a.nq * HD + (size_t)h * HD + d]);
+  // scores of the new positions j <= r (log2 domain), fixed-order block sum
+  for (int j = 0; j <= r; ++j) {
+    float p = qd * bf_lo(a.k_new[(size_t)j * a.nkv * HD + (size_t)kvh * HD + d]);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
+    if ((d & 31) == 0) s_red[d >> 5] = p;
+    __syncthreads();
+    if (d == 0) s_sc[j] = ((s_red[0] + s_red[1]) + (s_red[2] + s_red[3])) * a.scale_log2;
+    __syncthreads();
+  }
+  float M = -INFINITY;
+  for (int s = 0; s < splits; ++s) M = fmaxf(M, a.part_ml[(size_t)(kvh * splits + s) * 32 + 2 * i]);
+  for (int j = 0; j <= r; ++j) M = fmaxf(M, s_sc[j]);
+  float L = 0.f, O = 0.f;
+  for (int s = 0; s < splits; ++s) {
+    const float ms = a.part_ml[(size_t)(kvh * splits + s) * 32 + 2 * i];
+    if (ms == -INFINITY) continue;
+    const float f = exp2f(ms - M);
+    L += a.part_ml[(size_t)(kvh * splits + s) * 32 + 2 * i + 1] * f;
+    O += a.part_o[((size_t)(kvh * splits + s) * 16 + i) * HD + d] * f;
+  }
+  for (int j = 0; j <= r; ++j) {
+    const float f = exp2f(s_sc[j] - M);
+    L += f;
+    O += f * bf_lo(a.v_new[(size_t)j * a.nkv * HD + (size_t)kvh * HD + d]);
+  }
+  a.o[(size_t)r * a.nq * HD + (size_t)h * HD + d] = float_to_bf16_bits(O / L);
+}
+
+int attn_splits(int nkv) {
+  int s = (2 * num_sms() + nkv - 1) / nkv;
+  return s < 1 ? 1 : (s > kAttnMaxSplits ? kAttnMaxSplits : s);
+}
+
+cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s, bool pdl) {
+  const int splits = attn_splits(a.nkv);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(splits, a.nkv);
+  cfg.blockDim = dim3(kAttnWarps * 32);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, k_attn_split, a);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t c2 = cfg;
+  c2.gridDim = dim3(a.nq, a.K);
+  c2.blockDim = dim3(128);
+  return cudaLaunchKernelEx(&c2, k_attn_combine, a, splits);
+}
+
+}  // namespace moe

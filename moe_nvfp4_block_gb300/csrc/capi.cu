@@ -5,12 +5,17 @@
 // launch: each dependent kernel is scheduled while its predecessor drains and
 // waits (griddepcontrol.wait) before reading the predecessor's results.
 #include <atomic>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 
 #include "internal.h"
 
 using namespace moe;
+
+namespace moe {
+unsigned long long* g_trace = nullptr;
+}
 
 namespace {
 
@@ -34,21 +39,60 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D map over the codes of a projection stack viewed as [n_exp*rows][cols/2]
-// bytes; one box = box_rows rows x min(128, cols/2) bytes, swizzled.
-bool encode_codes(CUtensorMap* m, const uint8_t* codes, int n_exp, int rows, int cols, int box_rows) {
+// Map over the codes of a projection stack viewed as rows of cols/2 bytes,
+// read as box_rows x (cols/2) tiles laid out in shared memory as
+// [line chunk][row][min(128, cols/2) bytes] with the matching swizzle.
+// Preferred: one 3-D box per tile (dims: line bytes, rows, line chunks --
+// one large request); if the driver refuses that stride order, a 2-D map
+// whose box is one line chunk (the kernel then issues one request per chunk).
+bool encode_codes(CUtensorMap* m, const uint8_t* codes, int n_exp, int rows, int cols, int box_rows, bool* is3d) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t rb = (cuuint64_t)cols / 2;
   const cuuint32_t inner = rb >= 128 ? 128 : 64;
+  const CUtensorMapSwizzle sw = inner == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  {
+    cuuint64_t dims[3] = {inner, (cuuint64_t)n_exp * rows, rb / inner};
+    cuuint64_t strides[2] = {rb, inner};
+    cuuint32_t box[3] = {inner, (cuuint32_t)box_rows, (cuuint32_t)(rb / inner)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(codes), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS) {
+      *is3d = true;
+      return true;
+    }
+  }
   cuuint64_t dims[2] = {rb, (cuuint64_t)n_exp * rows};
   cuuint64_t strides[1] = {rb};
   cuuint32_t box[2] = {inner, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(codes), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  inner == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  *is3d = false;
+  return r == CUDA_SUCCESS;
+}
+
+// 2-D map over the E4M3 scales of a projection stack viewed as
+// [n_exp*rows][cols/16] bytes; one box = box_rows full rows, swizzled by the
+// row length (128, 64, 32 bytes) or unswizzled (16 bytes).
+bool encode_scales(CUtensorMap* m, const uint8_t* scales, int n_exp, int rows, int cols, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t rb = (cuuint64_t)cols / 16;
+  if (rb < 16 || rb > 128) return false;
+  cuuint64_t dims[2] = {rb, (cuuint64_t)n_exp * rows};
+  cuuint64_t strides[1] = {rb};
+  cuuint32_t box[2] = {(cuuint32_t)rb, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapSwizzle sw = rb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : rb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                : rb == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                           : CU_TENSOR_MAP_SWIZZLE_NONE;
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(scales), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -103,6 +147,7 @@ RouterArgs router_args(const moe_layer* L, const uint16_t* x, int K, const WsPtr
   a.idx_out = idx_out;
   a.w_out = w_out;
   a.group_out = group_out;
+  a.do_topk = 1;
   return a;
 }
 
@@ -135,7 +180,7 @@ moe_status moe_router_topk(const moe_layer* layer, const uint16_t* x_norm, int K
   return MOE_OK;
 }
 
-static moe_status run_layer(const moe_layer* layer, const uint16_t* x_norm, int K, const uint16_t* residual,
+__attribute__((visibility("hidden"))) moe_status run_layer(const moe_layer* layer, const uint16_t* x_norm, int K, const uint16_t* residual,
                             uint16_t* y, int32_t* idx_out, float* w_out, int32_t* group_out, void* ws,
                             size_t ws_bytes, void* stream, bool pdl, void* const* events) {
   moe_status s = check_layer(layer, K);
@@ -148,60 +193,78 @@ static moe_status run_layer(const moe_layer* layer, const uint16_t* x_norm, int 
   const int H = layer->hidden, E = layer->n_experts, I = layer->inter;
   const bool has_sh = layer->shared_inter > 0;
 
-  CUtensorMap tg, tu, td, tsg, tsu, tsd;
-  if (!encode_codes(&tg, layer->gate.codes, E, I, H, kGURows) ||
-      !encode_codes(&tu, layer->up.codes, E, I, H, kGURows) ||
-      !encode_codes(&td, layer->down.codes, E, H, I, kDNRows))
+  // codes: gate, up, down, sh_gate, sh_up, sh_down; scales: gate, up, sh_gate, sh_up
+  CUtensorMap maps[10];
+  bool d3[6] = {false, false, false, false, false, false};
+  if (!encode_codes(&maps[0], layer->gate.codes, E, I, H, kGURows, &d3[0]) ||
+      !encode_codes(&maps[1], layer->up.codes, E, I, H, kGURows, &d3[1]) ||
+      !encode_codes(&maps[2], layer->down.codes, E, H, I, kDNRows, &d3[2]) ||
+      !encode_scales(&maps[6], layer->gate.scales, E, I, H, kGURows) ||
+      !encode_scales(&maps[7], layer->up.scales, E, I, H, kGURows))
     return MOE_ERR_CUDA;
   if (has_sh) {
-    if (!encode_codes(&tsg, layer->sh_gate.codes, 1, I, H, kGURows) ||
-        !encode_codes(&tsu, layer->sh_up.codes, 1, I, H, kGURows) ||
-        !encode_codes(&tsd, layer->sh_down.codes, 1, H, I, kDNRows))
+    if (!encode_codes(&maps[3], layer->sh_gate.codes, 1, I, H, kGURows, &d3[3]) ||
+        !encode_codes(&maps[4], layer->sh_up.codes, 1, I, H, kGURows, &d3[4]) ||
+        !encode_codes(&maps[5], layer->sh_down.codes, 1, H, I, kDNRows, &d3[5]) ||
+        !encode_scales(&maps[8], layer->sh_gate.scales, 1, I, H, kGURows) ||
+        !encode_scales(&maps[9], layer->sh_up.scales, 1, I, H, kGURows))
       return MOE_ERR_CUDA;
   } else {
-    tsg = tg;
-    tsu = tu;
-    tsd = td;
+    maps[3] = maps[0];
+    maps[4] = maps[1];
+    maps[5] = maps[2];
+    maps[8] = maps[6];
+    maps[9] = maps[7];
+    d3[3] = d3[0];
+    d3[4] = d3[1];
+    d3[5] = d3[2];
   }
+  const bool code3d = d3[0] && d3[1] && d3[2] && d3[3] && d3[4] && d3[5];
+  if (!code3d && (d3[0] || d3[1] || d3[2] || d3[3] || d3[4] || d3[5])) return MOE_ERR_CUDA;  // mixed forms
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const uint64_t wait_ns = g_wait_ns.load();
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (events && cudaStreamIsCapturing(st, &cap) != cudaSuccess) return MOE_ERR_CUDA;
+  // inside a graph capture the events become external record nodes, so that
+  // their times can be read after a replay
+  const unsigned ev_flags = cap == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
   auto mark = [&](int i) {
-    return !events || cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) == cudaSuccess;
+    return !events || cudaEventRecordWithFlags(static_cast<cudaEvent_t>(events[i]), st, ev_flags) == cudaSuccess;
   };
 
-  RouterArgs ra = router_args(layer, x_norm, K, wp, idx_out, w_out, group_out);
-  if (!mark(0) || launch_router(ra, st, false) != cudaSuccess || !mark(1)) return MOE_ERR_CUDA;
+  RouterArgs ra = router_args(layer, x_norm, K, wp, nullptr, nullptr, nullptr);
+  ra.do_topk = 0;
+  // the router prefetches its weights before its dependency wait, so it may
+  // overlap the tail of whatever ran before it on the stream
+  if (!mark(0) || launch_router(ra, st, pdl) != cudaSuccess || !mark(1)) return MOE_ERR_CUDA;
 
-  GateUpArgs ga;
-  ga.x = x_norm;
-  ga.K = K;
-  ga.H = H;
-  ga.I = I;
-  ga.G = ra.G;
-  ga.has_shared = has_sh;
-  ga.gate = {layer->gate.scales, layer->gate.tensor_scale};
-  ga.up = {layer->up.scales, layer->up.tensor_scale};
-  ga.sh_gate = has_sh ? ProjPtrs{layer->sh_gate.scales, layer->sh_gate.tensor_scale} : ga.gate;
-  ga.sh_up = has_sh ? ProjPtrs{layer->sh_up.scales, layer->sh_up.tensor_scale} : ga.up;
-  ga.ws = wp;
-  ga.wait_ns = wait_ns;
-  if (launch_gateup(ga, tg, tu, tsg, tsu, st, pdl) != cudaSuccess || !mark(2)) return MOE_ERR_CUDA;
-
-  DownArgs da;
-  da.residual = residual;
-  da.y = y;
-  da.K = K;
-  da.H = H;
-  da.I = I;
-  da.k = layer->top_k;
-  da.G = ra.G;
-  da.has_shared = has_sh;
-  da.routed_scale = layer->routed_scale;
-  da.down = {layer->down.scales, layer->down.tensor_scale};
-  da.sh_down = has_sh ? ProjPtrs{layer->sh_down.scales, layer->sh_down.tensor_scale} : da.down;
-  da.ws = wp;
-  da.wait_ns = wait_ns;
-  if (launch_down(da, td, tsd, st, pdl) != cudaSuccess || !mark(3)) return MOE_ERR_CUDA;
+  ExpertsArgs ea;
+  ea.x = x_norm;
+  ea.residual = residual;
+  ea.y = y;
+  ea.K = K;
+  ea.H = H;
+  ea.I = I;
+  ea.E = E;
+  ea.k = layer->top_k;
+  ea.G = ra.G;
+  ea.has_shared = has_sh;
+  ea.routed_scale = layer->routed_scale;
+  ea.logits = wp.logits;
+  ea.gate = {layer->gate.scales, layer->gate.tensor_scale};
+  ea.up = {layer->up.scales, layer->up.tensor_scale};
+  ea.down = {layer->down.scales, layer->down.tensor_scale};
+  ea.sh_gate = has_sh ? ProjPtrs{layer->sh_gate.scales, layer->sh_gate.tensor_scale} : ea.gate;
+  ea.sh_up = has_sh ? ProjPtrs{layer->sh_up.scales, layer->sh_up.tensor_scale} : ea.up;
+  ea.sh_down = has_sh ? ProjPtrs{layer->sh_down.scales, layer->sh_down.tensor_scale} : ea.down;
+  ea.ws = wp;
+  ea.idx_out = idx_out;
+  ea.w_out = w_out;
+  ea.group_out = group_out;
+  ea.wait_ns = wait_ns;
+  ea.trace = g_trace;
+  ea.code3d = code3d ? 1 : 0;
+  if (launch_experts(ea, maps, st, pdl) != cudaSuccess || !mark(2) || !mark(3)) return MOE_ERR_CUDA;
   return MOE_OK;
 }
 
@@ -294,6 +357,176 @@ moe_status moe_lm_head_argmax(const uint16_t* x_norm, int K, int H, const uint16
   return MOE_OK;
 }
 
+struct AttnLayout {
+  size_t xn, q, kn, vn, o, part_o, part_ml, total;
+};
+
+static AttnLayout attn_layout(int K, int H, int nq, int nkv) {
+  AttnLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t b) {
+    size_t r = off;
+    off = align256(off + b);
+    return r;
+  };
+  L.xn = take(sizeof(uint16_t) * K * H);
+  L.q = take(sizeof(uint16_t) * K * nq * 128);
+  L.kn = take(sizeof(uint16_t) * K * nkv * 128);
+  L.vn = take(sizeof(uint16_t) * K * nkv * 128);
+  L.o = take(sizeof(uint16_t) * K * nq * 128);
+  L.part_o = take(sizeof(float) * (size_t)nkv * kAttnMaxSplits * 16 * 128);
+  L.part_ml = take(sizeof(float) * (size_t)nkv * kAttnMaxSplits * 32);
+  L.total = off;
+  return L;
+}
+
+static moe_status check_attn(int K, int H, int nq, int nkv, int hd, int C) {
+  if (K < 1 || K > MOE_MAX_ROWS || nq < 1 || nkv < 1 || C < 0) return MOE_ERR_INVALID_ARG;
+  if (hd != 128 || nq % nkv != 0 || K * (nq / nkv) > 16) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (H % 256 != 0 || H > 4096 || nq % 2 != 0 || nq * 128 > 4096 || C % 16 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+size_t moe_attention_workspace_size(int K, int H, int nq, int nkv, int head_dim) {
+  if (check_attn(K, H, nq, nkv, head_dim, 0) != MOE_OK) return 0;
+  return attn_layout(K, H, nq, nkv).total;
+}
+
+moe_status moe_attention_block(const uint16_t* x, int K, int H, int nq, int nkv, int head_dim, int C,
+                               const uint16_t* Wq, const uint16_t* Wk, const uint16_t* Wv, const uint16_t* Wo,
+                               const uint16_t* kcache, const uint16_t* vcache, float eps, uint16_t* x_out,
+                               uint16_t* k_new_out, uint16_t* v_new_out, void* ws, size_t ws_bytes,
+                               void* stream) {
+  moe_status st = check_attn(K, H, nq, nkv, head_dim, C);
+  if (st != MOE_OK) return st;
+  if (!x || !Wq || !Wk || !Wv || !Wo || !x_out || !ws || (C > 0 && (!kcache || !vcache)) || !(eps >= 0.f))
+    return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, Wq, Wk, Wv, Wo, kcache, vcache, x_out, k_new_out, v_new_out, ws};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return MOE_ERR_MISALIGNED;
+  const AttnLayout L = attn_layout(K, H, nq, nkv);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  char* b = static_cast<char*>(ws);
+  uint16_t* xn = reinterpret_cast<uint16_t*>(b + L.xn);
+  uint16_t* q = reinterpret_cast<uint16_t*>(b + L.q);
+  uint16_t* kn = k_new_out ? k_new_out : reinterpret_cast<uint16_t*>(b + L.kn);
+  uint16_t* vn = v_new_out ? v_new_out : reinterpret_cast<uint16_t*>(b + L.vn);
+  uint16_t* o = reinterpret_cast<uint16_t*>(b + L.o);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  if (launch_rmsnorm(x, K, H, eps, xn, s, false) != cudaSuccess) return MOE_ERR_CUDA;
+  GemvArgs g{};
+  g.x = xn;
+  g.K = K;
+  g.D = H;
+  g.seg[0] = {Wq, q, nullptr, nq * 128};
+  g.seg[1] = {Wk, kn, nullptr, nkv * 128};
+  g.seg[2] = {Wv, vn, nullptr, nkv * 128};
+  g.nseg = 3;
+  g.n_total = (nq + 2 * nkv) * 128;
+  if (launch_gemv(g, s, true) != cudaSuccess) return MOE_ERR_CUDA;
+  AttnArgs a{};
+  a.q = q;
+  a.kc = kcache;
+  a.vc = vcache;
+  a.k_new = kn;
+  a.v_new = vn;
+  a.o = o;
+  a.K = K;
+  a.nq = nq;
+  a.nkv = nkv;
+  a.C = C;
+  a.group = nq / nkv;
+  a.scale_log2 = 1.4426950408889634f / sqrtf(128.f);
+  a.part_o = reinterpret_cast<float*>(b + L.part_o);
+  a.part_ml = reinterpret_cast<float*>(b + L.part_ml);
+  if (launch_attention(a, s, true) != cudaSuccess) return MOE_ERR_CUDA;
+  GemvArgs go{};
+  go.x = o;
+  go.K = K;
+  go.D = nq * 128;
+  go.seg[0] = {Wo, x_out, x, H};
+  go.nseg = 1;
+  go.n_total = H;
+  if (launch_gemv(go, s, true) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+static moe_status check_model(const moe_verify_model* m, int K) {
+  if (!m || !m->layers || !m->lm_head || m->n_layers < 1 || m->vocab < 1 || !(m->eps >= 0.f))
+    return MOE_ERR_INVALID_ARG;
+  moe_status s = check_attn(K, m->hidden, m->n_q_heads, m->n_kv_heads, m->head_dim, m->ctx);
+  if (s != MOE_OK) return s;
+  if (m->hidden > 2048) return MOE_ERR_UNSUPPORTED_SHAPE;  // lm_head and MoE envelope
+  for (int l = 0; l < m->n_layers; ++l) {
+    const moe_decoder_layer& d = m->layers[l];
+    if (!d.Wq || !d.Wk || !d.Wv || !d.Wo || (m->ctx > 0 && (!d.kcache || !d.vcache))) return MOE_ERR_INVALID_ARG;
+    if ((s = check_layer(&d.moe, K)) != MOE_OK) return s;
+    if (d.moe.hidden != m->hidden) return MOE_ERR_INVALID_ARG;
+  }
+  return MOE_OK;
+}
+
+struct StepLayout {
+  size_t moe_ws, attn_ws, xn, lm_ws, total;
+  size_t moe_bytes, attn_bytes;
+};
+
+static StepLayout step_layout(const moe_verify_model* m, int K) {
+  StepLayout L{};
+  size_t mb = 0;
+  for (int l = 0; l < m->n_layers; ++l) {
+    const size_t b = layout_of(&m->layers[l].moe, K).total;
+    mb = b > mb ? b : mb;
+  }
+  const size_t ab = attn_layout(K, m->hidden, m->n_q_heads, m->n_kv_heads).total;
+  size_t off = 0;
+  L.moe_ws = off;
+  off = align256(off + mb);
+  L.attn_ws = off;
+  off = align256(off + ab);
+  L.xn = off;
+  off = align256(off + sizeof(uint16_t) * K * m->hidden);
+  L.lm_ws = off;
+  off = align256(off + lmhead_ws_bytes(K));
+  L.total = off;
+  L.moe_bytes = mb;
+  L.attn_bytes = ab;
+  return L;
+}
+
+size_t moe_verify_step_workspace_size(const moe_verify_model* m, int K) {
+  if (check_model(m, K) != MOE_OK) return 0;
+  return step_layout(m, K).total;
+}
+
+moe_status moe_verify_step(const moe_verify_model* m, uint16_t* x, int K, const int32_t* draft, int32_t* target,
+                           int32_t* n_accepted, void* ws, size_t ws_bytes, void* stream) {
+  moe_status s = check_model(m, K);
+  if (s != MOE_OK) return s;
+  if (!x || !draft || !target || !n_accepted || !ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(ws)) return MOE_ERR_MISALIGNED;
+  const StepLayout L = step_layout(m, K);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  char* b = static_cast<char*>(ws);
+  uint16_t* xn = reinterpret_cast<uint16_t*>(b + L.xn);
+  const int H = m->hidden;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  for (int l = 0; l < m->n_layers; ++l) {
+    const moe_decoder_layer& d = m->layers[l];
+    s = moe_attention_block(x, K, H, m->n_q_heads, m->n_kv_heads, m->head_dim, m->ctx, d.Wq, d.Wk, d.Wv, d.Wo,
+                            d.kcache, d.vcache, m->eps, x, nullptr, nullptr, b + L.attn_ws, L.attn_bytes, stream);
+    if (s != MOE_OK) return s;
+    if (launch_rmsnorm(x, K, H, m->eps, xn, st, true) != cudaSuccess) return MOE_ERR_CUDA;
+    s = run_layer(&d.moe, xn, K, x, x, nullptr, nullptr, nullptr, b + L.moe_ws, L.moe_bytes, stream, true, nullptr);
+    if (s != MOE_OK) return s;
+  }
+  if (launch_rmsnorm(x, K, H, m->eps, xn, st, false) != cudaSuccess) return MOE_ERR_CUDA;
+  s = moe_lm_head_argmax(xn, K, H, m->lm_head, m->vocab, target, nullptr, b + L.lm_ws, lmhead_ws_bytes(K), stream);
+  if (s != MOE_OK) return s;
+  return verify_accept_prefix(draft, target, K, n_accepted, stream);
+}
+
 moe_status moe_workspace_error(void* ws, int* code, void* stream) {
   if (!ws || !code) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -319,5 +552,7 @@ const char* moe_status_string(moe_status s) {
 }
 
 void moe_debug_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns); }
+
+void moe_debug_set_trace(void* buf) { g_trace = static_cast<unsigned long long*>(buf); }
 
 }  // extern "C"

@@ -16,8 +16,17 @@ constexpr int kGUWarps = 8;              // consumer warps, gate/up kernel
 constexpr int kDNWarps = 8;              // consumer warps, down kernel
 constexpr int kGURows = 16;              // intermediate rows per gate/up item
 constexpr int kDNRows = 64;              // hidden rows per down item
-constexpr int kGUStages = 4;
-constexpr int kDNStages = 6;
+constexpr int kExpWarps = 8;             // consumer warps of the experts kernel
+constexpr int kExpStages = 4;            // TMA ring depth of the experts kernel
+
+// Bytes of one ring stage: the larger of a gate/up item (codes and scales of
+// 16 rows of gate and up) and a down item (64 rows), 1024-aligned.
+__host__ __device__ inline int expert_stage_bytes(int H, int I) {
+  const int gu = 2 * (kGURows * H / 2) + 2 * (kGURows * H / 16);
+  const int dn = kDNRows * I / 2 + kDNRows * I / 16;
+  const int m = gu > dn ? gu : dn;
+  return (m + 1023) & ~1023;
+}
 
 // Byte offsets of the workspace regions (all 256-byte aligned).
 struct WsLayout {
@@ -30,6 +39,8 @@ struct WsLayout {
   size_t slotmap;  // int32 [G+1][K]: slot of the expert in row r's selection, -1 if none
   size_t hamax;    // uint32 [G+1][K]: max |h| bits per (expert, row)
   size_t tilecnt;  // uint32 [H/64]: completed down items per hidden tile
+  size_t done;     // uint32 [G+1]: gate/up items completed per distinct expert
+  size_t gridbar;  // uint32: CTAs of the experts kernel past their down items
   size_t h;        // bf16 [G+1][K][I]
   size_t dpart;    // float [K][k+1][H]
   size_t total;
@@ -57,6 +68,8 @@ inline WsLayout ws_layout(int K, int E, int k, int H, int I) {
   L.slotmap = take(sizeof(int32_t) * (G + 1) * K);
   L.hamax = take(sizeof(uint32_t) * (G + 1) * K);
   L.tilecnt = take(sizeof(uint32_t) * (H / kDNRows));
+  L.done = take(sizeof(uint32_t) * (G + 1));
+  L.gridbar = take(sizeof(uint32_t));
   L.h = take(sizeof(uint16_t) * (size_t)(G + 1) * K * I);
   L.dpart = take(sizeof(float) * (size_t)K * (k + 1) * H);
   L.total = o;
@@ -75,6 +88,8 @@ struct WsPtrs {
   int* slotmap;
   unsigned* hamax;
   unsigned* tilecnt;
+  unsigned* done;
+  unsigned* gridbar;
   uint16_t* h;
   float* dpart;
 };
@@ -92,6 +107,8 @@ inline WsPtrs ws_ptrs(void* ws, const WsLayout& L) {
   p.slotmap = reinterpret_cast<int*>(b + L.slotmap);
   p.hamax = reinterpret_cast<unsigned*>(b + L.hamax);
   p.tilecnt = reinterpret_cast<unsigned*>(b + L.tilecnt);
+  p.done = reinterpret_cast<unsigned*>(b + L.done);
+  p.gridbar = reinterpret_cast<unsigned*>(b + L.gridbar);
   p.h = reinterpret_cast<uint16_t*>(b + L.h);
   p.dpart = reinterpret_cast<float*>(b + L.dpart);
   return p;
@@ -108,6 +125,7 @@ struct RouterArgs {
   int32_t* idx_out;         // caller copies (nullable)
   float* w_out;
   int32_t* group_out;
+  int do_topk;              // 1: the last CTA also selects and groups (moe_router_topk)
 };
 
 // Per-projection pointers the expert kernels need besides the tensor maps.
@@ -116,25 +134,26 @@ struct ProjPtrs {
   const float* tscale;
 };
 
-struct GateUpArgs {
-  const uint16_t* x;  // [K][H] bf16
-  int K, H, I, G;
-  int has_shared;
-  ProjPtrs gate, up, sh_gate, sh_up;
-  WsPtrs ws;
-  uint64_t wait_ns;
-};
-
-struct DownArgs {
+struct ExpertsArgs {
+  const uint16_t* x;         // x_norm [K][H] bf16
   const uint16_t* residual;  // [K][H] or null
   uint16_t* y;               // [K][H]
-  int K, H, I, k, G;
+  int K, H, I, E, k, G;
   int has_shared;
   float routed_scale;
-  ProjPtrs down, sh_down;
+  const float* logits;       // [K][E], from the router kernel
+  ProjPtrs gate, up, down, sh_gate, sh_up, sh_down;
   WsPtrs ws;
+  int32_t* idx_out;          // routing copies for the caller (nullable)
+  float* w_out;
+  int32_t* group_out;
   uint64_t wait_ns;
+  unsigned long long* trace;  // [grid][kTraceSlots] milestone timestamps, or null
+  int code3d;                 // code maps are 3-D (one request per tile)
 };
+
+constexpr int kTraceSlots = 64;
+extern unsigned long long* g_trace;  // debug timeline buffer (null = off)
 
 struct LmHeadArgs {
   const uint16_t* x;  // [K][H] normalised rows
@@ -149,18 +168,52 @@ struct LmHeadArgs {
 
 constexpr int kLmMaxGrid = 1024;
 
+struct GemvSeg {
+  const uint16_t* W;    // [N][D]
+  uint16_t* out;        // [K][N]
+  const uint16_t* res;  // [K][N] or null
+  int N;
+};
+
+struct GemvArgs {
+  const uint16_t* x;  // [K][D]
+  int K, D;
+  GemvSeg seg[3];
+  int nseg, n_total;
+};
+
+struct AttnArgs {
+  const uint16_t* q;      // [K][nq*128]
+  const uint16_t* kc;     // [nkv][C][128]
+  const uint16_t* vc;
+  const uint16_t* k_new;  // [K][nkv*128]
+  const uint16_t* v_new;
+  uint16_t* o;            // [K][nq*128]
+  int K, nq, nkv, C, group;
+  float scale_log2;       // log2(e) / sqrt(128)
+  float* part_o;          // [nkv][splits][16][128]
+  float* part_ml;         // [nkv][splits][16][2]
+};
+
+constexpr int kAttnMaxSplits = 64;
+
+cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t s, bool pdl);
+cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s, bool pdl);
+int attn_splits(int nkv);
+
 inline size_t lmhead_ws_bytes(int K) { return 256 + align256(sizeof(float) * kLmMaxGrid * K) + sizeof(int) * kLmMaxGrid * K; }
 
 // Launchers (return cudaGetLastError()).
 cudaError_t launch_rmsnorm(const uint16_t* x, int K, int H, float eps, uint16_t* out, cudaStream_t s, bool pdl);
 cudaError_t launch_lmhead(const LmHeadArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s, bool pdl);
-cudaError_t launch_gateup(const GateUpArgs& a, const CUtensorMap& gate, const CUtensorMap& up,
-                          const CUtensorMap& sh_gate, const CUtensorMap& sh_up, cudaStream_t s, bool pdl);
-cudaError_t launch_down(const DownArgs& a, const CUtensorMap& down, const CUtensorMap& sh_down, cudaStream_t s,
-                        bool pdl);
+// maps: gate, up, down, sh_gate, sh_up, sh_down codes; gate, up, sh_gate, sh_up scales
+cudaError_t launch_experts(const ExpertsArgs& a, const CUtensorMap* maps, cudaStream_t s, bool pdl);
+size_t experts_smem_bytes(int K, int H, int I, int E, int k, int G);
 cudaError_t launch_accept(const int32_t* draft, const int32_t* target, int K, int32_t* out, cudaStream_t s);
 
 int num_sms();
 
 }  // namespace moe
+
+

@@ -60,7 +60,28 @@ __global__ void __launch_bounds__(kRouterWarps * 32) k_router(RouterArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = a.K, H = a.H, E = a.E, k = a.k, G = a.G;
 
+  // The router weights do not depend on earlier kernels: start loading them
+  // before the dependency wait.
+  const int e = blockIdx.x * kRouterWarps + warp;
+  const int nj = H / 256;  // <= 8
+  uint4 wv[8];
+  if (e < E) {
+    const uint4* wrow = reinterpret_cast<const uint4*>(a.router_w + (size_t)e * H);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (j < nj) wv[j] = ldg_nc_v4(wrow + j * 32 + lane);
+  }
+  pdl_wait();  // the rows and the workspace are ours from here on
   pdl_launch_dependents();
+
+  if (!a.do_topk) {  // clear the experts kernel's per-call counters (a slice per CTA)
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < (G + 1) * K; i += gridDim.x * blockDim.x)
+      a.ws.hamax[i] = 0u;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i <= G; i += gridDim.x * blockDim.x) a.ws.done[i] = 0u;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < a.n_tiles; i += gridDim.x * blockDim.x)
+      a.ws.tilecnt[i] = 0u;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *a.ws.gridbar = 0u;
+  }
 
   // ---------------------------------------------------------------- logits
   {
@@ -68,14 +89,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32) k_router(RouterArgs a) {
     const uint4* xg = reinterpret_cast<const uint4*>(a.x);
     for (int i = threadIdx.x; i < K * H / 8; i += blockDim.x) xs[i] = xg[i];
     __syncthreads();
-    const int e = blockIdx.x * kRouterWarps + warp;
     if (e < E) {
-      const int nj = H / 256;  // <= 8
-      const uint4* wrow = reinterpret_cast<const uint4*>(a.router_w + (size_t)e * H);
-      uint4 wv[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (j < nj) wv[j] = ldg_nc_v4(wrow + j * 32 + lane);
       float acc[KR];
 #pragma unroll
       for (int r = 0; r < KR; ++r) acc[r] = 0.f;
@@ -109,6 +123,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32) k_router(RouterArgs a) {
           if (r < K) a.ws.logits[(size_t)r * E + e] = a.bias ? __fadd_rn(acc[r], b) : acc[r];
       }
     }
+    if (!a.do_topk) return;
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -257,9 +272,6 @@ __global__ void __launch_bounds__(kRouterWarps * 32) k_router(RouterArgs a) {
       if (gout) gout[1 + 2 * G] = K * k;
     }
   }
-  // per-call state of the expert kernels
-  for (int i = threadIdx.x; i < (G + 1) * K; i += blockDim.x) a.ws.hamax[i] = 0u;
-  for (int i = threadIdx.x; i < a.n_tiles; i += blockDim.x) a.ws.tilecnt[i] = 0u;
   if (threadIdx.x == 0) *a.ws.ticket = 0u;
 }
 

@@ -270,3 +270,24 @@ def moe_stack(w, layers, x0, n_layers=None, L=None, collect=False):
         ol = OracleLayer.from_workload(w, layers(l))
         x = moe_layer(ol, rmsnorm(x, L=L), residual=x, L=L)["y"]
     return (x, xs) if collect else x
+
+
+def verify_step(w, layers, lm_head, x0, n_layers=None, L=None):
+    """The full verify step: per layer the attention block, then the MoE block
+    (x <- x + MoE(rmsnorm(x))), then the lm_head argmax of every row.
+    ``layers(l)`` returns (attention dict with Wq, Wk, Wv, Wo, kc, vc; MoE
+    synthgen.Layer).  Returns dict(x, target, best, att_in, moe_in, idx, xn)."""
+    x = _c(x0, np.uint16)
+    att_in, moe_in, idx = [], [], []
+    for l in range(n_layers or w.layers):
+        att, moe = layers(l)
+        att_in.append(x.copy())
+        x = attention(x, att["Wq"], att["Wk"], att["Wv"], att["Wo"], att["kc"], att["vc"], w.n_q_heads,
+                      w.n_kv_heads, w.head_dim, L=L)
+        moe_in.append(x.copy())
+        r = moe_layer(OracleLayer.from_workload(w, moe), rmsnorm(x, L=L), residual=x, L=L)
+        idx.append(r["idx"])
+        x = r["y"]
+    xn = rmsnorm(x, L=L)
+    tok, best = lm_argmax(xn, lm_head, L=L)
+    return dict(x=x, target=tok, best=best, att_in=att_in, moe_in=moe_in, idx=idx, xn=xn)

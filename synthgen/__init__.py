@@ -224,3 +224,33 @@ def make_x(w: Workload, instance: int = 0, K: int | None = None) -> np.ndarray:
     """Activation rows, bf16 N(0,1), [K, H]; ``instance`` selects a fresh draw."""
     K = w.K if K is None else K
     return normal_bf16(w.seed, instance, T_X, 0, K * w.H).reshape(K, w.H)
+
+
+def make_attention(w: Workload, layer: int) -> dict:
+    """bf16 attention weights N(0, 0.02) and a bf16 N(0,1) KV cache of w.ctx
+    positions for one layer (no positional encoding)."""
+    s, H, hd = w.seed, w.H, w.head_dim
+    nq, nkv, C = w.n_q_heads, w.n_kv_heads, w.ctx
+    return dict(
+        Wq=normal_bf16(s, layer, T_ATT_Q, 0, nq * hd * H, 0.0, ROUTER_SIGMA).reshape(nq * hd, H),
+        Wk=normal_bf16(s, layer, T_ATT_K, 0, nkv * hd * H, 0.0, ROUTER_SIGMA).reshape(nkv * hd, H),
+        Wv=normal_bf16(s, layer, T_ATT_V, 0, nkv * hd * H, 0.0, ROUTER_SIGMA).reshape(nkv * hd, H),
+        Wo=normal_bf16(s, layer, T_ATT_O, 0, H * nq * hd, 0.0, ROUTER_SIGMA).reshape(H, nq * hd),
+        kc=normal_bf16(s, layer, T_KCACHE, 0, nkv * C * hd).reshape(nkv, C, hd),
+        vc=normal_bf16(s, layer, T_VCACHE, 0, nkv * C * hd).reshape(nkv, C, hd),
+    )
+
+
+def make_lm_head(w: Workload) -> np.ndarray:
+    return normal_bf16(w.seed, 0, T_LM_HEAD, 0, w.vocab * w.H, 0.0, ROUTER_SIGMA).reshape(w.vocab, w.H)
+
+
+def make_drafts(w: Workload, target: np.ndarray, instance: int = 0):
+    """Drafted tokens for a verify step: the target's token for the first j
+    rows (j uniform in 0..K) and a different token afterwards, so the
+    accepted prefix is exactly j.  Returns (draft int32 [K], j)."""
+    K = target.shape[0]
+    j = int(uniform_int(w.seed, instance, T_DRAFT_J, 0, 1, K + 1)[0])
+    other = uniform_int(w.seed, instance, T_DRAFT_TOK, 0, K, w.vocab - 1)
+    draft = np.where(np.arange(K) < j, target, (target.astype(np.int64) + 1 + other) % w.vocab).astype(np.int32)
+    return draft, j

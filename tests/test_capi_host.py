@@ -80,5 +80,8 @@ def test_bad_call_arguments_rejected_on_host(M):
     assert M.lib.verify_accept_prefix(None, 16, 2, 16, None) == -1
     assert M.lib.verify_accept_prefix(16, 16, 2, None, None) == -1
     assert M.lib.verify_accept_prefix(16, 16, -1, 16, None) == -1
+    # attention envelope: one query head (o-projection shorter than 256) is refused
+    assert M.lib.moe_attention_workspace_size(16, 256, 1, 1, 128) == 0
+    assert M.lib.moe_attention_workspace_size(4, 2048, 32, 8, 128) > 0
     for s in range(-6, 1):
         assert M.status_string(s) not in ("", "unknown status")
