@@ -151,6 +151,37 @@ moe_status moe_verify_stack(const moe_layer* layers, int n_layers, uint16_t* x, 
                             size_t ws_bytes, void* stream);
 
 /*
+ * moe_verify_layer without a caller-provided workspace, for callers that
+ * cannot allocate device memory: for example an engine whose allocator owns
+ * the whole GPU and forbids outside cudaMalloc calls, or a latency-critical
+ * decode loop that cannot afford cudaMalloc's implicit device
+ * synchronisation.  The pages have no counterpart of this entry point.
+ *
+ * Same results as moe_verify_layer.  The scratch space (routing tables,
+ * intermediate activations, partial sums, counters) is a fixed 4 MiB array
+ * compiled into the library; every GPU that loads the library holds it until
+ * the process exits.  A call whose layer needs more workspace than that
+ * (moe_verify_layer_workspace_size) returns MOE_ERR_WORKSPACE_TOO_SMALL.
+ * The inputs and outputs are still the caller's device buffers.
+ *  - The call allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ *    library routine.
+ *  - The first call on a device looks up the array's address on that device
+ *    (the device current in the calling thread, which must be the device of
+ *    `stream`) and zero-fills it once; make that first call before any
+ *    stream capture.
+ *  - Every call on a device shares the one array and keeps the last call's
+ *    contents; each call clears the counters it needs.  Calls that overlap
+ *    on the GPU (different streams, or different host threads) race on the
+ *    array and give wrong results: serialise them.
+ *  - A device-side wait that runs out of time leaves y undefined and is not
+ *    reported by this entry point (use moe_verify_layer with your own
+ *    workspace and moe_workspace_error where that matters).
+ */
+moe_status moe_verify_layer_static(const moe_layer* layer, const uint16_t* x_norm, int K,
+                                   const uint16_t* residual, uint16_t* y, int32_t* idx_out, float* w_out,
+                                   int32_t* group_out, void* stream);
+
+/*
  * Profiling variant of moe_verify_layer for benchmarks: identical results,
  * but the two kernels (router, experts) are launched without programmatic
  * overlap and, when `events` is not NULL, the cudaEvent_t handles

@@ -31,7 +31,7 @@ MOE_MAX_ROWS = 16
 EXPORTS = ("moe_verify_layer_workspace_size", "moe_router_topk", "moe_group_ints", "moe_verify_layer",
            "moe_verify_layer_profiled", "verify_accept_prefix", "moe_rmsnorm", "moe_lm_head_workspace_size",
            "moe_lm_head_argmax", "moe_verify_stack_workspace_size", "moe_verify_stack",
-           "moe_attention_workspace_size", "moe_attention_block",
+           "moe_attention_workspace_size", "moe_attention_block", "moe_verify_layer_static",
            "moe_verify_step_workspace_size", "moe_verify_step", "moe_workspace_error", "moe_status_string", "moe_debug_set_wait_limit_ns",
            "moe_debug_set_trace")
 
@@ -81,6 +81,8 @@ def _load():
     L.moe_router_topk.argtypes = [lp, vp, ci, vp, vp, vp, vp, sz, vp]
     L.moe_verify_layer.restype = ci
     L.moe_verify_layer.argtypes = [lp, vp, ci, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.moe_verify_layer_static.restype = ci
+    L.moe_verify_layer_static.argtypes = [lp, vp, ci, vp, vp, vp, vp, vp, vp]
     L.moe_verify_layer_profiled.restype = ci
     L.moe_verify_layer_profiled.argtypes = [lp, vp, ci, vp, vp, vp, sz, vp, vp]
     L.verify_accept_prefix.restype = ci
@@ -207,6 +209,16 @@ def moe_verify_layer(layer: Layer, x_norm, residual, y, ws, idx_out=None, w_out=
     _check(lib.moe_verify_layer(ctypes.byref(c), _ptr(x_norm), x_norm.shape[0], _ptr(residual), _ptr(y),
                                 _ptr(idx_out), _ptr(w_out), _ptr(group_out), _ptr(ws), ws.numel(),
                                 _stream(stream)), "moe_verify_layer")
+
+
+def moe_verify_layer_static(layer: Layer, x_norm, residual, y, idx_out=None, w_out=None, group_out=None,
+                            stream=None):
+    """moe_verify_layer with the library's built-in scratch array (no workspace
+    argument, no allocation); see include/moe_verify.h for its limits."""
+    c = layer.c()
+    _check(lib.moe_verify_layer_static(ctypes.byref(c), _ptr(x_norm), x_norm.shape[0], _ptr(residual), _ptr(y),
+                                       _ptr(idx_out), _ptr(w_out), _ptr(group_out), _stream(stream)),
+           "moe_verify_layer_static")
 
 
 def moe_verify_layer_profiled(layer: Layer, x_norm, residual, y, ws, events=None, stream=None,

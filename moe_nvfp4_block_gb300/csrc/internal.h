@@ -215,5 +215,7 @@ cudaError_t launch_accept(const int32_t* draft, const int32_t* target, int K, in
 int num_sms();
 
 }  // namespace moe
-
-
+// The layer launch sequence behind moe_verify_layer (capi.cu; not exported).
+extern "C" __attribute__((visibility("hidden"))) moe_status run_layer(const moe_layer* layer, const uint16_t* x_norm, int K, const uint16_t* residual,
+                                uint16_t* y, int32_t* idx_out, float* w_out, int32_t* group_out, void* ws,
+                                size_t ws_bytes, void* stream, bool pdl, void* const* events);
