@@ -302,7 +302,7 @@ const char* moe_status_string(moe_status s);
 void moe_debug_set_wait_limit_ns(uint64_t ns);
 
 /*
- * Profiling hook: when `buf` (device memory, one row of 16 uint64 per SM)
+ * Profiling hook: when `buf` (device memory, one row of 80 uint64 per SM)
  * is not NULL, experts kernels launched afterwards record %globaltimer
  * stamps of their milestones in it (NULL turns it off).
  */

@@ -347,7 +347,7 @@ def moe_debug_set_wait_limit_ns(ns: int):
 
 
 def moe_debug_set_trace(buf):
-    """Device uint64 tensor [n_sms, 16] for milestone stamps, or None."""
+    """Device uint64 tensor [n_sms, 80] for milestone stamps, or None."""
     lib.moe_debug_set_trace(None if buf is None else ctypes.c_void_p(buf.data_ptr()))
 
 

@@ -43,11 +43,27 @@ namespace moe {
 
 namespace {
 
-constexpr int kConsumerThreads = 256;
-constexpr int kThreads = kConsumerThreads + 32;
+// Warp roles: kCompWarps compute warps (warp w decodes and multiplies
+// k-unit w, 128 wide, of every item, so H <= 2048, and reduces its share of
+// every item's outputs) and one producer warp that issues the TMA copies.
+constexpr int kCompWarps = 16;
+constexpr int kCompThreads = kCompWarps * 32;
+constexpr int kProducerWarp = kCompWarps;
+constexpr int kThreads = kCompThreads + 32;
 constexpr uint64_t kDrainNs = 2000000000ull;  // bound on waiting for our own copies before exit
 
-__device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// named barrier 1: the compute warps
+__device__ __forceinline__ void comp_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kCompThreads) : "memory"); }
+
+__device__ __forceinline__ unsigned ld_acquire_cta(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_cta_shared_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
 
 __device__ __forceinline__ void set_error(int* err, int code) { atomicCAS(err, 0, code); }
 
@@ -59,12 +75,6 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
 
 __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ unsigned atom_acq_rel_add(unsigned* p, unsigned v) {
-  unsigned old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
 }
 
 // Power-of-two shift that maps max |x| into [2^14, 2^15).
@@ -131,13 +141,15 @@ __device__ __forceinline__ void warp_top8(unsigned long long (&v)[8]) {
           else kx(v[j], v[i]);
         }
       }
-#pragma unroll
+#pragma unroll 1
   for (int d = 16; d >= 1; d >>= 1) {
-    unsigned long long p[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) p[j] = __shfl_xor_sync(0xffffffffu, v[j], d);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = v[j] > p[7 - j] ? v[j] : p[7 - j];
+    for (int j = 0; j < 4; ++j) {  // v[j] vs partner's v[7-j], and v[7-j] vs partner's v[j]
+      const unsigned long long pj = __shfl_xor_sync(0xffffffffu, v[j], d);
+      const unsigned long long pk = __shfl_xor_sync(0xffffffffu, v[7 - j], d);
+      v[j] = v[j] > pk ? v[j] : pk;
+      v[7 - j] = v[7 - j] > pj ? v[7 - j] : pj;
+    }
 #pragma unroll
     for (int dd = 4; dd >= 1; dd >>= 1)
 #pragma unroll
@@ -145,6 +157,91 @@ __device__ __forceinline__ void warp_top8(unsigned long long (&v)[8]) {
         const int j = i ^ dd;
         if (j > i) kx(v[i], v[j]);
       }
+  }
+}
+
+// Top-k of one row of E logits for any E <= 1024, k <= 32 (lane l holds
+// experts l + 32 i): k rounds of a warp arg-max, larger logit first and lower
+// index on ties; NaN logits rank last, lowest index first.  Lane 0 writes the
+// selected experts and their logits.
+__device__ __noinline__ void topk_general(const float* row, int E, int k, int* idx, float* w, int lane) {
+  float lv[32];
+  unsigned taken = 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int e = lane + 32 * i;
+    lv[i] = (e < E) ? __ldcg(row + e) : -INFINITY;
+  }
+  for (int s = 0; s < k; ++s) {
+    float bv = -INFINITY;
+    int be = INT_MAX;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u) && ranks_before(lv[i], e, bv, be)) {
+        bv = lv[i];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, d);
+      if (ranks_before(ov, oe, bv, be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if (be == INT_MAX) {  // only NaN logits left: lowest free index
+      int f = INT_MAX;
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (lane + 32 * i < E && !((taken >> i) & 1u)) f = min(f, lane + 32 * i);
+#pragma unroll
+      for (int d = 16; d >= 1; d >>= 1) f = min(f, __shfl_xor_sync(0xffffffffu, f, d));
+      be = f;
+      float mine = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (lane + 32 * i == be) mine = lv[i];
+      bv = __shfl_sync(0xffffffffu, mine, be & 31);
+    }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if (lane == 0) {
+      idx[s] = be;
+      w[s] = bv;  // logit for now
+    }
+  }
+}
+
+// The grouping of one call for the caller (one warp): the distinct experts,
+// the (row, slot) pairs before each, and each expert's pairs r * k + slot in
+// row order.
+__device__ __noinline__ void write_groups(int* go, int nu, int G, int K, int k, const int* uexp,
+                                         const unsigned* rowmask, const signed char* slot, int lane) {
+  if (lane == 0) {
+    go[0] = nu;
+    go[1 + 2 * G] = K * k;
+  }
+  int before = 0;
+  for (int v0 = 0; v0 < G; v0 += 32) {
+    const int v = v0 + lane;
+    const unsigned rm = v < nu ? rowmask[uexp[v]] : 0u;
+    const int c = __popc(rm);
+    int inc = c;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, inc, d);
+      if (lane >= d) inc += o;
+    }
+    int o = before + inc - c;
+    if (v < G) {
+      go[1 + v] = v < nu ? uexp[v] : -1;
+      go[1 + G + v] = o;
+    }
+    for (int r = 0; r < K; ++r)
+      if ((rm >> r) & 1u) go[2 + 2 * G + o++] = r * k + slot[v * K + r];
+    before += __shfl_sync(0xffffffffu, inc, 31);
   }
 }
 
@@ -179,14 +276,11 @@ __device__ __forceinline__ void unit_scales(uint2 s8, int t, uint32_t (&out)[4])
   out[3] = __byte_perm(hi, hi, 0x3232);
 }
 
-// One k-unit (128 k) of a 16-row m-tile against NB n-blocks of B.
-//   tile: shared address of the codes tile (box_rows rows per box)
-//   sg, sh: the row-g and row-(g+8) scales of this k-unit (unit_scales)
-template <int NB>
-__device__ __forceinline__ void kunit_mma(uint32_t tile, const TileGeo& geo, int box_rows, int row0, int ku,
-                                          const uint32_t (&sg)[4], const uint32_t (&sh)[4],
-                                          const uint32_t (&b)[NB][16], float (&acc0)[NB][4],
-                                          float (&acc1)[NB][4], int lane) {
+// The two ldmatrix offsets (swizzled, bytes from the tile start) a lane uses
+// for k-unit `ku` of a tile whose m-tile starts at row0: they depend only on
+// the warp's k-unit and the lane, so a warp computes them once.
+__device__ __forceinline__ void kunit_offsets(const TileGeo& geo, int box_rows, int row0, int ku, int lane,
+                                              uint32_t (&off)[2]) {
   const int q0 = (ku * 4) % geo.units;
   const int c = (ku * 4) / geo.units;
   const int mi = lane >> 3, rr = lane & 7;
@@ -194,11 +288,26 @@ __device__ __forceinline__ void kunit_mma(uint32_t tile, const TileGeo& geo, int
 #pragma unroll
   for (int p = 0; p < 2; ++p) {
     const int unit = q0 + 2 * p + (mi >> 1);
-    const uint32_t off = swizzle_off((uint32_t)((c * box_rows + lrow) * geo.inner + unit * 16), geo.mask);
-    uint32_t r0, r1, r2, r3;
-    ldmatrix_x4(tile + off, r0, r1, r2, r3);
-    // r0: row g unit q, r1: row g+8 unit q, r2: row g unit q+1, r3: row g+8 unit q+1
-    const uint32_t rq[2][2] = {{r0, r1}, {r2, r3}};
+    off[p] = swizzle_off((uint32_t)((c * box_rows + lrow) * geo.inner + unit * 16), geo.mask);
+  }
+}
+
+// The codes of one k-unit for this lane (kunit_offsets): a[p][0..3] are
+// row g unit q, row g+8 unit q, row g unit q+1, row g+8 unit q+1 (q = 2p).
+__device__ __forceinline__ void kunit_load(uint32_t tile, const uint32_t (&off)[2], uint32_t (&a)[2][4]) {
+#pragma unroll
+  for (int p = 0; p < 2; ++p) ldmatrix_x4(tile + off[p], a[p][0], a[p][1], a[p][2], a[p][3]);
+}
+
+// One k-unit (128 k) of a 16-row m-tile against NB n-blocks of B, from the
+// codes of kunit_load and the scales of unit_scales (rows g and g+8).
+template <int NB>
+__device__ __forceinline__ void kunit_mma_regs(const uint32_t (&a)[2][4], const uint32_t (&sg)[4],
+                                               const uint32_t (&sh)[4], const uint32_t (&b)[NB][16],
+                                               float (&acc0)[NB][4], float (&acc1)[NB][4]) {
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    const uint32_t rq[2][2] = {{a[p][0], a[p][1]}, {a[p][2], a[p][3]}};
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int q = 2 * p + h;
@@ -211,7 +320,7 @@ __device__ __forceinline__ void kunit_mma(uint32_t tile, const TileGeo& geo, int
         dh[i] = hmul2(dh[i], sh[q]);
       }
 #pragma unroll
-      for (int nb = 0; nb < NB; ++nb) {  // two independent accumulation chains
+      for (int nb = 0; nb < NB; ++nb) {
         mma_f16(acc0[nb], dg[0], dh[0], dg[1], dh[1], b[nb][q * 4 + 0], b[nb][q * 4 + 1]);
         mma_f16(acc1[nb], dg[2], dh[2], dg[3], dh[3], b[nb][q * 4 + 2], b[nb][q * 4 + 3]);
       }
@@ -219,8 +328,18 @@ __device__ __forceinline__ void kunit_mma(uint32_t tile, const TileGeo& geo, int
   }
 }
 
-// Item kinds of a CTA's sequence.
-constexpr int kShGU = 0, kRtGU = 1, kDN = 2;
+// kunit_mma_regs straight from shared memory.
+template <int NB>
+__device__ __forceinline__ void kunit_mma_at(uint32_t tile, const uint32_t (&off)[2], const uint32_t (&sg)[4],
+                                             const uint32_t (&sh)[4], const uint32_t (&b)[NB][16],
+                                             float (&acc0)[NB][4], float (&acc1)[NB][4]) {
+  uint32_t a[2][4];
+  kunit_load(tile, off, a);
+  kunit_mma_regs<NB>(a, sg, sh, b, acc0, acc1);
+}
+
+// Item kinds of a CTA's sequence (in this order).
+constexpr int kShGU = 0, kRtGU = 1, kDN = 2, kEnd = 3;
 
 struct Item {
   int kind;
@@ -228,75 +347,171 @@ struct Item {
   int tile;  // m-tile (gate/up, 16 rows) or hidden tile (down, 64 rows)
 };
 
-// The CTA's work: n_shb shared gate/up items (round-robin over CTAs), a
-// contiguous range of routed gate/up items balanced against them, then a
-// contiguous range of down items.
+// Items before part c when n items are dealt to `parts` parts as evenly as
+// possible, the low parts taking one more.
+__device__ __forceinline__ int split_before(int c, int n, int parts) { return c * (n / parts) + min(c, n % parts); }
+
+// The CTA's work: n_shb shared gate/up items (round-robin over CTAs: shared
+// item j goes to CTA j mod grid, so they can be issued before the routing is
+// known), a contiguous range [gu0, gu1) of the routed gate/up items, then a
+// contiguous range [dn0, dn1) of the down items.  CTA c's gate/up total is
+// its even share of all of them; the CTAs holding an extra shared item are
+// low CTAs that also hold an extra total, so no routed count is negative and
+// the ranges are monotone.
 struct Plan {
   int n_shb, gu0, gu1, dn0, dn1;
 };
 
-__device__ __forceinline__ int shared_before(int b, int n_sh, int grid) {
-  return (n_sh / grid) * b + min(b, n_sh % grid);
-}
-
-__device__ Plan make_plan(int n_sh, int n_rgu, int n_dn) {
+__device__ __forceinline__ Plan make_plan(int n_sh, int n_rgu, int n_dn) {
   const int grid = gridDim.x, b = blockIdx.x;
+  const int T = n_sh + n_rgu;
   Plan p;
-  p.n_shb = shared_before(b + 1, n_sh, grid) - shared_before(b, n_sh, grid);
-  const long long T = n_sh + n_rgu;
-  // routed items before CTA c: its share of all gate/up items minus the
-  // shared items already placed on CTAs < c.  When every CTA's share is at
-  // least its shared items this is monotone in c; otherwise take the running
-  // maximum (small workloads only).
-  auto R0 = [&](int c) {
-    long long v = (long long)c * T / grid - shared_before(c, n_sh, grid);
-    return v < 0 ? 0LL : (v > n_rgu ? (long long)n_rgu : v);
-  };
-  auto R = [&](int c) {
-    if (T >= (long long)grid * ((n_sh + grid - 1) / grid + 1)) return (int)R0(c);
-    long long best = 0;
-    for (int d = 0; d <= c; ++d) best = max(best, R0(d));
-    return (int)best;
-  };
-  p.gu0 = R(b);
-  p.gu1 = (b + 1 == grid) ? n_rgu : R(b + 1);
-  p.dn0 = (int)(((long long)b * n_dn) / grid);
-  p.dn1 = (int)(((long long)(b + 1) * n_dn) / grid);
+  p.n_shb = split_before(b + 1, n_sh, grid) - split_before(b, n_sh, grid);
+  p.gu0 = split_before(b, T, grid) - split_before(b, n_sh, grid);
+  p.gu1 = split_before(b + 1, T, grid) - split_before(b + 1, n_sh, grid);
+  p.dn0 = split_before(b, n_dn, grid);
+  p.dn1 = split_before(b + 1, n_dn, grid);
   return p;
 }
 
 __device__ __forceinline__ int plan_len(const Plan& p) { return p.n_shb + (p.gu1 - p.gu0) + (p.dn1 - p.dn0); }
 
-__device__ __forceinline__ Item plan_item(const Plan& p, int l, int mt_per, int n_tiles, int has_sh, int G,
-                                          int n_sh, int grid) {
+// Walks a CTA's items in order with no division per item.  Routed gate/up
+// items are slot-major (mt_per tiles per slot); down items are slot-major
+// with the shared slot first.
+struct Seq {
+  Plan p;
+  int mt_per, n_tiles, G, has_sh;
+  int rt_slot, rt_tile, dn_slot, dn_tile;  // first routed gate/up and first down item
+};
+
+__device__ __forceinline__ Seq make_seq(const Plan& p, int mt_per, int n_tiles, int G, int has_sh) {
+  Seq s;
+  s.p = p;
+  s.mt_per = mt_per;
+  s.n_tiles = n_tiles;
+  s.G = G;
+  s.has_sh = has_sh;
+  s.rt_slot = p.gu0 / mt_per;
+  s.rt_tile = p.gu0 - s.rt_slot * mt_per;
+  const int si = p.dn0 / n_tiles;
+  s.dn_tile = p.dn0 - si * n_tiles;
+  s.dn_slot = has_sh ? (si == 0 ? G : si - 1) : si;
+  return s;
+}
+
+struct Cursor {
   Item it;
-  if (l < p.n_shb) {
-    it.kind = kShGU;
-    it.slot = G;
-    it.tile = blockIdx.x + l * grid;  // shared items are round-robin
-    (void)n_sh;
-    return it;
+  int left;  // items left in the current phase, this one included
+};
+
+__device__ __forceinline__ void seq_phase(Cursor& c, const Seq& s, int kind) {
+  for (; kind < kEnd; ++kind) {
+    if (kind == kShGU) {
+      c.left = s.p.n_shb;
+      c.it.slot = s.G;
+      c.it.tile = blockIdx.x;
+    } else if (kind == kRtGU) {
+      c.left = s.p.gu1 - s.p.gu0;
+      c.it.slot = s.rt_slot;
+      c.it.tile = s.rt_tile;
+    } else {
+      c.left = s.p.dn1 - s.p.dn0;
+      c.it.slot = s.dn_slot;
+      c.it.tile = s.dn_tile;
+    }
+    c.it.kind = kind;
+    if (c.left > 0) return;
   }
-  l -= p.n_shb;
-  if (l < p.gu1 - p.gu0) {
-    const int v = p.gu0 + l;
-    it.kind = kRtGU;
-    it.slot = v / mt_per;
-    it.tile = v % mt_per;
-    return it;
+  c.it.kind = kEnd;
+  c.left = 0;
+}
+
+__device__ __forceinline__ Cursor seq_begin(const Seq& s) {
+  Cursor c;
+  seq_phase(c, s, kShGU);
+  return c;
+}
+
+__device__ __forceinline__ void seq_next(Cursor& c, const Seq& s) {
+  if (--c.left > 0) {
+    if (c.it.kind == kShGU) {
+      c.it.tile += gridDim.x;
+    } else if (c.it.kind == kRtGU) {
+      if (++c.it.tile == s.mt_per) {
+        c.it.tile = 0;
+        ++c.it.slot;
+      }
+    } else if (++c.it.tile == s.n_tiles) {
+      c.it.tile = 0;
+      c.it.slot = (c.it.slot == s.G) ? 0 : c.it.slot + 1;
+    }
+    return;
   }
-  l -= p.gu1 - p.gu0;
-  const int v = p.dn0 + l;
-  const int si = v / n_tiles;
-  it.kind = kDN;
-  it.tile = v % n_tiles;
-  it.slot = (has_sh && si == 0) ? G : si - has_sh;
-  return it;
+  if (c.it.kind < kEnd) seq_phase(c, s, c.it.kind + 1);
+}
+
+// Everything the producer needs to issue an item's copies.
+struct IssueCtx {
+  const CUtensorMap *gate, *up, *down, *sgate, *sup, *sdown, *gate_s, *up_s, *sgate_s, *sup_s;
+  const unsigned char *down_scales, *sh_down_scales;
+  const int* uexp;  // distinct experts (shared memory)
+  int H, I, G, code3d;
+  uint64_t pol;
+};
+
+// Issue the TMA copies of one item into stage `stg`, completion on `bar`
+// (called by the whole producer warp).
+__device__ __forceinline__ void issue_item(const IssueCtx& c, const Item it, unsigned char* stg, uint64_t* bar,
+                                        int lane) {
+  const int H = c.H, I = c.I;
+  if (it.kind != kDN) {
+    const TileGeo geo = tile_geo(H);
+    const int code = kGURows * H / 2, scale = kGURows * H / 16;
+    const bool sh = it.kind == kShGU;
+    const int e = sh ? 0 : c.uexp[it.slot];
+    const int row0 = e * I + it.tile * kGURows;
+    const CUtensorMap* mg = sh ? c.sgate : c.gate;
+    const CUtensorMap* mu = sh ? c.sup : c.up;
+    const CUtensorMap* msg = sh ? c.sgate_s : c.gate_s;
+    const CUtensorMap* msu = sh ? c.sup_s : c.up_s;
+    const int chunks = (H / 2) / geo.inner;
+    if (lane == 0) mbar_arrive_expect_tx(bar, 2 * code + 2 * scale);
+    __syncwarp();
+    if (c.code3d) {  // one request per projection tile
+      if (lane == 0) tma_load_3d(stg, mg, 0, row0, 0, bar, c.pol);
+      else if (lane == 1) tma_load_3d(stg + code, mu, 0, row0, 0, bar, c.pol);
+    } else if (lane < chunks)
+      tma_load_2d(stg + lane * kGURows * geo.inner, mg, lane * geo.inner, row0, bar, c.pol);
+    else if (lane >= 16 && lane < 16 + chunks)
+      tma_load_2d(stg + code + (lane - 16) * kGURows * geo.inner, mu, (lane - 16) * geo.inner, row0, bar, c.pol);
+    if (lane == 30)
+      tma_load_2d(stg + 2 * code, msg, 0, row0, bar, c.pol);
+    else if (lane == 31)
+      tma_load_2d(stg + 2 * code + scale, msu, 0, row0, bar, c.pol);
+  } else {
+    const TileGeo geo = tile_geo(I);
+    const int code = kDNRows * I / 2, scale = kDNRows * I / 16;
+    const bool sh = it.slot == c.G;
+    const int e = sh ? 0 : c.uexp[it.slot];
+    const int row0 = e * H + it.tile * kDNRows;
+    const CUtensorMap* m = sh ? c.sdown : c.down;
+    const unsigned char* sp = sh ? c.sh_down_scales : c.down_scales;
+    const int chunks = (I / 2) / geo.inner;
+    if (lane == 0) mbar_arrive_expect_tx(bar, code + scale);
+    __syncwarp();
+    if (c.code3d) {
+      if (lane == 0) tma_load_3d(stg, m, 0, row0, 0, bar, c.pol);
+    } else if (lane < chunks)
+      tma_load_2d(stg + lane * kDNRows * geo.inner, m, lane * geo.inner, row0, bar, c.pol);
+    if (lane == 31) bulk_load(stg + code, sp + (size_t)row0 * (I / 16), scale, bar, c.pol);
+  }
+  __syncwarp();
 }
 
 }  // namespace
 
-template <int NB, int KUG, int KUD>
+template <int NB>
 __global__ void __launch_bounds__(kThreads, 1)
     k_moe_experts(const __grid_constant__ CUtensorMap tm_gate, const __grid_constant__ CUtensorMap tm_up,
                   const __grid_constant__ CUtensorMap tm_down, const __grid_constant__ CUtensorMap tm_sgate,
@@ -307,43 +522,50 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full_bar[kExpStages], empty_bar[kExpStages];
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
   __shared__ unsigned s_xamax[16];
+  __shared__ unsigned s_used[32];  // bitmask of the experts any row selected
+  __shared__ unsigned s_hpub;      // compute-warp arrivals at ends of gate/up slot runs (monotonic)
   __shared__ int s_abort, s_nu;
-  __shared__ float s_hinv[16];
 
   const int H = a.H, I = a.I, K = a.K, G = a.G, E = a.E, k = a.k;
+  const int S = a.stages;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  const TileGeo ggu = tile_geo(H), gdn = tile_geo(I);
-  const int gu_code = kGURows * H / 2, gu_scale = kGURows * H / 16;
-  const int dn_code = kDNRows * I / 2, dn_scale = kDNRows * I / 16;
   const int stage_bytes = expert_stage_bytes(H, I);
   const int mt_per = I / kGURows, n_tiles = H / kDNRows;
   const int n_sh = a.has_shared ? I / kGURows : 0;
   const int grid = gridDim.x;
-  const int smask = (H / 16 >= 128) ? 7 : (H / 16 == 64 ? 3 : (H / 16 == 32 ? 1 : 0));
 
-  float* red = reinterpret_cast<float*>(smem + kExpStages * stage_bytes);  // [2][8][2][NB][128]
-  unsigned char* rsm = reinterpret_cast<unsigned char*>(red + 2 * 8 * 2 * NB * 128);
+  // reduction slots (two, alternating by item): the compute warps' FP32
+  // partials, then 16 per-row inverse h scales (down items).  Warp w's block
+  // starts at w * kWarpStride + red_skew(w): the skew puts the partials that
+  // the 4 lanes of an epilogue quad read (warps 4j + 0..3) in distinct banks.
+  constexpr int kWarpStride = 2 * NB * 128 + 32;
+  constexpr int kRedPart = kCompWarps * kWarpStride;
+  constexpr int kRedFloats = kRedPart + 16;
+  auto red_at = [](int w) { return w * kWarpStride + 2 * (w & 1) + 16 * ((w >> 1) & 1); };
+  float* red = reinterpret_cast<float*>(smem + (size_t)S * stage_bytes);
+  unsigned char* rsm = reinterpret_cast<unsigned char*>(red + 2 * kRedFloats);
   // routing state (shared by all warps after the routing step)
-  float* s_w = reinterpret_cast<float*>(rsm);                // [K][k]
-  int* s_idx = reinterpret_cast<int*>(s_w + K * k);          // [K][k]
-  unsigned* s_rowmask = reinterpret_cast<unsigned*>(s_idx + K * k);  // [E]
-  int* s_pos = reinterpret_cast<int*>(s_rowmask + E);        // [E]
-  int* s_uexp = s_pos + E;                                   // [G+1]
-  float* s_tse = reinterpret_cast<float*>(s_uexp + G + 1);  // [E+1][3] tensor scales per expert (E = shared)
+  float* s_w = reinterpret_cast<float*>(rsm);                         // [K][k]
+  int* s_idx = reinterpret_cast<int*>(s_w + K * k);                   // [K][k]
+  unsigned* s_rowmask = reinterpret_cast<unsigned*>(s_idx + K * k);   // [E] rows that chose expert e
+  int* s_uexp = reinterpret_cast<int*>(s_rowmask + E);                // [G+1] distinct experts, ascending
+  float* s_tse = reinterpret_cast<float*>(s_uexp + G + 1);            // [E+1][3] tensor scales (E = shared)
   signed char* s_slot = reinterpret_cast<signed char*>(s_tse + 3 * (E + 1));  // [(G+1)*K]
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kExpStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], kExpWarps);
+      mbar_init(&empty_bar[s], kCompWarps);
     }
     s_abort = 0;
+    s_hpub = 0u;
     fence_mbar_init();
   }
   if (threadIdx.x < 16) s_xamax[threadIdx.x] = 0u;
+  if (threadIdx.x < 32) s_used[threadIdx.x] = 0u;
   __syncthreads();
 
   // optional timeline: globaltimer stamps of this CTA's milestones
@@ -352,126 +574,114 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (trace) trace[m] = global_timer_ns();
   };
   if (threadIdx.x == 0) stamp(0);
-  const uint64_t pol = policy_evict_first();
-  // Producer: issue the TMA copies of item l of `p` into its stage.
-  auto issue = [&](const Plan& p, int l, const Item& it) {
-    const int st = l % kExpStages;
-    unsigned char* stg = smem + st * stage_bytes;
-    if (it.kind != kDN) {
-      const bool sh = it.kind == kShGU;
-      const int e = sh ? 0 : s_uexp[it.slot];
-      const int row0 = e * I + it.tile * kGURows;
-      const CUtensorMap* mg = sh ? &tm_sgate : &tm_gate;
-      const CUtensorMap* mu = sh ? &tm_sup : &tm_up;
-      const CUtensorMap* msg = sh ? &tm_sgate_s : &tm_gate_s;
-      const CUtensorMap* msu = sh ? &tm_sup_s : &tm_up_s;
-      const int chunks = (H / 2) / ggu.inner;
-      if (lane == 0) mbar_arrive_expect_tx(&full_bar[st], 2 * gu_code + 2 * gu_scale);
-      __syncwarp();
-      if (a.code3d) {  // one request per projection tile
-        if (lane == 0) tma_load_3d(stg, mg, 0, row0, 0, &full_bar[st], pol);
-        else if (lane == 1) tma_load_3d(stg + gu_code, mu, 0, row0, 0, &full_bar[st], pol);
-      } else if (lane < chunks)
-        tma_load_2d(stg + lane * kGURows * ggu.inner, mg, lane * ggu.inner, row0, &full_bar[st], pol);
-      else if (lane >= 16 && lane < 16 + chunks)
-        tma_load_2d(stg + gu_code + (lane - 16) * kGURows * ggu.inner, mu, (lane - 16) * ggu.inner, row0,
-                    &full_bar[st], pol);
-      if (lane == 30)
-        tma_load_2d(stg + 2 * gu_code, msg, 0, row0, &full_bar[st], pol);
-      else if (lane == 31)
-        tma_load_2d(stg + 2 * gu_code + gu_scale, msu, 0, row0, &full_bar[st], pol);
-    } else {
-      const bool sh = it.slot == G;
-      const int e = sh ? 0 : s_uexp[it.slot];
-      const int row0 = e * H + it.tile * kDNRows;
-      const CUtensorMap* m = sh ? &tm_sdown : &tm_down;
-      const unsigned char* sp = sh ? a.sh_down.scales : a.down.scales;
-      const int chunks = (I / 2) / gdn.inner;
-      if (lane == 0) mbar_arrive_expect_tx(&full_bar[st], dn_code + dn_scale);
-      __syncwarp();
-      if (a.code3d) {
-        if (lane == 0) tma_load_3d(stg, m, 0, row0, 0, &full_bar[st], pol);
-      } else if (lane < chunks)
-        tma_load_2d(stg + lane * kDNRows * gdn.inner, m, lane * gdn.inner, row0, &full_bar[st], pol);
-      if (lane == 31)
-        bulk_load(stg + dn_code, sp + (size_t)row0 * (I / 16), dn_scale, &full_bar[st], pol);
-    }
-    __syncwarp();
+  auto fail = [&]() {
+    s_abort = 1;
+    set_error(a.ws.err, MOE_ERR_DEVICE_TIMEOUT);
   };
+  auto aborted = [&]() { return *reinterpret_cast<volatile int*>(&s_abort) != 0; };
+  // a bounded wait whose outcome is the same on every lane of the warp
+  auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, a.wait_ns, &s_abort));
+    if (!ok && lane == 0) fail();
+    return ok;
+  };
+  // The CTA's item sequence, from the distinct-expert count.
+  auto make_cta_seq = [&]() {
+    const int n_u = *reinterpret_cast<volatile int*>(&s_nu);
+    const int n_slots = n_u + (a.has_shared ? 1 : 0);
+    return make_seq(make_plan(n_sh, n_u * mt_per, n_slots * n_tiles), mt_per, n_tiles, G, a.has_shared);
+  };
+  // all gate/up items of a slot are published: one count per item, summed
+  // over the CTAs that hold items of the slot
+  const unsigned gu_target = (unsigned)mt_per;
 
   // ---------------------------------------------------------------- before the dependency wait
   // The shared items of this CTA come first in its sequence and need no routing.
-  Plan pre;
-  pre.n_shb = shared_before(blockIdx.x + 1, n_sh, grid) - shared_before(blockIdx.x, n_sh, grid);
-  pre.gu0 = pre.gu1 = pre.dn0 = pre.dn1 = 0;
+  const int n_shb = split_before(blockIdx.x + 1, n_sh, grid) - split_before(blockIdx.x, n_sh, grid);
   int issued = 0;
-  if (warp == kExpWarps) {
+  IssueCtx ic;
+  if (warp == kProducerWarp) {
+    ic.gate = &tm_gate;
+    ic.up = &tm_up;
+    ic.down = &tm_down;
+    ic.sgate = &tm_sgate;
+    ic.sup = &tm_sup;
+    ic.sdown = &tm_sdown;
+    ic.gate_s = &tm_gate_s;
+    ic.up_s = &tm_up_s;
+    ic.sgate_s = &tm_sgate_s;
+    ic.sup_s = &tm_sup_s;
+    ic.down_scales = a.down.scales;
+    ic.sh_down_scales = a.sh_down.scales;
+    ic.uexp = s_uexp;
+    ic.H = H;
+    ic.I = I;
+    ic.G = G;
+    ic.code3d = a.code3d;
+    ic.pol = policy_evict_first();
     if (lane == 0) {
       prefetch_tensormap(&tm_gate);
       prefetch_tensormap(&tm_up);
       prefetch_tensormap(&tm_down);
+      prefetch_tensormap(&tm_gate_s);
+      prefetch_tensormap(&tm_up_s);
     }
-    for (; issued < pre.n_shb && issued < kExpStages; ++issued)
-      issue(pre, issued, plan_item(pre, issued, mt_per, n_tiles, a.has_shared, G, n_sh, grid));
-  }
-
-  // activations (the block input is complete before the router kernel started)
-  uint32_t bx[KUG][NB][16];
-  if (warp < kExpWarps) {
-    for (int e = threadIdx.x; e < E; e += kConsumerThreads) s_rowmask[e] = 0u;
-    for (int i = threadIdx.x; i < (G + 1) * K; i += kConsumerThreads) s_slot[i] = -1;
-    for (int e = threadIdx.x; e <= E; e += kConsumerThreads) {  // tensor scales, slot E = shared
+    Item it;
+    it.kind = kShGU;
+    it.slot = G;
+    it.tile = blockIdx.x;
+    for (; issued < n_shb && issued < S; ++issued, it.tile += grid)
+      issue_item(ic, it, smem + (size_t)issued * stage_bytes, &full_bar[issued], lane);
+  } else {
+    const int tid = threadIdx.x;
+    for (int e = tid; e < E; e += kCompThreads) s_rowmask[e] = 0u;
+    for (int i = tid; i < (G + 1) * K; i += kCompThreads) s_slot[i] = -1;
+    for (int e = tid; e <= E; e += kCompThreads) {  // tensor scales, slot E = shared
       const bool shx = e == E;
       if (shx && !a.has_shared) continue;
       s_tse[3 * e + 0] = shx ? a.sh_gate.tscale[0] : a.gate.tscale[e];
       s_tse[3 * e + 1] = shx ? a.sh_up.tscale[0] : a.up.tscale[e];
       s_tse[3 * e + 2] = shx ? a.sh_down.tscale[0] : a.down.tscale[e];
     }
-    uint4 raw[KUG][NB][4];
-    const int KU = H / 128;
+  }
+
+  // activations (the block input is complete before the router kernel
+  // started): compute warp w holds k-unit w of every row as FP16 B
+  // fragments; the row maxima now, the fragments after the routing, while
+  // the first weight tiles are in flight
+  auto load_x = [&](uint4 (&raw)[NB][4]) {
 #pragma unroll
-    for (int j = 0; j < KUG; ++j) {
-      const int ku = warp + kExpWarps * j;
+    for (int nb = 0; nb < NB; ++nb) {
+      const int n = nb * 8 + g;
 #pragma unroll
-      for (int nb = 0; nb < NB; ++nb) {
-        const int n = nb * 8 + g;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (ku < KU && n < K) v = *reinterpret_cast<const uint4*>(a.x + (size_t)n * H + ku * 128 + q * 32 + 8 * t);
-          raw[j][nb][q] = v;
-        }
+      for (int q = 0; q < 4; ++q) {
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (warp < H / 128 && n < K) v = *reinterpret_cast<const uint4*>(a.x + (size_t)n * H + warp * 128 + q * 32 + 8 * t);
+        raw[nb][q] = v;
       }
     }
+  };
+  if (warp < kCompWarps) {
+    uint4 raw[NB][4];
+    load_x(raw);
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
       unsigned mx = 0;
 #pragma unroll
-      for (int j = 0; j < KUG; ++j)
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t w4[4] = {raw[nb][q].x, raw[nb][q].y, raw[nb][q].z, raw[nb][q].w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t w4[4] = {raw[j][nb][q].x, raw[j][nb][q].y, raw[j][nb][q].z, raw[j][nb][q].w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            mx = max(mx, (w4[i] << 16) & 0x7FFFFFFFu);
-            mx = max(mx, w4[i] & 0x7FFF0000u);
-          }
+        for (int i = 0; i < 4; ++i) {
+          mx = max(mx, (w4[i] << 16) & 0x7FFFFFFFu);
+          mx = max(mx, w4[i] & 0x7FFF0000u);
         }
+      }
       mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
       mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
       const int n = nb * 8 + g;
       if (t == 0 && n < K) atomicMax(&s_xamax[n], mx);
     }
-    consumer_bar();
-#pragma unroll
-    for (int nb = 0; nb < NB; ++nb) {
-      const int n = nb * 8 + g;
-      const float sc = (n < K) ? pow2f(row_shift(s_xamax[n])) : 1.f;
-#pragma unroll
-      for (int j = 0; j < KUG; ++j)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) bf16x8_to_f16x8(raw[j][nb][q], sc, &bx[j][nb][q * 4]);
-    }
+    comp_bar();  // routing tables cleared before any warp marks them
   }
 
   if (threadIdx.x == 0) stamp(1);
@@ -479,9 +689,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) stamp(2);
 
   // ---------------------------------------------------------------- routing (every CTA, identical)
-  if (warp < kExpWarps) {
+  if (warp < kCompWarps) {
     const bool fast = E <= 256 && k <= 8;
-    for (int r = warp; r < K; r += kExpWarps) {
+    for (int r = warp; r < K; r += kCompWarps) {
       if (fast) {
         unsigned long long v[8];
 #pragma unroll
@@ -489,9 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int e = lane + 32 * i;
           v[i] = (e < E) ? sel_key(__ldcg(a.logits + (size_t)r * E + e), e) : 0ull;
         }
-        if (threadIdx.x == 0) stamp(10);
         warp_top8(v);
-        if (threadIdx.x == 0) stamp(11);
         if (lane == 0) {
 #pragma unroll
           for (int s = 0; s < 8; ++s)
@@ -501,53 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
       } else {
-        float lv[32];
-        unsigned taken = 0;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int e = lane + 32 * i;
-          lv[i] = (e < E) ? __ldcg(a.logits + (size_t)r * E + e) : -INFINITY;
-        }
-        for (int s = 0; s < k; ++s) {
-          float bv = -INFINITY;
-          int be = INT_MAX;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int e = lane + 32 * i;
-            if (e < E && !((taken >> i) & 1u) && ranks_before(lv[i], e, bv, be)) {
-              bv = lv[i];
-              be = e;
-            }
-          }
-#pragma unroll
-          for (int d = 16; d >= 1; d >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, d);
-            if (ranks_before(ov, oe, bv, be)) {
-              bv = ov;
-              be = oe;
-            }
-          }
-          if (be == INT_MAX) {  // only NaN logits left: lowest free index
-            int f = INT_MAX;
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (lane + 32 * i < E && !((taken >> i) & 1u)) f = min(f, lane + 32 * i);
-#pragma unroll
-            for (int d = 16; d >= 1; d >>= 1) f = min(f, __shfl_xor_sync(0xffffffffu, f, d));
-            be = f;
-            float mine = 0.f;
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (lane + 32 * i == be) mine = lv[i];
-            bv = __shfl_sync(0xffffffffu, mine, be & 31);
-          }
-          if ((be & 31) == lane) taken |= 1u << (be >> 5);
-          if (lane == 0) {
-            s_idx[r * k + s] = be;
-            s_w[r * k + s] = bv;  // logit for now
-          }
-        }
+        topk_general(a.logits + (size_t)r * E, E, k, s_idx + r * k, s_w + r * k, lane);
       }
       __syncwarp();
       const float m = s_w[r * k];
@@ -557,346 +719,440 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int d = 16; d >= 1; d >>= 1) z += __shfl_xor_sync(0xffffffffu, z, d);
       __syncwarp();
       if (lane < k) {
+        const int e = s_idx[r * k + lane];
         s_w[r * k + lane] = ev / z;
-        atomicOr(&s_rowmask[s_idx[r * k + lane]], 1u << r);
+        atomicOr(&s_rowmask[e], 1u << r);
+        atomicOr(&s_used[e >> 5], 1u << (e & 31));
       }
     }
-    if (threadIdx.x == 0) stamp(12);
-    // grouping: distinct experts ascending, (row, slot) per expert
-    consumer_bar();
+    comp_bar();
     if (threadIdx.x == 0) stamp(13);
-    if (warp == 0) {  // one warp: lane l owns experts [l*CH, l*CH + CH), scan in lane order
-      const int CH = (E + 31) / 32;
-      const int e0 = lane * CH;
-      int cnt = 0;
-      for (int e = e0; e < min(E, e0 + CH); ++e) cnt += s_rowmask[e] != 0u;
-      int inc = cnt;
+    // grouping: the distinct experts in ascending order are the set bits of
+    // s_used; an expert's position is the number of set bits before it
+    // (every warp forms the per-word prefix itself: no further barrier)
+    const int n_words = (E + 31) >> 5;
+    const unsigned used = lane < n_words ? s_used[lane] : 0u;
+    const int cnt = __popc(used);
+    int inc = cnt;
 #pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, inc, d);
-        if (lane >= d) inc += o;
-      }
-      int u = inc - cnt;
-      for (int e = e0; e < min(E, e0 + CH); ++e)
-        if (s_rowmask[e]) {
-          s_pos[e] = u;
-          s_uexp[u] = e;
-          ++u;
-        }
+    for (int d = 1; d < 32; d <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, inc, d);
+      if (lane >= d) inc += o;
+    }
+    const int excl = inc - cnt;
+    if (warp == 0) {
+      int u = excl;
+      for (unsigned m = used; m; m &= m - 1) s_uexp[u++] = lane * 32 + __ffs(m) - 1;
       if (lane == 31) s_nu = inc;
+      if (lane == 0) s_uexp[G] = E;  // the shared expert's scales sit at index E
     }
-    consumer_bar();
-    for (int q = threadIdx.x; q < K * k; q += kConsumerThreads)
-      s_slot[s_pos[s_idx[q]] * K + q / k] = (signed char)(q % k);
+    for (int base = 0; base < K * k; base += kCompThreads) {
+      const int q = base + (int)threadIdx.x;
+      const int e = q < K * k ? s_idx[q] : 0;
+      const int pre_w = __shfl_sync(0xffffffffu, excl, (e >> 5) & 31);
+      const unsigned uw = __shfl_sync(0xffffffffu, used, (e >> 5) & 31);
+      if (q < K * k) {
+        const int u = pre_w + __popc(uw & ((1u << (e & 31)) - 1u));
+        s_slot[u * K + q / k] = (signed char)(q % k);
+      }
+    }
     if (a.has_shared)
-      for (int r = threadIdx.x; r < K; r += kConsumerThreads) s_slot[G * K + r] = (signed char)k;
-    if (threadIdx.x < 1) s_uexp[G] = E;  // the shared expert's scales sit at index E
-    if (threadIdx.x == 0) stamp(14);
-    consumer_bar();
-    if (threadIdx.x == 0) stamp(15);
-    // the routing outputs of the call (one CTA writes them)
-    if (blockIdx.x == 0) {
-      for (int q = threadIdx.x; q < K * k; q += kConsumerThreads) {
-        if (a.idx_out) a.idx_out[q] = s_idx[q];
-        if (a.w_out) a.w_out[q] = s_w[q];
-      }
-      if (a.group_out) {
-        const int nu = s_nu;
-        int* go = a.group_out;
-        if (threadIdx.x == 0) {
-          go[0] = nu;
-          go[1 + 2 * G] = K * k;
-        }
-        for (int v = threadIdx.x; v < G; v += kConsumerThreads) {
-          go[1 + v] = v < nu ? s_uexp[v] : -1;
-          int o = 0;  // pairs of the experts before v
-          for (int u = 0; u < v && u < nu; ++u) o += __popc(s_rowmask[s_uexp[u]]);
-          go[1 + G + v] = o;
-          if (v < nu) {
-            const int ex = s_uexp[v];
-            for (int r = 0; r < K; ++r) {
-              if (!((s_rowmask[ex] >> r) & 1u)) continue;
-              go[2 + 2 * G + o] = r * k + s_slot[v * K + r];
-              ++o;
-            }
-          }
-        }
-      }
-    }
+      for (int r = threadIdx.x; r < K; r += kCompThreads) s_slot[G * K + r] = (signed char)k;
   }
   __syncthreads();
   pdl_launch_dependents();
   if (threadIdx.x == 0) stamp(3);
 
-  const int n_u = s_nu;
-  const int n_slots = n_u + (a.has_shared ? 1 : 0);
-  const Plan plan = make_plan(n_sh, n_u * mt_per, n_slots * n_tiles);
-  const int L = plan_len(plan);
-
-  if (warp == kExpWarps) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
-    for (int l = issued; l < L; ++l) {
-      const int st = l % kExpStages;
-      int ok = 1;
-      if (lane == 0 && l >= kExpStages) {
-        if (!mbar_wait_bounded(&empty_bar[st], ((l / kExpStages) - 1) & 1, a.wait_ns, &s_abort)) {
-          ok = 0;
-          s_abort = 1;
-          set_error(a.ws.err, MOE_ERR_DEVICE_TIMEOUT);
-        }
+    // Issues the copies of every item into the ring, and publishes each
+    // finished gate/up slot run of this CTA (a release at GPU scope on the
+    // slot's counter) once every compute warp has stored its h rows: the
+    // fences of the publication stay off the compute warps.
+    const Seq seq = make_cta_seq();
+    const int L = plan_len(seq.p);
+    const int L_gu = seq.p.n_shb + (seq.p.gu1 - seq.p.gu0);
+    Cursor cur = seq_begin(seq);
+    for (int l = 0; l < issued; ++l) seq_next(cur, seq);
+    // publication events: the runs of equal slot among the gate/up items
+    Cursor pc = seq_begin(seq);
+    int pl = 0, n_ev = 0;
+    int ev_slot = -1;
+    unsigned ev_count = 0;
+    auto next_event = [&]() {
+      ev_slot = -1;
+      ev_count = 0;
+      if (pl >= L_gu) return;
+      ev_slot = pc.it.slot;
+      while (pl < L_gu && pc.it.slot == ev_slot) {
+        ++ev_count;
+        ++pl;
+        seq_next(pc, seq);
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok || s_abort) break;
-      issue(plan, l, plan_item(plan, l, mt_per, n_tiles, a.has_shared, G, n_sh, grid));
-      issued = l + 1;
-    }
-    if (lane == 0 && trace) trace[9] = global_timer_ns();
-    if (lane == 0) {
-      for (int j = (issued > kExpStages ? issued - kExpStages : 0); j < issued; ++j)
-        mbar_wait_bounded(&full_bar[j % kExpStages], (j / kExpStages) & 1, kDrainNs, &s_abort);
-    }
-    return;
-  }
-
-  // -------------------------------------------------------------- consumers
-  const int KUgu = H / 128, KUdn = I / 128;
-  // gate/up items publish per epilogue warp (4 * NB of them), down items
-  // count per consumer warp (8), so neither needs a second CTA barrier
-  const unsigned gu_target = (unsigned)(mt_per * 4 * NB);
-  int pub_slot = -1;      // slot whose finished gate/up items are not yet published
-  unsigned pub_count = 0;  // how many of them (this warp's share of each)
-  uint32_t bh[KUD][NB][16];
-  int cur_slot = -1;
-  const int mt = warp & 3, kh = warp >> 2;  // down: m-tile of 16 rows, k-half
-  const int L_gu = plan.n_shb + (plan.gu1 - plan.gu0);  // all gate/up items precede the down items
-  for (int l = 0; l < L_gu; ++l) {
-    const Item it = plan_item(plan, l, mt_per, n_tiles, a.has_shared, G, n_sh, grid);
-    const int st = l % kExpStages;
-    unsigned char* stg = smem + st * stage_bytes;
-    float* rb = red + (size_t)(l & 1) * (8 * 2 * NB * 128);
-    {
-      // ------------------------------------------------ gate/up item
-      const bool ok = mbar_wait_bounded(&full_bar[st], (l / kExpStages) & 1, a.wait_ns, &s_abort);
-      if (threadIdx.x == 0 && l < 11) stamp(16 + 4 * l);
-      if (!ok && lane == 0) {
-        s_abort = 1;
-        set_error(a.ws.err, MOE_ERR_DEVICE_TIMEOUT);
-      }
-      float ag[NB][4], au[NB][4], ag1[NB][4], au1[NB][4];
-#pragma unroll
-      for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) ag[nb][i] = au[nb][i] = ag1[nb][i] = au1[nb][i] = 0.f;
-      if (ok) {
-        const uint32_t tg = smem_addr(stg), tu = smem_addr(stg + gu_code);
-        const unsigned char* sgt = stg + 2 * gu_code;
-        const unsigned char* sut = stg + 2 * gu_code + gu_scale;
-        const int sstride = H / 16;
-#pragma unroll
-        for (int j = 0; j < KUG; ++j) {
-          const int ku = warp + kExpWarps * j;
-          if (ku < KUgu) {
-            uint32_t s0[4], s1[4], u0[4], u1[4];
-            const uint32_t o0 = swizzle_off((uint32_t)(g * sstride + 8 * ku), smask);
-            const uint32_t o1 = swizzle_off((uint32_t)((g + 8) * sstride + 8 * ku), smask);
-            unit_scales(*reinterpret_cast<const uint2*>(sgt + o0), t, s0);
-            unit_scales(*reinterpret_cast<const uint2*>(sgt + o1), t, s1);
-            unit_scales(*reinterpret_cast<const uint2*>(sut + o0), t, u0);
-            unit_scales(*reinterpret_cast<const uint2*>(sut + o1), t, u1);
-            kunit_mma<NB>(tg, ggu, kGURows, 0, ku, s0, s1, bx[j], ag, ag1, lane);
-            kunit_mma<NB>(tu, ggu, kGURows, 0, ku, u0, u1, bx[j], au, au1, lane);
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[st]);
-      if (threadIdx.x == 0 && l < 11) stamp(17 + 4 * l);
-#pragma unroll
-      for (int nb = 0; nb < NB; ++nb) {
-        *reinterpret_cast<float4*>(rb + ((warp * 2 + 0) * NB + nb) * 128 + lane * 4) =
-            make_float4(ag[nb][0] + ag1[nb][0], ag[nb][1] + ag1[nb][1], ag[nb][2] + ag1[nb][2],
-                        ag[nb][3] + ag1[nb][3]);
-        *reinterpret_cast<float4*>(rb + ((warp * 2 + 1) * NB + nb) * 128 + lane * 4) =
-            make_float4(au[nb][0] + au1[nb][0], au[nb][1] + au1[nb][1], au[nb][2] + au1[nb][2],
-                        au[nb][3] + au1[nb][3]);
-      }
-      consumer_bar();
-      if (threadIdx.x == 0 && l < 11) stamp(18 + 4 * l);
-      if (s_abort) break;
-      // epilogue: 128 * NB threads; with NB = 1 the two halves of the warps
-      // take turns, so each warp's epilogue overlaps the other half's compute
-      const int etid = (NB == 1) ? (int)threadIdx.x - 128 * (l & 1) : (int)threadIdx.x;
-      if (etid >= 0 && etid < 128 * NB) {
-        const int nb = etid >> 7, o = etid & 127;
-        const int i = o >> 3, c = o & 7;
-        const int n = nb * 8 + c;
-        if (n < K) {
-          const int fl = (i & 7) * 4 + (c >> 1), fe = (i >> 3) * 2 + (c & 1);
-          float gs = 0.f, us = 0.f;
-#pragma unroll
-          for (int w = 0; w < kExpWarps; ++w) {
-            gs += rb[((w * 2 + 0) * NB + nb) * 128 + fl * 4 + fe];
-            us += rb[((w * 2 + 1) * NB + nb) * 128 + fl * 4 + fe];
-          }
-          const float inv = pow2f(-row_shift(s_xamax[n]));
-          const int ex = s_uexp[it.slot];
-          const float gv = gs * inv * s_tse[3 * ex + 0];
-          const float uv = us * inv * s_tse[3 * ex + 1];
-          const float hv = gv / (1.f + expf(-gv)) * uv;
-          const uint16_t hb = float_to_bf16_bits(hv);
-          a.ws.h[((size_t)it.slot * K + n) * I + it.tile * kGURows + i] = hb;
-          atomicMax(&a.ws.hamax[it.slot * K + n], (unsigned)(hb & 0x7FFFu));
-        }
-        pub_slot = it.slot;
-        ++pub_count;
-      }
-      // publish finished items once per slot: at the last item of a slot
-      // every warp with items of that slot releases its count (the warp sync
-      // makes the release cover every lane's h writes)
-      const bool boundary =
-          l + 1 == L_gu || plan_item(plan, l + 1, mt_per, n_tiles, a.has_shared, G, n_sh, grid).slot != it.slot;
-      if (boundary && pub_count) {
-        __syncwarp();
-        if (lane == 0) red_release_add(&a.ws.done[pub_slot], pub_count);
-        pub_count = 0;
-      }
-      if (threadIdx.x == 0) stamp(4);
-      if (threadIdx.x == 0 && l < 11) stamp(19 + 4 * l);
-    }
-  }
-  for (int l = L_gu; l < L && !s_abort; ++l) {
-    const Item it = plan_item(plan, l, mt_per, n_tiles, a.has_shared, G, n_sh, grid);
-    const int st = l % kExpStages;
-    unsigned char* stg = smem + st * stage_bytes;
-    float* rb = red + (size_t)(l & 1) * (8 * 2 * NB * 128);
-    {
-      // ------------------------------------------------ down item
-      if (it.slot != cur_slot) {
-        cur_slot = it.slot;
-        if (threadIdx.x == 0) {
+    };
+    next_event();
+    // lane 0: publish every event whose h rows are complete (wait for the
+    // next one when `block`)
+    auto publish = [&](bool block) {
+      while (ev_slot >= 0) {
+        const unsigned need = (unsigned)kCompWarps * (unsigned)(n_ev + 1);
+        bool ready = ld_acquire_cta(&s_hpub) >= need;
+        if (!ready && block) {
           const uint64_t t0 = global_timer_ns();
-          bool ready = false;
-          while (!(ready = ld_acquire(&a.ws.done[it.slot]) >= gu_target)) {
-            if (s_abort || a.wait_ns == 0 || global_timer_ns() - t0 > a.wait_ns) break;
+          while (!(ready = ld_acquire_cta(&s_hpub) >= need)) {
+            if (aborted() || a.wait_ns == 0 || global_timer_ns() - t0 > a.wait_ns) break;
+            __nanosleep(128);
           }
-          if (!ready) {
-            s_abort = 1;
-            set_error(a.ws.err, MOE_ERR_DEVICE_TIMEOUT);
-          }
-          if (trace && trace[5] == 0) {
-            trace[5] = t0;
-            trace[6] = global_timer_ns();
-          }
+          if (!ready) fail();
         }
-        consumer_bar();
-        if (s_abort) break;
-        if (threadIdx.x < K)
-          s_hinv[threadIdx.x] = pow2f(-row_shift(__ldcg(a.ws.hamax + it.slot * K + threadIdx.x) << 16));
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-          const int n = nb * 8 + g;
-          const float sc = (n < K) ? pow2f(row_shift(__ldcg(a.ws.hamax + it.slot * K + n) << 16)) : 1.f;
-#pragma unroll
-          for (int j = 0; j < KUD; ++j) {
-            const int ku = kh + 2 * j;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint4 v = make_uint4(0, 0, 0, 0);
-              if (ku < KUdn && n < K)
-                v = __ldcg(reinterpret_cast<const uint4*>(a.ws.h + ((size_t)it.slot * K + n) * I + ku * 128 +
-                                                          q * 32 + 8 * t));
-              bf16x8_to_f16x8(v, sc, &bh[j][nb][q * 4]);
+        if (!ready) return;
+        red_release_add(&a.ws.done[ev_slot], ev_count);
+        ++n_ev;
+        next_event();
+      }
+    };
+    int pass = issued / S, st = issued - pass * S;  // item l goes to stage l % S on pass l / S
+    for (int l = issued; l < L; ++l, seq_next(cur, seq)) {
+      int ok = 1;
+      if (lane == 0) {
+        // wait for the stage, publishing meanwhile: a compute warp may be
+        // waiting for this CTA's own publication before it frees a stage
+        publish(false);
+        if (pass > 0) {
+          const uint64_t t0 = global_timer_ns();
+          while (!mbar_try_wait_sleep(&empty_bar[st], (pass - 1) & 1, 500u)) {
+            publish(false);
+            if (aborted() || a.wait_ns == 0 || global_timer_ns() - t0 > a.wait_ns) {
+              ok = 0;
+              fail();
+              break;
             }
           }
         }
       }
-      const bool ok = mbar_wait_bounded(&full_bar[st], (l / kExpStages) & 1, a.wait_ns, &s_abort);
-      if (!ok && lane == 0) {
-        s_abort = 1;
-        set_error(a.ws.err, MOE_ERR_DEVICE_TIMEOUT);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      issue_item(ic, cur.it, smem + (size_t)st * stage_bytes, &full_bar[st], lane);
+      issued = l + 1;
+      if (++st == S) {
+        st = 0;
+        ++pass;
       }
-      float acc[NB][4], acc1[NB][4];
+    }
+    if (lane == 0 && trace) trace[9] = global_timer_ns();
+    if (lane == 0) {
+      if (!aborted()) publish(true);
+      // every copy of the last S items has landed before the CTA may exit
+      // (a stage is reissued only after the compute warps saw its previous
+      // copy complete, so older copies have landed)
+      for (int j = (issued > S ? issued - S : 0); j < issued; ++j)
+        mbar_wait_drain(&full_bar[j % S], (j / S) & 1, kDrainNs);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- compute warps
+  // Warp w owns k-unit w (128 k) of every gate/up item, and m-tile w % 4,
+  // k-unit w / 4 of every down item.  Per item: codes and scales to
+  // registers, the stage back to the producer, the MMAs, the FP32 partials
+  // to the item's reduction slot, one barrier of the compute warps, then each
+  // warp reduces its share of the item's outputs.  No wait ever leaves this
+  // loop early (a failed wait sets the abort flag and the remaining items run
+  // without work), so every compute warp meets every barrier.
+  {
+    uint32_t bx[NB][16];
+    {
+      uint4 raw[NB][4];
+      load_x(raw);
 #pragma unroll
-      for (int nb = 0; nb < NB; ++nb)
+      for (int nb = 0; nb < NB; ++nb) {
+        const int n = nb * 8 + g;
+        const float sc = (n < K) ? pow2f(row_shift(s_xamax[n])) : 1.f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) acc[nb][i] = acc1[nb][i] = 0.f;
-      if (ok) {
-        const uint32_t tc = smem_addr(stg);
-        const unsigned char* srow = stg + dn_code + (mt * 16 + g) * (I / 16);
+        for (int q = 0; q < 4; ++q) bf16x8_to_f16x8(raw[nb][q], sc, &bx[nb][q * 4]);
+      }
+    }
+    const int KUgu = H / 128, KUdn = I / 128;
+    const TileGeo ggu = tile_geo(H), gdn = tile_geo(I);
+    const int gu_code = kGURows * H / 2, gu_scale = kGURows * H / 16;
+    const int dn_code = kDNRows * I / 2;
+    const int smask = (H / 16 >= 128) ? 7 : (H / 16 == 64 ? 3 : (H / 16 == 32 ? 1 : 0));
+    const int sstride = H / 16;
+    const bool gu_active = warp < KUgu;
+    const uint32_t so0 = swizzle_off((uint32_t)(g * sstride + 8 * warp), smask);
+    const uint32_t so1 = swizzle_off((uint32_t)((g + 8) * sstride + 8 * warp), smask);
+    uint32_t goff[2];  // this lane's ldmatrix offsets in a gate/up codes tile
+    kunit_offsets(ggu, kGURows, 0, gu_active ? warp : 0, lane, goff);
+    const int q8 = lane >> 2, sub = lane & 3;  // epilogue: quad q8 = output column, sub = partial set
+    // this CTA's gate/up items: n_shb shared ones, then routed v = gu0..gu1-1
+    // (slot v / mt_per, tile v % mt_per); mt_per is a power of two
+    int L_gu, gu0;
+    {
+      const Plan p0 = make_cta_seq().p;
+      L_gu = p0.n_shb + (p0.gu1 - p0.gu0);
+      gu0 = p0.gu0;
+    }
+    const int lg_mt = __ffs(mt_per) - 1;
+    auto gu_slot = [&](int l) { return l < n_shb ? G : (gu0 + l - n_shb) >> lg_mt; };
+    int st = 0, fp = 0;  // item l: stage l % S on pass l / S
+    auto advance = [&]() {
+      if (++st == S) {
+        st = 0;
+        ++fp;
+      }
+    };
+    for (int l = 0; l < L_gu; ++l, advance()) {
+      unsigned char* stg = smem + (size_t)st * stage_bytes;
+      float* rb = red + (size_t)(l & 1) * kRedFloats;
+      const bool ok = warp_wait(&full_bar[st], fp & 1);
+      if (threadIdx.x == 0 && l < 9) stamp(16 + 4 * l);
+      // this warp's codes and scales to registers, then the stage goes back
+      uint32_t ag[2][4], au[2][4];
+      uint2 sr[4];
+      if (ok && gu_active) {
+        const uint32_t tg = smem_addr(stg);
+        kunit_load(tg, goff, ag);
+        kunit_load(tg + gu_code, goff, au);
+        const unsigned char* sgt = stg + 2 * gu_code;
+        sr[0] = *reinterpret_cast<const uint2*>(sgt + so0);
+        sr[1] = *reinterpret_cast<const uint2*>(sgt + so1);
+        sr[2] = *reinterpret_cast<const uint2*>(sgt + gu_scale + so0);
+        sr[3] = *reinterpret_cast<const uint2*>(sgt + gu_scale + so1);
+      }
+      __syncwarp();
+      if (ok && lane == 0) mbar_arrive(&empty_bar[st]);  // only a stage whose copy landed goes back
+      if (ok && gu_active) {
+        // gate and up inline: two independent chains
+        uint32_t s0[4], s1[4], u0[4], u1[4];
+        unit_scales(sr[0], t, s0);
+        unit_scales(sr[1], t, s1);
+        unit_scales(sr[2], t, u0);
+        unit_scales(sr[3], t, u1);
+        float cg[NB][4], cu[NB][4];
 #pragma unroll
-        for (int j = 0; j < KUD; ++j) {
-          const int ku = kh + 2 * j;
-          if (ku < KUdn) {
-            uint32_t s0[4], s1[4];
-            unit_scales(*reinterpret_cast<const uint2*>(srow + 8 * ku), t, s0);
-            unit_scales(*reinterpret_cast<const uint2*>(srow + 8 * (I / 16) + 8 * ku), t, s1);
-            kunit_mma<NB>(tc, gdn, kDNRows, mt * 16, ku, s0, s1, bh[j], acc, acc1, lane);
+        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) cg[nb][i] = cu[nb][i] = 0.f;
+        kunit_mma_regs<NB>(ag, s0, s1, bx, cg, cg);
+        kunit_mma_regs<NB>(au, u0, u1, bx, cu, cu);
+        float* wb = rb + red_at(warp) + lane * 4;
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          float* pg = wb + (0 * NB + nb) * 128;
+          float* pu = wb + (1 * NB + nb) * 128;
+          *reinterpret_cast<float2*>(pg) = make_float2(cg[nb][0], cg[nb][1]);
+          *reinterpret_cast<float2*>(pg + 2) = make_float2(cg[nb][2], cg[nb][3]);
+          *reinterpret_cast<float2*>(pu) = make_float2(cu[nb][0], cu[nb][1]);
+          *reinterpret_cast<float2*>(pu + 2) = make_float2(cu[nb][2], cu[nb][3]);
+        }
+      }
+      if (threadIdx.x == 0 && l < 9) stamp(17 + 4 * l);
+      comp_bar();
+      if (threadIdx.x == 0 && l < 9) stamp(18 + 4 * l);
+      // epilogue: warp w owns intermediate row w of the item's 16 rows, the
+      // quads of the warp its 8 (x NB) columns; a quad's 4 lanes each sum 4
+      // of the k-unit partials, then two xor steps sum the 4 in a fixed order
+      if (!aborted()) {
+        const int slot = gu_slot(l);
+        const int tile = l < n_shb ? (int)blockIdx.x + l * grid : ((gu0 + l - n_shb) & (mt_per - 1));
+        const int ex = s_uexp[slot];
+        const float tg = s_tse[3 * ex + 0], tu = s_tse[3 * ex + 1];
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          const int n = nb * 8 + q8;
+          const int f = nb * 128 + ((warp & 7) * 4 + (q8 >> 1)) * 4 + (warp >> 3) * 2 + (q8 & 1);
+          float pg[4], pu[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int w = sub + 4 * j;
+            pg[j] = w < KUgu ? rb[red_at(w) + f] : 0.f;
+            pu[j] = w < KUgu ? rb[red_at(w) + NB * 128 + f] : 0.f;
+          }
+          float gs = ((pg[0] + pg[1]) + pg[2]) + pg[3];
+          float us = ((pu[0] + pu[1]) + pu[2]) + pu[3];
+          gs += __shfl_xor_sync(0xffffffffu, gs, 1);
+          us += __shfl_xor_sync(0xffffffffu, us, 1);
+          gs += __shfl_xor_sync(0xffffffffu, gs, 2);
+          us += __shfl_xor_sync(0xffffffffu, us, 2);
+          if (sub == 0 && n < K) {
+            const float inv = pow2f(-row_shift(s_xamax[n]));
+            const float gv = gs * inv * tg;
+            const float uv = us * inv * tu;
+            const float hv = gv * __frcp_rn(1.f + expf(-gv)) * uv;
+            const uint16_t hb = float_to_bf16_bits(hv);
+            a.ws.h[((size_t)slot * K + n) * I + tile * kGURows + warp] = hb;
+            atomicMax(&a.ws.hamax[slot * K + n], (unsigned)(hb & 0x7FFFu));
+          }
+        }
+        // the last item of a slot run: this warp's h rows are stored
+        if (l + 1 == L_gu || gu_slot(l + 1) != slot) {
+          __syncwarp();
+          if (lane == 0) red_release_cta_shared_add(&s_hpub, 1u);
+        }
+      }
+      if (threadIdx.x == 0 && l < 9) stamp(19 + 4 * l);
+    }
+    // down items: 4 m-tiles of 16 rows x I/128 k-units over the 16 warps
+    {
+      const Seq seq = make_cta_seq();
+      const int L = plan_len(seq.p);
+      const int mt = warp & 3, kq = warp >> 2;
+      const bool dn_active = kq < KUdn;
+      uint32_t doff[2];  // this lane's ldmatrix offsets in a down codes tile
+      kunit_offsets(gdn, kDNRows, mt * 16, dn_active ? kq : 0, lane, doff);
+      uint32_t bh[NB][16];
+      float hinv = 1.f, hinv1 = 1.f;  // inverse h scales of rows g and 8 + g
+      int cur_slot = -1;
+      Cursor dc;
+      seq_phase(dc, seq, kDN);
+      for (int l = L_gu; l < L; ++l, seq_next(dc, seq), advance()) {
+        const Item it = dc.it;
+        unsigned char* stg = smem + (size_t)st * stage_bytes;
+        float* rb = red + (size_t)(l & 1) * kRedFloats;
+        bool ok = !aborted();
+        if (ok && it.slot != cur_slot) {
+          // h of this slot: every warp waits (bounded, no CTA barrier) until
+          // all gate/up items of the slot are published, then reads it as B
+          // fragments
+          cur_slot = it.slot;
+          int ready = 0;
+          if (lane == 0) {
+            const uint64_t t0 = global_timer_ns();
+            while (!(ready = ld_acquire(&a.ws.done[it.slot]) >= gu_target)) {
+              if (aborted() || a.wait_ns == 0 || global_timer_ns() - t0 > a.wait_ns) break;
+              __nanosleep(256);
+            }
+            if (!ready) fail();
+          }
+          ok = __shfl_sync(0xffffffffu, ready, 0) != 0;
+          if (ok) {
+            (void)ld_acquire(&a.ws.done[it.slot]);  // this lane's own acquire before it reads h
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+              const int n = nb * 8 + g;
+              const int sh = (n < K) ? row_shift(__ldcg(a.ws.hamax + it.slot * K + n) << 16) : 0;
+              const float sc = pow2f(sh);
+              if (nb == 0) hinv = pow2f(-sh);
+              else hinv1 = pow2f(-sh);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (dn_active && n < K)
+                  v = __ldcg(reinterpret_cast<const uint4*>(a.ws.h + ((size_t)it.slot * K + n) * I + kq * 128 +
+                                                            q * 32 + 8 * t));
+                bf16x8_to_f16x8(v, sc, &bh[nb][q * 4]);
+              }
+            }
+          }
+        }
+        const bool landed = warp_wait(&full_bar[st], fp & 1);
+        ok = landed && ok;
+        uint32_t ad[2][4];
+        uint2 sd0, sd1;
+        if (ok && dn_active) {
+          kunit_load(smem_addr(stg), doff, ad);
+          const unsigned char* srow = stg + dn_code + (mt * 16 + g) * (I / 16);
+          sd0 = *reinterpret_cast<const uint2*>(srow + 8 * kq);
+          sd1 = *reinterpret_cast<const uint2*>(srow + 8 * (I / 16) + 8 * kq);
+        }
+        __syncwarp();
+        if (landed && lane == 0) mbar_arrive(&empty_bar[st]);  // only a stage whose copy landed goes back
+        if (ok && dn_active) {
+          float c0[NB][4], c1[NB][4];
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) c0[nb][i] = c1[nb][i] = 0.f;
+          uint32_t s0[4], s1[4];
+          unit_scales(sd0, t, s0);
+          unit_scales(sd1, t, s1);
+          if (NB == 1)
+            kunit_mma_regs<NB>(ad, s0, s1, bh, c0, c1);
+          else
+            kunit_mma_regs<NB>(ad, s0, s1, bh, c0, c0);
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) {
+            float4 v;
+            if (NB == 1)
+              v = make_float4(c0[nb][0] + c1[nb][0], c0[nb][1] + c1[nb][1], c0[nb][2] + c1[nb][2],
+                              c0[nb][3] + c1[nb][3]);
+            else
+              v = make_float4(c0[nb][0], c0[nb][1], c0[nb][2], c0[nb][3]);
+            float* pd = rb + red_at(warp) + nb * 128 + lane * 4;
+            *reinterpret_cast<float2*>(pd) = make_float2(v.x, v.y);
+            *reinterpret_cast<float2*>(pd + 2) = make_float2(v.z, v.w);
+          }
+        }
+        if (warp == 0 && t == 0) {
+          rb[kRedPart + g] = hinv;
+          if (NB == 2) rb[kRedPart + 8 + g] = hinv1;
+        }
+        comp_bar();
+        // epilogue: thread (warp, lane) -> m-tile m, output (i, c) of each
+        // n-block; the k-unit partials of m-tile m sit at warps m, m+4, ...
+        if (!aborted()) {
+          const float ts = s_tse[3 * s_uexp[it.slot] + 2];
+          const int tid = (int)threadIdx.x;
+          const int m = tid >> 7, oo = tid & 127;
+          const int i = oo >> 3, c = oo & 7;
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) {
+            const int n = nb * 8 + c;
+            if (n >= K) continue;
+            const int s = s_slot[it.slot * K + n];
+            if (s < 0) continue;
+            const int f = nb * 128 + ((i & 7) * 4 + (c >> 1)) * 4 + (i >> 3) * 2 + (c & 1);
+            float v4[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) v4[q] = q < KUdn ? rb[red_at(q * 4 + m) + f] : 0.f;
+            const float v = ((v4[0] + v4[1]) + v4[2]) + v4[3];  // k-units in order
+            a.ws.dpart[((size_t)n * (k + 1) + s) * H + it.tile * kDNRows + m * 16 + i] = v * rb[kRedPart + n] * ts;
           }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[st]);
-#pragma unroll
-      for (int nb = 0; nb < NB; ++nb)
-        *reinterpret_cast<float4*>(rb + (warp * NB + nb) * 128 + lane * 4) =
-            make_float4(acc[nb][0] + acc1[nb][0], acc[nb][1] + acc1[nb][1], acc[nb][2] + acc1[nb][2],
-                        acc[nb][3] + acc1[nb][3]);
-      consumer_bar();
-      if (s_abort) break;
-      const float ts = s_tse[3 * s_uexp[it.slot] + 2];
-      for (int o = threadIdx.x; o < 4 * NB * 128; o += kConsumerThreads) {
-        const int m = o / (NB * 128), rem = o % (NB * 128);
-        const int nb = rem >> 7, oo = rem & 127;
-        const int i = oo >> 3, c = oo & 7;
-        const int n = nb * 8 + c;
-        if (n >= K) continue;
-        const int s = s_slot[it.slot * K + n];
-        if (s < 0) continue;
-        const int fl = (i & 7) * 4 + (c >> 1), fe = (i >> 3) * 2 + (c & 1);
-        const float v = rb[(m * NB + nb) * 128 + fl * 4 + fe] + rb[((m + 4) * NB + nb) * 128 + fl * 4 + fe];
-        a.ws.dpart[((size_t)n * (k + 1) + s) * H + it.tile * kDNRows + m * 16 + i] = v * s_hinv[n] * ts;
-      }
     }
   }
+
   // every CTA's partials are written: grid-wide barrier (the launch is
-  // cooperative, all CTAs are resident; the wait is bounded), then CTA b
-  // combines hidden tiles b, b + grid, ... :
+  // cooperative, all CTAs are resident; the wait is bounded), then the
+  // CTAs share the outputs:
   //   y = bf16(routed_scale * sum_s w_s d_s + d_shared + residual), slots in order
-  consumer_bar();
+  comp_bar();
   if (threadIdx.x == 0) {
     __threadfence();
     atomicAdd(a.ws.gridbar, 1u);
     const uint64_t t0 = global_timer_ns();
     while (ld_acquire(a.ws.gridbar) < (unsigned)grid) {
-      if (s_abort || a.wait_ns == 0 || global_timer_ns() - t0 > a.wait_ns) {
-        s_abort = 1;
-        set_error(a.ws.err, MOE_ERR_DEVICE_TIMEOUT);
+      if (aborted() || a.wait_ns == 0 || global_timer_ns() - t0 > a.wait_ns) {
+        fail();
         break;
       }
+      __nanosleep(64);
     }
     if (trace) trace[60] = global_timer_ns();
   }
-  consumer_bar();
-  if (!s_abort) {
-    for (int tile = blockIdx.x; tile < n_tiles; tile += grid) {
-      for (int o = threadIdx.x; o < K * kDNRows; o += kConsumerThreads) {
-        const int n = o / kDNRows, j = tile * kDNRows + o % kDNRows;
-        float acc2 = 0.f;
-        for (int s = 0; s < k; ++s)
-          acc2 = __fmaf_rn(s_w[n * k + s], __ldcg(a.ws.dpart + ((size_t)n * (k + 1) + s) * H + j), acc2);
-        float v = a.routed_scale * acc2;
-        if (a.has_shared) v += __ldcg(a.ws.dpart + ((size_t)n * (k + 1) + k) * H + j);
-        if (a.residual) v += bf16_bits_to_float(a.residual[(size_t)n * H + j]);
-        a.y[(size_t)n * H + j] = float_to_bf16_bits(v);
-      }
+  comp_bar();
+  if (!aborted()) {
+    for (int o = blockIdx.x * kCompThreads + threadIdx.x; o < K * H; o += grid * kCompThreads) {
+      const int n = o / H, j = o - n * H;
+      float acc2 = 0.f;
+      for (int s = 0; s < k; ++s)
+        acc2 = __fmaf_rn(s_w[n * k + s], __ldcg(a.ws.dpart + ((size_t)n * (k + 1) + s) * H + j), acc2);
+      float v = a.routed_scale * acc2;
+      if (a.has_shared) v += __ldcg(a.ws.dpart + ((size_t)n * (k + 1) + k) * H + j);
+      if (a.residual) v += bf16_bits_to_float(a.residual[(size_t)n * H + j]);
+      a.y[(size_t)n * H + j] = float_to_bf16_bits(v);
     }
   }
-  if (threadIdx.x == 0) {
-    stamp(7);
-    if (trace) trace[8] = (unsigned long long)L | ((unsigned long long)plan.n_shb << 16) |
-                          ((unsigned long long)(plan.gu1 - plan.gu0) << 24) |
-                          ((unsigned long long)(plan.dn1 - plan.dn0) << 40);
+  // the routing outputs of the call (one CTA writes them, off the critical path)
+  if (blockIdx.x == 0) {
+    for (int q = threadIdx.x; q < K * k; q += kCompThreads) {
+      if (a.idx_out) a.idx_out[q] = s_idx[q];
+      if (a.w_out) a.w_out[q] = s_w[q];
+    }
+    if (a.group_out && warp == 0) write_groups(a.group_out, s_nu, G, K, k, s_uexp, s_rowmask, s_slot, lane);
   }
+  if (threadIdx.x == 0) stamp(7);
 }
 
 // =====================================================================
@@ -915,18 +1171,38 @@ int num_sms() {
   return g_num_sms;
 }
 
-size_t experts_smem_bytes(int K, int H, int I, int E, int k, int G) {
-  const int NB = K > 8 ? 2 : 1;
-  size_t s = 1024 + (size_t)kExpStages * expert_stage_bytes(H, I) + sizeof(float) * 2 * 8 * 2 * NB * 128;
-  s += sizeof(float) * K * k + sizeof(int) * K * k + sizeof(unsigned) * E + sizeof(int) * E + sizeof(int) * (G + 1) +
-       sizeof(float) * 3 * (G + 1) + sizeof(float) * 3 * (E + 1) + (size_t)(G + 1) * K;
-  return s;
+// Dynamic shared memory of the experts kernel: the TMA ring, the reduction
+// ring and the routing arrays.  stages/nred are chosen to fill the
+// opt-in limit (at most kMaxStages stages).
+static size_t routing_smem_bytes(int K, int E, int k, int G) {
+  return sizeof(float) * K * k + sizeof(int) * K * k + sizeof(unsigned) * E + sizeof(int) * (G + 1) +
+         sizeof(float) * 3 * (E + 1) + (size_t)(G + 1) * K + 16;
 }
 
-template <int NB, int KUG, int KUD>
+static size_t red_slot_bytes(int NB) { return sizeof(float) * ((size_t)kCompWarps * (2 * NB * 128 + 32) + 16); }
+
+size_t experts_smem_bytes(int K, int H, int I, int E, int k, int G, int* stages, int* nred) {
+  const int NB = K > 8 ? 2 : 1;
+  const int nr = 2;
+  const size_t fixed = 1024 + routing_smem_bytes(K, E, k, G) + nr * red_slot_bytes(NB);
+  const size_t limit = 232448 - 2048;  // opt-in maximum less the static shared memory
+  const size_t sb = expert_stage_bytes(H, I);
+  int st = fixed < limit ? (int)((limit - fixed) / sb) : 0;
+  if (st > kMaxStages) st = kMaxStages;
+  if (stages) *stages = st;
+  if (nred) *nred = nr;
+  return fixed + (size_t)st * sb;
+}
+
+template <int NB>
 static cudaError_t launch_experts_t(const ExpertsArgs& a, const CUtensorMap* maps, cudaStream_t s, bool pdl) {
-  auto kern = k_moe_experts<NB, KUG, KUD>;
-  const size_t smem = experts_smem_bytes(a.K, a.H, a.I, a.E, a.k, a.G);
+  auto kern = k_moe_experts<NB>;
+  int stages = 0, nred = 0;
+  const size_t smem = experts_smem_bytes(a.K, a.H, a.I, a.E, a.k, a.G, &stages, &nred);
+  if (stages < 2 || a.H > 128 * kCompWarps || a.I > 128 * 4) return cudaErrorInvalidValue;
+  ExpertsArgs b = a;
+  b.stages = stages;
+  b.nred = nred;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
@@ -942,26 +1218,18 @@ static cudaError_t launch_experts_t(const ExpertsArgs& a, const CUtensorMap* map
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   err = cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7],
-                           maps[8], maps[9], a);
+                           maps[8], maps[9], b);
   if (err != cudaSuccess && pdl) {  // fall back to a cooperative launch without overlap
     cudaGetLastError();
     attr[0].val.programmaticStreamSerializationAllowed = 0;
     err = cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7],
-                             maps[8], maps[9], a);
+                             maps[8], maps[9], b);
   }
   return err;
 }
 
 cudaError_t launch_experts(const ExpertsArgs& a, const CUtensorMap* maps, cudaStream_t s, bool pdl) {
-  const bool nb2 = a.K > 8;
-  const bool kug2 = a.H > 1024;
-  const bool kud2 = a.I > 256;
-  if (!nb2) {
-    if (kug2) return kud2 ? launch_experts_t<1, 2, 2>(a, maps, s, pdl) : launch_experts_t<1, 2, 1>(a, maps, s, pdl);
-    return kud2 ? launch_experts_t<1, 1, 2>(a, maps, s, pdl) : launch_experts_t<1, 1, 1>(a, maps, s, pdl);
-  }
-  if (kug2) return kud2 ? launch_experts_t<2, 2, 2>(a, maps, s, pdl) : launch_experts_t<2, 2, 1>(a, maps, s, pdl);
-  return kud2 ? launch_experts_t<2, 1, 2>(a, maps, s, pdl) : launch_experts_t<2, 1, 1>(a, maps, s, pdl);
+  return a.K > 8 ? launch_experts_t<2>(a, maps, s, pdl) : launch_experts_t<1>(a, maps, s, pdl);
 }
 
 }  // namespace moe

@@ -12,12 +12,10 @@
 namespace moe {
 
 constexpr int kRouterWarps = 8;          // experts per router CTA
-constexpr int kGUWarps = 8;              // consumer warps, gate/up kernel
-constexpr int kDNWarps = 8;              // consumer warps, down kernel
 constexpr int kGURows = 16;              // intermediate rows per gate/up item
 constexpr int kDNRows = 64;              // hidden rows per down item
-constexpr int kExpWarps = 8;             // consumer warps of the experts kernel
-constexpr int kExpStages = 4;            // TMA ring depth of the experts kernel
+constexpr int kMaxStages = 6;            // TMA ring depth limit of the experts kernel
+constexpr int kMaxRed = 4;               // reduction ring depth limit of the experts kernel
 
 // Bytes of one ring stage: the larger of a gate/up item (codes and scales of
 // 16 rows of gate and up) and a down item (64 rows), 1024-aligned.
@@ -150,9 +148,10 @@ struct ExpertsArgs {
   uint64_t wait_ns;
   unsigned long long* trace;  // [grid][kTraceSlots] milestone timestamps, or null
   int code3d;                 // code maps are 3-D (one request per tile)
+  int stages, nred;           // ring depths (set by the launcher)
 };
 
-constexpr int kTraceSlots = 64;
+constexpr int kTraceSlots = 80;
 extern unsigned long long* g_trace;  // debug timeline buffer (null = off)
 
 struct LmHeadArgs {
@@ -209,12 +208,13 @@ cudaError_t launch_lmhead(const LmHeadArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s, bool pdl);
 // maps: gate, up, down, sh_gate, sh_up, sh_down codes; gate, up, sh_gate, sh_up scales
 cudaError_t launch_experts(const ExpertsArgs& a, const CUtensorMap* maps, cudaStream_t s, bool pdl);
-size_t experts_smem_bytes(int K, int H, int I, int E, int k, int G);
+size_t experts_smem_bytes(int K, int H, int I, int E, int k, int G, int* stages, int* nred);
 cudaError_t launch_accept(const int32_t* draft, const int32_t* target, int K, int32_t* out, cudaStream_t s);
 
 int num_sms();
 
 }  // namespace moe
+
 // The layer launch sequence behind moe_verify_layer (capi.cu; not exported).
 extern "C" __attribute__((visibility("hidden"))) moe_status run_layer(const moe_layer* layer, const uint16_t* x_norm, int K, const uint16_t* residual,
                                 uint16_t* y, int32_t* idx_out, float* w_out, int32_t* group_out, void* ws,

@@ -49,6 +49,40 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread sleeps in hardware until the
+// phase completes or about `hint_ns` pass, so a waiting warp takes no issue
+// slots from the warps that work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// The waiting part of mbar_wait_bounded, kept out of line (one copy).
+static __device__ __noinline__ bool mbar_wait_loop(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
+                                                   const volatile int* abort) {
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// Waits (bounded by `limit_ns`, never cut short by an abort flag) for the
+// copies that complete phase `parity` of `bar`: a CTA must not exit while
+// its own bulk copies may still write its shared memory.
+static __device__ __noinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait_sleep(bar, parity, 20000u))
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  return true;
+}
+
 // Waits for phase `parity` of `bar` to complete.  Gives up (returns false)
 // after `limit_ns` nanoseconds, or at once when *abort is set by another
 // warp; limit_ns == 0 gives up immediately.
@@ -56,12 +90,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
                                                   const volatile int* abort) {
   if (limit_ns == 0) return false;
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (global_timer_ns() - t0 > limit_ns) return false;
-  }
+  return mbar_wait_loop(bar, parity, limit_ns, abort);
 }
 
 // ---------------------------------------------------------------- TMA
