@@ -49,11 +49,18 @@ namespace {
 constexpr int kCompWarps = 16;
 constexpr int kCompThreads = kCompWarps * 32;
 constexpr int kProducerWarp = kCompWarps;
-constexpr int kThreads = kCompThreads + 32;
+constexpr int kPublisherWarp = kCompWarps + 1;  // publishes finished gate/up items at GPU scope
+constexpr int kThreads = kCompThreads + 64;
 constexpr uint64_t kDrainNs = 2000000000ull;  // bound on waiting for our own copies before exit
 
 // named barrier 1: the compute warps
 __device__ __forceinline__ void comp_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kCompThreads) : "memory"); }
+
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+__device__ __forceinline__ void red_relaxed_add(unsigned* p, unsigned v) {
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
 __device__ __forceinline__ unsigned ld_acquire_cta(const unsigned* p) {
   unsigned v;
@@ -71,10 +78,6 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
-}
-
-__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // Power-of-two shift that maps max |x| into [2^14, 2^15).
@@ -351,15 +354,15 @@ struct Item {
 // possible, the low parts taking one more.
 __device__ __forceinline__ int split_before(int c, int n, int parts) { return c * (n / parts) + min(c, n % parts); }
 
-// The CTA's work: n_shb shared gate/up items (round-robin over CTAs: shared
-// item j goes to CTA j mod grid, so they can be issued before the routing is
-// known), a contiguous range [gu0, gu1) of the routed gate/up items, then a
-// contiguous range [dn0, dn1) of the down items.  CTA c's gate/up total is
-// its even share of all of them; the CTAs holding an extra shared item are
-// low CTAs that also hold an extra total, so no routed count is negative and
-// the ranges are monotone.
+// The CTA's work: its gate/up items, dealt round-robin in the global order
+// (shared items first, then the routed ones slot-major), so every slot's
+// items finish in one early round across the CTAs and the down items of a
+// slot rarely wait; then a contiguous range [dn0, dn1) of the down items.
+// Gate/up item V of the global order goes to CTA V mod grid: CTA b holds
+// n_shb shared items (V = b, b + grid, ...) then rt_count routed ones, the
+// first being routed item rt_first, the next ones grid apart.
 struct Plan {
-  int n_shb, gu0, gu1, dn0, dn1;
+  int n_shb, rt_first, rt_count, dn0, dn1;
 };
 
 __device__ __forceinline__ Plan make_plan(int n_sh, int n_rgu, int n_dn) {
@@ -367,22 +370,22 @@ __device__ __forceinline__ Plan make_plan(int n_sh, int n_rgu, int n_dn) {
   const int T = n_sh + n_rgu;
   Plan p;
   p.n_shb = split_before(b + 1, n_sh, grid) - split_before(b, n_sh, grid);
-  p.gu0 = split_before(b, T, grid) - split_before(b, n_sh, grid);
-  p.gu1 = split_before(b + 1, T, grid) - split_before(b + 1, n_sh, grid);
+  p.rt_count = split_before(b + 1, T, grid) - split_before(b, T, grid) - p.n_shb;
+  p.rt_first = b + p.n_shb * grid - n_sh;
   p.dn0 = split_before(b, n_dn, grid);
   p.dn1 = split_before(b + 1, n_dn, grid);
   return p;
 }
 
-__device__ __forceinline__ int plan_len(const Plan& p) { return p.n_shb + (p.gu1 - p.gu0) + (p.dn1 - p.dn0); }
+__device__ __forceinline__ int plan_len(const Plan& p) { return p.n_shb + p.rt_count + (p.dn1 - p.dn0); }
 
 // Walks a CTA's items in order with no division per item.  Routed gate/up
-// items are slot-major (mt_per tiles per slot); down items are slot-major
-// with the shared slot first.
+// item v is tile v % mt_per of slot v / mt_per (mt_per a power of two); down
+// items are slot-major with the shared slot first.
 struct Seq {
   Plan p;
-  int mt_per, n_tiles, G, has_sh;
-  int rt_slot, rt_tile, dn_slot, dn_tile;  // first routed gate/up and first down item
+  int mt_per, lg_mt, n_tiles, G, has_sh;
+  int dn_slot, dn_tile;  // first down item
 };
 
 __device__ __forceinline__ Seq make_seq(const Plan& p, int mt_per, int n_tiles, int G, int has_sh) {
@@ -392,8 +395,7 @@ __device__ __forceinline__ Seq make_seq(const Plan& p, int mt_per, int n_tiles, 
   s.n_tiles = n_tiles;
   s.G = G;
   s.has_sh = has_sh;
-  s.rt_slot = p.gu0 / mt_per;
-  s.rt_tile = p.gu0 - s.rt_slot * mt_per;
+  s.lg_mt = __ffs(mt_per) - 1;
   const int si = p.dn0 / n_tiles;
   s.dn_tile = p.dn0 - si * n_tiles;
   s.dn_slot = has_sh ? (si == 0 ? G : si - 1) : si;
@@ -403,6 +405,7 @@ __device__ __forceinline__ Seq make_seq(const Plan& p, int mt_per, int n_tiles, 
 struct Cursor {
   Item it;
   int left;  // items left in the current phase, this one included
+  int v;     // routed gate/up item index (routed phase)
 };
 
 __device__ __forceinline__ void seq_phase(Cursor& c, const Seq& s, int kind) {
@@ -412,9 +415,10 @@ __device__ __forceinline__ void seq_phase(Cursor& c, const Seq& s, int kind) {
       c.it.slot = s.G;
       c.it.tile = blockIdx.x;
     } else if (kind == kRtGU) {
-      c.left = s.p.gu1 - s.p.gu0;
-      c.it.slot = s.rt_slot;
-      c.it.tile = s.rt_tile;
+      c.left = s.p.rt_count;
+      c.v = s.p.rt_first;
+      c.it.slot = c.v >> s.lg_mt;
+      c.it.tile = c.v & (s.mt_per - 1);
     } else {
       c.left = s.p.dn1 - s.p.dn0;
       c.it.slot = s.dn_slot;
@@ -438,10 +442,9 @@ __device__ __forceinline__ void seq_next(Cursor& c, const Seq& s) {
     if (c.it.kind == kShGU) {
       c.it.tile += gridDim.x;
     } else if (c.it.kind == kRtGU) {
-      if (++c.it.tile == s.mt_per) {
-        c.it.tile = 0;
-        ++c.it.slot;
-      }
+      c.v += gridDim.x;
+      c.it.slot = c.v >> s.lg_mt;
+      c.it.tile = c.v & (s.mt_per - 1);
     } else if (++c.it.tile == s.n_tiles) {
       c.it.tile = 0;
       c.it.slot = (c.it.slot == s.G) ? 0 : c.it.slot + 1;
@@ -632,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     it.tile = blockIdx.x;
     for (; issued < n_shb && issued < S; ++issued, it.tile += grid)
       issue_item(ic, it, smem + (size_t)issued * stage_bytes, &full_bar[issued], lane);
-  } else {
+  } else if (warp < kCompWarps) {
     const int tid = threadIdx.x;
     for (int e = tid; e < E; e += kCompThreads) s_rowmask[e] = 0u;
     for (int i = tid; i < (G + 1) * K; i += kCompThreads) s_slot[i] = -1;
@@ -763,72 +766,47 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_launch_dependents();
   if (threadIdx.x == 0) stamp(3);
 
+  if (warp == kPublisherWarp) {
+    // ------------------------------------------------------------ publisher
+    // Publishes this CTA's finished gate/up items on their slots' counters
+    // (GPU scope) once their duty warps have stored the h rows: one fence per
+    // batch of finished items, on a warp that nothing else waits for.
+    if (lane == 0) {
+      const Seq seq = make_cta_seq();
+      const int L_gu = seq.p.n_shb + seq.p.rt_count;
+      Cursor pc = seq_begin(seq);
+      int pl = 0;  // items published so far
+      const uint64_t t0 = global_timer_ns();
+      while (pl < L_gu) {
+        const int done_items = (int)(ld_acquire_cta(&s_hpub) >> 2);  // 4 duty warps per item
+        if (done_items > pl) {
+          fence_acq_rel_gpu();
+          for (; pl < done_items && pl < L_gu; ++pl) {
+            red_relaxed_add(&a.ws.done[pc.it.slot], 1u);
+            seq_next(pc, seq);
+          }
+          continue;
+        }
+        if (aborted() || a.wait_ns == 0 || global_timer_ns() - t0 > a.wait_ns) break;
+        __nanosleep(128);
+      }
+    }
+    return;
+  }
+
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
-    // Issues the copies of every item into the ring, and publishes each
-    // finished gate/up slot run of this CTA (a release at GPU scope on the
-    // slot's counter) once every compute warp has stored its h rows: the
-    // fences of the publication stay off the compute warps.
+    // Issues the copies of every item into the ring.
     const Seq seq = make_cta_seq();
     const int L = plan_len(seq.p);
-    const int L_gu = seq.p.n_shb + (seq.p.gu1 - seq.p.gu0);
     Cursor cur = seq_begin(seq);
     for (int l = 0; l < issued; ++l) seq_next(cur, seq);
-    // publication events: the runs of equal slot among the gate/up items
-    Cursor pc = seq_begin(seq);
-    int pl = 0, n_ev = 0;
-    int ev_slot = -1;
-    unsigned ev_count = 0;
-    auto next_event = [&]() {
-      ev_slot = -1;
-      ev_count = 0;
-      if (pl >= L_gu) return;
-      ev_slot = pc.it.slot;
-      while (pl < L_gu && pc.it.slot == ev_slot) {
-        ++ev_count;
-        ++pl;
-        seq_next(pc, seq);
-      }
-    };
-    next_event();
-    // lane 0: publish every event whose h rows are complete (wait for the
-    // next one when `block`)
-    auto publish = [&](bool block) {
-      while (ev_slot >= 0) {
-        const unsigned need = (unsigned)kCompWarps * (unsigned)(n_ev + 1);
-        bool ready = ld_acquire_cta(&s_hpub) >= need;
-        if (!ready && block) {
-          const uint64_t t0 = global_timer_ns();
-          while (!(ready = ld_acquire_cta(&s_hpub) >= need)) {
-            if (aborted() || a.wait_ns == 0 || global_timer_ns() - t0 > a.wait_ns) break;
-            __nanosleep(128);
-          }
-          if (!ready) fail();
-        }
-        if (!ready) return;
-        red_release_add(&a.ws.done[ev_slot], ev_count);
-        ++n_ev;
-        next_event();
-      }
-    };
     int pass = issued / S, st = issued - pass * S;  // item l goes to stage l % S on pass l / S
     for (int l = issued; l < L; ++l, seq_next(cur, seq)) {
       int ok = 1;
-      if (lane == 0) {
-        // wait for the stage, publishing meanwhile: a compute warp may be
-        // waiting for this CTA's own publication before it frees a stage
-        publish(false);
-        if (pass > 0) {
-          const uint64_t t0 = global_timer_ns();
-          while (!mbar_try_wait_sleep(&empty_bar[st], (pass - 1) & 1, 500u)) {
-            publish(false);
-            if (aborted() || a.wait_ns == 0 || global_timer_ns() - t0 > a.wait_ns) {
-              ok = 0;
-              fail();
-              break;
-            }
-          }
-        }
+      if (lane == 0 && pass > 0 && !mbar_wait_bounded(&empty_bar[st], (pass - 1) & 1, a.wait_ns, &s_abort)) {
+        ok = 0;
+        fail();
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
@@ -841,7 +819,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (lane == 0 && trace) trace[9] = global_timer_ns();
     if (lane == 0) {
-      if (!aborted()) publish(true);
       // every copy of the last S items has landed before the CTA may exit
       // (a stage is reissued only after the compute warps saw its previous
       // copy complete, so older copies have landed)
@@ -883,17 +860,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t so1 = swizzle_off((uint32_t)((g + 8) * sstride + 8 * warp), smask);
     uint32_t goff[2];  // this lane's ldmatrix offsets in a gate/up codes tile
     kunit_offsets(ggu, kGURows, 0, gu_active ? warp : 0, lane, goff);
-    const int q8 = lane >> 2, sub = lane & 3;  // epilogue: quad q8 = output column, sub = partial set
-    // this CTA's gate/up items: n_shb shared ones, then routed v = gu0..gu1-1
-    // (slot v / mt_per, tile v % mt_per); mt_per is a power of two
-    int L_gu, gu0;
+    // this CTA's gate/up items: global items V = b + l * grid, shared tile V
+    // for V < n_sh, else routed v = V - n_sh (slot v / mt_per, tile
+    // v % mt_per; mt_per is a power of two)
+    int L_gu;
     {
       const Plan p0 = make_cta_seq().p;
-      L_gu = p0.n_shb + (p0.gu1 - p0.gu0);
-      gu0 = p0.gu0;
+      L_gu = p0.n_shb + p0.rt_count;
     }
     const int lg_mt = __ffs(mt_per) - 1;
-    auto gu_slot = [&](int l) { return l < n_shb ? G : (gu0 + l - n_shb) >> lg_mt; };
+    auto gu_slot = [&](int l) {
+      const int V = (int)blockIdx.x + l * grid;
+      return V < n_sh ? G : (V - n_sh) >> lg_mt;
+    };
     int st = 0, fp = 0;  // item l: stage l % S on pass l / S
     auto advance = [&]() {
       if (++st == S) {
@@ -905,7 +884,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       unsigned char* stg = smem + (size_t)st * stage_bytes;
       float* rb = red + (size_t)(l & 1) * kRedFloats;
       const bool ok = warp_wait(&full_bar[st], fp & 1);
-      if (threadIdx.x == 0 && l < 9) stamp(16 + 4 * l);
+      if (threadIdx.x == 0 && l < 4) stamp(16 + 4 * l);
       // this warp's codes and scales to registers, then the stage goes back
       uint32_t ag[2][4], au[2][4];
       uint2 sr[4];
@@ -946,60 +925,60 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<float2*>(pu + 2) = make_float2(cu[nb][2], cu[nb][3]);
         }
       }
-      if (threadIdx.x == 0 && l < 9) stamp(17 + 4 * l);
+      if (threadIdx.x == 0 && l < 4) stamp(17 + 4 * l);
       comp_bar();
-      if (threadIdx.x == 0 && l < 9) stamp(18 + 4 * l);
-      // epilogue: warp w owns intermediate row w of the item's 16 rows, the
-      // quads of the warp its 8 (x NB) columns; a quad's 4 lanes each sum 4
-      // of the k-unit partials, then two xor steps sum the 4 in a fixed order
-      if (!aborted()) {
+      if (threadIdx.x == 0 && l < 4) stamp(18 + 4 * l);
+      // epilogue, by the 4 warps of group l % 4 (the others move on to the
+      // next item): thread o of the group owns output o (row o / 8 of the
+      // item's 16, column o % 8 of each n-block) and sums its 16 k-unit
+      // partials in k-unit order
+      if ((warp >> 2) == (l & 3) && !aborted()) {
         const int slot = gu_slot(l);
-        const int tile = l < n_shb ? (int)blockIdx.x + l * grid : ((gu0 + l - n_shb) & (mt_per - 1));
+        const int Vg = (int)blockIdx.x + l * grid;
+        const int tile = Vg < n_sh ? Vg : ((Vg - n_sh) & (mt_per - 1));
         const int ex = s_uexp[slot];
         const float tg = s_tse[3 * ex + 0], tu = s_tse[3 * ex + 1];
+        const int o = (warp & 3) * 32 + lane;
+        const int i = o >> 3, c = o & 7;
+        const int f0 = ((i & 7) * 4 + (c >> 1)) * 4 + (i >> 3) * 2 + (c & 1);
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
-          const int n = nb * 8 + q8;
-          const int f = nb * 128 + ((warp & 7) * 4 + (q8 >> 1)) * 4 + (warp >> 3) * 2 + (q8 & 1);
-          float pg[4], pu[4];
+          const int n = nb * 8 + c;
+          const int f = nb * 128 + f0;
+          float gs = 0.f, us = 0.f;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int w = sub + 4 * j;
-            pg[j] = w < KUgu ? rb[red_at(w) + f] : 0.f;
-            pu[j] = w < KUgu ? rb[red_at(w) + NB * 128 + f] : 0.f;
+          for (int w = 0; w < kCompWarps; ++w) {
+            if (w < KUgu) {
+              gs += rb[red_at(w) + f];
+              us += rb[red_at(w) + NB * 128 + f];
+            }
           }
-          float gs = ((pg[0] + pg[1]) + pg[2]) + pg[3];
-          float us = ((pu[0] + pu[1]) + pu[2]) + pu[3];
-          gs += __shfl_xor_sync(0xffffffffu, gs, 1);
-          us += __shfl_xor_sync(0xffffffffu, us, 1);
-          gs += __shfl_xor_sync(0xffffffffu, gs, 2);
-          us += __shfl_xor_sync(0xffffffffu, us, 2);
-          if (sub == 0 && n < K) {
+          if (n < K) {
             const float inv = pow2f(-row_shift(s_xamax[n]));
             const float gv = gs * inv * tg;
             const float uv = us * inv * tu;
             const float hv = gv * __frcp_rn(1.f + expf(-gv)) * uv;
             const uint16_t hb = float_to_bf16_bits(hv);
-            a.ws.h[((size_t)slot * K + n) * I + tile * kGURows + warp] = hb;
+            a.ws.h[((size_t)slot * K + n) * I + tile * kGURows + i] = hb;
             atomicMax(&a.ws.hamax[slot * K + n], (unsigned)(hb & 0x7FFFu));
           }
         }
-        // the last item of a slot run: this warp's h rows are stored
-        if (l + 1 == L_gu || gu_slot(l + 1) != slot) {
-          __syncwarp();
-          if (lane == 0) red_release_cta_shared_add(&s_hpub, 1u);
-        }
+        // every gate/up item: this duty warp's h rows are stored
+        __syncwarp();
+        if (lane == 0) red_release_cta_shared_add(&s_hpub, 1u);
       }
-      if (threadIdx.x == 0 && l < 9) stamp(19 + 4 * l);
+      if (threadIdx.x == 0 && l < 4) stamp(19 + 4 * l);
     }
-    // down items: 4 m-tiles of 16 rows x I/128 k-units over the 16 warps
+    // down items: 8 m-tiles of 16 rows x I/128 k-units; warp w takes k-unit
+    // w / 4 of m-tiles w % 4 and w % 4 + 4 (one set of h fragments for both)
     {
       const Seq seq = make_cta_seq();
       const int L = plan_len(seq.p);
-      const int mt = warp & 3, kq = warp >> 2;
+      const int mA = warp & 3, kq = warp >> 2;
       const bool dn_active = kq < KUdn;
-      uint32_t doff[2];  // this lane's ldmatrix offsets in a down codes tile
-      kunit_offsets(gdn, kDNRows, mt * 16, dn_active ? kq : 0, lane, doff);
+      uint32_t doffA[2], doffB[2];  // this lane's ldmatrix offsets in a down codes tile
+      kunit_offsets(gdn, kDNRows, mA * 16, dn_active ? kq : 0, lane, doffA);
+      kunit_offsets(gdn, kDNRows, (mA + 4) * 16, dn_active ? kq : 0, lane, doffB);
       uint32_t bh[NB][16];
       float hinv = 1.f, hinv1 = 1.f;  // inverse h scales of rows g and 8 + g
       int cur_slot = -1;
@@ -1009,6 +988,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Item it = dc.it;
         unsigned char* stg = smem + (size_t)st * stage_bytes;
         float* rb = red + (size_t)(l & 1) * kRedFloats;
+        const int dj = l - L_gu;  // down item index (trace stamps 32 + 4 dj ..)
+        if (threadIdx.x == 0 && dj < 4) stamp(32 + 4 * dj);
         bool ok = !aborted();
         if (ok && it.slot != cur_slot) {
           // h of this slot: every warp waits (bounded, no CTA barrier) until
@@ -1045,42 +1026,47 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        if (threadIdx.x == 0 && dj < 4) stamp(33 + 4 * dj);
         const bool landed = warp_wait(&full_bar[st], fp & 1);
+        if (threadIdx.x == 0 && dj < 4) stamp(34 + 4 * dj);
         ok = landed && ok;
-        uint32_t ad[2][4];
-        uint2 sd0, sd1;
+        uint32_t adA[2][4], adB[2][4];
+        uint2 sr[4];
         if (ok && dn_active) {
-          kunit_load(smem_addr(stg), doff, ad);
-          const unsigned char* srow = stg + dn_code + (mt * 16 + g) * (I / 16);
-          sd0 = *reinterpret_cast<const uint2*>(srow + 8 * kq);
-          sd1 = *reinterpret_cast<const uint2*>(srow + 8 * (I / 16) + 8 * kq);
+          const uint32_t tc = smem_addr(stg);
+          kunit_load(tc, doffA, adA);
+          kunit_load(tc, doffB, adB);
+          const unsigned char* srA = stg + dn_code + (mA * 16 + g) * (I / 16) + 8 * kq;
+          const unsigned char* srB = srA + 64 * (I / 16);  // 4 m-tiles further
+          sr[0] = *reinterpret_cast<const uint2*>(srA);
+          sr[1] = *reinterpret_cast<const uint2*>(srA + 8 * (I / 16));
+          sr[2] = *reinterpret_cast<const uint2*>(srB);
+          sr[3] = *reinterpret_cast<const uint2*>(srB + 8 * (I / 16));
         }
         __syncwarp();
         if (landed && lane == 0) mbar_arrive(&empty_bar[st]);  // only a stage whose copy landed goes back
         if (ok && dn_active) {
-          float c0[NB][4], c1[NB][4];
+          float cA[NB][4], cB[NB][4];
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) c0[nb][i] = c1[nb][i] = 0.f;
-          uint32_t s0[4], s1[4];
-          unit_scales(sd0, t, s0);
-          unit_scales(sd1, t, s1);
-          if (NB == 1)
-            kunit_mma_regs<NB>(ad, s0, s1, bh, c0, c1);
-          else
-            kunit_mma_regs<NB>(ad, s0, s1, bh, c0, c0);
+            for (int i = 0; i < 4; ++i) cA[nb][i] = cB[nb][i] = 0.f;
+          uint32_t s0[4], s1[4], u0[4], u1[4];
+          unit_scales(sr[0], t, s0);
+          unit_scales(sr[1], t, s1);
+          unit_scales(sr[2], t, u0);
+          unit_scales(sr[3], t, u1);
+          kunit_mma_regs<NB>(adA, s0, s1, bh, cA, cA);
+          kunit_mma_regs<NB>(adB, u0, u1, bh, cB, cB);
+          float* wb = rb + red_at(warp) + lane * 4;
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb) {
-            float4 v;
-            if (NB == 1)
-              v = make_float4(c0[nb][0] + c1[nb][0], c0[nb][1] + c1[nb][1], c0[nb][2] + c1[nb][2],
-                              c0[nb][3] + c1[nb][3]);
-            else
-              v = make_float4(c0[nb][0], c0[nb][1], c0[nb][2], c0[nb][3]);
-            float* pd = rb + red_at(warp) + nb * 128 + lane * 4;
-            *reinterpret_cast<float2*>(pd) = make_float2(v.x, v.y);
-            *reinterpret_cast<float2*>(pd + 2) = make_float2(v.z, v.w);
+            float* pa = wb + (0 * NB + nb) * 128;
+            float* pb = wb + (1 * NB + nb) * 128;
+            *reinterpret_cast<float2*>(pa) = make_float2(cA[nb][0], cA[nb][1]);
+            *reinterpret_cast<float2*>(pa + 2) = make_float2(cA[nb][2], cA[nb][3]);
+            *reinterpret_cast<float2*>(pb) = make_float2(cB[nb][0], cB[nb][1]);
+            *reinterpret_cast<float2*>(pb + 2) = make_float2(cB[nb][2], cB[nb][3]);
           }
         }
         if (warp == 0 && t == 0) {
@@ -1088,25 +1074,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (NB == 2) rb[kRedPart + 8 + g] = hinv1;
         }
         comp_bar();
-        // epilogue: thread (warp, lane) -> m-tile m, output (i, c) of each
-        // n-block; the k-unit partials of m-tile m sit at warps m, m+4, ...
+        if (threadIdx.x == 0 && dj < 4) stamp(35 + 4 * dj);
+        // epilogue: thread (warp, lane) -> output (i, c) of m-tiles M and
+        // M + 4 in each n-block; the k-unit partials of m-tile M sit at warps
+        // M % 4 + 4 q, in their first or second half
         if (!aborted()) {
           const float ts = s_tse[3 * s_uexp[it.slot] + 2];
           const int tid = (int)threadIdx.x;
-          const int m = tid >> 7, oo = tid & 127;
+          const int m0 = tid >> 7, oo = tid & 127;
           const int i = oo >> 3, c = oo & 7;
+          const int f0 = ((i & 7) * 4 + (c >> 1)) * 4 + (i >> 3) * 2 + (c & 1);
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb) {
             const int n = nb * 8 + c;
             if (n >= K) continue;
             const int s = s_slot[it.slot * K + n];
             if (s < 0) continue;
-            const int f = nb * 128 + ((i & 7) * 4 + (c >> 1)) * 4 + (i >> 3) * 2 + (c & 1);
-            float v4[4];
+            const float sc = rb[kRedPart + n] * ts;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) v4[q] = q < KUdn ? rb[red_at(q * 4 + m) + f] : 0.f;
-            const float v = ((v4[0] + v4[1]) + v4[2]) + v4[3];  // k-units in order
-            a.ws.dpart[((size_t)n * (k + 1) + s) * H + it.tile * kDNRows + m * 16 + i] = v * rb[kRedPart + n] * ts;
+            for (int hh = 0; hh < 2; ++hh) {
+              const int M = m0 + 4 * hh;
+              const int f = (hh * NB + nb) * 128 + f0;
+              float v4[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) v4[q] = q < KUdn ? rb[red_at(q * 4 + m0) + f] : 0.f;
+              const float v = ((v4[0] + v4[1]) + v4[2]) + v4[3];  // k-units in order
+              a.ws.dpart[((size_t)n * (k + 1) + s) * H + it.tile * kDNRows + M * 16 + i] = v * sc;
+            }
           }
         }
       }

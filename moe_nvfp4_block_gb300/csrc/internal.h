@@ -13,12 +13,12 @@ namespace moe {
 
 constexpr int kRouterWarps = 8;          // experts per router CTA
 constexpr int kGURows = 16;              // intermediate rows per gate/up item
-constexpr int kDNRows = 64;              // hidden rows per down item
+constexpr int kDNRows = 128;             // hidden rows per down item
 constexpr int kMaxStages = 6;            // TMA ring depth limit of the experts kernel
 constexpr int kMaxRed = 4;               // reduction ring depth limit of the experts kernel
 
 // Bytes of one ring stage: the larger of a gate/up item (codes and scales of
-// 16 rows of gate and up) and a down item (64 rows), 1024-aligned.
+// 16 rows of gate and up) and a down item (128 rows), 1024-aligned.
 __host__ __device__ inline int expert_stage_bytes(int H, int I) {
   const int gu = 2 * (kGURows * H / 2) + 2 * (kGURows * H / 16);
   const int dn = kDNRows * I / 2 + kDNRows * I / 16;
