@@ -342,7 +342,7 @@ __device__ __forceinline__ void kunit_mma_at(uint32_t tile, const uint32_t (&off
 }
 
 // Item kinds of a CTA's sequence (in this order).
-constexpr int kShGU = 0, kRtGU = 1, kDN = 2, kEnd = 3;
+constexpr int kShGU = 0, kRtGU = 1, kDN = 2, kDN2 = 3, kEnd = 4;  // kDN2: the second down range
 
 struct Item {
   int kind;
@@ -357,12 +357,15 @@ __device__ __forceinline__ int split_before(int c, int n, int parts) { return c 
 // The CTA's work: its gate/up items, dealt round-robin in the global order
 // (shared items first, then the routed ones slot-major), so every slot's
 // items finish in one early round across the CTAs and the down items of a
-// slot rarely wait; then a contiguous range [dn0, dn1) of the down items.
+// slot rarely wait; then two contiguous ranges of the down items: [dn0, dn1)
+// in the first half of the slot-major down list (slots that finish early,
+// dealt to the CTAs in order) and [dn2, dn3) in the second half (dealt in
+// reverse order), so every CTA starts its down work on early slots.
 // Gate/up item V of the global order goes to CTA V mod grid: CTA b holds
 // n_shb shared items (V = b, b + grid, ...) then rt_count routed ones, the
 // first being routed item rt_first, the next ones grid apart.
 struct Plan {
-  int n_shb, rt_first, rt_count, dn0, dn1;
+  int n_shb, rt_first, rt_count, dn0, dn1, dn2, dn3;
 };
 
 __device__ __forceinline__ Plan make_plan(int n_sh, int n_rgu, int n_dn) {
@@ -372,12 +375,15 @@ __device__ __forceinline__ Plan make_plan(int n_sh, int n_rgu, int n_dn) {
   p.n_shb = split_before(b + 1, n_sh, grid) - split_before(b, n_sh, grid);
   p.rt_count = split_before(b + 1, T, grid) - split_before(b, T, grid) - p.n_shb;
   p.rt_first = b + p.n_shb * grid - n_sh;
-  p.dn0 = split_before(b, n_dn, grid);
-  p.dn1 = split_before(b + 1, n_dn, grid);
+  const int h1 = n_dn / 2, h2 = n_dn - h1;
+  p.dn0 = split_before(b, h1, grid);
+  p.dn1 = split_before(b + 1, h1, grid);
+  p.dn2 = h1 + split_before(grid - 1 - b, h2, grid);
+  p.dn3 = h1 + split_before(grid - b, h2, grid);
   return p;
 }
 
-__device__ __forceinline__ int plan_len(const Plan& p) { return p.n_shb + p.rt_count + (p.dn1 - p.dn0); }
+__device__ __forceinline__ int plan_len(const Plan& p) { return p.n_shb + p.rt_count + (p.dn1 - p.dn0) + (p.dn3 - p.dn2); }
 
 // Walks a CTA's items in order with no division per item.  Routed gate/up
 // item v is tile v % mt_per of slot v / mt_per (mt_per a power of two); down
@@ -385,7 +391,7 @@ __device__ __forceinline__ int plan_len(const Plan& p) { return p.n_shb + p.rt_c
 struct Seq {
   Plan p;
   int mt_per, lg_mt, n_tiles, G, has_sh;
-  int dn_slot, dn_tile;  // first down item
+  int dn_slot, dn_tile, dn2_slot, dn2_tile;  // first item of each down range
 };
 
 __device__ __forceinline__ Seq make_seq(const Plan& p, int mt_per, int n_tiles, int G, int has_sh) {
@@ -399,6 +405,9 @@ __device__ __forceinline__ Seq make_seq(const Plan& p, int mt_per, int n_tiles, 
   const int si = p.dn0 / n_tiles;
   s.dn_tile = p.dn0 - si * n_tiles;
   s.dn_slot = has_sh ? (si == 0 ? G : si - 1) : si;
+  const int si2 = p.dn2 / n_tiles;
+  s.dn2_tile = p.dn2 - si2 * n_tiles;
+  s.dn2_slot = has_sh ? (si2 == 0 ? G : si2 - 1) : si2;
   return s;
 }
 
@@ -419,10 +428,14 @@ __device__ __forceinline__ void seq_phase(Cursor& c, const Seq& s, int kind) {
       c.v = s.p.rt_first;
       c.it.slot = c.v >> s.lg_mt;
       c.it.tile = c.v & (s.mt_per - 1);
-    } else {
+    } else if (kind == kDN) {
       c.left = s.p.dn1 - s.p.dn0;
       c.it.slot = s.dn_slot;
       c.it.tile = s.dn_tile;
+    } else {
+      c.left = s.p.dn3 - s.p.dn2;
+      c.it.slot = s.dn2_slot;
+      c.it.tile = s.dn2_tile;
     }
     c.it.kind = kind;
     if (c.left > 0) return;
@@ -468,7 +481,7 @@ struct IssueCtx {
 __device__ __forceinline__ void issue_item(const IssueCtx& c, const Item it, unsigned char* stg, uint64_t* bar,
                                         int lane) {
   const int H = c.H, I = c.I;
-  if (it.kind != kDN) {
+  if (it.kind < kDN) {  // gate/up
     const TileGeo geo = tile_geo(H);
     const int code = kGURows * H / 2, scale = kGURows * H / 16;
     const bool sh = it.kind == kShGU;
@@ -1075,14 +1088,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         comp_bar();
         if (threadIdx.x == 0 && dj < 4) stamp(35 + 4 * dj);
-        // epilogue: thread (warp, lane) -> output (i, c) of m-tiles M and
-        // M + 4 in each n-block; the k-unit partials of m-tile M sit at warps
-        // M % 4 + 4 q, in their first or second half
-        if (!aborted()) {
+        // epilogue, by the 4 warps of group l % 4 (the others move on to the
+        // next item): thread o of the group owns output (i, c) of m-tiles
+        // M = 0..7 in each n-block; the k-unit partials of m-tile M sit at
+        // warps M % 4 + 4 q, in their first (M < 4) or second half
+        if ((warp >> 2) == (l & 3) && !aborted()) {
           const float ts = s_tse[3 * s_uexp[it.slot] + 2];
-          const int tid = (int)threadIdx.x;
-          const int m0 = tid >> 7, oo = tid & 127;
-          const int i = oo >> 3, c = oo & 7;
+          const int o = (warp & 3) * 32 + lane;
+          const int i = o >> 3, c = o & 7;
           const int f0 = ((i & 7) * 4 + (c >> 1)) * 4 + (i >> 3) * 2 + (c & 1);
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb) {
@@ -1091,15 +1104,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int s = s_slot[it.slot * K + n];
             if (s < 0) continue;
             const float sc = rb[kRedPart + n] * ts;
+            float* dst = a.ws.dpart + ((size_t)n * (k + 1) + s) * H + it.tile * kDNRows + i;
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              const int M = m0 + 4 * hh;
-              const int f = (hh * NB + nb) * 128 + f0;
+            for (int M = 0; M < 8; ++M) {
+              const int f = ((M >> 2) * NB + nb) * 128 + f0;
               float v4[4];
 #pragma unroll
-              for (int q = 0; q < 4; ++q) v4[q] = q < KUdn ? rb[red_at(q * 4 + m0) + f] : 0.f;
+              for (int q = 0; q < 4; ++q) v4[q] = q < KUdn ? rb[red_at(q * 4 + (M & 3)) + f] : 0.f;
               const float v = ((v4[0] + v4[1]) + v4[2]) + v4[3];  // k-units in order
-              a.ws.dpart[((size_t)n * (k + 1) + s) * H + it.tile * kDNRows + M * 16 + i] = v * sc;
+              dst[M * 16] = v * sc;
             }
           }
         }
