@@ -86,8 +86,9 @@ typedef struct {
 /*
  * Bytes of device workspace a layer call with K rows needs (0 on an invalid
  * layer or K).  The workspace must be zero-filled once before its first use
- * (e.g. cudaMemsetAsync); every call leaves it ready for the next call.
- * After a call that returned MOE_ERR_DEVICE_TIMEOUT zero-fill it again.
+ * (e.g. cudaMemsetAsync); every call leaves it ready for the next call,
+ * with any K and layer whose size fits in it.  After a call that returned
+ * MOE_ERR_DEVICE_TIMEOUT zero-fill it again.
  */
 size_t moe_verify_layer_workspace_size(const moe_layer* layer, int K);
 
@@ -158,7 +159,7 @@ moe_status moe_verify_stack(const moe_layer* layers, int n_layers, uint16_t* x, 
  * synchronisation.  The pages have no counterpart of this entry point.
  *
  * Same results as moe_verify_layer.  The scratch space (routing tables,
- * intermediate activations, partial sums, counters) is a fixed 4 MiB array
+ * intermediate activations, partial sums, counters) is a fixed 8 MiB array
  * compiled into the library; every GPU that loads the library holds it until
  * the process exits.  A call whose layer needs more workspace than that
  * (moe_verify_layer_workspace_size) returns MOE_ERR_WORKSPACE_TOO_SMALL.
@@ -170,7 +171,7 @@ moe_status moe_verify_stack(const moe_layer* layers, int n_layers, uint16_t* x, 
  *    `stream`) and zero-fills it once; make that first call before any
  *    stream capture.
  *  - Every call on a device shares the one array and keeps the last call's
- *    contents; each call clears the counters it needs.  Calls that overlap
+ *    contents (later calls rely on them).  Calls that overlap
  *    on the GPU (different streams, or different host threads) race on the
  *    array and give wrong results: serialise them.
  *  - A device-side wait that runs out of time leaves y undefined and is not

@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(256) k_gemv_bf16(GemvArgs a) {
   pdl_wait();
   pdl_launch_dependents();
   uint4* xs = reinterpret_cast<uint4*>(smem);
-  for (int i = threadIdx.x; i < K * D / 8; i += blockDim.x) xs[i] = reinterpret_cast<const uint4*>(a.x)[i];
+  block_copy_g2s(xs, reinterpret_cast<const uint4*>(a.x), K * D / 8);
   __syncthreads();
   const int nw = gridDim.x * (blockDim.x >> 5);
   for (int n = blockIdx.x * (blockDim.x >> 5) + warp; n < a.n_total; n += nw) {

@@ -142,12 +142,10 @@ RouterArgs router_args(const moe_layer* L, const uint16_t* x, int K, const WsPtr
   a.k = L->top_k;
   a.G = group_cap(K, L->n_experts, L->top_k);
   a.has_shared = L->shared_inter > 0;
-  a.n_tiles = L->hidden / kDNRows;
   a.ws = wp;
   a.idx_out = idx_out;
   a.w_out = w_out;
   a.group_out = group_out;
-  a.do_topk = 1;
   return a;
 }
 
@@ -232,11 +230,9 @@ __attribute__((visibility("hidden"))) moe_status run_layer(const moe_layer* laye
     return !events || cudaEventRecordWithFlags(static_cast<cudaEvent_t>(events[i]), st, ev_flags) == cudaSuccess;
   };
 
-  RouterArgs ra = router_args(layer, x_norm, K, wp, nullptr, nullptr, nullptr);
-  ra.do_topk = 0;
-  // the router prefetches its weights before its dependency wait, so it may
-  // overlap the tail of whatever ran before it on the stream
-  if (!mark(0) || launch_router(ra, st, pdl) != cudaSuccess || !mark(1)) return MOE_ERR_CUDA;
+  // one launch: the experts kernel computes the router logits itself
+  // (events 0 and 1 bracket no work)
+  if (!mark(0) || !mark(1)) return MOE_ERR_CUDA;
 
   ExpertsArgs ea;
   ea.x = x_norm;
@@ -247,10 +243,11 @@ __attribute__((visibility("hidden"))) moe_status run_layer(const moe_layer* laye
   ea.I = I;
   ea.E = E;
   ea.k = layer->top_k;
-  ea.G = ra.G;
+  ea.G = group_cap(K, E, layer->top_k);
   ea.has_shared = has_sh;
   ea.routed_scale = layer->routed_scale;
-  ea.logits = wp.logits;
+  ea.router_w = layer->router_w;
+  ea.router_bias = layer->router_bias;
   ea.gate = {layer->gate.scales, layer->gate.tensor_scale};
   ea.up = {layer->up.scales, layer->up.tensor_scale};
   ea.down = {layer->down.scales, layer->down.tensor_scale};

@@ -1,21 +1,28 @@
-// experts.cu -- the experts of one MoE verify-layer call in one persistent kernel.
+// experts.cu -- one MoE verify-layer call in one persistent kernel: router
+// logits, top-k routing and grouping, the NVFP4 experts, and the combine.
 //
 // One CTA per SM: a producer warp streams weight tiles into a ring of shared
-// memory stages with TMA (2-D tiled copies with swizzle for the 4-bit codes
-// and the gate/up E4M3 scales, 1-D bulk copies for the down scales) and eight
-// consumer warps decode and multiply.  The CTA's work is a fixed sequence of
-// items: its shared-expert gate/up items, its routed gate/up items, then its
-// down items.  Every distinct expert is streamed exactly once per call
-// however many rows chose it (PR #844, "8. What I looked at": the stock gather
-// re-reads an expert once per (row, slot)).
+// memory stages with TMA (tiled copies with swizzle for the 4-bit codes
+// and the gate/up E4M3 scales, 1-D bulk copies for the down scales) and
+// sixteen compute warps decode and multiply.  The CTA's work is a fixed
+// sequence of items: its shared-expert gate/up items, its routed gate/up
+// items, then its down items.  Every distinct expert is streamed exactly once
+// per call however many rows chose it (PR #844, "8. What I looked at": the
+// stock gather re-reads an expert once per (row, slot)).
 //
-// Overlap: before the programmatic-launch wait the producer already streams
-// the shared expert's first tiles (they do not depend on the routing) and the
-// consumers stage the activations.  After it, every CTA reads the router
-// logits and computes the same routing (top-k with lower-index tie-break,
-// renormalised softmax weights, grouping) on its own -- no serial hand-off.
-// A down item of expert u waits (bounded) until all gate/up items of u have
-// published h; its weight tiles are already in flight by then.
+// Router: the CTAs share the K x E logits (each forms those of its own
+// experts, in the fixed order of the router GEMV, and publishes them as
+// tagged words), then every CTA reads all of them and computes the same
+// routing (top-k with lower-index tie-break, renormalised softmax weights,
+// grouping) on its own -- no second kernel, no serial hand-off.  Before the
+// programmatic-launch wait the producer already streams the shared expert's
+// first tiles and the compute warps hold their router rows.
+//
+// Exchange between CTAs: h (gate/up -> down), the down partials (down ->
+// combine) and the logits are tagged 64-bit words (the call's tag next to a
+// 32-bit payload), so a reader validates each word itself: no fences, no
+// grid barrier, no per-call clearing.  Relaxed counters, cleared a call
+// ahead, only tell readers when to look.
 //
 // Decode: ldmatrix pulls 32 bits of codes per thread and row; the hardware
 // FP4 -> FP16 convert turns 8 codes into four f16x2, and one f16x2 multiply
@@ -25,11 +32,10 @@
 // FP32 accumulation; the tensor scale is applied to the accumulator.  The k
 // index of an mma step is a permutation of the physical k (any order is a
 // valid dot product): thread t's elements are its own 8 consecutive codes.
-// Activations enter as FP16 after an exact per-row power-of-two rescaling
-// (max |value| into [2^14, 2^15)), undone in FP32.
+// Activations enter as FP16 after an exact power-of-two rescaling (per row;
+// h per row and 128-wide k-unit), undone in FP32.
 //
-// Combine: per-(row, slot) FP32 partials; the CTA that completes the last
-// item of a 64-row hidden tile (atomic count, no waiting) forms
+// Combine: per-(row, slot) FP32 partials; the outputs are shared by the CTAs,
 // y = bf16(routed_scale * sum_s w_s d_s + d_shared + residual) in slot order
 // (PR #844, "4. What I ported": weighted sum, routed scale, shared add,
 // residual add in one pass).
@@ -49,35 +55,63 @@ namespace {
 constexpr int kCompWarps = 16;
 constexpr int kCompThreads = kCompWarps * 32;
 constexpr int kProducerWarp = kCompWarps;
-constexpr int kPublisherWarp = kCompWarps + 1;  // publishes finished gate/up items at GPU scope
-constexpr int kThreads = kCompThreads + 64;
+constexpr int kThreads = kCompThreads + 32;
 constexpr uint64_t kDrainNs = 2000000000ull;  // bound on waiting for our own copies before exit
 
 // named barrier 1: the compute warps
 __device__ __forceinline__ void comp_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kCompThreads) : "memory"); }
 
-__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
-
 __device__ __forceinline__ void red_relaxed_add(unsigned* p, unsigned v) {
   asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ unsigned ld_acquire_cta(const unsigned* p) {
+__device__ __forceinline__ unsigned ld_relaxed(const unsigned* p) {
   unsigned v;
-  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
-}
-
-__device__ __forceinline__ void red_release_cta_shared_add(unsigned* p, unsigned v) {
-  asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ void set_error(int* err, int code) { atomicCAS(err, 0, code); }
 
-__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+// Tagged words: a 32-bit payload in the low half and the call's tag in the
+// high half, written and read as one naturally aligned 64-bit access, which
+// is single-copy atomic.  A reader that sees this call's tag sees the payload
+// written with it, so the words need no fence and no flag, and stale words
+// of earlier calls (older tags) need no clearing.  Counters only tell a
+// reader when to look.
+__device__ __forceinline__ unsigned long long tagged(unsigned tag, unsigned v) {
+  return ((unsigned long long)tag << 32) | v;
+}
+__device__ __forceinline__ bool has_tag(unsigned long long w, unsigned tag) { return (unsigned)(w >> 32) == tag; }
+
+__device__ __forceinline__ void st_tagged(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// The same by an atomic exchange, for words every CTA waits on at once (the
+// router logits): plain stores from some SMs reached readers on other SMs
+// microseconds late on this two-die part, while atomics, performed where the
+// line lives, were visible at the next read.
+__device__ __forceinline__ void xchg_tagged(unsigned long long* p, unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.relaxed.gpu.global.exch.b64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+  (void)old;
+}
+
+// Between two attempts of a poll (measured: a short sleep beats spinning on
+// loads, for the waiting warp and for the L2 lines every CTA polls).
+__device__ __forceinline__ void poll_pause() { __nanosleep(128); }
+
+__device__ __forceinline__ unsigned long long ld_tagged(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
+}
+
+// Two consecutive tagged words (16-byte aligned); each element is one
+// 64-bit access.
+__device__ __forceinline__ void ld_tagged2(const unsigned long long* p, unsigned long long& a, unsigned long long& b) {
+  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
 }
 
 // Power-of-two shift that maps max |x| into [2^14, 2^15).
@@ -163,17 +197,41 @@ __device__ __forceinline__ void warp_top8(unsigned long long (&v)[8]) {
   }
 }
 
-// Top-k of one row of E logits for any E <= 1024, k <= 32 (lane l holds
-// experts l + 32 i): k rounds of a warp arg-max, larger logit first and lower
-// index on ties; NaN logits rank last, lowest index first.  Lane 0 writes the
-// selected experts and their logits.
-__device__ __noinline__ void topk_general(const float* row, int E, int k, int* idx, float* w, int lane) {
+// Whether a warp's bounded wait that began at t0 gives up now (the abort
+// flag is set, or the limit has passed): lane 0 decides for the warp.
+__device__ __forceinline__ bool warp_gives_up(uint64_t t0, uint64_t wait_ns, const int* abort_flag, int lane) {
+  int stop = 0;
+  if (lane == 0)
+    stop = *reinterpret_cast<const volatile int*>(abort_flag) != 0 || wait_ns == 0 || global_timer_ns() - t0 > wait_ns;
+  return __shfl_sync(0xffffffffu, stop, 0) != 0;
+}
+
+// Top-k of one row of E tagged logits for any E <= 1024, k <= 32 (lane l
+// holds experts l + 32 i), read once every word carries `tag` (a bounded
+// wait; false if it gave up): k rounds of a warp arg-max, larger logit first
+// and lower index on ties; NaN logits rank last, lowest index first.  Lane 0
+// writes the selected experts and their logits.
+__device__ __noinline__ bool topk_general(const unsigned long long* row, unsigned tag, uint64_t wait_ns,
+                                          const int* abort_flag, int E, int k, int* idx, float* w, int lane) {
   float lv[32];
   unsigned taken = 0;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    bool mine = true;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const int e = lane + 32 * i;
-    lv[i] = (e < E) ? __ldcg(row + e) : -INFINITY;
+    for (int i = 0; i < 32; ++i) {
+      const int e = lane + 32 * i;
+      float v = -INFINITY;
+      if (e < E) {
+        const unsigned long long wv = ld_tagged(row + e);
+        mine &= has_tag(wv, tag);
+        v = __uint_as_float((unsigned)wv);
+      }
+      lv[i] = v;
+    }
+    if (__all_sync(0xffffffffu, mine)) break;
+    if (warp_gives_up(t0, wait_ns, abort_flag, lane)) return false;
+    poll_pause();
   }
   for (int s = 0; s < k; ++s) {
     float bv = -INFINITY;
@@ -215,6 +273,7 @@ __device__ __noinline__ void topk_general(const float* row, int E, int k, int* i
       w[s] = bv;  // logit for now
     }
   }
+  return true;
 }
 
 // The grouping of one call for the caller (one warp): the distinct experts,
@@ -541,8 +600,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
   __shared__ unsigned s_xamax[16];
   __shared__ unsigned s_used[32];  // bitmask of the experts any row selected
-  __shared__ unsigned s_hpub;      // compute-warp arrivals at ends of gate/up slot runs (monotonic)
   __shared__ int s_abort, s_nu;
+  __shared__ unsigned long long s_call;
 
   const int H = a.H, I = a.I, K = a.K, G = a.G, E = a.E, k = a.k;
   const int S = a.stages;
@@ -554,12 +613,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int grid = gridDim.x;
 
   // reduction slots (two, alternating by item): the compute warps' FP32
-  // partials, then 16 per-row inverse h scales (down items).  Warp w's block
+  // partials, then the inverse h scales of down items ([k-unit][row], 4 x 16).  Warp w's block
   // starts at w * kWarpStride + red_skew(w): the skew puts the partials that
   // the 4 lanes of an epilogue quad read (warps 4j + 0..3) in distinct banks.
   constexpr int kWarpStride = 2 * NB * 128 + 32;
   constexpr int kRedPart = kCompWarps * kWarpStride;
-  constexpr int kRedFloats = kRedPart + 16;
+  constexpr int kRedFloats = kRedPart + 64;
   auto red_at = [](int w) { return w * kWarpStride + 2 * (w & 1) + 16 * ((w >> 1) & 1); };
   float* red = reinterpret_cast<float*>(smem + (size_t)S * stage_bytes);
   unsigned char* rsm = reinterpret_cast<unsigned char*>(red + 2 * kRedFloats);
@@ -577,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&empty_bar[s], kCompWarps);
     }
     s_abort = 0;
-    s_hpub = 0u;
+    s_call = 0ull;
     fence_mbar_init();
   }
   if (threadIdx.x < 16) s_xamax[threadIdx.x] = 0u;
@@ -607,10 +666,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_slots = n_u + (a.has_shared ? 1 : 0);
     return make_seq(make_plan(n_sh, n_u * mt_per, n_slots * n_tiles), mt_per, n_tiles, G, a.has_shared);
   };
-  // all gate/up items of a slot are published: one count per item, summed
-  // over the CTAs that hold items of the slot
-  const unsigned gu_target = (unsigned)mt_per;
-
   // ---------------------------------------------------------------- before the dependency wait
   // The shared items of this CTA come first in its sequence and need no routing.
   const int n_shb = split_before(blockIdx.x + 1, n_sh, grid) - split_before(blockIdx.x, n_sh, grid);
@@ -661,8 +716,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  // activations (the block input is complete before the router kernel
-  // started): compute warp w holds k-unit w of every row as FP16 B
+  // Router logits, spread over the CTAs: CTA b owns experts b + grid m
+  // (m < M) and its compute warps take the (expert, row) pairs p = warp,
+  // warp + 16, ... (m = p % M, row p / M).  A warp's first router row goes to
+  // registers before the dependency wait (the weights do not depend on it).
+  const int M = (E + grid - 1) / grid;
+  const int n_pairs = M * K;
+  uint4 lw[8];  // the warp's current router row: lane l holds pieces 256 j + 8 l .. + 7
+  int lw_e = -1;
+  auto load_router_row = [&](int e) {
+    const uint4* wrow = reinterpret_cast<const uint4*>(a.router_w + (size_t)e * H);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (j < H / 256) lw[j] = ldg_nc_v4(wrow + j * 32 + lane);
+    lw_e = e;
+  };
+  if (warp < kCompWarps && warp < n_pairs) {
+    const int e = (int)blockIdx.x + grid * (warp % M);
+    if (e < E) load_router_row(e);
+  }
+
+  if (threadIdx.x == 0) stamp(1);
+  pdl_wait();  // the block input (and the workspace) are complete from here on
+  if (threadIdx.x == 0) stamp(2);
+
+  // The call's index is the number of CTA exits of all earlier calls over the
+  // grid (a CTA of this call exits only after this read, and adds one exit,
+  // so the quotient is the same for every CTA).  Thread 0 reads it for the
+  // CTA (one read, not one per thread, of the word every CTA reads).
+  if (threadIdx.x == 0) s_call = __ldcg(a.ws.exits) / (unsigned long long)grid;
+
+  // activations: compute warp w holds k-unit w of every row as FP16 B
   // fragments; the row maxima now, the fragments after the routing, while
   // the first weight tiles are in flight
   auto load_x = [&](uint4 (&raw)[NB][4]) {
@@ -672,12 +756,51 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (warp < H / 128 && n < K) v = *reinterpret_cast<const uint4*>(a.x + (size_t)n * H + warp * 128 + q * 32 + 8 * t);
+        if (warp < H / 128 && n < K)
+          v = __ldcg(reinterpret_cast<const uint4*>(a.x + (size_t)n * H + warp * 128 + q * 32 + 8 * t));
         raw[nb][q] = v;
       }
     }
   };
   if (warp < kCompWarps) {
+    // this CTA's router logits: per lane, products in element order over
+    // the pieces j, then xor rounds 16 .. 1, then the bias (the arithmetic
+    // of the router GEMV, so the logits are the same bits)
+    // (lane 0 of each such warp reads the call index for the tag itself, so
+    // the logits leave as soon as they are formed)
+    unsigned long long wcall = 0ull;
+    if (lane == 0 && warp < n_pairs) wcall = __ldcg(a.ws.exits) / (unsigned long long)grid;
+    for (int p = warp; p < n_pairs; p += kCompWarps) {
+      const int e = (int)blockIdx.x + grid * (p % M), r = p / M;
+      if (e >= E) continue;
+      if (e != lw_e) load_router_row(e);
+      const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)r * H);
+      uint4 xv[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j < H / 256) xv[j] = __ldcg(xr + j * 32 + lane);
+      float acc = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j >= H / 256) break;
+        const uint32_t xq[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+        const uint32_t wq[4] = {lw[j].x, lw[j].y, lw[j].z, lw[j].w};
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float xf = __uint_as_float((u & 1) ? (xq[u >> 1] & 0xFFFF0000u) : (xq[u >> 1] << 16));
+          const float wf = __uint_as_float((u & 1) ? (wq[u >> 1] & 0xFFFF0000u) : (wq[u >> 1] << 16));
+          acc = __fmaf_rn(xf, wf, acc);
+        }
+      }
+#pragma unroll
+      for (int d = 16; d >= 1; d >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, d));
+      if (lane == 0) {
+        const float lg = a.router_bias ? __fadd_rn(acc, a.router_bias[e]) : acc;
+        xchg_tagged(a.ws.tlog + (size_t)r * E + e, tagged((unsigned)(wcall % 0xFFFFFFFFull) + 1u, __float_as_uint(lg)));
+      }
+    }
+
+    if (threadIdx.x == 0) stamp(14);
     uint4 raw[NB][4];
     load_x(raw);
 #pragma unroll
@@ -697,36 +820,71 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = nb * 8 + g;
       if (t == 0 && n < K) atomicMax(&s_xamax[n], mx);
     }
-    comp_bar();  // routing tables cleared before any warp marks them
+    comp_bar();  // routing tables cleared before any warp marks them; s_call written
+    if (threadIdx.x == 0) stamp(15);
   }
-
-  if (threadIdx.x == 0) stamp(1);
-  pdl_wait();  // router logits complete; per-call counters cleared
-  if (threadIdx.x == 0) stamp(2);
+  // (the producer warp reads s_call too early; it uses none of these)
+  const unsigned long long call = *reinterpret_cast<volatile unsigned long long*>(&s_call);
+  // the tag of this call's words, never 0 (the value of a zero-filled
+  // workspace); counter set call % 2 is this call's, and this call clears
+  // the other one for the next call
+  const unsigned tag = (unsigned)(call % 0xFFFFFFFFull) + 1u;
+  unsigned* cnt = a.ws.cnt + (call & 1ull) * kCntSet;
+  unsigned* cnt_tiles = cnt + kCntDone;
+  if (warp < kCompWarps) {
+    unsigned* other = a.ws.cnt + ((call + 1ull) & 1ull) * kCntSet;
+    for (int i = (int)blockIdx.x * kCompThreads + (int)threadIdx.x; i < kCntSet; i += grid * kCompThreads) other[i] = 0u;
+  }
 
   // ---------------------------------------------------------------- routing (every CTA, identical)
   if (warp < kCompWarps) {
     const bool fast = E <= 256 && k <= 8;
     for (int r = warp; r < K; r += kCompWarps) {
+      // row r's logits, once every word of it carries this call's tag (a
+      // bounded wait; on giving up, experts 0 .. k-1 keep the tables in
+      // range and the abort flag stops the work)
+      const unsigned long long* row = a.ws.tlog + (size_t)r * E;
+      bool got = true;
       if (fast) {
         unsigned long long v[8];
+        const uint64_t t0 = global_timer_ns();
+        for (;;) {
+          bool mine = true;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int e = lane + 32 * i;
-          v[i] = (e < E) ? sel_key(__ldcg(a.logits + (size_t)r * E + e), e) : 0ull;
+          for (int i = 0; i < 8; ++i) {
+            const int e = lane + 32 * i;
+            v[i] = 0ull;
+            if (e < E) {
+              const unsigned long long wv = ld_tagged(row + e);
+              mine &= has_tag(wv, tag);
+              v[i] = sel_key(__uint_as_float((unsigned)wv), e);
+            }
+          }
+          if (__all_sync(0xffffffffu, mine)) break;
+          if (warp_gives_up(t0, a.wait_ns, &s_abort, lane)) {
+            got = false;
+            break;
+          }
+          poll_pause();
         }
         warp_top8(v);
         if (lane == 0) {
 #pragma unroll
           for (int s = 0; s < 8; ++s)
             if (s < k) {
-              s_idx[r * k + s] = key_index(v[s]);
-              s_w[r * k + s] = key_value(v[s]);  // logit for now
+              s_idx[r * k + s] = got ? key_index(v[s]) : s;
+              s_w[r * k + s] = got ? key_value(v[s]) : 0.f;  // logit for now
             }
         }
       } else {
-        topk_general(a.logits + (size_t)r * E, E, k, s_idx + r * k, s_w + r * k, lane);
+        got = topk_general(row, tag, a.wait_ns, &s_abort, E, k, s_idx + r * k, s_w + r * k, lane);
+        if (!got && lane == 0)
+          for (int s = 0; s < k; ++s) {
+            s_idx[r * k + s] = s;
+            s_w[r * k + s] = 0.f;
+          }
       }
+      if (!got && lane == 0) fail();
       __syncwarp();
       const float m = s_w[r * k];
       const float ev = (lane < k) ? expf(s_w[r * k + lane] - m) : 0.f;
@@ -778,34 +936,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   pdl_launch_dependents();
   if (threadIdx.x == 0) stamp(3);
-
-  if (warp == kPublisherWarp) {
-    // ------------------------------------------------------------ publisher
-    // Publishes this CTA's finished gate/up items on their slots' counters
-    // (GPU scope) once their duty warps have stored the h rows: one fence per
-    // batch of finished items, on a warp that nothing else waits for.
-    if (lane == 0) {
-      const Seq seq = make_cta_seq();
-      const int L_gu = seq.p.n_shb + seq.p.rt_count;
-      Cursor pc = seq_begin(seq);
-      int pl = 0;  // items published so far
-      const uint64_t t0 = global_timer_ns();
-      while (pl < L_gu) {
-        const int done_items = (int)(ld_acquire_cta(&s_hpub) >> 2);  // 4 duty warps per item
-        if (done_items > pl) {
-          fence_acq_rel_gpu();
-          for (; pl < done_items && pl < L_gu; ++pl) {
-            red_relaxed_add(&a.ws.done[pc.it.slot], 1u);
-            seq_next(pc, seq);
-          }
-          continue;
-        }
-        if (aborted() || a.wait_ns == 0 || global_timer_ns() - t0 > a.wait_ns) break;
-        __nanosleep(128);
-      }
-    }
-    return;
-  }
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -945,7 +1075,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // next item): thread o of the group owns output o (row o / 8 of the
       // item's 16, column o % 8 of each n-block) and sums its 16 k-unit
       // partials in k-unit order
-      if ((warp >> 2) == (l & 3) && !aborted()) {
+      const bool live = !__any_sync(0xffffffffu, aborted());
+      if ((warp >> 2) == (l & 3) && live) {
         const int slot = gu_slot(l);
         const int Vg = (int)blockIdx.x + l * grid;
         const int tile = Vg < n_sh ? Vg : ((Vg - n_sh) & (mt_per - 1));
@@ -966,19 +1097,22 @@ __global__ void __launch_bounds__(kThreads, 1)
               us += rb[red_at(w) + NB * 128 + f];
             }
           }
-          if (n < K) {
-            const float inv = pow2f(-row_shift(s_xamax[n]));
-            const float gv = gs * inv * tg;
-            const float uv = us * inv * tu;
-            const float hv = gv * __frcp_rn(1.f + expf(-gv)) * uv;
-            const uint16_t hb = float_to_bf16_bits(hv);
-            a.ws.h[((size_t)slot * K + n) * I + tile * kGURows + i] = hb;
-            atomicMax(&a.ws.hamax[slot * K + n], (unsigned)(hb & 0x7FFFu));
-          }
+          // (rows n >= K have zero activations, so h = 0 there)
+          const float inv = pow2f(-row_shift(s_xamax[n]));
+          const float gv = gs * inv * tg;
+          const float uv = us * inv * tu;
+          const float hv = gv * __frcp_rn(1.f + expf(-gv)) * uv;
+          const unsigned hb = float_to_bf16_bits(hv);
+          // h rows i and i + 1 (lanes o and o + 8 of this warp) share a word
+          const unsigned hn = __shfl_down_sync(0xffffffffu, hb, 8);
+          if (n < K && (i & 1) == 0)
+            st_tagged(a.ws.h + ((size_t)slot * K + n) * (I / 2) + ((tile * kGURows + i) >> 1),
+                      tagged(tag, hb | (hn << 16)));
         }
-        // every gate/up item: this duty warp's h rows are stored
+        // this duty warp's h words are written (the count only tells readers
+        // when to look; the tags make the words themselves safe to read)
         __syncwarp();
-        if (lane == 0) red_release_cta_shared_add(&s_hpub, 1u);
+        if (lane == 0) red_relaxed_add(cnt + slot, 1u);
       }
       if (threadIdx.x == 0 && l < 4) stamp(19 + 4 * l);
     }
@@ -1003,39 +1137,73 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* rb = red + (size_t)(l & 1) * kRedFloats;
         const int dj = l - L_gu;  // down item index (trace stamps 32 + 4 dj ..)
         if (threadIdx.x == 0 && dj < 4) stamp(32 + 4 * dj);
-        bool ok = !aborted();
+        bool ok = !__any_sync(0xffffffffu, aborted());
         if (ok && it.slot != cur_slot) {
-          // h of this slot: every warp waits (bounded, no CTA barrier) until
-          // all gate/up items of the slot are published, then reads it as B
-          // fragments
+          // h of this slot, k-unit kq: every warp waits (bounded, no CTA
+          // barrier) until the slot's count shows all 4 mt_per duty warps of
+          // its gate/up items, then reads its words, again after a pause in
+          // the rare case that one is not visible yet, as B fragments; each
+          // k-unit takes its own per-row power-of-two scale
           cur_slot = it.slot;
           int ready = 0;
           if (lane == 0) {
             const uint64_t t0 = global_timer_ns();
-            while (!(ready = ld_acquire(&a.ws.done[it.slot]) >= gu_target)) {
+            while (!(ready = ld_relaxed(cnt + it.slot) >= 4u * (unsigned)mt_per)) {
               if (aborted() || a.wait_ns == 0 || global_timer_ns() - t0 > a.wait_ns) break;
-              __nanosleep(256);
+              poll_pause();
             }
-            if (!ready) fail();
           }
           ok = __shfl_sync(0xffffffffu, ready, 0) != 0;
+          unsigned mx[NB];
           if (ok) {
-            (void)ld_acquire(&a.ws.done[it.slot]);  // this lane's own acquire before it reads h
+            const unsigned long long* hs = a.ws.h + (size_t)it.slot * K * (I / 2) + kq * 64 + 4 * t;
+            const uint64_t t0 = global_timer_ns();
+            for (;;) {
+              bool mine = true;
+#pragma unroll
+              for (int nb = 0; nb < NB; ++nb) {
+                const int n = nb * 8 + g;
+                mx[nb] = 0u;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  unsigned long long w0 = 0ull, w1 = 0ull, w2 = 0ull, w3 = 0ull;
+                  if (dn_active && n < K) {
+                    ld_tagged2(hs + (size_t)n * (I / 2) + q * 16, w0, w1);
+                    ld_tagged2(hs + (size_t)n * (I / 2) + q * 16 + 2, w2, w3);
+                    mine &= has_tag(w0, tag) & has_tag(w1, tag) & has_tag(w2, tag) & has_tag(w3, tag);
+                  }
+                  const uint32_t hw[4] = {(uint32_t)w0, (uint32_t)w1, (uint32_t)w2, (uint32_t)w3};
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    bh[nb][q * 4 + j] = hw[j];  // bf16 pairs for now
+                    mx[nb] = max(mx[nb], (hw[j] << 16) & 0x7FFFFFFFu);
+                    mx[nb] = max(mx[nb], hw[j] & 0x7FFF0000u);
+                  }
+                }
+              }
+              if (__all_sync(0xffffffffu, mine)) break;
+              if (warp_gives_up(t0, a.wait_ns, &s_abort, lane)) {
+                ok = false;
+                break;
+              }
+              poll_pause();
+            }
+          }
+          if (!ok && lane == 0) fail();
+          if (ok) {
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb) {
+              mx[nb] = max(mx[nb], __shfl_xor_sync(0xffffffffu, mx[nb], 1));
+              mx[nb] = max(mx[nb], __shfl_xor_sync(0xffffffffu, mx[nb], 2));
               const int n = nb * 8 + g;
-              const int sh = (n < K) ? row_shift(__ldcg(a.ws.hamax + it.slot * K + n) << 16) : 0;
+              const int sh = (n < K) ? row_shift(mx[nb]) : 0;
               const float sc = pow2f(sh);
               if (nb == 0) hinv = pow2f(-sh);
               else hinv1 = pow2f(-sh);
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (dn_active && n < K)
-                  v = __ldcg(reinterpret_cast<const uint4*>(a.ws.h + ((size_t)it.slot * K + n) * I + kq * 128 +
-                                                            q * 32 + 8 * t));
-                bf16x8_to_f16x8(v, sc, &bh[nb][q * 4]);
-              }
+              for (int q = 0; q < 4; ++q)
+                bf16x8_to_f16x8(make_uint4(bh[nb][q * 4 + 0], bh[nb][q * 4 + 1], bh[nb][q * 4 + 2], bh[nb][q * 4 + 3]),
+                                sc, &bh[nb][q * 4]);
             }
           }
         }
@@ -1082,9 +1250,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<float2*>(pb + 2) = make_float2(cB[nb][2], cB[nb][3]);
           }
         }
-        if (warp == 0 && t == 0) {
-          rb[kRedPart + g] = hinv;
-          if (NB == 2) rb[kRedPart + 8 + g] = hinv1;
+        if (mA == 0 && dn_active && t == 0) {  // the inverse h scales of k-unit kq
+          rb[kRedPart + kq * 16 + g] = hinv;
+          if (NB == 2) rb[kRedPart + kq * 16 + 8 + g] = hinv1;
         }
         comp_bar();
         if (threadIdx.x == 0 && dj < 4) stamp(35 + 4 * dj);
@@ -1092,7 +1260,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // next item): thread o of the group owns output (i, c) of m-tiles
         // M = 0..7 in each n-block; the k-unit partials of m-tile M sit at
         // warps M % 4 + 4 q, in their first (M < 4) or second half
-        if ((warp >> 2) == (l & 3) && !aborted()) {
+        const bool live = !__any_sync(0xffffffffu, aborted());
+        if ((warp >> 2) == (l & 3) && live) {
           const float ts = s_tse[3 * s_uexp[it.slot] + 2];
           const int o = (warp & 3) * 32 + lane;
           const int i = o >> 3, c = o & 7;
@@ -1103,51 +1272,92 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (n >= K) continue;
             const int s = s_slot[it.slot * K + n];
             if (s < 0) continue;
-            const float sc = rb[kRedPart + n] * ts;
-            float* dst = a.ws.dpart + ((size_t)n * (k + 1) + s) * H + it.tile * kDNRows + i;
+            float iq[4];  // inverse h scale of each k-unit (exact powers of two)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) iq[q] = q < KUdn ? rb[kRedPart + q * 16 + n] : 0.f;
+            unsigned long long* dst = a.ws.dpart + ((size_t)n * (k + 1) + s) * H + it.tile * kDNRows + i;
 #pragma unroll
             for (int M = 0; M < 8; ++M) {
               const int f = ((M >> 2) * NB + nb) * 128 + f0;
               float v4[4];
 #pragma unroll
-              for (int q = 0; q < 4; ++q) v4[q] = q < KUdn ? rb[red_at(q * 4 + (M & 3)) + f] : 0.f;
+              for (int q = 0; q < 4; ++q) v4[q] = q < KUdn ? rb[red_at(q * 4 + (M & 3)) + f] * iq[q] : 0.f;
               const float v = ((v4[0] + v4[1]) + v4[2]) + v4[3];  // k-units in order
-              dst[M * 16] = v * sc;
+              st_tagged(dst + M * 16, tagged(tag, __float_as_uint(v * ts)));
             }
           }
+          // this duty warp's partials of the hidden tile are written
+          __syncwarp();
+          if (lane == 0) red_relaxed_add(cnt_tiles + it.tile, 1u);
         }
       }
     }
   }
 
-  // every CTA's partials are written: grid-wide barrier (the launch is
-  // cooperative, all CTAs are resident; the wait is bounded), then the
-  // CTAs share the outputs:
+  // The outputs, shared by the CTAs (no grid barrier): the 32 outputs of a
+  // warp lie in one hidden tile (H is a multiple of 256), lane 0 waits
+  // (bounded) until the tile's count shows the 4 duty warps of every slot's
+  // down item, then each lane reads its partials with their tags (again after
+  // a pause in the rare case that one is not visible yet):
   //   y = bf16(routed_scale * sum_s w_s d_s + d_shared + residual), slots in order
-  comp_bar();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(a.ws.gridbar, 1u);
-    const uint64_t t0 = global_timer_ns();
-    while (ld_acquire(a.ws.gridbar) < (unsigned)grid) {
-      if (aborted() || a.wait_ns == 0 || global_timer_ns() - t0 > a.wait_ns) {
-        fail();
-        break;
-      }
-      __nanosleep(64);
-    }
-    if (trace) trace[60] = global_timer_ns();
-  }
-  comp_bar();
-  if (!aborted()) {
+  if (threadIdx.x == 0) stamp(60);
+  if (!__any_sync(0xffffffffu, aborted())) {
+    const unsigned tile_target = 4u * (unsigned)(*reinterpret_cast<volatile int*>(&s_nu) + (a.has_shared ? 1 : 0));
+    const int ns = k + (a.has_shared ? 1 : 0);  // partials per output
     for (int o = blockIdx.x * kCompThreads + threadIdx.x; o < K * H; o += grid * kCompThreads) {
       const int n = o / H, j = o - n * H;
-      float acc2 = 0.f;
-      for (int s = 0; s < k; ++s)
-        acc2 = __fmaf_rn(s_w[n * k + s], __ldcg(a.ws.dpart + ((size_t)n * (k + 1) + s) * H + j), acc2);
+      int ready = 0;
+      if (lane == 0) {
+        const unsigned* tc = cnt_tiles + j / kDNRows;
+        const uint64_t t0 = global_timer_ns();
+        while (!(ready = ld_relaxed(tc) >= tile_target)) {
+          if (aborted() || a.wait_ns == 0 || global_timer_ns() - t0 > a.wait_ns) break;
+          poll_pause();
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, ready, 0)) {
+        if (lane == 0) fail();
+        break;
+      }
+      const unsigned long long* dp = a.ws.dpart + (size_t)n * (k + 1) * H + j;
+      const float rv = a.residual ? bf16_bits_to_float(a.residual[(size_t)n * H + j]) : 0.f;
+      float acc2 = 0.f, shv = 0.f;
+      bool good = true;
+      for (int s0 = 0; s0 < ns && good; s0 += 8) {
+        unsigned long long pw[8];
+        const uint64_t t0 = global_timer_ns();
+        for (;;) {  // every load of the chunk in flight at once
+          bool all = true;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            pw[u] = 0ull;
+            if (s0 + u < ns) {
+              pw[u] = ld_tagged(dp + (size_t)(s0 + u) * H);
+              all &= has_tag(pw[u], tag);
+            }
+          }
+          if (all) break;
+          if (aborted() || a.wait_ns == 0 || global_timer_ns() - t0 > a.wait_ns) {
+            good = false;
+            break;
+          }
+          poll_pause();
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int s = s0 + u;
+          const float pv = __uint_as_float((unsigned)pw[u]);
+          if (s < k) acc2 = __fmaf_rn(s_w[n * k + s], pv, acc2);
+          else if (s == k) shv = pv;
+        }
+      }
+      if (!__all_sync(0xffffffffu, good)) {
+        if (lane == 0) fail();
+        break;
+      }
       float v = a.routed_scale * acc2;
-      if (a.has_shared) v += __ldcg(a.ws.dpart + ((size_t)n * (k + 1) + k) * H + j);
-      if (a.residual) v += bf16_bits_to_float(a.residual[(size_t)n * H + j]);
+      if (a.has_shared) v += shv;
+      if (a.residual) v += rv;
       a.y[(size_t)n * H + j] = float_to_bf16_bits(v);
     }
   }
@@ -1159,7 +1369,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (a.group_out && warp == 0) write_groups(a.group_out, s_nu, G, K, k, s_uexp, s_rowmask, s_slot, lane);
   }
-  if (threadIdx.x == 0) stamp(7);
+  // one exit per CTA and call, whatever happened: the next call's index
+  if (threadIdx.x == 0) {
+    atomicAdd(a.ws.exits, 1ull);
+    stamp(7);
+  }
 }
 
 // =====================================================================
@@ -1186,7 +1400,7 @@ static size_t routing_smem_bytes(int K, int E, int k, int G) {
          sizeof(float) * 3 * (E + 1) + (size_t)(G + 1) * K + 16;
 }
 
-static size_t red_slot_bytes(int NB) { return sizeof(float) * ((size_t)kCompWarps * (2 * NB * 128 + 32) + 16); }
+static size_t red_slot_bytes(int NB) { return sizeof(float) * ((size_t)kCompWarps * (2 * NB * 128 + 32) + 64); }
 
 size_t experts_smem_bytes(int K, int H, int I, int E, int k, int G, int* stages, int* nred) {
   const int NB = K > 8 ? 2 : 1;
@@ -1206,6 +1420,7 @@ static cudaError_t launch_experts_t(const ExpertsArgs& a, const CUtensorMap* map
   auto kern = k_moe_experts<NB>;
   int stages = 0, nred = 0;
   const size_t smem = experts_smem_bytes(a.K, a.H, a.I, a.E, a.k, a.G, &stages, &nred);
+  const int grid = num_sms();
   if (stages < 2 || a.H > 128 * kCompWarps || a.I > 128 * 4) return cudaErrorInvalidValue;
   ExpertsArgs b = a;
   b.stages = stages;
@@ -1213,7 +1428,7 @@ static cudaError_t launch_experts_t(const ExpertsArgs& a, const CUtensorMap* map
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(num_sms());
+  cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;

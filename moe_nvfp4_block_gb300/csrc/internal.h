@@ -26,21 +26,29 @@ __host__ __device__ inline int expert_stage_bytes(int H, int I) {
   return (m + 1023) & ~1023;
 }
 
-// Byte offsets of the workspace regions (all 256-byte aligned).
+// Per-call counters of the experts kernel, two sets used by alternate calls
+// (a call clears the set the next call uses): per set, kCntDone words
+// counting finished gate/up duty warps per slot, then kCntTiles words
+// counting finished down duty warps per hidden tile.  Their place and size do
+// not depend on K, E or the layer, so a workspace stays valid across shapes.
+constexpr int kCntDone = 1025;  // slots: at most 1024 distinct experts + the shared one
+constexpr int kCntTiles = 16;   // hidden tiles: H / kDNRows <= 2048 / 128
+constexpr int kCntSet = 1056;   // words per set (kCntDone + kCntTiles, rounded up)
+
+// Byte offsets of the workspace regions (all 256-byte aligned).  Regions
+// before `logits` sit at fixed offsets.
 struct WsLayout {
-  size_t hdr;      // int32[64]: [0] error word, [1] router ticket
-  size_t logits;   // float [K][E]
+  size_t hdr;      // 256 bytes: int32 error word, uint32 router ticket, uint64 experts-kernel CTA exits
+  size_t cnt;      // uint32 [2][kCntSet]: the per-call counters
+  size_t logits;   // float [K][E] (moe_router_topk)
   size_t idx;      // int32 [K][k]
   size_t w;        // float [K][k]
   size_t group;    // int32 [2 + 2G + K*k]
   size_t urow;     // uint32 [G+1]: rows routed to each distinct expert (bitmask)
   size_t slotmap;  // int32 [G+1][K]: slot of the expert in row r's selection, -1 if none
-  size_t hamax;    // uint32 [G+1][K]: max |h| bits per (expert, row)
-  size_t tilecnt;  // uint32 [H/64]: completed down items per hidden tile
-  size_t done;     // uint32 [G+1]: gate/up items completed per distinct expert
-  size_t gridbar;  // uint32: CTAs of the experts kernel past their down items
-  size_t h;        // bf16 [G+1][K][I]
-  size_t dpart;    // float [K][k+1][H]
+  size_t tlog;     // tagged [K][E]: router logits of the experts kernel
+  size_t h;        // tagged [G+1][K][I/2]: h, two bf16 per word
+  size_t dpart;    // tagged [K][k+1][H]: FP32 down partials per (row, slot)
   size_t total;
 };
 
@@ -58,18 +66,16 @@ inline WsLayout ws_layout(int K, int E, int k, int H, int I) {
     return r;
   };
   L.hdr = take(256);
+  L.cnt = take(sizeof(uint32_t) * 2 * kCntSet);
   L.logits = take(sizeof(float) * K * E);
   L.idx = take(sizeof(int32_t) * K * k);
   L.w = take(sizeof(float) * K * k);
   L.group = take(sizeof(int32_t) * (2 + 2 * G + K * k));
   L.urow = take(sizeof(uint32_t) * (G + 1));
   L.slotmap = take(sizeof(int32_t) * (G + 1) * K);
-  L.hamax = take(sizeof(uint32_t) * (G + 1) * K);
-  L.tilecnt = take(sizeof(uint32_t) * (H / kDNRows));
-  L.done = take(sizeof(uint32_t) * (G + 1));
-  L.gridbar = take(sizeof(uint32_t));
-  L.h = take(sizeof(uint16_t) * (size_t)(G + 1) * K * I);
-  L.dpart = take(sizeof(float) * (size_t)K * (k + 1) * H);
+  L.tlog = take(sizeof(uint64_t) * K * E);
+  L.h = take(sizeof(uint64_t) * (size_t)(G + 1) * K * (I / 2));
+  L.dpart = take(sizeof(uint64_t) * (size_t)K * (k + 1) * H);
   L.total = o;
   return L;
 }
@@ -84,12 +90,11 @@ struct WsPtrs {
   int* group;
   unsigned* urow;
   int* slotmap;
-  unsigned* hamax;
-  unsigned* tilecnt;
-  unsigned* done;
-  unsigned* gridbar;
-  uint16_t* h;
-  float* dpart;
+  unsigned long long* exits;  // CTA exits of the experts kernel, all calls (the call index is exits / grid)
+  unsigned* cnt;              // [2][kCntSet]
+  unsigned long long* tlog;
+  unsigned long long* h;
+  unsigned long long* dpart;
 };
 
 inline WsPtrs ws_ptrs(void* ws, const WsLayout& L) {
@@ -103,12 +108,11 @@ inline WsPtrs ws_ptrs(void* ws, const WsLayout& L) {
   p.group = reinterpret_cast<int*>(b + L.group);
   p.urow = reinterpret_cast<unsigned*>(b + L.urow);
   p.slotmap = reinterpret_cast<int*>(b + L.slotmap);
-  p.hamax = reinterpret_cast<unsigned*>(b + L.hamax);
-  p.tilecnt = reinterpret_cast<unsigned*>(b + L.tilecnt);
-  p.done = reinterpret_cast<unsigned*>(b + L.done);
-  p.gridbar = reinterpret_cast<unsigned*>(b + L.gridbar);
-  p.h = reinterpret_cast<uint16_t*>(b + L.h);
-  p.dpart = reinterpret_cast<float*>(b + L.dpart);
+  p.exits = reinterpret_cast<unsigned long long*>(b + L.hdr + 8);
+  p.cnt = reinterpret_cast<unsigned*>(b + L.cnt);
+  p.tlog = reinterpret_cast<unsigned long long*>(b + L.tlog);
+  p.h = reinterpret_cast<unsigned long long*>(b + L.h);
+  p.dpart = reinterpret_cast<unsigned long long*>(b + L.dpart);
   return p;
 }
 
@@ -118,12 +122,10 @@ struct RouterArgs {
   const float* bias;        // [E] or null
   int K, H, E, k, G;
   int has_shared;
-  int n_tiles;              // H / kDNRows
   WsPtrs ws;
   int32_t* idx_out;         // caller copies (nullable)
   float* w_out;
   int32_t* group_out;
-  int do_topk;              // 1: the last CTA also selects and groups (moe_router_topk)
 };
 
 // Per-projection pointers the expert kernels need besides the tensor maps.
@@ -139,7 +141,8 @@ struct ExpertsArgs {
   int K, H, I, E, k, G;
   int has_shared;
   float routed_scale;
-  const float* logits;       // [K][E], from the router kernel
+  const uint16_t* router_w;  // [E][H] bf16
+  const float* router_bias;  // [E] or null
   ProjPtrs gate, up, down, sh_gate, sh_up, sh_down;
   WsPtrs ws;
   int32_t* idx_out;          // routing copies for the caller (nullable)

@@ -216,6 +216,26 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   return v;
 }
 
+// Copies n 16-byte words from global to shared memory with the whole block.
+// Each thread puts up to 8 loads in flight before it stores them: a plain
+// strided copy loop waits for every load before it issues the next, so its
+// time grows with n in whole L2 round trips.
+__device__ __forceinline__ void block_copy_g2s(uint4* dst, const uint4* src, int n) {
+  for (int i0 = threadIdx.x; i0 < n; i0 += 8 * (int)blockDim.x) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * (int)blockDim.x;
+      if (i < n) v[u] = __ldcg(src + i);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * (int)blockDim.x;
+      if (i < n) dst[i] = v[u];
+    }
+  }
+}
+
 // Byte offset of a 16-byte unit inside a TMA tile written with the 128-byte
 // (mask 7) or 64-byte (mask 3) swizzle: bits [6:4] (or [5:4]) of the address
 // are XORed with bits [9:7] (or [8:7]).  `off` is relative to a tile base

@@ -1,4 +1,6 @@
-// router.cu -- router GEMV + softmax + top-k + expert grouping (one launch).
+// router.cu -- router GEMV + softmax + top-k + expert grouping (one launch),
+// the moe_router_topk entry point.  (A layer call computes its router
+// logits inside the experts kernel, with the same arithmetic.)
 //
 // Each warp forms the logits of one expert for all K rows: lane l streams the
 // 16-byte pieces 256*j + 8*l .. +7 of the expert's bf16 router row and adds
@@ -12,7 +14,7 @@
 // router scores, renormalised), and groups the (row, slot) pairs by expert so
 // that each distinct expert is streamed once by the expert kernels (PR #844,
 // "8. What I looked at": the stock gather reads an expert once per
-// (row, slot)).  It also clears the per-call counters of the later kernels.
+// (row, slot)).
 #include <cfloat>
 #include <climits>
 
@@ -74,20 +76,11 @@ __global__ void __launch_bounds__(kRouterWarps * 32) k_router(RouterArgs a) {
   pdl_wait();  // the rows and the workspace are ours from here on
   pdl_launch_dependents();
 
-  if (!a.do_topk) {  // clear the experts kernel's per-call counters (a slice per CTA)
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < (G + 1) * K; i += gridDim.x * blockDim.x)
-      a.ws.hamax[i] = 0u;
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i <= G; i += gridDim.x * blockDim.x) a.ws.done[i] = 0u;
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < a.n_tiles; i += gridDim.x * blockDim.x)
-      a.ws.tilecnt[i] = 0u;
-    if (blockIdx.x == 0 && threadIdx.x == 0) *a.ws.gridbar = 0u;
-  }
-
   // ---------------------------------------------------------------- logits
   {
     uint4* xs = reinterpret_cast<uint4*>(smem);  // [K][H/8]
     const uint4* xg = reinterpret_cast<const uint4*>(a.x);
-    for (int i = threadIdx.x; i < K * H / 8; i += blockDim.x) xs[i] = xg[i];
+    block_copy_g2s(xs, xg, K * H / 8);
     __syncthreads();
     if (e < E) {
       float acc[KR];
@@ -123,7 +116,6 @@ __global__ void __launch_bounds__(kRouterWarps * 32) k_router(RouterArgs a) {
           if (r < K) a.ws.logits[(size_t)r * E + e] = a.bias ? __fadd_rn(acc[r], b) : acc[r];
       }
     }
-    if (!a.do_topk) return;
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {

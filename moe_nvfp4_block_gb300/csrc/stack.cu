@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(kLmWarps * 32) k_lmhead_argmax(LmHeadArgs a) {
   pdl_wait();
   pdl_launch_dependents();
   uint4* xs = reinterpret_cast<uint4*>(smem);
-  for (int i = threadIdx.x; i < K * H / 8; i += blockDim.x) xs[i] = reinterpret_cast<const uint4*>(a.x)[i];
+  block_copy_g2s(xs, reinterpret_cast<const uint4*>(a.x), K * H / 8);
   __syncthreads();
 
   float bv[KR];

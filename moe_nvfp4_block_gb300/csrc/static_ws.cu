@@ -14,7 +14,7 @@
 
 namespace {
 
-constexpr size_t kStaticWsBytes = size_t(4) << 20;  // 4 MiB
+constexpr size_t kStaticWsBytes = size_t(8) << 20;  // 8 MiB: enough for K <= 16 on the largest supported layer
 constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
@@ -48,8 +48,9 @@ extern "C" moe_status moe_verify_layer_static(const moe_layer* layer, const uint
   if (need > kStaticWsBytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
   void* ws = static_ws_on_current_device();
   if (!ws) return MOE_ERR_CUDA;
-  // counters and the error word of the previous call start again from zero
-  if (cudaMemsetAsync(ws, 0, 256, static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  // the error word of the previous call starts again from zero (the rest of
+  // the header, the count of earlier calls, must persist)
+  if (cudaMemsetAsync(ws, 0, sizeof(int), static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;
   return run_layer(layer, x_norm, K, residual, y, idx_out, w_out, group_out, ws, kStaticWsBytes, stream, true,
                    nullptr);
 }

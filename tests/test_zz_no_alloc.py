@@ -55,8 +55,8 @@ def test_static_scratch_matches_caller_workspace(cuda_ok, name):
 
 def test_static_scratch_refuses_oversized_layer(cuda_ok):
     import moe_nvfp4_block_gb300 as M
-    # 1024 experts, K=16, hidden 2048, intermediate 512: more than 4 MiB of scratch
+    # 1024 experts, top-32, K=16, hidden 2048, intermediate 512: more than 8 MiB of scratch
     L = M.moe_layer(2048, 1024, 32, 512, 512, 1.0, 16, None, *([M.moe_nvfp4(16, 16, 16)] * 6))
-    assert M.lib.moe_verify_layer_workspace_size(ctypes.byref(L), 16) > (4 << 20)
+    assert M.lib.moe_verify_layer_workspace_size(ctypes.byref(L), 16) > (8 << 20)
     st = M.lib.moe_verify_layer_static(ctypes.byref(L), 16, 16, None, 16, None, None, None, None)
     assert st == M.MOE_ERR_WORKSPACE_TOO_SMALL
