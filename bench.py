@@ -4,8 +4,8 @@
 Workload (default ``k2_layer``): DFlash K=2 verify through one MoE layer --
 hidden 2048, 256 routed experts, top-8, expert intermediate 512, a shared
 expert of intermediate 512, NVFP4 expert weights, bf16 router, 2 bf16 rows.
-A step is one layer call (router logits, then one persistent experts kernel:
-top-k -> dedup -> gate/up+SwiGLU -> down+combine) on one batch of K rows.  Steps cycle over a ring of distinct
+A step is one layer call -- one persistent kernel: router logits -> top-k ->
+dedup -> gate/up+SwiGLU -> down -> combine -- on one batch of K rows.  Steps cycle over a ring of distinct
 seeded layers whose touched bytes exceed L2 several times, so every step
 streams its experts from HBM.  The timed steps run as CUDA-graph replays.
 
@@ -15,9 +15,9 @@ value     = algorithmic bytes / time (GB/s): router weights + the distinct
 e2e       = the same metric through the C ABI from pinned host buffers, the
             host->device copy of x and device->host copy of y inside the
             timed region, one eager call per step.
-roofline  = the dominant kernel's algorithmic bytes per launch over its mean
+roofline  = the experts kernel's algorithmic bytes per launch over its mean
             CUDA-event duration (a graph-captured profiling pass with events
-            between the two kernels), against the measured HBM copy bandwidth.
+            around each launch), against the measured HBM copy bandwidth.
 stack_sweep = 40-layer verify steps at K = 1, 2, 4, 8, 16 (and the Zipf-biased
             K = 16 stack): verified tokens/s = K / step time.
 cpu_baseline = the CPU oracle on a bounded sample of the same workload.
@@ -82,16 +82,15 @@ def nvfp4_bytes(rows, cols):
 
 
 def kernel_bytes(w, n_u, residual=False, K=None):
-    """Algorithmic bytes of one layer call, per kernel: the router reads its
-    weights and x; the experts kernel reads each distinct expert once (gate,
-    up, down, plus the shared expert), x, the residual, and writes y."""
+    """Algorithmic bytes of one layer call (one kernel): the router weights
+    (and bias), each distinct expert once (gate, up, down, plus the shared
+    expert), x, the residual, and y."""
     K = w.K if K is None else K
     act = K * w.H * 2
     slots = n_u + (1 if w.Is else 0)
-    router = w.E * w.H * 2 + act + (w.E * 4 if w.zipf_s else 0)
-    experts = slots * (2 * nvfp4_bytes(w.I, w.H) + nvfp4_bytes(w.H, w.I)) + act * (3 if residual else 2)
-    layer = router + experts - act  # x is read by both kernels but counted once
-    return dict(router=router, experts=experts, layer=layer)
+    router = w.E * w.H * 2 + (w.E * 4 if w.zipf_s else 0)
+    experts = router + slots * (2 * nvfp4_bytes(w.I, w.H) + nvfp4_bytes(w.H, w.I)) + act * (3 if residual else 2)
+    return dict(experts=experts, layer=experts)
 
 
 class Clocks:
@@ -302,8 +301,8 @@ def run_gpu(args):
     gbs = total_bytes / (ms * 1e-3) / 1e9
     hbm, peak_src = peaks()
 
-    # per-kernel durations: the profiling variant (events between the two
-    # kernels, no overlap) captured in a graph, so host gaps do not count
+    # kernel duration: the profiling variant (events around the launch, no
+    # overlap with the next call) captured in a graph, so host gaps do not count
     n_prof = 4 * R
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_prof)]
     for e4 in evs:
@@ -319,9 +318,8 @@ def run_gpu(args):
     with torch.cuda.stream(stream):
         g_prof.replay()
     stream.synchronize()
-    dur = {"router": [], "experts": []}
+    dur = {"experts": []}
     for e in evs:
-        dur["router"].append(e[0].elapsed_time(e[1]))
         dur["experts"].append(e[1].elapsed_time(e[2]))
     mean_ms = {k: float(np.mean(v)) for k, v in dur.items()}
     dom = max(mean_ms, key=mean_ms.get)
@@ -359,8 +357,8 @@ def run_gpu(args):
                    "K": w.K, "ring_layers": R,
                    "l2": f"inputs larger than L2: steps cycle over {R} distinct layers "
                          f"({R * 257 * 3 * nvfp4_bytes(w.I, w.H) / 1e9:.1f} GB resident)",
-                   "launch": "CUDA graph replay; per call a router kernel and one persistent experts kernel "
-                             "(programmatic dependent launch between them)",
+                   "launch": "CUDA graph replay; per call one persistent kernel (router, experts, combine), "
+                             "programmatic dependent launch between calls",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "pct_of_peak": round(100 * gbs / hbm, 1),
         "row_layers_per_s": round(w.K * steps / (ms * 1e-3) * world, 1),
@@ -369,7 +367,7 @@ def run_gpu(args):
         "clocks": clk,
         "e2e": {"value": round(e2e_gbs, 1), "unit": "GB/s", "h2d_bytes_per_step": act, "d2h_bytes_per_step": act,
                 "steps": n_e2e},
-        "gpu_launches": 2 * steps,
+        "gpu_launches": steps,
         "kernel_ms": {k: round(v, 5) for k, v in mean_ms.items()},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm,
                      "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / hbm, 3),
@@ -448,7 +446,7 @@ def stack_sweep(M, torch, synthgen, dev, stream, hbm, steps):
                         "verified_tokens_per_s": round(K / (ms * 1e-3), 1), "GBps": round(gbs, 1),
                         "pct_of_peak": round(100 * gbs / hbm, 1),
                         "distinct_experts_mean": round(float(np.mean(n_u)), 2), "steps": steps,
-                        "gpu_launches_per_step": 3 * w.layers})
+                        "gpu_launches_per_step": 2 * w.layers})
         del layers, carr
         torch.cuda.empty_cache()
     return res

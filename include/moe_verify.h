@@ -184,11 +184,12 @@ moe_status moe_verify_layer_static(const moe_layer* layer, const uint16_t* x_nor
 
 /*
  * Profiling variant of moe_verify_layer for benchmarks: identical results,
- * but the two kernels (router, experts) are launched without programmatic
- * overlap and, when `events` is not NULL, the cudaEvent_t handles
- * events[0..3] are recorded on `stream` before the router, after the router,
- * and (twice) after the experts kernel, so each kernel can be timed.  Inside
- * a stream capture the events are recorded as external event nodes.
+ * but the layer's one kernel is launched without programmatic overlap with
+ * its neighbours and, when `events` is not NULL, the cudaEvent_t handles
+ * events[0..3] are recorded on `stream`: events 0 and 1 before the kernel
+ * (they bracket no work; older layouts had a separate router kernel there)
+ * and events 2 and 3 after it, so events 1 -> 2 time the kernel.  Inside a
+ * stream capture the events are recorded as external event nodes.
  */
 moe_status moe_verify_layer_profiled(const moe_layer* layer, const uint16_t* x_norm, int K,
                                      const uint16_t* residual, uint16_t* y, void* ws, size_t ws_bytes,
