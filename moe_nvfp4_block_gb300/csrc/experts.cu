@@ -162,10 +162,14 @@ __device__ __forceinline__ void kx(unsigned long long& a, unsigned long long& b)
 }
 
 // The 8 largest keys of a warp's 256 candidates (8 per lane), in descending
-// order, on every lane: lane-local bitonic sort, then five xor rounds that
-// keep the largest 8 of two sorted lists (the elementwise max of a[j] and
-// b[7-j] is their top 8 as a bitonic sequence, sorted by a 3-stage merge).
-__device__ __forceinline__ void warp_top8(unsigned long long (&v)[8]) {
+// order: lane s (< 8) gets the s-th into `mine`, every lane the first into
+// `first`.  A lane-local bitonic sort puts each lane's best first, then 8
+// rounds of a warp arg-max, each two redux.sync max steps (the high word,
+// then the low word among the lanes holding the high word's maximum; the low
+// word encodes the expert index, so the maximum key is unique) after which
+// its lane drops it.
+__device__ __forceinline__ void warp_top8(unsigned long long (&v)[8], int lane, unsigned long long& mine,
+                                          unsigned long long& first) {
 #pragma unroll
   for (int size = 2; size <= 8; size <<= 1)
 #pragma unroll
@@ -178,22 +182,20 @@ __device__ __forceinline__ void warp_top8(unsigned long long (&v)[8]) {
           else kx(v[j], v[i]);
         }
       }
-#pragma unroll 1
-  for (int d = 16; d >= 1; d >>= 1) {
+  mine = 0ull;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {  // v[j] vs partner's v[7-j], and v[7-j] vs partner's v[j]
-      const unsigned long long pj = __shfl_xor_sync(0xffffffffu, v[j], d);
-      const unsigned long long pk = __shfl_xor_sync(0xffffffffu, v[7 - j], d);
-      v[j] = v[j] > pk ? v[j] : pk;
-      v[7 - j] = v[7 - j] > pj ? v[7 - j] : pj;
+  for (int s = 0; s < 8; ++s) {
+    const unsigned hi = (unsigned)(v[0] >> 32), lo = (unsigned)v[0];
+    const unsigned mh = __reduce_max_sync(0xffffffffu, hi);
+    const unsigned ml = __reduce_max_sync(0xffffffffu, hi == mh ? lo : 0u);
+    const unsigned long long key = ((unsigned long long)mh << 32) | ml;
+    if (s == 0) first = key;
+    if (lane == s) mine = key;
+    if (hi == mh && lo == ml) {
+#pragma unroll
+      for (int i = 0; i < 7; ++i) v[i] = v[i + 1];
+      v[7] = 0ull;
     }
-#pragma unroll
-    for (int dd = 4; dd >= 1; dd >>= 1)
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int j = i ^ dd;
-        if (j > i) kx(v[i], v[j]);
-      }
   }
 }
 
@@ -274,6 +276,56 @@ __device__ __noinline__ bool topk_general(const unsigned long long* row, unsigne
     }
   }
   return true;
+}
+
+// Routing of row r when E <= 256 and k <= 8 (one warp, in its own function
+// so that its registers do not weigh on the item loops): waits (bounded)
+// until the row's tagged logits all carry `tag`, selects the top k, and
+// writes the renormalised softmax weights, the experts and the row's bits of
+// the expert masks.  On giving up it writes experts 0 .. k-1 (in range for
+// the tables) and returns false.
+__device__ __noinline__ bool route_row_fast(const unsigned long long* row, unsigned tag, int E, int k, int r,
+                                            uint64_t wait_ns, const int* abort_flag, int* s_idx, float* s_w,
+                                            unsigned* s_rowmask, unsigned* s_used, int lane) {
+  bool got = true;
+  unsigned long long v[8];
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    bool mine = true;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = 0ull;
+      if (e < E) {
+        const unsigned long long wv = ld_tagged(row + e);
+        mine &= has_tag(wv, tag);
+        v[i] = sel_key(__uint_as_float((unsigned)wv), e);
+      }
+    }
+    if (__all_sync(0xffffffffu, mine)) break;
+    if (warp_gives_up(t0, wait_ns, abort_flag, lane)) {
+      got = false;
+      break;
+    }
+    poll_pause();
+  }
+  unsigned long long sel, first;  // lane s < k takes selection s
+  warp_top8(v, lane, sel, first);
+  const int sel_e = got ? key_index(sel) : lane;
+  const float top = key_value(first);
+  // renormalised softmax over the selected logits (selections live in lanes
+  // < k; the others add exact zeros to the sum)
+  const float ev = (lane < k && got) ? expf(key_value(sel) - top) : 0.f;
+  float z = ev;
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) z += __shfl_xor_sync(0xffffffffu, z, d);
+  if (lane < k) {
+    s_idx[r * k + lane] = sel_e;
+    s_w[r * k + lane] = got ? ev / z : 0.f;
+    atomicOr(&s_rowmask[sel_e], 1u << r);
+    atomicOr(&s_used[sel_e >> 5], 1u << (sel_e & 31));
+  }
+  return got;
 }
 
 // The grouping of one call for the caller (one warp): the distinct experts,
@@ -707,13 +759,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x;
     for (int e = tid; e < E; e += kCompThreads) s_rowmask[e] = 0u;
     for (int i = tid; i < (G + 1) * K; i += kCompThreads) s_slot[i] = -1;
-    for (int e = tid; e <= E; e += kCompThreads) {  // tensor scales, slot E = shared
-      const bool shx = e == E;
-      if (shx && !a.has_shared) continue;
-      s_tse[3 * e + 0] = shx ? a.sh_gate.tscale[0] : a.gate.tscale[e];
-      s_tse[3 * e + 1] = shx ? a.sh_up.tscale[0] : a.up.tscale[e];
-      s_tse[3 * e + 2] = shx ? a.sh_down.tscale[0] : a.down.tscale[e];
-    }
+  }
+  // the tensor scales (slot E = shared): their loads come from DRAM and are
+  // not needed before the first epilogue, so a thread's first triple waits
+  // in registers and goes to shared memory only after the router step (the
+  // rest, for E >= 512, are stored at once)
+  auto tse_of = [&](int e, int j) {
+    const ProjPtrs& pr = j == 0 ? (e == E ? a.sh_gate : a.gate) : (j == 1 ? (e == E ? a.sh_up : a.up) : (e == E ? a.sh_down : a.down));
+    return pr.tscale[e == E ? 0 : e];
+  };
+  float tse0[3] = {0.f, 0.f, 0.f};
+  if (warp < kCompWarps) {
+    const int e0 = threadIdx.x;
+    if (e0 < E || (e0 == E && a.has_shared))
+      for (int j = 0; j < 3; ++j) tse0[j] = tse_of(e0, j);
+    for (int e = e0 + kCompThreads; e <= E; e += kCompThreads)
+      if (e < E || a.has_shared)
+        for (int j = 0; j < 3; ++j) s_tse[3 * e + j] = tse_of(e, j);
   }
 
   // Router logits, spread over the CTAs: CTA b owns experts b + grid m
@@ -820,7 +882,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = nb * 8 + g;
       if (t == 0 && n < K) atomicMax(&s_xamax[n], mx);
     }
-    comp_bar();  // routing tables cleared before any warp marks them; s_call written
+    if ((int)threadIdx.x <= E)
+      for (int j = 0; j < 3; ++j) s_tse[3 * threadIdx.x + j] = tse0[j];
+    comp_bar();  // routing tables cleared before any warp marks them; s_call and s_tse written
     if (threadIdx.x == 0) stamp(15);
   }
   // (the producer warp reads s_call too early; it uses none of these)
@@ -844,60 +908,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       // bounded wait; on giving up, experts 0 .. k-1 keep the tables in
       // range and the abort flag stops the work)
       const unsigned long long* row = a.ws.tlog + (size_t)r * E;
-      bool got = true;
+      bool got;
       if (fast) {
-        unsigned long long v[8];
-        const uint64_t t0 = global_timer_ns();
-        for (;;) {
-          bool mine = true;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int e = lane + 32 * i;
-            v[i] = 0ull;
-            if (e < E) {
-              const unsigned long long wv = ld_tagged(row + e);
-              mine &= has_tag(wv, tag);
-              v[i] = sel_key(__uint_as_float((unsigned)wv), e);
-            }
-          }
-          if (__all_sync(0xffffffffu, mine)) break;
-          if (warp_gives_up(t0, a.wait_ns, &s_abort, lane)) {
-            got = false;
-            break;
-          }
-          poll_pause();
-        }
-        warp_top8(v);
-        if (lane == 0) {
-#pragma unroll
-          for (int s = 0; s < 8; ++s)
-            if (s < k) {
-              s_idx[r * k + s] = got ? key_index(v[s]) : s;
-              s_w[r * k + s] = got ? key_value(v[s]) : 0.f;  // logit for now
-            }
-        }
+        got = route_row_fast(row, tag, E, k, r, a.wait_ns, &s_abort, s_idx, s_w, s_rowmask, s_used, lane);
       } else {
         got = topk_general(row, tag, a.wait_ns, &s_abort, E, k, s_idx + r * k, s_w + r * k, lane);
-        if (!got && lane == 0)
-          for (int s = 0; s < k; ++s) {
-            s_idx[r * k + s] = s;
-            s_w[r * k + s] = 0.f;
-          }
+        __syncwarp();
+        const int sel_e = got ? (lane < k ? s_idx[r * k + lane] : 0) : lane;
+        const float sel_l = got ? (lane < k ? s_w[r * k + lane] : 0.f) : 0.f;
+        const float top = got ? s_w[r * k] : 0.f;
+        __syncwarp();
+        const float ev = (lane < k) ? expf(sel_l - top) : 0.f;
+        float z = ev;
+#pragma unroll
+        for (int d = 16; d >= 1; d >>= 1) z += __shfl_xor_sync(0xffffffffu, z, d);
+        if (lane < k) {
+          s_idx[r * k + lane] = sel_e;
+          s_w[r * k + lane] = ev / z;
+          atomicOr(&s_rowmask[sel_e], 1u << r);
+          atomicOr(&s_used[sel_e >> 5], 1u << (sel_e & 31));
+        }
       }
       if (!got && lane == 0) fail();
-      __syncwarp();
-      const float m = s_w[r * k];
-      const float ev = (lane < k) ? expf(s_w[r * k + lane] - m) : 0.f;
-      float z = ev;
-#pragma unroll
-      for (int d = 16; d >= 1; d >>= 1) z += __shfl_xor_sync(0xffffffffu, z, d);
-      __syncwarp();
-      if (lane < k) {
-        const int e = s_idx[r * k + lane];
-        s_w[r * k + lane] = ev / z;
-        atomicOr(&s_rowmask[e], 1u << r);
-        atomicOr(&s_used[e >> 5], 1u << (e & 31));
-      }
     }
     comp_bar();
     if (threadIdx.x == 0) stamp(13);
