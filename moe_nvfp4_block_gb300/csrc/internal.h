@@ -27,13 +27,11 @@ __host__ __device__ inline int expert_stage_bytes(int H, int I) {
 }
 
 // Per-call counters of the experts kernel, two sets used by alternate calls
-// (a call clears the set the next call uses): per set, kCntDone words
-// counting finished gate/up duty warps per slot, then kCntTiles words
-// counting finished down duty warps per hidden tile.  Their place and size do
-// not depend on K, E or the layer, so a workspace stays valid across shapes.
+// (a call clears the set the next call uses): per set, one word per slot
+// counting the finished gate/up duty warps.  Their place and size do not
+// depend on K, E or the layer, so a workspace stays valid across shapes.
 constexpr int kCntDone = 1025;  // slots: at most 1024 distinct experts + the shared one
-constexpr int kCntTiles = 16;   // hidden tiles: H / kDNRows <= 2048 / 128
-constexpr int kCntSet = 1056;   // words per set (kCntDone + kCntTiles, rounded up)
+constexpr int kCntSet = 1056;   // words per set (kCntDone rounded up)
 
 // Byte offsets of the workspace regions (all 256-byte aligned).  Regions
 // before `logits` sit at fixed offsets.
