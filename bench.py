@@ -62,6 +62,8 @@ def parse():
     p.add_argument("--no-sweep", action="store_true", help="skip the 40-layer stack sweep")
     p.add_argument("--sweep-steps", type=int, default=100)
     p.add_argument("--no-full-step", action="store_true", help="skip the full verify step (attention + MoE)")
+    p.add_argument("--only-full-step", action="store_true",
+                   help="run only the full verify step and print its JSON object (for profiling its launches)")
     return p.parse_args()
 
 
@@ -213,6 +215,12 @@ def run_gpu(args):
         dist.init_process_group("nccl", init_method="env://")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if args.only_full_step:
+        hbm, _ = peaks()
+        stream = torch.cuda.Stream(device=dev)
+        print(json.dumps({"full_step": full_step(M, torch, synthgen, dev, stream, hbm, max(3, args.sweep_steps // 4))}),
+              flush=True)
+        return
     w = synthgen.WORKLOADS[args.workload]
     R = args.ring
     t_gen = time.perf_counter()

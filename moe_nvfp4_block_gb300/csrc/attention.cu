@@ -66,18 +66,33 @@ __global__ void __launch_bounds__(256) k_gemv_bf16(GemvArgs a) {
   block_copy_g2s(xs, reinterpret_cast<const uint4*>(a.x), K * D / 8);
   __syncthreads();
   const int nw = gridDim.x * (blockDim.x >> 5);
-  for (int n = blockIdx.x * (blockDim.x >> 5) + warp; n < a.n_total; n += nw) {
-    int sg = 0, nl = n;
+  // row n of the concatenated segments: segment and local row
+  auto locate = [&](int n, int& sg, int& nl) {
+    sg = 0;
+    nl = n;
     while (sg + 1 < a.nseg && nl >= a.seg[sg].N) {
       nl -= a.seg[sg].N;
       ++sg;
     }
-    const GemvSeg& S = a.seg[sg];
-    const uint4* wrow = reinterpret_cast<const uint4*>(S.W + (size_t)nl * D);
-    uint4 wv[NJ];
+  };
+  auto load_row = [&](int n, uint4 (&w)[NJ]) {
+    int sg, nl;
+    locate(n, sg, nl);
+    const uint4* wrow = reinterpret_cast<const uint4*>(a.seg[sg].W + (size_t)nl * D);
 #pragma unroll
     for (int j = 0; j < NJ; ++j)
-      if (j < nj) wv[j] = ldg_nc_v4(wrow + j * 32 + lane);
+      if (j < nj) w[j] = ldg_nc_v4(wrow + j * 32 + lane);
+  };
+  // (loading the next row's weights ahead of this row's products measured
+  // slower in the full verify step)
+  uint4 wv[NJ];
+  for (int n = blockIdx.x * (blockDim.x >> 5) + warp; n < a.n_total; n += nw) {
+    int sg, nl;
+    locate(n, sg, nl);
+    const GemvSeg& S = a.seg[sg];
+    load_row(n, wv);
+    // lane r < K: row r's residual, issued with the weights
+    const float resv = (S.res && lane < K) ? bf_lo(S.res[(size_t)lane * S.N + nl]) : 0.f;
     float acc[KR];
 #pragma unroll
     for (int r = 0; r < KR; ++r) acc[r] = 0.f;
@@ -107,7 +122,7 @@ __global__ void __launch_bounds__(256) k_gemv_bf16(GemvArgs a) {
     for (int r = 0; r < KR; ++r) {
       if (r < K && lane == r) {
         float v = acc[r];
-        if (S.res) v += bf_lo(S.res[(size_t)r * S.N + nl]);
+        if (S.res) v += resv;
         S.out[(size_t)r * S.N + nl] = float_to_bf16_bits(v);
       }
     }
@@ -318,41 +333,75 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn_split(AttnArgs a) {
 
 // One CTA per (query head h, row r); 128 threads = head dims.  Merges the
 // splits of KV head h/group in split order with the row's visible new
-// positions 0..r and writes o = bf16(O / L).
+// positions 0..r and writes o = bf16(O / L).  Every global load is issued up
+// front (the split maxima and sums to shared memory, this thread's split
+// outputs, q and the new keys and values to registers), so the kernel waits
+// for about one memory round trip instead of one per split or position.
 __global__ void __launch_bounds__(128) k_attn_combine(AttnArgs a, int splits) {
-  __shared__ float s_red[4];
+  __shared__ float s_red[4][16];
   __shared__ float s_sc[16];
+  __shared__ float s_ms[kAttnMaxSplits], s_ls[kAttnMaxSplits];
   const int h = blockIdx.x, r = blockIdx.y, d = threadIdx.x;
   const int HD = 128, kvh = h / a.group, hh = h % a.group;
   const int i = r * a.group + hh;
   pdl_wait();
   pdl_launch_dependents();
+  const float* pml = a.part_ml + (size_t)kvh * splits * 32 + 2 * i;
+  const float* po = a.part_o + ((size_t)kvh * splits * 16 + i) * HD + d;
+  if (d < splits) {
+    s_ms[d] = __ldcg(pml + (size_t)d * 32);
+    s_ls[d] = __ldcg(pml + (size_t)d * 32 + 1);
+  }
+  float ov[2][32];  // this thread's split outputs (splits <= 64)
+#pragma unroll
+  for (int c = 0; c < 2; ++c)
+#pragma unroll
+    for (int u = 0; u < 32; ++u) ov[c][u] = 32 * c + u < splits ? __ldcg(po + (size_t)(32 * c + u) * 16 * HD) : 0.f;
   const float qd = bf_lo(a.q[(size_t)r * a.nq * HD + (size_t)h * HD + d]);
-  // scores of the new positions j <= r (log2 domain), fixed-order block sum
-  for (int j = 0; j <= r; ++j) {
-    float p = qd * bf_lo(a.k_new[(size_t)j * a.nkv * HD + (size_t)kvh * HD + d]);
+  float kd[16], vd[16];  // the new positions j <= r (r < K <= 16)
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    kd[j] = vd[j] = 0.f;
+    if (j <= r) {
+      kd[j] = bf_lo(a.k_new[(size_t)j * a.nkv * HD + (size_t)kvh * HD + d]);
+      vd[j] = bf_lo(a.v_new[(size_t)j * a.nkv * HD + (size_t)kvh * HD + d]);
+    }
+  }
+  // scores of the new positions (log2 domain): per warp a xor sum, then the
+  // four warps in a fixed order
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    if (j > r) break;
+    float p = qd * kd[j];
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
-    if ((d & 31) == 0) s_red[d >> 5] = p;
-    __syncthreads();
-    if (d == 0) s_sc[j] = ((s_red[0] + s_red[1]) + (s_red[2] + s_red[3])) * a.scale_log2;
-    __syncthreads();
+    if ((d & 31) == 0) s_red[d >> 5][j] = p;
   }
+  __syncthreads();
+  if (d <= r) s_sc[d] = ((s_red[0][d] + s_red[1][d]) + (s_red[2][d] + s_red[3][d])) * a.scale_log2;
+  __syncthreads();
   float M = -INFINITY;
-  for (int s = 0; s < splits; ++s) M = fmaxf(M, a.part_ml[(size_t)(kvh * splits + s) * 32 + 2 * i]);
+  for (int s = 0; s < splits; ++s) M = fmaxf(M, s_ms[s]);
   for (int j = 0; j <= r; ++j) M = fmaxf(M, s_sc[j]);
   float L = 0.f, O = 0.f;
-  for (int s = 0; s < splits; ++s) {
-    const float ms = a.part_ml[(size_t)(kvh * splits + s) * 32 + 2 * i];
-    if (ms == -INFINITY) continue;
-    const float f = exp2f(ms - M);
-    L += a.part_ml[(size_t)(kvh * splits + s) * 32 + 2 * i + 1] * f;
-    O += a.part_o[((size_t)(kvh * splits + s) * 16 + i) * HD + d] * f;
-  }
-  for (int j = 0; j <= r; ++j) {
+#pragma unroll
+  for (int c = 0; c < 2; ++c)
+#pragma unroll
+    for (int u = 0; u < 32; ++u) {
+      const int s = 32 * c + u;
+      if (s >= splits) break;
+      const float ms = s_ms[s];
+      if (ms == -INFINITY) continue;
+      const float f = exp2f(ms - M);
+      L += s_ls[s] * f;
+      O += ov[c][u] * f;
+    }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    if (j > r) break;
     const float f = exp2f(s_sc[j] - M);
     L += f;
-    O += f * bf_lo(a.v_new[(size_t)j * a.nkv * HD + (size_t)kvh * HD + d]);
+    O += f * vd[j];
   }
   a.o[(size_t)r * a.nq * HD + (size_t)h * HD + d] = float_to_bf16_bits(O / L);
 }

@@ -36,7 +36,9 @@ __device__ __forceinline__ bool ranks_before(float la, int a, float lb, int b) {
 // ------------------------------------------------------------------ RMSNorm
 // One warp per row: ss = fixed-order sum of x*x, mean = ss / H,
 // inv = 1 / sqrt(mean + eps), out = bf16(x * inv); each step one correctly
-// rounded FP32 operation.
+// rounded FP32 operation.  The row's pieces are loaded in chunks of 8 per
+// lane, each chunk's loads all in flight before its first product, so a row
+// of H <= 2048 costs one memory round trip, not one per piece.
 __global__ void __launch_bounds__(512) k_rmsnorm(const uint16_t* __restrict__ x, int K, int H, float eps,
                                                  uint16_t* __restrict__ out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -45,31 +47,46 @@ __global__ void __launch_bounds__(512) k_rmsnorm(const uint16_t* __restrict__ x,
   const int r = blockIdx.x * (blockDim.x >> 5) + warp;
   if (r >= K) return;
   const uint4* row = reinterpret_cast<const uint4*>(x + (size_t)r * H);
-  float acc = 0.f;
-  for (int j = 0; j < H / 256; ++j) {
-    const uint4 v = row[j * 32 + lane];
-    const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+  const int nj = H / 256;
+  uint4 xv[8];
+  auto load_chunk = [&](int j0) {
 #pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      const float f = (t & 1) ? bf16_hi(q[t >> 1]) : bf16_lo(q[t >> 1]);
-      acc = __fmaf_rn(f, f, acc);
+    for (int u = 0; u < 8; ++u)
+      if (j0 + u < nj) xv[u] = __ldcg(row + (j0 + u) * 32 + lane);
+  };
+  float acc = 0.f;
+  for (int j0 = 0; j0 < nj; j0 += 8) {
+    load_chunk(j0);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (j0 + u >= nj) break;
+      const uint32_t q[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const float f = (t & 1) ? bf16_hi(q[t >> 1]) : bf16_lo(q[t >> 1]);
+        acc = __fmaf_rn(f, f, acc);
+      }
     }
   }
   const float ss = warp_sum_xor(acc);
   const float mean = __fdiv_rn(ss, (float)H);
   const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
   uint4* o = reinterpret_cast<uint4*>(out + (size_t)r * H);
-  for (int j = 0; j < H / 256; ++j) {
-    const uint4 v = row[j * 32 + lane];
-    const uint32_t q[4] = {v.x, v.y, v.z, v.w};
-    uint32_t res[4];
+  for (int j0 = 0; j0 < nj; j0 += 8) {
+    if (nj > 8) load_chunk(j0);  // (with one chunk the registers still hold it)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t lo = float_to_bf16_bits(__fmul_rn(bf16_lo(q[i]), inv));
-      const uint32_t hi = float_to_bf16_bits(__fmul_rn(bf16_hi(q[i]), inv));
-      res[i] = lo | (hi << 16);
+    for (int u = 0; u < 8; ++u) {
+      if (j0 + u >= nj) break;
+      const uint32_t q[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
+      uint32_t res[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t lo = float_to_bf16_bits(__fmul_rn(bf16_lo(q[i]), inv));
+        const uint32_t hi = float_to_bf16_bits(__fmul_rn(bf16_hi(q[i]), inv));
+        res[i] = lo | (hi << 16);
+      }
+      o[(j0 + u) * 32 + lane] = make_uint4(res[0], res[1], res[2], res[3]);
     }
-    o[j * 32 + lane] = make_uint4(res[0], res[1], res[2], res[3]);
   }
 }
 
