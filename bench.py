@@ -154,7 +154,7 @@ def dominant_traffic(kernel: str, workload: str):
         if ":" in line and not line.startswith(" "):
             k, v = line.split(":", 1)
             kv[k.strip()] = v.strip()
-    if kv.get("source_sha256") != source_hash():
+    if (kv.get("source_sha256", "").split() or [""])[0] != source_hash(kernel):
         return None
     try:
         return float(kv["dram_bytes_per_launch"])
@@ -162,12 +162,20 @@ def dominant_traffic(kernel: str, workload: str):
         return None
 
 
-def source_hash():
+# the sources each profiled kernel is compiled from (None: all kernel sources)
+KERNEL_SOURCES = {"experts": ["experts.cu", "internal.h", "ptx.cuh", "../../include/moe_verify.h"]}
+
+
+def source_hash(kernel=None):
+    """Hash of the sources a kernel is built from, to tell whether a stored
+    ncu summary still describes it."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "moe_nvfp4_block_gb300", "csrc")
-    for fn in sorted(os.listdir(d)):
-        if fn.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(d, fn), "rb").read())
+    files = KERNEL_SOURCES.get(kernel) if kernel else None
+    if files is None:
+        files = [fn for fn in sorted(os.listdir(d)) if fn.endswith((".cu", ".cuh", ".h"))]
+    for fn in files:
+        h.update(open(os.path.join(d, fn), "rb").read())
     return h.hexdigest()[:16]
 
 

@@ -950,6 +950,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (unsigned m = used; m; m &= m - 1) s_uexp[u++] = lane * 32 + __ffs(m) - 1;
       if (lane == 31) s_nu = inc;
       if (lane == 0) s_uexp[G] = E;  // the shared expert's scales sit at index E
+      // the producer needs only the distinct experts and their count: hand
+      // them over now (named barrier 2: this warp arrives, the producer waits)
+      __syncwarp();
+      asm volatile("bar.arrive 2, 64;" ::: "memory");
     }
     for (int base = 0; base < K * k; base += kCompThreads) {
       const int q = base + (int)threadIdx.x;
@@ -963,8 +967,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (a.has_shared)
       for (int r = threadIdx.x; r < K; r += kCompThreads) s_slot[G * K + r] = (signed char)k;
+    comp_bar();  // the (row, slot) map is complete
+  } else if (warp == kProducerWarp) {
+    asm volatile("bar.sync 2, 64;" ::: "memory");  // the distinct experts are listed
   }
-  __syncthreads();
   pdl_launch_dependents();
   if (threadIdx.x == 0) stamp(3);
 
