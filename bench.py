@@ -439,7 +439,7 @@ def stack_sweep(M, torch, synthgen, dev, stream, hbm, steps):
                     M.moe_verify_layer(layers[l], xn, x, x, wl, group_out=grp, stream=stream)
                     stream.synchronize()
                     n_u.append(int(grp[0].item()))
-            step_bytes = sum(kernel_bytes(w, n, residual=True, K=K)["layer"] + 2 * K * w.H * 2 for n in n_u)
+            step_bytes = sum(kernel_bytes(w, n, residual=True, K=K)["layer"] for n in n_u)  # (RMSNorm inside)
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 x.copy_(x0)
@@ -462,7 +462,7 @@ def stack_sweep(M, torch, synthgen, dev, stream, hbm, steps):
                         "verified_tokens_per_s": round(K / (ms * 1e-3), 1), "GBps": round(gbs, 1),
                         "pct_of_peak": round(100 * gbs / hbm, 1),
                         "distinct_experts_mean": round(float(np.mean(n_u)), 2), "steps": steps,
-                        "gpu_launches_per_step": 2 * w.layers})
+                        "gpu_launches_per_step": w.layers})
         del layers, carr
         torch.cuda.empty_cache()
     return res
@@ -515,7 +515,7 @@ def full_step(M, torch, synthgen, dev, stream, hbm, steps):
     act = K * w.H * 2
     att_bytes = 2 * (w.n_q_heads + 2 * w.n_kv_heads) * 128 * w.H + 2 * w.H * w.n_q_heads * 128 + \
         2 * 2 * w.n_kv_heads * w.ctx * 128 + 2 * act
-    step_bytes = sum(att_bytes + kernel_bytes(w, nu, residual=True, K=K)["layer"] + 2 * act for nu in n_u) + \
+    step_bytes = sum(att_bytes + kernel_bytes(w, nu, residual=True, K=K)["layer"] for nu in n_u) + \
         w.vocab * w.H * 2 + 2 * act
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):

@@ -139,9 +139,10 @@ moe_status moe_verify_layer(const moe_layer* layer, const uint16_t* x_norm, int 
 /*
  * A stack of MoE decoder blocks for the K verify rows, in place:
  *   for l in 0 .. n_layers-1:  x <- x + MoE_l( rmsnorm(x) )
- * (moe_rmsnorm with `eps`, then moe_verify_layer with residual = x and
- * y = x), all enqueued on `stream` with programmatic overlap between
- * kernels.  All layers share `hidden`.
+ * (the results of moe_rmsnorm with `eps`, then moe_verify_layer with
+ * residual = x and y = x; each layer is one kernel, which applies the
+ * RMSNorm itself), all enqueued on `stream` with programmatic overlap
+ * between kernels.  All layers share `hidden`.
  *   layers   host array of n_layers layer descriptions (read during the call)
  *   x        bf16 [K][hidden], the residual stream, updated in place
  *   ws       moe_verify_stack_workspace_size(layers, n_layers, K) bytes,

@@ -180,7 +180,7 @@ moe_status moe_router_topk(const moe_layer* layer, const uint16_t* x_norm, int K
 
 __attribute__((visibility("hidden"))) moe_status run_layer(const moe_layer* layer, const uint16_t* x_norm, int K, const uint16_t* residual,
                             uint16_t* y, int32_t* idx_out, float* w_out, int32_t* group_out, void* ws,
-                            size_t ws_bytes, void* stream, bool pdl, void* const* events) {
+                            size_t ws_bytes, void* stream, bool pdl, void* const* events, float norm_eps) {
   moe_status s = check_layer(layer, K);
   if (s != MOE_OK) return s;
   if (!x_norm || !y || !ws) return MOE_ERR_INVALID_ARG;
@@ -261,6 +261,8 @@ __attribute__((visibility("hidden"))) moe_status run_layer(const moe_layer* laye
   ea.wait_ns = wait_ns;
   ea.trace = g_trace;
   ea.code3d = code3d ? 1 : 0;
+  ea.norm = norm_eps >= 0.f ? 1 : 0;
+  ea.norm_eps = norm_eps >= 0.f ? norm_eps : 0.f;
   if (launch_experts(ea, maps, st, pdl) != cudaSuccess || !mark(2) || !mark(3)) return MOE_ERR_CUDA;
   return MOE_OK;
 }
@@ -309,12 +311,8 @@ moe_status moe_verify_stack(const moe_layer* layers, int n_layers, uint16_t* x, 
   }
   if (ws_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
   if (!aligned16(x) || !aligned16(ws)) return MOE_ERR_MISALIGNED;
-  const int H = layers[0].hidden;
-  uint16_t* xn = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + need - align256(sizeof(uint16_t) * K * H));
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  for (int l = 0; l < n_layers; ++l) {
-    if (launch_rmsnorm(x, K, H, eps, xn, st, l > 0) != cudaSuccess) return MOE_ERR_CUDA;
-    moe_status s = run_layer(&layers[l], xn, K, x, x, nullptr, nullptr, nullptr, ws, ws_bytes, stream, true, nullptr);
+  for (int l = 0; l < n_layers; ++l) {  // each layer kernel applies its RMSNorm to x itself
+    moe_status s = run_layer(&layers[l], x, K, x, x, nullptr, nullptr, nullptr, ws, ws_bytes, stream, true, nullptr, eps);
     if (s != MOE_OK) return s;
   }
   return MOE_OK;
@@ -514,8 +512,9 @@ moe_status moe_verify_step(const moe_verify_model* m, uint16_t* x, int K, const 
     s = moe_attention_block(x, K, H, m->n_q_heads, m->n_kv_heads, m->head_dim, m->ctx, d.Wq, d.Wk, d.Wv, d.Wo,
                             d.kcache, d.vcache, m->eps, x, nullptr, nullptr, b + L.attn_ws, L.attn_bytes, stream);
     if (s != MOE_OK) return s;
-    if (launch_rmsnorm(x, K, H, m->eps, xn, st, true) != cudaSuccess) return MOE_ERR_CUDA;
-    s = run_layer(&d.moe, xn, K, x, x, nullptr, nullptr, nullptr, b + L.moe_ws, L.moe_bytes, stream, true, nullptr);
+    // the MoE layer kernel applies its RMSNorm to x itself
+    s = run_layer(&d.moe, x, K, x, x, nullptr, nullptr, nullptr, b + L.moe_ws, L.moe_bytes, stream, true, nullptr,
+                  m->eps);
     if (s != MOE_OK) return s;
   }
   if (launch_rmsnorm(x, K, H, m->eps, xn, st, false) != cudaSuccess) return MOE_ERR_CUDA;

@@ -808,6 +808,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   // CTA (one read, not one per thread, of the word every CTA reads).
   if (threadIdx.x == 0) s_call = __ldcg(a.ws.exits) / (unsigned long long)grid;
 
+  // The K input rows, staged once per CTA in the reduction slots (idle until
+  // the first item's partials): [K][H] bf16, normalised on the way when the
+  // call asks for it, with the arithmetic of the RMSNorm kernel (a fixed-order
+  // FP32 sum of squares, then each step one correctly rounded operation), so
+  // the rows are bit for bit that kernel's output.  Every CTA has staged its
+  // rows before it publishes its logits, and no CTA writes y before it has
+  // read all logits, so y may be the input itself.
+  uint4* xs = reinterpret_cast<uint4*>(red);
   // activations: compute warp w holds k-unit w of every row as FP16 B
   // fragments; the row maxima now, the fragments after the routing, while
   // the first weight tiles are in flight
@@ -818,13 +826,52 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (warp < H / 128 && n < K)
-          v = __ldcg(reinterpret_cast<const uint4*>(a.x + (size_t)n * H + warp * 128 + q * 32 + 8 * t));
+        if (warp < H / 128 && n < K) v = xs[n * (H / 8) + warp * 16 + q * 4 + t];
         raw[nb][q] = v;
       }
     }
   };
   if (warp < kCompWarps) {
+    for (int r = warp; r < K; r += kCompWarps) {
+      const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)r * H);
+      uint4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j < H / 256) v[j] = __ldcg(xr + j * 32 + lane);
+      if (a.norm) {
+        float ss = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (j >= H / 256) break;
+          const uint32_t q[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float f = __uint_as_float((u & 1) ? (q[u >> 1] & 0xFFFF0000u) : (q[u >> 1] << 16));
+            ss = __fmaf_rn(f, f, ss);
+          }
+        }
+#pragma unroll
+        for (int d = 16; d >= 1; d >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, d));
+        const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)H), a.norm_eps)));
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (j >= H / 256) break;
+          uint32_t q[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t lo = float_to_bf16_bits(__fmul_rn(__uint_as_float(q[i] << 16), inv));
+            const uint32_t hi = float_to_bf16_bits(__fmul_rn(__uint_as_float(q[i] & 0xFFFF0000u), inv));
+            q[i] = lo | (hi << 16);
+          }
+          v[j] = make_uint4(q[0], q[1], q[2], q[3]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j < H / 256) xs[r * (H / 8) + j * 32 + lane] = v[j];
+    }
+    comp_bar();  // the rows are staged
+
     // this CTA's router logits: per lane, products in element order over
     // the pieces j, then xor rounds 16 .. 1, then the bias (the arithmetic
     // of the router GEMV, so the logits are the same bits)
@@ -836,11 +883,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int e = (int)blockIdx.x + grid * (p % M), r = p / M;
       if (e >= E) continue;
       if (e != lw_e) load_router_row(e);
-      const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)r * H);
       uint4 xv[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j)
-        if (j < H / 256) xv[j] = __ldcg(xr + j * 32 + lane);
+        if (j < H / 256) xv[j] = xs[r * (H / 8) + j * 32 + lane];
       float acc = 0.f;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -1029,6 +1075,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < 4; ++q) bf16x8_to_f16x8(raw[nb][q], sc, &bx[nb][q * 4]);
       }
     }
+    comp_bar();  // every warp is done with the staged rows before partials overwrite them
     const int KUgu = H / 128, KUdn = I / 128;
     const TileGeo ggu = tile_geo(H), gdn = tile_geo(I);
     const int gu_code = kGURows * H / 2, gu_scale = kGURows * H / 16;
@@ -1440,7 +1487,9 @@ static cudaError_t launch_experts_t(const ExpertsArgs& a, const CUtensorMap* map
   int stages = 0, nred = 0;
   const size_t smem = experts_smem_bytes(a.K, a.H, a.I, a.E, a.k, a.G, &stages, &nred);
   const int grid = num_sms();
-  if (stages < 2 || a.H > 128 * kCompWarps || a.I > 128 * 4) return cudaErrorInvalidValue;
+  if (stages < 2 || a.H > 128 * kCompWarps || a.I > 128 * 4 ||
+      sizeof(uint16_t) * (size_t)a.K * a.H > 2 * red_slot_bytes(NB))  // the staged rows fit the reduction slots
+    return cudaErrorInvalidValue;
   ExpertsArgs b = a;
   b.stages = stages;
   b.nred = nred;

@@ -133,7 +133,7 @@ struct ProjPtrs {
 };
 
 struct ExpertsArgs {
-  const uint16_t* x;         // x_norm [K][H] bf16
+  const uint16_t* x;         // [K][H] bf16: the normalised rows, or the rows to normalise (norm)
   const uint16_t* residual;  // [K][H] or null
   uint16_t* y;               // [K][H]
   int K, H, I, E, k, G;
@@ -150,6 +150,8 @@ struct ExpertsArgs {
   unsigned long long* trace;  // [grid][kTraceSlots] milestone timestamps, or null
   int code3d;                 // code maps are 3-D (one request per tile)
   int stages, nred;           // ring depths (set by the launcher)
+  int norm;                   // 1: x is the residual stream; the kernel applies the RMSNorm (unit gain)
+  float norm_eps;
 };
 
 constexpr int kTraceSlots = 80;
@@ -217,6 +219,9 @@ int num_sms();
 }  // namespace moe
 
 // The layer launch sequence behind moe_verify_layer (capi.cu; not exported).
+// norm_eps >= 0: x_norm holds the un-normalised rows and the layer kernel
+// applies the RMSNorm (unit gain, this eps) itself.
 extern "C" __attribute__((visibility("hidden"))) moe_status run_layer(const moe_layer* layer, const uint16_t* x_norm, int K, const uint16_t* residual,
                                 uint16_t* y, int32_t* idx_out, float* w_out, int32_t* group_out, void* ws,
-                                size_t ws_bytes, void* stream, bool pdl, void* const* events);
+                                size_t ws_bytes, void* stream, bool pdl, void* const* events,
+                                float norm_eps = -1.f);
