@@ -143,6 +143,23 @@ def test_deterministic_and_workspace_reuse(M):
         assert np.array_equal(u, v)
 
 
+def test_one_workspace_across_shapes(M):
+    # The workspace's counters sit at fixed offsets and the words the CTAs
+    # exchange carry the call's tag, so one zero-filled workspace serves calls
+    # of any K and layer that fit in it: every call matches the oracle even
+    # right after calls whose layouts put other data where its words lie.
+    cases = []
+    for K, E in ((16, 32), (3, 32), (9, 64), (1, 32), (16, 64), (5, 32)):
+        w = synthgen.Workload(f"s{K}e{E}", K=K, layers=1, seed=400 + K + E, **dict(SMALL, E=E))
+        L, x, res = _case(w, res_inst=3)
+        cases.append((w, L, x, res, upload(L, w)))
+    n = max(M.moe_verify_layer_workspace_size(dl, w.K) for w, _, _, _, dl in cases)
+    ws = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    for rep in range(2):
+        for w, L, x, res, dl in cases:
+            check(w, L, x, res, run_layer(M, dl, x, res, ws=ws), what=f"shared workspace {w.name}, pass {rep}")
+
+
 def test_router_topk_entry_matches_layer_routing(M):
     w = synthgen.WORKLOADS["k16_zipf_stack40"]
     L, x, _ = _case(w, layer=1, x_inst=2)
