@@ -49,7 +49,7 @@ FALLBACK_HBM_GBS = 6800.0
 RING = 24
 
 
-def parse():
+def parse(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=48000)
@@ -64,7 +64,7 @@ def parse():
     p.add_argument("--no-full-step", action="store_true", help="skip the full verify step (attention + MoE)")
     p.add_argument("--only-full-step", action="store_true",
                    help="run only the full verify step and print its JSON object (for profiling its launches)")
-    return p.parse_args()
+    return p.parse_args(argv)
 
 
 # --------------------------------------------------------------------------- helpers
@@ -205,6 +205,18 @@ def oracle_sample(w, seconds, first_layer=0):
     return b_total / t_total, n, t_total, threads
 
 
+# --------------------------------------------------------------------------- replicas
+
+def combine_ranks(dist, torch, world, ms, total_bytes, device):
+    """Whole-job figures of N independent replicas: the slowest rank's time and
+    the bytes all ranks moved (every rank calls this; an all-gather, no
+    reduction order to depend on)."""
+    t = torch.tensor([ms, total_bytes], dtype=torch.float64, device=device)
+    tl = [torch.zeros_like(t) for _ in range(world)]
+    dist.all_gather(tl, t)
+    return max(float(x[0]) for x in tl), sum(float(x[1]) for x in tl)
+
+
 # --------------------------------------------------------------------------- GPU arm
 
 def run_gpu(args):
@@ -309,11 +321,7 @@ def run_gpu(args):
     assert M.moe_workspace_error(ws, stream) == 0
     total_bytes = sum(kb[i % R]["layer"] for i in range(steps))
     if dist:
-        t = torch.tensor([ms, total_bytes], dtype=torch.float64, device=dev)
-        tl = [torch.zeros_like(t) for _ in range(world)]
-        dist.all_gather(tl, t)
-        ms = max(float(x[0]) for x in tl)
-        total_bytes = sum(float(x[1]) for x in tl)
+        ms, total_bytes = combine_ranks(dist, torch, world, ms, total_bytes, dev)
     gbs = total_bytes / (ms * 1e-3) / 1e9
     hbm, peak_src = peaks()
 
