@@ -101,6 +101,18 @@ def test_top_k_equals_experts(M):
     check(w, L, x, res, got, what="top_k = E")
 
 
+@pytest.mark.parametrize("K,E,top_k", [(3, 1024, 8), (2, 300, 16), (16, 1024, 32)])
+def test_general_topk_path(M, K, E, top_k):
+    # more than 256 experts or more than 8 selections take the general top-k
+    # (k rounds of a warp arg-max over up to 32 logits per lane); the last
+    # case is the largest expert count and selection the library accepts
+    w = synthgen.Workload(f"g{E}k{top_k}", K=K, H=256, E=E, top_k=top_k, I=128, Is=128, layers=1,
+                          seed=500 + top_k, zipf_s=1.1)
+    L, x, res = _case(w, res_inst=4)
+    got = run_layer(M, upload(L, w), x, res)
+    check(w, L, x, res, got, what=f"E={E}, top-{top_k}")
+
+
 def test_routed_scale_and_no_shared(M):
     w = synthgen.Workload("rs", K=4, H=1024, E=64, top_k=6, I=128, Is=0, layers=1, seed=9, routed_scale=2.5)
     L, x, res = _case(w, res_inst=3)
