@@ -60,10 +60,12 @@ def parse(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-sweep", action="store_true", help="skip the 40-layer stack sweep")
-    p.add_argument("--sweep-steps", type=int, default=100)
+    p.add_argument("--sweep-steps", type=int, default=200)
     p.add_argument("--no-full-step", action="store_true", help="skip the full verify step (attention + MoE)")
     p.add_argument("--only-full-step", action="store_true",
                    help="run only the full verify step and print its JSON object (for profiling its launches)")
+    p.add_argument("--oracle-sample", type=float, default=None,
+                   help="(internal) time the CPU oracle for this many seconds and print bytes/s as JSON")
     return p.parse_args(argv)
 
 
@@ -77,6 +79,59 @@ def peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def pctl(ms_list):
+    """median, p10 and p90 of per-replay times (ms)."""
+    a = np.asarray(ms_list, np.float64)
+    return {"median": float(np.median(a)), "p10": float(np.percentile(a, 10)), "p90": float(np.percentile(a, 90)),
+            "n": int(a.size)}
+
+
+def timed_replays(torch, stream, g, n):
+    """Replays graph g n times back to back on `stream`, an event pair around
+    each replay; returns the per-replay times (ms) and the total (ms)."""
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    with torch.cuda.stream(stream):
+        evs[0].record(stream)
+        for i in range(n):
+            g.replay()
+            evs[i + 1].record(stream)
+    stream.synchronize()
+    per = [evs[i].elapsed_time(evs[i + 1]) for i in range(n)]
+    return per, evs[0].elapsed_time(evs[n])
+
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def oracle_single_thread(workload, seconds):
+    """The oracle on one host thread (OpenMP limited to 1 in a child
+    process): bytes/s, or None if the child failed."""
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    try:
+        out = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample", str(seconds),
+                              "--workload", workload], capture_output=True, text=True, env=env,
+                             timeout=max(120.0, 10 * seconds))
+        d = json.loads(out.stdout.strip().splitlines()[-1])
+        return d
+    except Exception:
+        return None
 
 
 def nvfp4_bytes(rows, cols):
@@ -238,7 +293,7 @@ def run_gpu(args):
     if args.only_full_step:
         hbm, _ = peaks()
         stream = torch.cuda.Stream(device=dev)
-        print(json.dumps({"full_step": full_step(M, torch, synthgen, dev, stream, hbm, max(3, args.sweep_steps // 4))}),
+        print(json.dumps({"full_step": full_step(M, torch, synthgen, dev, stream, hbm, max(3, args.sweep_steps))}),
               flush=True)
         return
     w = synthgen.WORKLOADS[args.workload]
@@ -300,6 +355,10 @@ def run_gpu(args):
 
     clocks = Clocks(local)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # one event after every replay of the ring graph (R steps), for the
+    # per-replay distribution; the events sit between graph launches and do
+    # not split the programmatic overlap inside a replay
+    evr = [torch.cuda.Event(enable_timing=True) for _ in range(full)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -307,8 +366,9 @@ def run_gpu(args):
     time.sleep(0.3)
     with torch.cuda.stream(stream):
         ev0.record(stream)
-        for _ in range(full):
+        for i in range(full):
             g_full.replay()
+            evr[i].record(stream)
         if g_rem is not None:
             g_rem.replay()
         ev1.record(stream)
@@ -318,6 +378,9 @@ def run_gpu(args):
     if dist:
         dist.barrier()
     ms = ev0.elapsed_time(ev1)
+    per_replay = [(ev0 if i == 0 else evr[i - 1]).elapsed_time(evr[i]) / R for i in range(full)]
+    if len(per_replay) < 200:  # too few timed replays for a distribution: 200 more, outside the timed region
+        per_replay = [t / R for t in timed_replays(torch, stream, g_full, 200)[0]]
     assert M.moe_workspace_error(ws, stream) == 0
     total_bytes = sum(kb[i % R]["layer"] for i in range(steps))
     if dist:
@@ -385,6 +448,8 @@ def run_gpu(args):
                              "programmatic dependent launch between calls",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "pct_of_peak": round(100 * gbs / hbm, 1),
+        "ms_per_step_dist": dict({k: (round(v, 5) if isinstance(v, float) else v) for k, v in pctl(per_replay).items()},
+                                 replay=f"one graph replay = {R} steps (one pass over the layer ring)"),
         "row_layers_per_s": round(w.K * steps / (ms * 1e-3) * world, 1),
         "layers_per_s": round(steps / (ms * 1e-3) * world, 1),
         "distinct_experts_mean": float(np.mean(n_u)),
@@ -393,20 +458,34 @@ def run_gpu(args):
                 "steps": n_e2e},
         "gpu_launches": steps,
         "kernel_ms": {k: round(v, 5) for k, v in mean_ms.items()},
+        "kernel_ms_dist": {k: {kk: (round(vv, 5) if isinstance(vv, float) else vv) for kk, vv in pctl(v).items()}
+                           for k, v in dur.items()},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm,
                      "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / hbm, 3),
-                     "traffic": traffic, "algorithmic_bytes_per_launch": dom_bytes},
+                     "traffic": traffic, "algorithmic_bytes_per_launch": dom_bytes,
+                     "timing": "achieved: the kernel launched alone (no programmatic overlap), CUDA events "
+                               "around each launch in a graph; achieved_in_step_mode: the same bytes over the "
+                               "headline's per-step time (one launch per step, overlapped with its neighbours)",
+                     "achieved_in_step_mode": round(gbs / world, 1),
+                     "frac_in_step_mode": round(gbs / world / hbm, 3)},
         "setup_s": round(t_gen, 1),
     }
     if not args.no_sweep:
         out["stack_sweep"] = stack_sweep(M, torch, synthgen, dev, stream, hbm, args.sweep_steps)
     if not args.no_full_step:
-        out["full_step"] = full_step(M, torch, synthgen, dev, stream, hbm, max(10, args.sweep_steps // 4))
+        out["full_step"] = full_step(M, torch, synthgen, dev, stream, hbm, max(10, args.sweep_steps))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         bps, n, secs, threads = oracle_sample(w, args.cpu_seconds)
+        st = oracle_single_thread(args.workload, min(10.0, args.cpu_seconds))
         out["cpu_baseline"] = {"value": round(bps / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                                "sample": f"{n} whole {args.workload} layers (K={w.K}) of the same workload, "
-                                         f"{secs:.1f} s of oracle time"}
+                                         f"{secs:.1f} s of oracle time",
+                               "nproc": os.cpu_count(), "cpu_model": cpu_model(),
+                               "single_thread": None if st is None else
+                               {"value": round(st["bytes_per_s"] / 1e9, 4), "unit": "GB/s", "cores": 1,
+                                "sample": f"{st['layers']} whole layers, {st['seconds']:.1f} s of oracle time",
+                                "ms_per_layer": round(st["seconds"] / st["layers"] * 1e3, 2)},
+                               "ms_per_layer": round(secs / n * 1e3, 2)}
     if rank == 0:
         print(json.dumps(out), flush=True)
     if dist:
@@ -456,21 +535,17 @@ def stack_sweep(M, torch, synthgen, dev, stream, hbm, steps):
                 for _ in range(3):
                     g.replay()
             stream.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(stream):
-                e0.record(stream)
-                for _ in range(steps):
-                    g.replay()
-                e1.record(stream)
-            stream.synchronize()
+            per, tot = timed_replays(torch, stream, g, steps)
             assert M.moe_workspace_error(ws, stream) == 0
-            ms = e0.elapsed_time(e1) / steps
+            ms = tot / steps
             gbs = step_bytes / (ms * 1e-3) / 1e9
+            dist_ = pctl(per)
             res.append({"workload": wname, "K": K, "layers": w.layers, "ms_per_step": round(ms, 4),
                         "verified_tokens_per_s": round(K / (ms * 1e-3), 1), "GBps": round(gbs, 1),
                         "pct_of_peak": round(100 * gbs / hbm, 1),
                         "distinct_experts_mean": round(float(np.mean(n_u)), 2), "steps": steps,
-                        "gpu_launches_per_step": w.layers})
+                        "ms_median": round(dist_["median"], 4), "ms_p10": round(dist_["p10"], 4),
+                        "ms_p90": round(dist_["p90"], 4), "gpu_launches_per_step": w.layers})
         del layers, carr
         torch.cuda.empty_cache()
     return res
@@ -533,15 +608,10 @@ def full_step(M, torch, synthgen, dev, stream, hbm, steps):
         for _ in range(3):
             g.replay()
     stream.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(steps):
-            g.replay()
-        e1.record(stream)
-    stream.synchronize()
+    per, tot = timed_replays(torch, stream, g, steps)
     assert M.moe_workspace_error(ws, stream) == 0
-    ms = e0.elapsed_time(e1) / steps
+    ms = tot / steps
+    dist_ = pctl(per)
     acc = int(n.item())
     gbs = step_bytes / (ms * 1e-3) / 1e9
     res = {"workload": "k4_full_step", "K": K, "layers": w.layers, "ctx": w.ctx, "vocab": w.vocab,
@@ -549,7 +619,8 @@ def full_step(M, torch, synthgen, dev, stream, hbm, steps):
            "accepted": acc, "accepted_expected": j,
            "emitted_tokens_per_s": round((acc + 1 if acc < K else K) / (ms * 1e-3), 1),
            "GBps": round(gbs, 1), "pct_of_peak": round(100 * gbs / hbm, 1),
-           "step_bytes": step_bytes, "distinct_experts_mean": round(float(np.mean(n_u)), 2), "steps": steps}
+           "step_bytes": step_bytes, "distinct_experts_mean": round(float(np.mean(n_u)), 2), "steps": steps,
+           "ms_median": round(dist_["median"], 4), "ms_p10": round(dist_["p10"], 4), "ms_p90": round(dist_["p90"], 4)}
     del layers, model
     torch.cuda.empty_cache()
     return res
@@ -593,7 +664,11 @@ def run_reference(args):
 
 if __name__ == "__main__":
     a = parse()
-    if a.impl == "reference":
+    if a.oracle_sample is not None:
+        import synthgen
+        bps, n, secs, threads = oracle_sample(synthgen.WORKLOADS[a.workload], a.oracle_sample)
+        print(json.dumps({"bytes_per_s": bps, "layers": n, "seconds": secs, "threads": threads}))
+    elif a.impl == "reference":
         run_reference(a)
     else:
         run_gpu(a)

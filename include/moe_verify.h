@@ -245,7 +245,8 @@ moe_status moe_lm_head_argmax(const uint16_t* x_norm, int K, int H, const uint16
  *   x, x_out bf16 [K][H] (x_out may alias x); Wq [nq*128][H], Wk, Wv
  *   [nkv*128][H], Wo [H][nq*128]; kcache, vcache [nkv][C][128];
  *   k_new_out, v_new_out: optional [K][nkv*128] copies of the new keys and
- *   values (to append to the cache once rows are accepted).
+ *   values (to append to the cache once rows are accepted); o_out: optional
+ *   [K][nq*128] copy of the attention output o (before the o-projection).
  * Envelope: head_dim 128, nq even, nq % nkv == 0, K * nq/nkv <= 16, H a
  * multiple of 256 up to 4096, nq*128 <= 4096, C a multiple of 16.
  */
@@ -253,8 +254,8 @@ size_t moe_attention_workspace_size(int K, int H, int nq, int nkv, int head_dim)
 moe_status moe_attention_block(const uint16_t* x, int K, int H, int nq, int nkv, int head_dim, int C,
                                const uint16_t* Wq, const uint16_t* Wk, const uint16_t* Wv, const uint16_t* Wo,
                                const uint16_t* kcache, const uint16_t* vcache, float eps, uint16_t* x_out,
-                               uint16_t* k_new_out, uint16_t* v_new_out, void* ws, size_t ws_bytes,
-                               void* stream);
+                               uint16_t* k_new_out, uint16_t* v_new_out, uint16_t* o_out, void* ws,
+                               size_t ws_bytes, void* stream);
 
 /*
  * The full verify step of a decoder with GQA attention and MoE blocks:

@@ -95,7 +95,7 @@ def _load():
     L.moe_attention_workspace_size.argtypes = [ci, ci, ci, ci, ci]
     L.moe_attention_block.restype = ci
     L.moe_attention_block.argtypes = [vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp,
-                                      vp, vp, sz, vp]
+                                      vp, vp, vp, sz, vp]
     mp = ctypes.POINTER(moe_verify_model)
     L.moe_verify_step_workspace_size.restype = sz
     L.moe_verify_step_workspace_size.argtypes = [mp, ci]
@@ -270,12 +270,13 @@ def attention_workspace(K, H, nq, nkv, head_dim=128, device="cuda") -> torch.Ten
 
 
 def moe_attention_block(x, Wq, Wk, Wv, Wo, kcache, vcache, x_out, ws, nq, nkv, eps=1e-6, k_new=None, v_new=None,
-                        stream=None):
+                        stream=None, o_out=None):
     K, H = x.shape
     C = kcache.shape[1]
     _check(lib.moe_attention_block(_ptr(x), K, H, nq, nkv, 128, C, _ptr(Wq), _ptr(Wk), _ptr(Wv), _ptr(Wo),
                                    _ptr(kcache) if C else None, _ptr(vcache) if C else None, float(eps),
-                                   _ptr(x_out), _ptr(k_new), _ptr(v_new), _ptr(ws), ws.numel(), _stream(stream)),
+                                   _ptr(x_out), _ptr(k_new), _ptr(v_new), _ptr(o_out), _ptr(ws), ws.numel(),
+                                   _stream(stream)),
            "moe_attention_block")
 
 

@@ -1,9 +1,11 @@
 // capi.cu -- the C ABI: argument checks, workspace carving, TMA descriptors
-// and the launch sequence router -> gate/up -> down on the caller's stream.
+// and the launch sequences on the caller's stream.
 //
-// The three kernels of a layer are chained with programmatic dependent
-// launch: each dependent kernel is scheduled while its predecessor drains and
-// waits (griddepcontrol.wait) before reading the predecessor's results.
+// A layer call is one launch of the persistent experts kernel (router,
+// routing, experts and combine in one grid).  Consecutive kernels of a stack
+// or a verify step are chained with programmatic dependent launch: each
+// dependent kernel is scheduled while its predecessor drains and waits
+// (griddepcontrol.wait) before reading the predecessor's results.
 #include <atomic>
 #include <cmath>
 #include <cstring>
@@ -390,13 +392,13 @@ size_t moe_attention_workspace_size(int K, int H, int nq, int nkv, int head_dim)
 moe_status moe_attention_block(const uint16_t* x, int K, int H, int nq, int nkv, int head_dim, int C,
                                const uint16_t* Wq, const uint16_t* Wk, const uint16_t* Wv, const uint16_t* Wo,
                                const uint16_t* kcache, const uint16_t* vcache, float eps, uint16_t* x_out,
-                               uint16_t* k_new_out, uint16_t* v_new_out, void* ws, size_t ws_bytes,
-                               void* stream) {
+                               uint16_t* k_new_out, uint16_t* v_new_out, uint16_t* o_out, void* ws,
+                               size_t ws_bytes, void* stream) {
   moe_status st = check_attn(K, H, nq, nkv, head_dim, C);
   if (st != MOE_OK) return st;
   if (!x || !Wq || !Wk || !Wv || !Wo || !x_out || !ws || (C > 0 && (!kcache || !vcache)) || !(eps >= 0.f))
     return MOE_ERR_INVALID_ARG;
-  const void* ptrs[] = {x, Wq, Wk, Wv, Wo, kcache, vcache, x_out, k_new_out, v_new_out, ws};
+  const void* ptrs[] = {x, Wq, Wk, Wv, Wo, kcache, vcache, x_out, k_new_out, v_new_out, o_out, ws};
   for (const void* p : ptrs)
     if (!aligned16(p)) return MOE_ERR_MISALIGNED;
   const AttnLayout L = attn_layout(K, H, nq, nkv);
@@ -406,7 +408,7 @@ moe_status moe_attention_block(const uint16_t* x, int K, int H, int nq, int nkv,
   uint16_t* q = reinterpret_cast<uint16_t*>(b + L.q);
   uint16_t* kn = k_new_out ? k_new_out : reinterpret_cast<uint16_t*>(b + L.kn);
   uint16_t* vn = v_new_out ? v_new_out : reinterpret_cast<uint16_t*>(b + L.vn);
-  uint16_t* o = reinterpret_cast<uint16_t*>(b + L.o);
+  uint16_t* o = o_out ? o_out : reinterpret_cast<uint16_t*>(b + L.o);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   if (launch_rmsnorm(x, K, H, eps, xn, s, false) != cudaSuccess) return MOE_ERR_CUDA;
@@ -510,7 +512,8 @@ moe_status moe_verify_step(const moe_verify_model* m, uint16_t* x, int K, const 
   for (int l = 0; l < m->n_layers; ++l) {
     const moe_decoder_layer& d = m->layers[l];
     s = moe_attention_block(x, K, H, m->n_q_heads, m->n_kv_heads, m->head_dim, m->ctx, d.Wq, d.Wk, d.Wv, d.Wo,
-                            d.kcache, d.vcache, m->eps, x, nullptr, nullptr, b + L.attn_ws, L.attn_bytes, stream);
+                            d.kcache, d.vcache, m->eps, x, nullptr, nullptr, nullptr, b + L.attn_ws, L.attn_bytes,
+                            stream);
     if (s != MOE_OK) return s;
     // the MoE layer kernel applies its RMSNorm to x itself
     s = run_layer(&d.moe, x, K, x, x, nullptr, nullptr, nullptr, b + L.moe_ws, L.moe_bytes, stream, true, nullptr,

@@ -14,7 +14,10 @@
 
 namespace {
 
-constexpr size_t kStaticWsBytes = size_t(8) << 20;  // 8 MiB: enough for K <= 16 on the largest supported layer
+// 8 MiB.  Enough for K <= 16 at hidden 2048, 256 experts, top-8,
+// intermediate 512 with a shared expert (about 6.7 MB at K = 16); larger
+// layers (e.g. 1024 experts at top-32) are refused.
+constexpr size_t kStaticWsBytes = size_t(8) << 20;
 constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
@@ -22,16 +25,18 @@ __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
 std::mutex g_mu;
 void* g_addr[kMaxDevices] = {};
 
-// Device address of g_static_ws on the current device (set up on first use:
-// looked up and zero-filled once).  nullptr on failure.
-void* static_ws_on_current_device() {
+// Device address of g_static_ws on the current device, set up on first use:
+// looked up, then zero-filled once on `stream` (the caller's stream, so the
+// fill is ordered before the kernel that follows it on that stream, whatever
+// kind of stream it is).  nullptr on failure.
+void* static_ws_on_current_device(cudaStream_t stream) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lock(g_mu);
   if (!g_addr[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || !p) return nullptr;
-    if (cudaMemset(p, 0, kStaticWsBytes) != cudaSuccess) return nullptr;
+    if (cudaMemsetAsync(p, 0, kStaticWsBytes, stream) != cudaSuccess) return nullptr;
     g_addr[dev] = p;
   }
   return g_addr[dev];
@@ -46,11 +51,10 @@ extern "C" moe_status moe_verify_layer_static(const moe_layer* layer, const uint
   if (need == 0)  // invalid layer or K: the shared checks give the precise status, nothing is enqueued
     return run_layer(layer, x_norm, K, residual, y, idx_out, w_out, group_out, nullptr, 0, stream, true, nullptr);
   if (need > kStaticWsBytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  void* ws = static_ws_on_current_device();
+  void* ws = static_ws_on_current_device(static_cast<cudaStream_t>(stream));
   if (!ws) return MOE_ERR_CUDA;
-  // the error word of the previous call starts again from zero (the rest of
-  // the header, the count of earlier calls, must persist)
-  if (cudaMemsetAsync(ws, 0, sizeof(int), static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  // (the kernel only ever sets the array's error word, with a compare-and-swap
+  // from zero, and never reads it; nothing exposes it, so it is not reset)
   return run_layer(layer, x_norm, K, residual, y, idx_out, w_out, group_out, ws, kStaticWsBytes, stream, true,
                    nullptr);
 }

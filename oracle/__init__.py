@@ -74,7 +74,7 @@ def _bind(L):
     L.orc_moe_layer.argtypes = [vp, vp, ci, vp, vp, vp, vp, vp, vp]
     L.orc_rmsnorm.argtypes = [vp, ci, ci, cd, vp]
     L.orc_linear_bf16.argtypes = [vp, vp, ci, ci, ci, vp]
-    L.orc_attention.argtypes = [vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, vp, vp, vp, cd, vp]
+    L.orc_attention.argtypes = [vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, vp, vp, vp, cd, vp, vp]
     L.orc_lm_argmax.argtypes = [vp, vp, ci, ci, ci, vp, vp]
     L.orc_accept_prefix.restype = ci
     L.orc_accept_prefix.argtypes = [vp, vp, ci]
@@ -234,14 +234,17 @@ def linear_bf16(x, W, L=None):
     return out
 
 
-def attention(x, Wq, Wk, Wv, Wo, kc, vc, nq, nkv, hd, eps=RMS_EPS, L=None):
+def attention(x, Wq, Wk, Wv, Wo, kc, vc, nq, nkv, hd, eps=RMS_EPS, L=None, with_o=False):
+    """The block output x + o.Wo^T (bf16 [K, H]); with ``with_o`` also the
+    attention output o itself (bf16 [K, nq*hd])."""
     x = _c(x, np.uint16)
     K, H = x.shape
     C = kc.shape[1]
     arrs = [_c(a, np.uint16) for a in (Wq, Wk, Wv, Wo, kc, vc)]
     out = np.empty_like(x)
-    (L or lib()).orc_attention(_p(x), K, H, nq, nkv, hd, C, *[_p(a) for a in arrs], eps, _p(out))
-    return out
+    o = np.empty((K, nq * hd), np.uint16) if with_o else None
+    (L or lib()).orc_attention(_p(x), K, H, nq, nkv, hd, C, *[_p(a) for a in arrs], eps, _p(out), _p(o))
+    return (out, o) if with_o else out
 
 
 def lm_argmax(x_norm, W, L=None):
@@ -276,18 +279,20 @@ def verify_step(w, layers, lm_head, x0, n_layers=None, L=None):
     """The full verify step: per layer the attention block, then the MoE block
     (x <- x + MoE(rmsnorm(x))), then the lm_head argmax of every row.
     ``layers(l)`` returns (attention dict with Wq, Wk, Wv, Wo, kc, vc; MoE
-    synthgen.Layer).  Returns dict(x, target, best, att_in, moe_in, idx, xn)."""
+    synthgen.Layer).  Returns dict(x, target, best, att_in, att_o, moe_in, idx,
+    xn): att_o[l] is layer l's attention output o (before the o-projection)."""
     x = _c(x0, np.uint16)
-    att_in, moe_in, idx = [], [], []
+    att_in, moe_in, idx, att_o = [], [], [], []
     for l in range(n_layers or w.layers):
         att, moe = layers(l)
         att_in.append(x.copy())
-        x = attention(x, att["Wq"], att["Wk"], att["Wv"], att["Wo"], att["kc"], att["vc"], w.n_q_heads,
-                      w.n_kv_heads, w.head_dim, L=L)
+        x, o = attention(x, att["Wq"], att["Wk"], att["Wv"], att["Wo"], att["kc"], att["vc"], w.n_q_heads,
+                         w.n_kv_heads, w.head_dim, L=L, with_o=True)
+        att_o.append(o)
         moe_in.append(x.copy())
         r = moe_layer(OracleLayer.from_workload(w, moe), rmsnorm(x, L=L), residual=x, L=L)
         idx.append(r["idx"])
         x = r["y"]
     xn = rmsnorm(x, L=L)
     tok, best = lm_argmax(xn, lm_head, L=L)
-    return dict(x=x, target=tok, best=best, att_in=att_in, moe_in=moe_in, idx=idx, xn=xn)
+    return dict(x=x, target=tok, best=best, att_in=att_in, att_o=att_o, moe_in=moe_in, idx=idx, xn=xn)

@@ -31,10 +31,10 @@
  *    elements along a row shares one E4M3 scale, and the projection carries
  *    one FP32 tensor scale; value = e2m1 * e4m3 * tensor_scale.
  *
- * Readings where the pages are silent (each is listed with its reason in the
- * design notes): softmax scoring with top-k renormalisation; exact ties in
- * selection go to the lower index; router and lm_head logits are formed in
- * one fixed FP32 order (below) because an integer decision depends on them;
+ * Readings where the pages are silent: softmax scoring with top-k
+ * renormalisation; exact ties in selection go to the lower index; router
+ * and lm_head logits are formed in one fixed FP32 order (below) because an
+ * integer decision depends on them;
  * RMSNorm with unit gain and eps 1e-6 before every MoE block, attention
  * block and the lm_head; low nibble holds the even column.
  */
@@ -407,11 +407,12 @@ void orc_linear_bf16(const uint16_t* x, const uint16_t* W, int K, int D, int N, 
  *   Wq [nq*hd][H], Wk, Wv [nkv*hd][H], Wo [H][nq*hd] (bf16)
  *   kc, vc [nkv][C][hd] (bf16): the cache
  *   x_out[K][H] = bf16( x + o . Wo^T ), o = bf16(softmax(q k^T / sqrt(hd)) v)
+ *   o_out[K][nq*hd] (optional): o itself
  * The block's own input normalisation is applied first (orc_rmsnorm).
  */
 void orc_attention(const uint16_t* x, int K, int H, int nq, int nkv, int hd, int C,
                    const uint16_t* Wq, const uint16_t* Wk, const uint16_t* Wv, const uint16_t* Wo,
-                   const uint16_t* kc, const uint16_t* vc, double eps, uint16_t* x_out) {
+                   const uint16_t* kc, const uint16_t* vc, double eps, uint16_t* x_out, uint16_t* o_out) {
   int QD = nq * hd, KD = nkv * hd, grp = nq / nkv;
   uint16_t* xn = (uint16_t*)malloc(2 * (size_t)K * H);
   uint16_t* q = (uint16_t*)malloc(2 * (size_t)K * QD);
@@ -458,6 +459,7 @@ void orc_attention(const uint16_t* x, int K, int H, int nq, int nkv, int hd, int
       for (int c = 0; c < QD; ++c) s += orc_bf16(o[(size_t)r * QD + c]) * orc_bf16(Wo[(size_t)j * QD + c]);
       x_out[(size_t)r * H + j] = orc_round_bf16(orc_bf16(x[(size_t)r * H + j]) + s);
     }
+  if (o_out) memcpy(o_out, o, 2 * (size_t)K * QD);
   free(xn); free(q); free(kn); free(vn); free(o);
 }
 

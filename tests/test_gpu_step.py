@@ -2,7 +2,8 @@
 lm_head argmax of every row, accepted prefix) against the oracle.
 
 Teacher-forced on the oracle's own inputs for each block: the attention
-block's output within tolerance, RMSNorm and routing bit-exact, the MoE
+output o (before the o-projection) and the attention block's output within
+tolerance, RMSNorm and routing bit-exact, the MoE
 block's output within tolerance, the greedy tokens and the accepted length
 exact.  The native moe_verify_step then runs free on the GPU from the same
 input; its accepted length must equal the oracle's wherever its greedy tokens
@@ -49,16 +50,20 @@ def test_verify_step(cuda_ok, n_layers):
     lws = M.workspace(model.layers[0].moe, K)
     xn = torch.empty(K, H, dtype=torch.bfloat16, device="cuda")
     idx = torch.empty((K, w.top_k), dtype=torch.int32, device="cuda")
+    o = torch.empty(K, w.n_q_heads * w.head_dim, dtype=torch.bfloat16, device="cuda")
     for l in range(n_layers):
         dl = model.layers[l]
         xa = to_dev_bf16(ref["att_in"][l])
         M.moe_attention_block(xa, dl.Wq, dl.Wk, dl.Wv, dl.Wo, dl.kcache, dl.vcache, xa, aws, w.n_q_heads,
-                              w.n_kv_heads)
+                              w.n_kv_heads, o_out=o)
         xm = to_dev_bf16(ref["moe_in"][l])
         M.moe_rmsnorm(xm, xn)
         y = torch.empty_like(xm)
         M.moe_verify_layer(dl.moe, xn, xm, y, lws, idx_out=idx)
         torch.cuda.synchronize()
+        # the attention output itself, not only the block output (the term is
+        # ~1.5% of x + attn at this shape)
+        assert_parity(bf16_bits(o), ref["att_o"][l], f"attention output o, layer {l}")
         assert_parity(bf16_bits(xa), ref["moe_in"][l], f"attention block {l}")
         np.testing.assert_array_equal(bf16_bits(xn), oracle.rmsnorm(ref["moe_in"][l]), err_msg=f"rmsnorm {l}")
         np.testing.assert_array_equal(idx.cpu().numpy(), ref["idx"][l], err_msg=f"routing {l}")

@@ -231,6 +231,76 @@ def test_topk_against_library_and_invariants(k2layer):
         assert np.all(np.diff(l32[r, idx[r]]) <= 0)
 
 
+@pytest.fixture(scope="module")
+def zipf_layer():
+    # the skewed-routing workload: router bias b[e] = -1.1 ln(e + 1) (a Zipf
+    # log-prior over the experts, added to the logits before the softmax)
+    w = synthgen.WORKLOADS["k16_zipf_stack40"]
+    L = synthgen.make_layer(w, 0, experts=[])
+    return w, L, oracle.OracleLayer.from_workload(w, L)
+
+
+def test_zipf_bias_is_the_log_prior(zipf_layer):
+    w, L, _ = zipf_layer
+    e = np.arange(w.E, dtype=np.float64)
+    assert np.allclose(L.router_b, -1.1 * np.log(e + 1.0), rtol=0, atol=1e-6)
+    assert L.router_b[0] == 0.0 and np.all(np.diff(L.router_b) < 0)
+
+
+def test_router_logits_with_bias_match_library(zipf_layer):
+    w, L, ol = zipf_layer
+    x = synthgen.make_x(w, 3)
+    ref = (_bf(x) @ _bf(L.router_w).T + torch.from_numpy(L.router_b.astype(np.float64))).numpy()
+    assert np.allclose(oracle.router_logits_f64(ol, x), ref, rtol=0, atol=1e-12)
+    # FP32 fixed order: the dot product's error bound, plus the rounding of
+    # the final bias add (half an ulp of the result)
+    got = oracle.router_logits_f32(ol, x).astype(np.float64)
+    bound = (_bf(x).abs() @ _bf(L.router_w).abs().T).numpy() * (w.H + 5) * 2.0 ** -24 + np.abs(ref) * 2.0 ** -24
+    assert np.all(np.abs(got - ref) <= bound)
+
+
+def test_topk_with_bias_against_library(zipf_layer):
+    w, L, ol = zipf_layer
+    x = synthgen.make_x(w, 4)
+    l32 = oracle.router_logits_f32(ol, x)
+    idx, wt = oracle.topk(l32, w.top_k)
+    l64 = torch.from_numpy(l32.astype(np.float64))
+    _, ref_idx = torch.topk(l64, w.top_k, dim=1)
+    assert np.array_equal(idx, ref_idx.numpy())
+    p = torch.softmax(l64, dim=1)
+    sel = torch.gather(p, 1, ref_idx)
+    assert np.allclose(wt, (sel / sel.sum(1, keepdim=True)).numpy(), rtol=1e-6, atol=0)
+    # the prior shows: low expert ids are chosen far more often than without it
+    unb = oracle.topk(l32 - L.router_b[None, :], w.top_k)[0]
+    assert (idx < 16).sum() > 3 * (unb < 16).sum()
+
+
+def test_router_bias_flips_selection_hand_worked():
+    # H = 256, x = e_0 (1.0 at k = 0), router column 0 = (1.0, 0.5, 0, 0):
+    # unbiased logits (1.0, 0.5, 0, 0).  Bias (0, 0.75, 0, -1) added before
+    # the softmax gives (1.0, 1.25, 0, -1): top-1 is expert 1 (it would be 0
+    # without the bias, or with the bias subtracted), and the top-2 weights
+    # are the softmax of (1.25, 1.0) over the pair: 1 / (1 + e^-0.25) and
+    # 1 / (1 + e^0.25).  A bias added after the softmax, or used for the
+    # selection only, would weight expert 1 by e^0.5 / (e^1 + e^0.5) instead.
+    H, E = 256, 4
+    x = np.zeros((1, H), np.uint16)
+    x[0, 0] = 0x3F80
+    W = np.zeros((E, H), np.uint16)
+    W[0, 0], W[1, 0] = 0x3F80, 0x3F00
+    b = np.array([0.0, 0.75, 0.0, -1.0], np.float32)
+    lay = synthgen.Layer(router_w=W, router_b=b, gate=None, up=None, down=None)
+    ol = oracle.OracleLayer(lay, H, E, 2, 16, 0)
+    l32 = oracle.router_logits_f32(ol, x)
+    assert l32.tolist() == [[1.0, 1.25, 0.0, -1.0]]
+    idx, wt = oracle.topk(l32, 1)
+    assert idx.tolist() == [[1]] and wt.tolist() == [[1.0]]
+    idx, wt = oracle.topk(l32, 2)
+    assert idx.tolist() == [[1, 0]]
+    assert abs(wt[0, 0] - 1 / (1 + math.exp(-0.25))) < 1e-7
+    assert abs(wt[0, 1] - 1 / (1 + math.exp(0.25))) < 1e-7
+
+
 def test_topk_exact_ties_go_to_lower_index():
     logits = np.array([[1.0, 3.0, 3.0, 0.5, 3.0, 2.0]], np.float32)
     idx, w = oracle.topk(logits, 3)
@@ -365,6 +435,29 @@ def test_rmsnorm_against_library():
     ref = (x64 * torch.rsqrt(x64.pow(2).mean(1, keepdim=True) + 1e-6)).numpy()
     assert np.allclose(got, ref, rtol=2.0 ** -8, atol=0)
     assert np.allclose(np.sqrt((got ** 2).mean(1)), 1.0, atol=1e-2)
+
+
+def test_rmsnorm_fp32_steps_hand_worked():
+    # H = 256, two nonzero entries: x[10] = 1.9375, x[77] = 3.34375.
+    #   ss   = 1.9375^2 + 3.34375^2 = 14.9345703125       (exact in FP32)
+    #   mean = ss / 256 = 0.058338165283203125             (exact)
+    #   mean + eps -> 0.058339164 (FP32), sqrt -> 0.24153501 (FP32),
+    #   inv = 1 / 0.24153501 -> 4.140187 (FP32)
+    #   x[77] * inv -> 13.84375 exactly, the midpoint of the bf16 neighbours
+    #   13.8125 (0x415D) and 13.875 (0x415E): ties to even give 0x415E;
+    #   x[10] * inv -> 8.021612 -> bf16 8.0 (0x4100).
+    # A single rounding of 1/sqrt(mean + eps) gives inv = 4.1401863, one
+    # FP32 ulp lower, and x[77] -> 0x415D; evaluating in double also gives
+    # 0x415D: the oracle's two correctly rounded FP32 steps are what this pins.
+    x = np.zeros((1, 256), np.uint16)
+    x[0, 10], x[0, 77] = 0x3FF8, 0x4056
+    out = oracle.rmsnorm(x)
+    expect = np.zeros((1, 256), np.uint16)
+    expect[0, 10], expect[0, 77] = 0x4100, 0x415E
+    assert np.array_equal(out, expect), (hex(out[0, 10]), hex(out[0, 77]))
+    f32 = np.float32
+    inv_single = f32(1.0 / np.sqrt(np.float64(f32(14.9345703125 / 256)) + np.float64(f32(1e-6))))
+    assert inv_single == f32(4.1401863) and f32(3.34375) * inv_single < f32(13.84375)
 
 
 def _att_inputs(K, H, nq, nkv, hd, C, seed):

@@ -3,11 +3,15 @@
 Some callers cannot allocate device memory (an engine whose allocator owns
 the GPU, a decode loop that cannot afford cudaMalloc's implicit
 synchronisation); for them the layer keeps its scratch in a fixed array
-inside the library.  This checks, through the C ABI, that two calls in a row
-give the same routing and outputs as moe_verify_layer with a caller-owned
-workspace (within the layer's parity tolerance), and that a layer needing
-more scratch than the array holds is refused.  This file is collected last
-on purpose and does not depend on the other tests having run."""
+inside the library.  Through the C ABI, two calls in a row must give exactly
+the routing and outputs of moe_verify_layer with a caller-owned workspace:
+both run the same deterministic kernel, so the results are compared bit for
+bit (a race on the shared array would show up here).  The calls run on a
+side stream (torch's pool streams do not wait for the legacy default
+stream), so the one-time zero fill of the array must be ordered on the
+caller's stream.  A layer needing more scratch than the array holds is
+refused.  This file is collected last on purpose and does not depend on the
+other tests having run."""
 import ctypes
 
 import numpy as np
@@ -15,7 +19,7 @@ import pytest
 import torch
 
 import synthgen
-from helpers import assert_parity, bf16_bits, to_dev_bf16, upload
+from helpers import bf16_bits, to_dev_bf16, upload
 
 pytestmark = pytest.mark.gpu
 
@@ -26,31 +30,34 @@ def test_static_scratch_matches_caller_workspace(cuda_ok, name):
     w = synthgen.WORKLOADS[name]
     dl = upload(synthgen.make_layer(w, 2), w)
     c = dl.c()
-    stream = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    ws = M.workspace(dl, w.K)
     for call in range(2):
         x = to_dev_bf16(synthgen.make_x(w, 40 + call))
         res = to_dev_bf16(synthgen.make_x(w, 50 + call))
+        torch.cuda.synchronize()
         outs = []
         for static in (True, False):
-            y = torch.empty_like(x)
-            idx = torch.empty((w.K, w.top_k), dtype=torch.int32, device="cuda")
-            wt = torch.empty((w.K, w.top_k), dtype=torch.float32, device="cuda")
-            grp = torch.empty(M.moe_group_ints(w.K, w.E, w.top_k), dtype=torch.int32, device="cuda")
-            if static:
-                st = M.lib.moe_verify_layer_static(ctypes.byref(c), x.data_ptr(), w.K, res.data_ptr(),
-                                                   y.data_ptr(), idx.data_ptr(), wt.data_ptr(), grp.data_ptr(),
-                                                   ctypes.c_void_p(stream.cuda_stream))
-                assert st == M.MOE_OK, M.status_string(st)
-            else:
-                ws = M.workspace(dl, w.K)
-                M.moe_verify_layer(dl, x, res, y, ws, idx, wt, grp)
-            torch.cuda.synchronize()
+            with torch.cuda.stream(side):
+                y = torch.empty_like(x)
+                idx = torch.empty((w.K, w.top_k), dtype=torch.int32, device="cuda")
+                wt = torch.empty((w.K, w.top_k), dtype=torch.float32, device="cuda")
+                grp = torch.empty(M.moe_group_ints(w.K, w.E, w.top_k), dtype=torch.int32, device="cuda")
+                if static:
+                    st = M.lib.moe_verify_layer_static(ctypes.byref(c), x.data_ptr(), w.K, res.data_ptr(),
+                                                       y.data_ptr(), idx.data_ptr(), wt.data_ptr(),
+                                                       grp.data_ptr(), ctypes.c_void_p(side.cuda_stream))
+                    assert st == M.MOE_OK, M.status_string(st)
+                else:
+                    M.moe_verify_layer(dl, x, res, y, ws, idx, wt, grp, stream=side)
+            side.synchronize()
             outs.append((bf16_bits(y), idx.cpu().numpy(), wt.cpu().numpy(), grp.cpu().numpy()))
         (ys, idxs, ws_, gs), (yr, idxr, wr, gr) = outs
-        np.testing.assert_array_equal(idxs, idxr)
-        np.testing.assert_array_equal(gs, gr)
-        np.testing.assert_allclose(ws_, wr, rtol=4e-6, atol=1e-7)
-        assert_parity(ys, yr, f"{name} static scratch, call {call}")
+        np.testing.assert_array_equal(idxs, idxr, err_msg=f"{name} call {call}: routing")
+        np.testing.assert_array_equal(gs, gr, err_msg=f"{name} call {call}: grouping")
+        np.testing.assert_array_equal(ws_.view(np.uint32), wr.view(np.uint32), err_msg=f"{name} call {call}: weights")
+        np.testing.assert_array_equal(ys, yr, err_msg=f"{name} call {call}: y")
+    assert M.moe_workspace_error(ws) == 0
 
 
 def test_static_scratch_refuses_oversized_layer(cuda_ok):
