@@ -64,6 +64,28 @@ typedef struct {
 } moe_nvfp4;
 
 /*
+ * Router scoring (moe_layer.scoring).
+ *  MOE_SCORE_SOFTMAX  probabilities softmax(logit + bias) over all experts;
+ *                     the top_k largest logit + bias are selected and their
+ *                     probabilities renormalised over the selection.
+ *  MOE_SCORE_SIGMOID  the router tail of the Laguna checkpoint (PR #844,
+ *                     "4. What I ported", router-tail row; "5. Numerical
+ *                     safety": renormalised top-k, routed scaling 2.5):
+ *                     scores s = sigmoid(logit) in FP32, the bias added to
+ *                     the scores for the selection only (the top_k largest
+ *                     s + bias), weights = the selected s / their sum.
+ *                     The sigmoid is one fixed sequence of correctly rounded
+ *                     FP32 operations, so the selection is reproducible:
+ *                       l <- clamp(l, -80, 80), t = -l,
+ *                       n = rint(t * log2 e), r = t - n ln2 (ln 2 split in a
+ *                       16-bit head and a tail, two fused multiply-adds),
+ *                       e = (degree-7 Taylor polynomial of e^r) * 2^n,
+ *                       s = 1 / (1 + e).
+ */
+#define MOE_SCORE_SOFTMAX 0
+#define MOE_SCORE_SIGMOID 1
+
+/*
  * One MoE layer.  gate/up: rows = inter, cols = hidden; down: rows = hidden,
  * cols = inter; the sh_* projections hold one expert of intermediate
  * shared_inter (0 = no shared expert, the sh_* fields are then ignored).
@@ -75,9 +97,12 @@ typedef struct {
   int hidden, n_experts, top_k, inter, shared_inter;
   float routed_scale;          /* multiplies the routed sum (1.0 = none) */
   const uint16_t* router_w;    /* bf16 [n_experts][hidden] */
-  const float* router_bias;    /* [n_experts], added to the logits; NULL = 0 */
+  const float* router_bias;    /* [n_experts] or NULL = 0: added to the logits
+                                  (softmax scoring) or to the sigmoid scores
+                                  for the selection only (sigmoid scoring) */
   moe_nvfp4 gate, up, down;
   moe_nvfp4 sh_gate, sh_up, sh_down;
+  int scoring;                 /* MOE_SCORE_SOFTMAX (0) or MOE_SCORE_SIGMOID */
 } moe_layer;
 
 /* Largest number of verify rows one call accepts. */
@@ -124,6 +149,10 @@ size_t moe_group_ints(int K, int n_experts, int top_k);
  * (PR #844, "4. What I ported" and "5. Numerical safety": silu(gate)*up,
  * weighted expert sum, routed scaling, shared add and decoder residual add
  * in that order).  Each distinct expert's weights are read once per call.
+ * The combine is one FP32 expression per output, each operation rounded
+ * (no fused multiply-add), one bf16 rounding at the end:
+ *   acc = 0;  acc = acc + w_{r,s} * d_{r,s}  for s = 0 .. top_k-1
+ *   y   = bf16( ((routed_scale * acc) + d_sh) + residual )
  *   x_norm    bf16 [K][hidden], the normalised block input
  *   residual  bf16 [K][hidden] or NULL
  *   y         bf16 [K][hidden] out (may alias residual, not x_norm)
@@ -304,6 +333,14 @@ const char* moe_status_string(moe_status s);
  * up at once, which exercises the timeout path without hanging a GPU.
  */
 void moe_debug_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Test hook: byte offset, inside a moe_verify_layer workspace, of the down
+ * partials d_{r,s} the combine reads: [K][top_k + 1][hidden] 64-bit words
+ * whose low 32 bits are the FP32 partial (slot top_k = the shared expert);
+ * they hold the last call's values.  0 on an invalid layer or K.
+ */
+size_t moe_debug_partials_offset(const moe_layer* layer, int K);
 
 /*
  * Profiling hook: when `buf` (device memory, one row of 80 uint64 per SM)

@@ -32,8 +32,8 @@ EXPORTS = ("moe_verify_layer_workspace_size", "moe_router_topk", "moe_group_ints
            "moe_verify_layer_profiled", "verify_accept_prefix", "moe_rmsnorm", "moe_lm_head_workspace_size",
            "moe_lm_head_argmax", "moe_verify_stack_workspace_size", "moe_verify_stack",
            "moe_attention_workspace_size", "moe_attention_block", "moe_verify_layer_static",
-           "moe_verify_step_workspace_size", "moe_verify_step", "moe_workspace_error", "moe_status_string", "moe_debug_set_wait_limit_ns",
-           "moe_debug_set_trace")
+           "moe_verify_step_workspace_size", "moe_verify_step", "moe_workspace_error", "moe_status_string",
+           "moe_debug_set_wait_limit_ns", "moe_debug_set_trace", "moe_debug_partials_offset")
 
 
 class MoeError(RuntimeError):
@@ -51,7 +51,11 @@ class moe_layer(ctypes.Structure):
                 ("inter", ctypes.c_int), ("shared_inter", ctypes.c_int), ("routed_scale", ctypes.c_float),
                 ("router_w", ctypes.c_void_p), ("router_bias", ctypes.c_void_p),
                 ("gate", moe_nvfp4), ("up", moe_nvfp4), ("down", moe_nvfp4),
-                ("sh_gate", moe_nvfp4), ("sh_up", moe_nvfp4), ("sh_down", moe_nvfp4)]
+                ("sh_gate", moe_nvfp4), ("sh_up", moe_nvfp4), ("sh_down", moe_nvfp4), ("scoring", ctypes.c_int)]
+
+
+MOE_SCORE_SOFTMAX = 0
+MOE_SCORE_SIGMOID = 1
 
 
 class moe_decoder_layer(ctypes.Structure):
@@ -115,6 +119,8 @@ def _load():
     L.moe_debug_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     L.moe_debug_set_trace.restype = None
     L.moe_debug_set_trace.argtypes = [vp]
+    L.moe_debug_partials_offset.restype = sz
+    L.moe_debug_partials_offset.argtypes = [lp, ci]
     return L
 
 
@@ -168,6 +174,7 @@ class Layer:
     sh_gate: Proj | None = None
     sh_up: Proj | None = None
     sh_down: Proj | None = None
+    scoring: int = MOE_SCORE_SOFTMAX
 
     def c(self) -> moe_layer:
         z = moe_nvfp4(None, None, None)
@@ -177,7 +184,7 @@ class Layer:
                          None if self.router_bias is None else self.router_bias.data_ptr(),
                          self.gate.c(), self.up.c(), self.down.c(),
                          self.sh_gate.c() if sh else z, self.sh_up.c() if sh else z,
-                         self.sh_down.c() if sh else z)
+                         self.sh_down.c() if sh else z, self.scoring)
 
 
 def moe_group_ints(K: int, n_experts: int, top_k: int) -> int:
@@ -360,7 +367,7 @@ def _dev(a, device, dtype=None):
 
 
 def layer_from_arrays(router_w, router_bias, gate, up, down, sh=None, top_k=8, routed_scale=1.0,
-                      device="cuda") -> Layer:
+                      device="cuda", scoring=MOE_SCORE_SOFTMAX) -> Layer:
     """Uploads host arrays to a device ``Layer``.  ``gate``/``up``/``down`` (and
     the optional ``sh`` triple) are (codes uint8, scales uint8, tscale float32)
     numpy arrays shaped [n_exp, rows, cols//2], [n_exp, rows, cols//16], [n_exp];
@@ -376,4 +383,4 @@ def layer_from_arrays(router_w, router_bias, gate, up, down, sh=None, top_k=8, r
                  router_bias=None if router_bias is None else _dev(router_bias, device),
                  gate=proj(gate), up=proj(up), down=proj(down),
                  sh_gate=None if sh is None else proj(sh[0]), sh_up=None if sh is None else proj(sh[1]),
-                 sh_down=None if sh is None else proj(sh[2]))
+                 sh_down=None if sh is None else proj(sh[2]), scoring=scoring)

@@ -115,6 +115,7 @@ moe_status check_layer(const moe_layer* L, int K) {
   if (!(I == 128 || I == 256 || I == 512)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!(Is == 0 || Is == I)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (k > 32 || k > E || E > 1024) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (L->scoring != MOE_SCORE_SOFTMAX && L->scoring != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
   if (!L->router_w) return MOE_ERR_INVALID_ARG;
   if (!aligned16(L->router_w) || !aligned16(L->router_bias)) return MOE_ERR_MISALIGNED;
   moe_status s;
@@ -144,6 +145,7 @@ RouterArgs router_args(const moe_layer* L, const uint16_t* x, int K, const WsPtr
   a.k = L->top_k;
   a.G = group_cap(K, L->n_experts, L->top_k);
   a.has_shared = L->shared_inter > 0;
+  a.scoring = L->scoring;
   a.ws = wp;
   a.idx_out = idx_out;
   a.w_out = w_out;
@@ -247,6 +249,7 @@ __attribute__((visibility("hidden"))) moe_status run_layer(const moe_layer* laye
   ea.k = layer->top_k;
   ea.G = group_cap(K, E, layer->top_k);
   ea.has_shared = has_sh;
+  ea.scoring = layer->scoring;
   ea.routed_scale = layer->routed_scale;
   ea.router_w = layer->router_w;
   ea.router_bias = layer->router_bias;
@@ -548,6 +551,11 @@ const char* moe_status_string(moe_status s) {
     case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
   }
   return "unknown status";
+}
+
+size_t moe_debug_partials_offset(const moe_layer* layer, int K) {
+  if (check_layer(layer, K) != MOE_OK) return 0;
+  return layout_of(layer, K).dpart;
 }
 
 void moe_debug_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns); }

@@ -36,7 +36,8 @@
 // h per row and 128-wide k-unit), undone in FP32.
 //
 // Combine: per-(row, slot) FP32 partials; the outputs are shared by the CTAs,
-// y = bf16(routed_scale * sum_s w_s d_s + d_shared + residual) in slot order
+// y = bf16(routed_scale * sum_s w_s d_s + d_shared + residual) in slot order,
+// every FP32 operation rounded on its own
 // (PR #844, "4. What I ported": weighted sum, routed scale, shared add,
 // residual add in one pass).
 #include <cfloat>
@@ -212,9 +213,11 @@ __device__ __forceinline__ bool warp_gives_up(uint64_t t0, uint64_t wait_ns, con
 // holds experts l + 32 i), read once every word carries `tag` (a bounded
 // wait; false if it gave up): k rounds of a warp arg-max, larger logit first
 // and lower index on ties; NaN logits rank last, lowest index first.  Lane 0
-// writes the selected experts and their logits.
+// writes the selected experts and their keys.  With `sel_bias` (sigmoid
+// scoring) the words hold scores and the keys are score + bias.
 __device__ __noinline__ bool topk_general(const unsigned long long* row, unsigned tag, uint64_t wait_ns,
-                                          const int* abort_flag, int E, int k, int* idx, float* w, int lane) {
+                                          const int* abort_flag, int E, int k, int* idx, float* w,
+                                          const float* sel_bias, int lane) {
   float lv[32];
   unsigned taken = 0;
   const uint64_t t0 = global_timer_ns();
@@ -228,6 +231,7 @@ __device__ __noinline__ bool topk_general(const unsigned long long* row, unsigne
         const unsigned long long wv = ld_tagged(row + e);
         mine &= has_tag(wv, tag);
         v = __uint_as_float((unsigned)wv);
+        if (sel_bias) v = __fadd_rn(v, sel_bias[e]);  // sigmoid scoring: selection key = score + bias
       }
       lv[i] = v;
     }
@@ -281,14 +285,19 @@ __device__ __noinline__ bool topk_general(const unsigned long long* row, unsigne
 // Routing of row r when E <= 256 and k <= 8 (one warp, in its own function
 // so that its registers do not weigh on the item loops): waits (bounded)
 // until the row's tagged logits all carry `tag`, selects the top k, and
-// writes the renormalised softmax weights, the experts and the row's bits of
-// the expert masks.  On giving up it writes experts 0 .. k-1 (in range for
-// the tables) and returns false.
+// writes the renormalised weights, the experts and the row's bits of the
+// expert masks.  Softmax scoring: the words are logits (bias included), the
+// weights the softmax over the selection.  Sigmoid scoring: the words are
+// scores, the keys score + bias, the weights the selected scores over their
+// sum.  On giving up it writes experts 0 .. k-1 (in range for the tables)
+// and returns false.
 __device__ __noinline__ bool route_row_fast(const unsigned long long* row, unsigned tag, int E, int k, int r,
                                             uint64_t wait_ns, const int* abort_flag, int* s_idx, float* s_w,
-                                            unsigned* s_rowmask, unsigned* s_used, int lane) {
+                                            unsigned* s_rowmask, unsigned* s_used, int scoring,
+                                            const float* sel_bias, int lane) {
   bool got = true;
   unsigned long long v[8];
+  float sc[8];  // sigmoid scoring: the raw scores of this lane's experts
   const uint64_t t0 = global_timer_ns();
   for (;;) {
     bool mine = true;
@@ -296,10 +305,13 @@ __device__ __noinline__ bool route_row_fast(const unsigned long long* row, unsig
     for (int i = 0; i < 8; ++i) {
       const int e = lane + 32 * i;
       v[i] = 0ull;
+      sc[i] = 0.f;
       if (e < E) {
         const unsigned long long wv = ld_tagged(row + e);
         mine &= has_tag(wv, tag);
-        v[i] = sel_key(__uint_as_float((unsigned)wv), e);
+        const float val = __uint_as_float((unsigned)wv);
+        sc[i] = val;
+        v[i] = sel_key(scoring && sel_bias ? __fadd_rn(val, sel_bias[e]) : val, e);
       }
     }
     if (__all_sync(0xffffffffu, mine)) break;
@@ -312,10 +324,22 @@ __device__ __noinline__ bool route_row_fast(const unsigned long long* row, unsig
   unsigned long long sel, first;  // lane s < k takes selection s
   warp_top8(v, lane, sel, first);
   const int sel_e = got ? key_index(sel) : lane;
-  const float top = key_value(first);
-  // renormalised softmax over the selected logits (selections live in lanes
-  // < k; the others add exact zeros to the sum)
-  const float ev = (lane < k && got) ? expf(key_value(sel) - top) : 0.f;
+  float ev;
+  if (scoring) {
+    // the selected expert's own score (not its key) from the lane holding it
+    float mys = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float t = __shfl_sync(0xffffffffu, sc[i], sel_e & 31);
+      if (i == (sel_e >> 5)) mys = t;
+    }
+    ev = (lane < k && got) ? mys : 0.f;
+  } else {
+    // renormalised softmax over the selected logits (selections live in
+    // lanes < k; the others add exact zeros to the sum)
+    const float top = key_value(first);
+    ev = (lane < k && got) ? expf(key_value(sel) - top) : 0.f;
+  }
   float z = ev;
 #pragma unroll
   for (int d = 16; d >= 1; d >>= 1) z += __shfl_xor_sync(0xffffffffu, z, d);
@@ -680,7 +704,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned* s_rowmask = reinterpret_cast<unsigned*>(s_idx + K * k);   // [E] rows that chose expert e
   int* s_uexp = reinterpret_cast<int*>(s_rowmask + E);                // [G+1] distinct experts, ascending
   float* s_tse = reinterpret_cast<float*>(s_uexp + G + 1);            // [E+1][3] tensor scales (E = shared)
-  signed char* s_slot = reinterpret_cast<signed char*>(s_tse + 3 * (E + 1));  // [(G+1)*K]
+  float* s_bias = s_tse + 3 * (E + 1);                                // [E] router bias (0 if none)
+  signed char* s_slot = reinterpret_cast<signed char*>(s_bias + E);   // [(G+1)*K]
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -753,11 +778,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     it.kind = kShGU;
     it.slot = G;
     it.tile = blockIdx.x;
-    for (; issued < n_shb && issued < S; ++issued, it.tile += grid)
+    for (; issued < n_shb && issued < S; ++issued, it.tile += grid) {
+      if (lane == 0 && trace && issued < 24) trace[40 + issued] = global_timer_ns();
       issue_item(ic, it, smem + (size_t)issued * stage_bytes, &full_bar[issued], lane);
+    }
   } else if (warp < kCompWarps) {
     const int tid = threadIdx.x;
-    for (int e = tid; e < E; e += kCompThreads) s_rowmask[e] = 0u;
+    for (int e = tid; e < E; e += kCompThreads) {
+      s_rowmask[e] = 0u;
+      s_bias[e] = a.router_bias ? a.router_bias[e] : 0.f;  // weights of the layer: no dependency
+    }
     for (int i = tid; i < (G + 1) * K; i += kCompThreads) s_slot[i] = -1;
   }
   // the tensor scales (slot E = shared): their loads come from DRAM and are
@@ -903,7 +933,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int d = 16; d >= 1; d >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, d));
       if (lane == 0) {
-        const float lg = a.router_bias ? __fadd_rn(acc, a.router_bias[e]) : acc;
+        // softmax scoring: the logit with its bias; sigmoid scoring: the
+        // score (the bias only enters the selection keys)
+        const float lg = a.scoring ? sigmoid_score(acc) : (a.router_bias ? __fadd_rn(acc, s_bias[e]) : acc);
         xchg_tagged(a.ws.tlog + (size_t)r * E + e, tagged((unsigned)(wcall % 0xFFFFFFFFull) + 1u, __float_as_uint(lg)));
       }
     }
@@ -954,16 +986,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       // range and the abort flag stops the work)
       const unsigned long long* row = a.ws.tlog + (size_t)r * E;
       bool got;
+      const float* sel_bias = (a.scoring && a.router_bias) ? s_bias : nullptr;
       if (fast) {
-        got = route_row_fast(row, tag, E, k, r, a.wait_ns, &s_abort, s_idx, s_w, s_rowmask, s_used, lane);
+        got = route_row_fast(row, tag, E, k, r, a.wait_ns, &s_abort, s_idx, s_w, s_rowmask, s_used, a.scoring,
+                             sel_bias, lane);
       } else {
-        got = topk_general(row, tag, a.wait_ns, &s_abort, E, k, s_idx + r * k, s_w + r * k, lane);
+        got = topk_general(row, tag, a.wait_ns, &s_abort, E, k, s_idx + r * k, s_w + r * k, sel_bias, lane);
         __syncwarp();
         const int sel_e = got ? (lane < k ? s_idx[r * k + lane] : 0) : lane;
         const float sel_l = got ? (lane < k ? s_w[r * k + lane] : 0.f) : 0.f;
         const float top = got ? s_w[r * k] : 0.f;
         __syncwarp();
-        const float ev = (lane < k) ? expf(sel_l - top) : 0.f;
+        // softmax over the selected logits; sigmoid scoring: the selected
+        // experts' own scores (their words already carry this call's tag)
+        const float ev = (lane < k) ? (a.scoring ? (got ? __uint_as_float((unsigned)ld_tagged(row + sel_e)) : 0.f)
+                                                 : expf(sel_l - top))
+                                    : 0.f;
         float z = ev;
 #pragma unroll
         for (int d = 16; d >= 1; d >>= 1) z += __shfl_xor_sync(0xffffffffu, z, d);
@@ -1036,6 +1074,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
+      if (lane == 0 && trace && l < 24) trace[40 + l] = global_timer_ns();  // item l issued
       issue_item(ic, cur.it, smem + (size_t)st * stage_bytes, &full_bar[st], lane);
       issued = l + 1;
       if (++st == S) {
@@ -1094,6 +1133,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       const Plan p0 = make_cta_seq().p;
       L_gu = p0.n_shb + p0.rt_count;
+      if (threadIdx.x == 0 && trace) {  // (counts, not times: for reading the item stamps)
+        trace[66] = (unsigned long long)L_gu;
+        trace[67] = (unsigned long long)plan_len(p0);
+      }
     }
     const int lg_mt = __ffs(mt_per) - 1;
     auto gu_slot = [&](int l) {
@@ -1111,7 +1154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       unsigned char* stg = smem + (size_t)st * stage_bytes;
       float* rb = red + (size_t)(l & 1) * kRedFloats;
       const bool ok = warp_wait(&full_bar[st], fp & 1);
-      if (threadIdx.x == 0 && l < 4) stamp(16 + 4 * l);
+      if (threadIdx.x == 0 && l < 24) stamp(16 + l);  // item l landed
       // this warp's codes and scales to registers, then the stage goes back
       uint32_t ag[2][4], au[2][4];
       uint2 sr[4];
@@ -1152,9 +1195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<float2*>(pu + 2) = make_float2(cu[nb][2], cu[nb][3]);
         }
       }
-      if (threadIdx.x == 0 && l < 4) stamp(17 + 4 * l);
       comp_bar();
-      if (threadIdx.x == 0 && l < 4) stamp(18 + 4 * l);
       // epilogue, by the 4 warps of group l % 4 (the others move on to the
       // next item): thread o of the group owns output o (row o / 8 of the
       // item's 16, column o % 8 of each n-block) and sums its 16 k-unit
@@ -1198,7 +1239,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) red_relaxed_add(cnt + slot, 1u);
       }
-      if (threadIdx.x == 0 && l < 4) stamp(19 + 4 * l);
     }
     // down items: 8 m-tiles of 16 rows x I/128 k-units; warp w takes k-unit
     // w / 4 of m-tiles w % 4 and w % 4 + 4 (one set of h fragments for both)
@@ -1219,8 +1259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Item it = dc.it;
         unsigned char* stg = smem + (size_t)st * stage_bytes;
         float* rb = red + (size_t)(l & 1) * kRedFloats;
-        const int dj = l - L_gu;  // down item index (trace stamps 32 + 4 dj ..)
-        if (threadIdx.x == 0 && dj < 4) stamp(32 + 4 * dj);
+        const int dj = l - L_gu;  // down item index
         bool ok = !__any_sync(0xffffffffu, aborted());
         if (ok && it.slot != cur_slot) {
           // h of this slot, k-unit kq: every warp waits (bounded, no CTA
@@ -1291,9 +1330,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (threadIdx.x == 0 && dj < 4) stamp(33 + 4 * dj);
+        if (threadIdx.x == 0 && dj == 0) stamp(65);  // first down item: its h is in
         const bool landed = warp_wait(&full_bar[st], fp & 1);
-        if (threadIdx.x == 0 && dj < 4) stamp(34 + 4 * dj);
+        if (threadIdx.x == 0 && l < 24) stamp(16 + l);  // item l landed
         ok = landed && ok;
         uint32_t adA[2][4], adB[2][4];
         uint2 sr[4];
@@ -1339,7 +1378,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (NB == 2) rb[kRedPart + kq * 16 + 8 + g] = hinv1;
         }
         comp_bar();
-        if (threadIdx.x == 0 && dj < 4) stamp(35 + 4 * dj);
         // epilogue, by the 4 warps of group l % 4 (the others move on to the
         // next item): thread o of the group owns output (i, c) of m-tiles
         // M = 0..7 in each n-block; the k-unit partials of m-tile M sit at
@@ -1380,7 +1418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // faster than gating on a per-tile count first, which costs one more L2
   // round trip after the last down item:
   //   y = bf16(routed_scale * sum_s w_s d_s + d_shared + residual), slots in order
-  if (threadIdx.x == 0) stamp(60);
+  if (threadIdx.x == 0) stamp(64);
   if (!__any_sync(0xffffffffu, aborted())) {
     const int ns = k + (a.has_shared ? 1 : 0);  // partials per output
     for (int o = blockIdx.x * kCompThreads + threadIdx.x; o < K * H; o += grid * kCompThreads) {
@@ -1413,7 +1451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = 0; u < 8; ++u) {
           const int s = s0 + u;
           const float pv = __uint_as_float((unsigned)pw[u]);
-          if (s < k) acc2 = __fmaf_rn(s_w[n * k + s], pv, acc2);
+          if (s < k) acc2 = __fadd_rn(acc2, __fmul_rn(s_w[n * k + s], pv));
           else if (s == k) shv = pv;
         }
       }
@@ -1421,9 +1459,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) fail();
         break;
       }
-      float v = a.routed_scale * acc2;
-      if (a.has_shared) v += shv;
-      if (a.residual) v += rv;
+      // each operation rounded on its own (no contraction into a fused
+      // multiply-add): ((routed_scale * acc) + shared) + residual
+      float v = __fmul_rn(a.routed_scale, acc2);
+      if (a.has_shared) v = __fadd_rn(v, shv);
+      if (a.residual) v = __fadd_rn(v, rv);
       a.y[(size_t)n * H + j] = float_to_bf16_bits(v);
     }
   }
@@ -1463,7 +1503,7 @@ int num_sms() {
 // opt-in limit (at most kMaxStages stages).
 static size_t routing_smem_bytes(int K, int E, int k, int G) {
   return sizeof(float) * K * k + sizeof(int) * K * k + sizeof(unsigned) * E + sizeof(int) * (G + 1) +
-         sizeof(float) * 3 * (E + 1) + (size_t)(G + 1) * K + 16;
+         sizeof(float) * 3 * (E + 1) + sizeof(float) * E + (size_t)(G + 1) * K + 16;
 }
 
 static size_t red_slot_bytes(int NB) { return sizeof(float) * ((size_t)kCompWarps * (2 * NB * 128 + 32) + 64); }

@@ -120,6 +120,7 @@ struct RouterArgs {
   const float* bias;        // [E] or null
   int K, H, E, k, G;
   int has_shared;
+  int scoring;              // MOE_SCORE_SOFTMAX or MOE_SCORE_SIGMOID
   WsPtrs ws;
   int32_t* idx_out;         // caller copies (nullable)
   float* w_out;
@@ -138,6 +139,7 @@ struct ExpertsArgs {
   uint16_t* y;               // [K][H]
   int K, H, I, E, k, G;
   int has_shared;
+  int scoring;               // MOE_SCORE_SOFTMAX or MOE_SCORE_SIGMOID
   float routed_scale;
   const uint16_t* router_w;  // [E][H] bf16
   const float* router_bias;  // [E] or null

@@ -200,6 +200,32 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) { return __uint_as_float(b16 << 16); }
 
+// Router score of the sigmoid-scored router (MOE_SCORE_SIGMOID): the logistic
+// function as one fixed sequence of correctly rounded FP32 operations, so any
+// implementation of the same sequence selects the same experts.  exp(-l) by
+// Cody and Waite's argument reduction -- n = rint(-l log2 e), r = -l - n ln2
+// with ln 2 split into a 16-bit head (n * head exact) and a tail -- and the
+// degree-7 Taylor polynomial of e^r (|r| <= ln2/2: truncation below 1e-8),
+// scaled by 2^n (exact: the clamp keeps |n| <= 116); then 1 / (1 + e).
+__device__ __forceinline__ float sigmoid_score(float l) {
+  if (l < -80.f) l = -80.f;
+  if (l > 80.f) l = 80.f;
+  const float t = -l;
+  const float n = rintf(__fmul_rn(t, 0x1.715476p+0f));  // log2(e)
+  float r = __fmaf_rn(-n, 0x1.62e4p-1f, t);            // ln 2, head: 45426 / 2^16
+  r = __fmaf_rn(-n, 0x1.7f7d1cp-20f, r);                // ln 2, tail
+  float p = 0x1.a01a02p-13f;                            // 1/7!
+  p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);                 // 1/6!
+  p = __fmaf_rn(p, r, 0x1.111112p-7f);                  // 1/5!
+  p = __fmaf_rn(p, r, 0x1.555556p-5f);                  // 1/4!
+  p = __fmaf_rn(p, r, 0x1.555556p-3f);                  // 1/3!
+  p = __fmaf_rn(p, r, 0.5f);
+  p = __fmaf_rn(p, r, 1.0f);
+  p = __fmaf_rn(p, r, 1.0f);
+  const float e = __fmul_rn(p, __int_as_float(((int)n + 127) << 23));
+  return __fdiv_rn(1.0f, __fadd_rn(1.0f, e));
+}
+
 // Round a float to bf16 (nearest even), returning the bit pattern.
 __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
   uint16_t r;

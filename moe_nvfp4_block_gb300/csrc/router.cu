@@ -11,7 +11,8 @@
 // The last CTA to finish (atomic ticket, no spinning) selects the top-k per
 // row (larger logit first, lower index on an exact tie), renormalises the
 // selected softmax probabilities (PR #844, "4. What I ported": top-k of the
-// router scores, renormalised), and groups the (row, slot) pairs by expert so
+// router scores, renormalised) -- or, with sigmoid scoring, selects by
+// score + bias and renormalises the selected scores -- and groups the (row, slot) pairs by expert so
 // that each distinct expert is streamed once by the expert kernels (PR #844,
 // "8. What I looked at": the stock gather reads an expert once per
 // (row, slot)).
@@ -110,10 +111,14 @@ __global__ void __launch_bounds__(kRouterWarps * 32) k_router(RouterArgs a) {
         for (int d = 16; d >= 1; d >>= 1) acc[r] = __fadd_rn(acc[r], __shfl_xor_sync(0xffffffffu, acc[r], d));
       }
       if (lane == 0) {
+        // softmax scoring: logit + bias; sigmoid scoring: the score alone
+        // (the bias enters the selection keys below)
         const float b = a.bias ? a.bias[e] : 0.f;
 #pragma unroll
         for (int r = 0; r < KR; ++r)
-          if (r < K) a.ws.logits[(size_t)r * E + e] = a.bias ? __fadd_rn(acc[r], b) : acc[r];
+          if (r < K)
+            a.ws.logits[(size_t)r * E + e] =
+                a.scoring ? sigmoid_score(acc[r]) : (a.bias ? __fadd_rn(acc[r], b) : acc[r]);
       }
     }
     __threadfence();
@@ -141,7 +146,8 @@ __global__ void __launch_bounds__(kRouterWarps * 32) k_router(RouterArgs a) {
     float* l = lg + (size_t)r * E;
     unsigned char* tk = taken + (size_t)r * E;
     for (int e = lane; e < E; e += 32) {
-      l[e] = __ldcg(a.ws.logits + (size_t)r * E + e);
+      const float v = __ldcg(a.ws.logits + (size_t)r * E + e);
+      l[e] = (a.scoring && a.bias) ? __fadd_rn(v, a.bias[e]) : v;  // selection keys
       tk[e] = 0;
     }
     __syncwarp();
@@ -178,9 +184,12 @@ __global__ void __launch_bounds__(kRouterWarps * 32) k_router(RouterArgs a) {
       }
       __syncwarp();
     }
-    // renormalised softmax over the selected logits (k <= 32)
+    // renormalised softmax over the selected logits (k <= 32); sigmoid
+    // scoring: the selected experts' own scores over their sum
     const float m = selv[r * k];
-    const float ev = (lane < k) ? expf(selv[r * k + lane] - m) : 0.f;
+    float ev = 0.f;
+    if (lane < k)
+      ev = a.scoring ? __ldcg(a.ws.logits + (size_t)r * E + seli[r * k + lane]) : expf(selv[r * k + lane] - m);
     float z = ev;
 #pragma unroll
     for (int d = 16; d >= 1; d >>= 1) z += __shfl_xor_sync(0xffffffffu, z, d);

@@ -49,8 +49,10 @@ class LayerC(ctypes.Structure):
                 ("Is", ctypes.c_int), ("routed_scale", ctypes.c_double),
                 ("router_w", ctypes.c_void_p), ("router_b", ctypes.c_void_p),
                 ("gate", Proj), ("up", Proj), ("down", Proj),
-                ("sh_gate", Proj), ("sh_up", Proj), ("sh_down", Proj)]
+                ("sh_gate", Proj), ("sh_up", Proj), ("sh_down", Proj), ("scoring", ctypes.c_int)]
 
+
+SCORE_SOFTMAX, SCORE_SIGMOID = 0, 1
 
 _lib = None
 
@@ -69,6 +71,9 @@ def _bind(L):
     L.orc_router_logits_f32.argtypes = [vp, vp, ci, vp]
     L.orc_router_logits_f64.argtypes = [vp, vp, ci, vp]
     L.orc_topk.argtypes = [vp, ci, ci, ci, vp, vp]
+    L.orc_sigmoid_f32.restype = ctypes.c_float
+    L.orc_sigmoid_f32.argtypes = [ctypes.c_float]
+    L.orc_topk_sigmoid.argtypes = [vp, vp, ci, ci, ci, vp, vp]
     L.orc_group.argtypes = [vp, ci, ci, ci, vp]
     L.orc_expert.argtypes = [vp, vp, vp, ci, ci, ci, vp, vp, vp]
     L.orc_moe_layer.argtypes = [vp, vp, ci, vp, vp, vp, vp, vp, vp]
@@ -105,7 +110,7 @@ RMS_EPS = 1e-6
 class OracleLayer:
     """Keeps numpy arrays alive and exposes the C struct."""
 
-    def __init__(self, layer, H, E, top_k, I, Is, routed_scale=1.0):
+    def __init__(self, layer, H, E, top_k, I, Is, routed_scale=1.0, scoring=SCORE_SOFTMAX):
         self.keep = []
 
         def arr(a, dt):
@@ -121,12 +126,13 @@ class OracleLayer:
         rb = None if layer.router_b is None else arr(layer.router_b, np.float32)
         self.c = LayerC(H, E, top_k, I, Is, routed_scale, _p(arr(layer.router_w, np.uint16)), _p(rb),
                         proj(layer.gate), proj(layer.up), proj(layer.down),
-                        proj(layer.sh_gate), proj(layer.sh_up), proj(layer.sh_down))
+                        proj(layer.sh_gate), proj(layer.sh_up), proj(layer.sh_down), scoring)
         self.H, self.E, self.k, self.I, self.Is = H, E, top_k, I, Is
 
     @classmethod
-    def from_workload(cls, w, layer, routed_scale=None):
-        return cls(layer, w.H, w.E, w.top_k, w.I, w.Is, w.routed_scale if routed_scale is None else routed_scale)
+    def from_workload(cls, w, layer, routed_scale=None, scoring=None):
+        return cls(layer, w.H, w.E, w.top_k, w.I, w.Is, w.routed_scale if routed_scale is None else routed_scale,
+                   getattr(w, "scoring", SCORE_SOFTMAX) if scoring is None else scoring)
 
     @property
     def ref(self):
@@ -178,6 +184,23 @@ def topk(logits, k, L=None):
     idx = np.empty((K, k), np.int32)
     w = np.empty((K, k), np.float32)
     (L or lib()).orc_topk(_p(logits), K, E, k, _p(idx), _p(w))
+    return idx, w
+
+
+def sigmoid_f32(v: float, L=None) -> float:
+    """The FP32 sigmoid of the sigmoid-scored router (a fixed sequence of
+    correctly rounded FP32 operations)."""
+    return float((L or lib()).orc_sigmoid_f32(float(v)))
+
+
+def topk_sigmoid(logits, bias, k, L=None):
+    """Sigmoid scoring with a selection-only bias: (idx, w) per row."""
+    logits = _c(logits, np.float32)
+    K, E = logits.shape
+    b = None if bias is None else _c(bias, np.float32)
+    idx = np.empty((K, k), np.int32)
+    w = np.empty((K, k), np.float32)
+    (L or lib()).orc_topk_sigmoid(_p(logits), _p(b), K, E, k, _p(idx), _p(w))
     return idx, w
 
 

@@ -123,6 +123,8 @@ typedef struct {
   const float* router_b;     /* [E] or NULL */
   orc_proj gate, up, down;   /* gate/up: rows I, cols H; down: rows H, cols I */
   orc_proj sh_gate, sh_up, sh_down;  /* one expert; used when Is > 0 */
+  int scoring;               /* 0: softmax, bias added to the logits;
+                                1: sigmoid, bias added to the scores for the selection only */
 } orc_layer;
 
 /* Value of element (row r, column c) of expert e of a projection. */
@@ -239,6 +241,82 @@ void orc_topk(const float* logits, int K, int E, int k, int32_t* idx, float* w) 
 }
 
 /* ------------------------------------------------------------------ */
+/* Sigmoid scoring with a selection-only bias (the Laguna router tail)  */
+/* ------------------------------------------------------------------ */
+/*
+ * PR #844, "4. What I ported", router-tail row: the router logits are cast
+ * to FP32 and passed through a sigmoid, and a bias is added to the scores
+ * for the selection only (the top-k is taken over score + bias); the
+ * selected experts' own scores, renormalised over the selection, weight
+ * their outputs (the renormalisation is deferred into the combine, fusion
+ * row 4), and the routed sum is scaled (x2.5 in the Laguna checkpoint,
+ * "5. Numerical safety").
+ *
+ * The selection is an integer decision taken on FP32 values, so the sigmoid
+ * is defined as a fixed sequence of correctly rounded FP32 operations (the
+ * kernel evaluates the same sequence): exp by Cody and Waite's argument
+ * reduction (ln 2 split into a 16-bit head and a tail, so n * head is exact)
+ * and the degree-7 Taylor polynomial of e^r on |r| <= ln2/2 (truncation
+ * below 1e-8 relative), then 1 / (1 + e):
+ *   l <- clamp(l, -80, 80);  t = -l
+ *   n = rint(t * log2(e));   r = fma(-n, LN2_HI, t);  r = fma(-n, LN2_LO, r)
+ *   p = ((((((c7 r + c6) r + c5) r + c4) r + c3) r + c2) r + c1) r + c0,  c_i = 1/i!
+ *   e = p * 2^n   (exact: |n| <= 116 keeps 2^n and the product normal)
+ *   s = 1 / (1 + e)
+ */
+static const float SG_LOG2E = 0x1.715476p+0f;   /* log2(e) rounded to float */
+static const float SG_LN2_HI = 0x1.62e4p-1f;    /* 45426 / 2^16 */
+static const float SG_LN2_LO = 0x1.7f7d1cp-20f; /* ln 2 - SG_LN2_HI, rounded to float */
+
+float orc_sigmoid_f32(float l) {
+  static const float c[8] = {1.0f, 1.0f, 0.5f, 0x1.555556p-3f, 0x1.555556p-5f, 0x1.111112p-7f,
+                             0x1.6c16c2p-10f, 0x1.a01a02p-13f};  /* 1/i! rounded to float */
+  if (l < -80.0f) l = -80.0f;
+  if (l > 80.0f) l = 80.0f;
+  float t = -l;
+  float n = rintf(t * SG_LOG2E);
+  float r = fmaf(-n, SG_LN2_HI, t);
+  r = fmaf(-n, SG_LN2_LO, r);
+  float p = c[7];
+  for (int i = 6; i >= 0; --i) p = fmaf(p, r, c[i]);
+  float e = p * ldexpf(1.0f, (int)n);
+  return 1.0f / (1.0f + e);
+}
+
+/* For each row: scores s_e = sigmoid(l_e) (l without bias), selection keys
+ * s_e + bias_e (FP32 add; bias NULL = 0), the k largest keys in rank order
+ * (lower index on an exact tie), and weights s / sum of the selected s
+ * (double, stored as float). */
+void orc_topk_sigmoid(const float* logits, const float* bias, int K, int E, int k, int32_t* idx, float* w) {
+  int* sel = (int*)malloc(sizeof(int) * E);
+  float* sc = (float*)malloc(sizeof(float) * E);
+  float* key = (float*)malloc(sizeof(float) * E);
+  for (int r = 0; r < K; ++r) {
+    const float* l = logits + (size_t)r * E;
+    for (int e = 0; e < E; ++e) {
+      sc[e] = orc_sigmoid_f32(l[e]);
+      key[e] = bias ? sc[e] + bias[e] : sc[e];
+      sel[e] = 0;
+    }
+    double ssum = 0.0;
+    for (int s = 0; s < k; ++s) {
+      int best = -1;
+      for (int e = 0; e < E; ++e) {
+        if (sel[e]) continue;
+        if (best < 0 || ranks_before(key[e], e, key[best], best)) best = e;
+      }
+      sel[best] = 1;
+      idx[(size_t)r * k + s] = best;
+      ssum += (double)sc[best];
+    }
+    for (int s = 0; s < k; ++s) w[(size_t)r * k + s] = (float)((double)sc[idx[(size_t)r * k + s]] / ssum);
+  }
+  free(sel);
+  free(sc);
+  free(key);
+}
+
+/* ------------------------------------------------------------------ */
 /* Grouping of (row, slot) pairs by expert                             */
 /* ------------------------------------------------------------------ */
 /*
@@ -314,7 +392,8 @@ void orc_expert(const orc_proj* gp, const orc_proj* upj, const orc_proj* dp, int
 /* ------------------------------------------------------------------ */
 /*
  * For each row r: route (fixed-order FP32 logits, softmax, top-k,
- * renormalise), evaluate each selected expert, and form
+ * renormalise; or, with scoring 1, sigmoid scores, top-k of score + bias,
+ * renormalised scores), evaluate each selected expert, and form
  *   y_r = bf16( routed_scale * sum_{s=0..k-1} w_{r,s} d_{r,s}
  *               + d_shared_r + residual_r )
  * with the slot sum taken in slot order.  idx, w, group and y_f64 (the value
@@ -327,8 +406,15 @@ void orc_moe_layer(const orc_layer* L, const uint16_t* x_norm, int K, const uint
   float* logits = (float*)malloc(sizeof(float) * (size_t)K * E);
   int32_t* idx = (int32_t*)malloc(sizeof(int32_t) * (size_t)K * k);
   float* w = (float*)malloc(sizeof(float) * (size_t)K * k);
-  orc_router_logits_f32(L, x_norm, K, logits);
-  orc_topk(logits, K, E, k, idx, w);
+  if (L->scoring == 1) {  /* sigmoid scores; the bias only steers the selection */
+    orc_layer nob = *L;
+    nob.router_b = NULL;
+    orc_router_logits_f32(&nob, x_norm, K, logits);
+    orc_topk_sigmoid(logits, L->router_b, K, E, k, idx, w);
+  } else {
+    orc_router_logits_f32(L, x_norm, K, logits);
+    orc_topk(logits, K, E, k, idx, w);
+  }
   if (group_out) orc_group(idx, K, E, k, group_out);
 
   /* d[r][s][H], slot k holds the shared expert */

@@ -8,14 +8,14 @@ REL_L2 = 5e-3
 MAX_ABS_FRAC = 3e-2
 
 
-def upload(L: "synthgen.Layer", w: "synthgen.Workload", device="cuda", routed_scale=None):
+def upload(L: "synthgen.Layer", w: "synthgen.Workload", device="cuda", routed_scale=None, scoring=0):
     import moe_nvfp4_block_gb300 as M
     t = lambda p: (p.codes, p.scales, p.tscale)
     sh = None if L.sh_gate is None else (t(L.sh_gate), t(L.sh_up), t(L.sh_down))
     zero_bias = L.router_b is None or not np.any(L.router_b)
     return M.layer_from_arrays(L.router_w, None if zero_bias else L.router_b, t(L.gate), t(L.up), t(L.down), sh,
                                top_k=w.top_k, routed_scale=w.routed_scale if routed_scale is None else routed_scale,
-                               device=device)
+                               device=device, scoring=scoring)
 
 
 def bf16_bits(t):

@@ -317,6 +317,60 @@ def test_softmax_closed_form_two_experts():
     assert abs(w[0, 0] - 1 / (1 + math.exp(-1.25))) < 1e-7
 
 
+# ---------------------------------------------------------------- sigmoid scoring (Laguna router tail)
+
+def test_sigmoid_f32_against_exact_values():
+    # within a few FP32 ulps of the exact logistic function over the range
+    # routing logits take, exact at 0, clamped beyond |l| = 80
+    xs = np.concatenate([np.linspace(-30, 30, 60001), [-79.9, -50.0, 50.0, 79.9]])
+    got = np.array([oracle.sigmoid_f32(v) for v in np.float32(xs)], np.float64)
+    ex = 1.0 / (1.0 + np.exp(-np.float32(xs).astype(np.float64)))
+    ulp = np.spacing(np.float32(ex)).astype(np.float64)
+    assert np.max(np.abs(got - ex) / ulp) <= 4.0
+    assert oracle.sigmoid_f32(0.0) == 0.5
+    assert oracle.sigmoid_f32(100.0) == oracle.sigmoid_f32(80.0) == 1.0
+    assert oracle.sigmoid_f32(-100.0) == oracle.sigmoid_f32(-80.0) > 0.0
+    # monotone (non-decreasing) and symmetric to FP32 accuracy
+    assert np.all(np.diff(got[:60001]) >= 0)
+    sym = np.array([oracle.sigmoid_f32(v) + oracle.sigmoid_f32(-v) for v in np.float32(xs[::97])])
+    assert np.max(np.abs(sym - 1.0)) <= 2.0 ** -22
+
+
+def test_topk_sigmoid_selection_bias_hand_worked():
+    # logits (2, 0, -1): scores sigma = (0.8808, 0.5, 0.2689).  Selection bias
+    # (0, 0.9, 0) makes the keys (0.8808, 1.4, 0.2689): expert 1 ranks first
+    # (expert 0 without the bias or with it subtracted), yet the weights are
+    # the unbiased scores renormalised over the selection: top-2 weights
+    # 0.5 / 1.3808 and 0.8808 / 1.3808 -- expert 1, selected first, weighs
+    # less (weights from the keys would give 1.4 / 2.2808 instead).
+    logits = np.array([[2.0, 0.0, -1.0]], np.float32)
+    bias = np.array([0.0, 0.9, 0.0], np.float32)
+    s = [1 / (1 + math.exp(-2.0)), 0.5]
+    idx, w = oracle.topk_sigmoid(logits, bias, 1)
+    assert idx.tolist() == [[1]] and w.tolist() == [[1.0]]
+    idx, w = oracle.topk_sigmoid(logits, bias, 2)
+    assert idx.tolist() == [[1, 0]]
+    assert abs(w[0, 0] - s[1] / (s[0] + s[1])) < 1e-6 and abs(w[0, 1] - s[0] / (s[0] + s[1])) < 1e-6
+    idx, _ = oracle.topk_sigmoid(logits, None, 2)
+    assert idx.tolist() == [[0, 1]]
+
+
+def test_topk_sigmoid_against_library(zipf_layer):
+    w, L, ol = zipf_layer
+    x = synthgen.make_x(w, 5)
+    nob = oracle.OracleLayer(synthgen.Layer(router_w=L.router_w, router_b=None, gate=None, up=None, down=None),
+                             w.H, w.E, w.top_k, w.I, 0)
+    l32 = oracle.router_logits_f32(nob, x)
+    bias = (np.arange(w.E) % 7 - 3).astype(np.float32) * 0.05
+    idx, wt = oracle.topk_sigmoid(l32, bias, w.top_k)
+    s64 = torch.sigmoid(torch.from_numpy(l32.astype(np.float64)))
+    keys = s64 + torch.from_numpy(bias.astype(np.float64))
+    _, ref_idx = torch.topk(keys, w.top_k, dim=1)
+    assert np.array_equal(idx, ref_idx.numpy())
+    sel = torch.gather(s64, 1, ref_idx)
+    assert np.allclose(wt, (sel / sel.sum(1, keepdim=True)).numpy(), rtol=1e-6, atol=0)
+
+
 # ---------------------------------------------------------------- grouping
 
 def _group_brute(idx, E):
@@ -410,6 +464,28 @@ def test_layer_against_brute_force_dense(with_shared):
     assert np.allclose(r["y_f64"], y.numpy(), rtol=0, atol=1e-6 * float(y.abs().max()))
     yb = synthgen.bf16_to_f32(r["y"]).astype(np.float64)
     assert np.allclose(yb, y.numpy(), rtol=2.0 ** -8, atol=1e-6)
+
+
+def test_sigmoid_layer_against_brute_force_dense():
+    # the Laguna variant end to end: sigmoid scores, selection-only bias,
+    # renormalised scores, routed scale 2.5, shared expert, residual
+    w = synthgen.Workload("sg", K=4, H=256, E=16, top_k=4, I=128, Is=128, layers=1, seed=14, routed_scale=2.5)
+    L = synthgen.make_layer(w, 0)
+    L.router_b = (np.arange(w.E, dtype=np.float32) % 5 - 2) * 0.04
+    x = synthgen.make_x(w, 0)
+    res = synthgen.make_x(w, 9)
+    r = oracle.moe_layer(oracle.OracleLayer.from_workload(w, L, scoring=oracle.SCORE_SIGMOID), x, residual=res)
+    x64 = _bf(x)
+    dense = torch.stack([_dense_expert_torch(L, e, x64) for e in range(w.E)])
+    s64 = torch.sigmoid(x64 @ _bf(L.router_w).T)
+    keys = s64 + torch.from_numpy(L.router_b.astype(np.float64))
+    mask = torch.zeros(w.K, w.E)
+    for rr in range(w.K):
+        top = torch.topk(keys[rr], w.top_k).indices
+        mask[rr, top] = s64[rr, top] / s64[rr, top].sum()
+        assert r["idx"][rr].tolist() == top.tolist()
+    y = 2.5 * torch.einsum("ke,ekh->kh", mask, dense) + _dense_expert_torch(L, 0, x64, shared=True) + _bf(res)
+    assert np.allclose(r["y_f64"], y.numpy(), rtol=0, atol=1e-6 * float(y.abs().max()))
 
 
 def test_combine_linearity_routed_scale_and_residual():
