@@ -614,16 +614,77 @@ def full_step(M, torch, synthgen, dev, stream, hbm, steps):
     dist_ = pctl(per)
     acc = int(n.item())
     gbs = step_bytes / (ms * 1e-3) / 1e9
+    loop = verify_loop(M, torch, synthgen, dev, stream, model, w, steps)
     res = {"workload": "k4_full_step", "K": K, "layers": w.layers, "ctx": w.ctx, "vocab": w.vocab,
            "ms_per_step": round(ms, 4), "verified_tokens_per_s": round(K / (ms * 1e-3), 1),
            "accepted": acc, "accepted_expected": j,
            "emitted_tokens_per_s": round((acc + 1 if acc < K else K) / (ms * 1e-3), 1),
            "GBps": round(gbs, 1), "pct_of_peak": round(100 * gbs / hbm, 1),
            "step_bytes": step_bytes, "distinct_experts_mean": round(float(np.mean(n_u)), 2), "steps": steps,
-           "ms_median": round(dist_["median"], 4), "ms_p10": round(dist_["p10"], 4), "ms_p90": round(dist_["p90"], 4)}
+           "ms_median": round(dist_["median"], 4), "ms_p10": round(dist_["p10"], 4), "ms_p90": round(dist_["p90"], 4),
+           "verify_loop": loop}
     del layers, model
     torch.cuda.empty_cache()
     return res
+
+
+def verify_loop(M, torch, synthgen, dev, stream, model, w, steps, rounds=16, accept_pct=75):
+    """The multi-round verify loop on the full-step model: each layer's
+    16,384 cached positions copied into caches with room for the rounds, a
+    device-side length, and `rounds` rounds per replay (forward with in-place
+    KV append, greedy tokens, synthetic drafts accepted with probability
+    accept_pct % per row, accepted prefix, commit) -- one call, no host
+    involvement between rounds.  Committed tokens/s counts min(n + 1, K) per
+    round."""
+    out = []
+    for K in (2, 4):
+        cap = ((w.ctx + rounds * K + 15) // 16) * 16
+        layers = []
+        for d in model.layers:
+            kc = torch.zeros(d.kcache.shape[0], cap, d.kcache.shape[2], dtype=d.kcache.dtype, device=dev)
+            vc = torch.zeros_like(kc)
+            kc[:, :w.ctx].copy_(d.kcache)
+            vc[:, :w.ctx].copy_(d.vcache)
+            layers.append(M.DecoderLayer(d.Wq, d.Wk, d.Wv, d.Wo, kc, vc, d.moe))
+        kv_len = torch.tensor([w.ctx], dtype=torch.int32, device=dev)
+        kv0 = kv_len.clone()
+        lm = M.VerifyModel(layers, model.lm_head, w.n_q_heads, w.n_kv_heads, kv_len=kv_len)
+        import dataclasses
+        wk = dataclasses.replace(w, K=K)
+        xr = torch.from_numpy(np.stack([synthgen.make_x(wk, 700 + t) for t in range(rounds)])).view(torch.bfloat16).to(dev)
+        coin, alt = synthgen.make_coins(wk, rounds, accept_pct)
+        coin_d, alt_d = torch.from_numpy(coin).to(dev), torch.from_numpy(alt).to(dev)
+        xw = torch.empty(K, w.H, dtype=torch.bfloat16, device=dev)
+        tg = torch.empty(rounds, K, dtype=torch.int32, device=dev)
+        df = torch.empty_like(tg)
+        na = torch.empty(rounds, dtype=torch.int32, device=dev)
+        ws = lm.workspace(K, device=dev)
+        with torch.cuda.stream(stream):
+            kv_len.copy_(kv0)
+            M.moe_verify_rounds(lm, xr, coin_d, alt_d, xw, tg, df, na, ws, stream=stream)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            kv_len.copy_(kv0)
+            M.moe_verify_rounds(lm, xr, coin_d, alt_d, xw, tg, df, na, ws, stream=stream)
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                g.replay()
+        stream.synchronize()
+        n_rep = max(3, steps // rounds)
+        per, tot = timed_replays(torch, stream, g, n_rep)
+        assert M.moe_workspace_error(ws, stream) == 0
+        n = na.cpu().numpy()
+        committed = int(np.minimum(n + 1, K).sum())
+        ms_round = tot / n_rep / rounds
+        out.append({"K": K, "rounds": rounds, "accept_pct": accept_pct, "ms_per_round": round(ms_round, 4),
+                    "ms_per_round_median": round(float(np.median(per)) / rounds, 4),
+                    "rounds_accepting": int((n > 0).sum()), "mean_accepted": round(float(n.mean()), 3),
+                    "kv_len_final": int(kv_len.item()), "committed_tokens_per_round": round(committed / rounds, 3),
+                    "committed_tokens_per_s": round(committed / (tot / n_rep * 1e-3), 1), "replays": n_rep})
+        del layers, lm
+        torch.cuda.empty_cache()
+    return out
 
 
 # --------------------------------------------------------------------------- reference arm (CPU oracle)

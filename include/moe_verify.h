@@ -45,7 +45,8 @@ typedef enum {
   MOE_ERR_WORKSPACE_TOO_SMALL = -3,
   MOE_ERR_MISALIGNED = -4,         /* a pointer is not 16-byte aligned */
   MOE_ERR_CUDA = -5,               /* a CUDA runtime/driver call failed */
-  MOE_ERR_DEVICE_TIMEOUT = -6      /* a bounded device-side wait expired */
+  MOE_ERR_DEVICE_TIMEOUT = -6,     /* a bounded device-side wait expired */
+  MOE_ERR_CAPACITY = -7            /* a KV cache append past the cache's capacity */
 } moe_status;
 
 /*
@@ -268,23 +269,30 @@ moe_status moe_lm_head_argmax(const uint16_t* x_norm, int K, int H, const uint16
  *   xn = rmsnorm(x)  (as moe_rmsnorm)
  *   q = bf16(xn . Wq^T), k_new = bf16(xn . Wk^T), v_new = bf16(xn . Wv^T)
  *   o[r, h] = bf16( softmax_p( q[r,h] . key_p / sqrt(128) ) . value_p )
- *             over the C cached positions of KV head h / (nq/nkv) and the
+ *             over the cached positions of KV head h / (nq/nkv) and the
  *             new positions 0..r (block-causal)
  *   x_out = bf16( x + o . Wo^T )
  *   x, x_out bf16 [K][H] (x_out may alias x); Wq [nq*128][H], Wk, Wv
  *   [nkv*128][H], Wo [H][nq*128]; kcache, vcache [nkv][C][128];
+ *   kv_len: NULL -- all C cached positions are valid and the caches are
+ *     only read; or a device int32: *kv_len of the C positions are valid
+ *     and the K new keys and values are written into the caches in place at
+ *     positions *kv_len .. *kv_len + K - 1 (the caches then hold C positions
+ *     of capacity; an append past C is refused and recorded as
+ *     MOE_ERR_CAPACITY in the workspace error word).  The length itself is
+ *     not changed here: moe_kv_commit counts the accepted rows in.
  *   k_new_out, v_new_out: optional [K][nkv*128] copies of the new keys and
- *   values (to append to the cache once rows are accepted); o_out: optional
- *   [K][nq*128] copy of the attention output o (before the o-projection).
+ *   values; o_out: optional [K][nq*128] copy of the attention output o
+ *   (before the o-projection).
  * Envelope: head_dim 128, nq even, nq % nkv == 0, K * nq/nkv <= 16, H a
  * multiple of 256 up to 4096, nq*128 <= 4096, C a multiple of 16.
  */
 size_t moe_attention_workspace_size(int K, int H, int nq, int nkv, int head_dim);
 moe_status moe_attention_block(const uint16_t* x, int K, int H, int nq, int nkv, int head_dim, int C,
                                const uint16_t* Wq, const uint16_t* Wk, const uint16_t* Wv, const uint16_t* Wo,
-                               const uint16_t* kcache, const uint16_t* vcache, float eps, uint16_t* x_out,
-                               uint16_t* k_new_out, uint16_t* v_new_out, uint16_t* o_out, void* ws,
-                               size_t ws_bytes, void* stream);
+                               uint16_t* kcache, uint16_t* vcache, const int32_t* kv_len, float eps,
+                               uint16_t* x_out, uint16_t* k_new_out, uint16_t* v_new_out, uint16_t* o_out,
+                               void* ws, size_t ws_bytes, void* stream);
 
 /*
  * The full verify step of a decoder with GQA attention and MoE blocks:
@@ -298,7 +306,7 @@ moe_status moe_attention_block(const uint16_t* x, int K, int H, int nq, int nkv,
  */
 typedef struct {
   const uint16_t *Wq, *Wk, *Wv, *Wo;  /* bf16 attention projections (see moe_attention_block) */
-  const uint16_t *kcache, *vcache;    /* bf16 [nkv][ctx][128] */
+  uint16_t *kcache, *vcache;          /* bf16 [nkv][ctx][128] */
   moe_layer moe;                      /* the MoE block of the layer */
 } moe_decoder_layer;
 
@@ -307,6 +315,11 @@ typedef struct {
   float eps;                          /* RMSNorm epsilon */
   const moe_decoder_layer* layers;    /* host array of n_layers (read during the call) */
   const uint16_t* lm_head;            /* bf16 [vocab][hidden] */
+  const int32_t* kv_len;              /* NULL: every layer attends over all ctx cached positions,
+                                         caches read only; else a device int32 shared by the
+                                         layers: ctx is the caches' capacity, *kv_len positions
+                                         are valid, and each step appends its K rows' keys and
+                                         values in place (see moe_attention_block) */
 } moe_verify_model;
 
 size_t moe_verify_step_workspace_size(const moe_verify_model* model, int K);
@@ -317,6 +330,50 @@ size_t moe_verify_step_workspace_size(const moe_verify_model* model, int K);
  *   ws         moe_verify_step_workspace_size bytes, zero-filled before first use */
 moe_status moe_verify_step(const moe_verify_model* model, uint16_t* x, int K, const int32_t* draft,
                            int32_t* target, int32_t* n_accepted, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * The multi-round verify loop with an in-place KV cache (PR #844, "8. What I
+ * looked at and did NOT ship", items 1 and 2, and "10. Next step": keep the
+ * verify rows' keys and values in a temporally ordered arena and drop the
+ * rejected rows by trimming, with no snapshot and no replay forward).
+ *
+ * moe_kv_commit: after a step of K rows with n accepted drafts, rows
+ * 0 .. min(n + 1, K) - 1 hold committed tokens (row 0 the last committed
+ * token, row i + 1 the draft the target confirmed at row i), so
+ *   *kv_len += min(*n_accepted + 1, K)   (clamped to `capacity`)
+ * Their keys and values were already appended in place by the step; the
+ * other rows' entries lie past the new length and are overwritten by the
+ * next step.  One device thread; nothing is copied.
+ */
+moe_status moe_kv_commit(int32_t* kv_len, const int32_t* n_accepted, int K, int capacity, void* stream);
+
+/*
+ * A drafter with a controlled acceptance rate, for benchmarks and tests: no
+ * draft model, the drafts are made from the target's own greedy tokens:
+ *   draft_r = target_r                          if coin[r] != 0
+ *           = (target_r + 1 + alt[r]) mod vocab otherwise (never target_r)
+ *   target, alt int32 [K] (0 <= alt[r] < vocab - 1); coin uint8 [K]; draft int32 [K] out.
+ * (The verify rows are synthetic activations, so the drafts do not feed the
+ * forward; they only decide how far each round advances.)
+ */
+moe_status moe_synthetic_drafts(const int32_t* target, const uint8_t* coin, const int32_t* alt, int K, int vocab,
+                                int32_t* draft, void* stream);
+
+/*
+ * R verify rounds on the device, one after the other, with no host
+ * involvement between them: for round t
+ *   x_work <- x_rounds[t];  forward (every layer appends its K rows' keys and
+ *   values in place at *kv_len ..);  targets[t] = greedy tokens;
+ *   drafts[t] = moe_synthetic_drafts(targets[t], coin[t], alt[t]);
+ *   n_accepted[t] = accepted prefix;  moe_kv_commit.
+ *   model->kv_len must be set; x_rounds bf16 [R][K][hidden]; coin uint8
+ *   [R][K]; alt int32 [R][K]; x_work bf16 [K][hidden]; targets, drafts int32
+ *   [R][K] out; n_accepted int32 [R] out; ws as moe_verify_step.
+ * A round whose append would pass the capacity records MOE_ERR_CAPACITY.
+ */
+moe_status moe_verify_rounds(const moe_verify_model* model, const uint16_t* x_rounds, int R, int K, const uint8_t* coin,
+                             const int32_t* alt, uint16_t* x_work, int32_t* targets, int32_t* drafts,
+                             int32_t* n_accepted, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Reads the device error word of a workspace (0 = none, else a negative

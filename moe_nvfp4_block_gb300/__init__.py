@@ -25,6 +25,7 @@ MOE_ERR_WORKSPACE_TOO_SMALL = -3
 MOE_ERR_MISALIGNED = -4
 MOE_ERR_CUDA = -5
 MOE_ERR_DEVICE_TIMEOUT = -6
+MOE_ERR_CAPACITY = -7
 MOE_MAX_ROWS = 16
 
 # Every symbol the header declares (checked by the tests).
@@ -33,7 +34,8 @@ EXPORTS = ("moe_verify_layer_workspace_size", "moe_router_topk", "moe_group_ints
            "moe_lm_head_argmax", "moe_verify_stack_workspace_size", "moe_verify_stack",
            "moe_attention_workspace_size", "moe_attention_block", "moe_verify_layer_static",
            "moe_verify_step_workspace_size", "moe_verify_step", "moe_workspace_error", "moe_status_string",
-           "moe_debug_set_wait_limit_ns", "moe_debug_set_trace", "moe_debug_partials_offset")
+           "moe_debug_set_wait_limit_ns", "moe_debug_set_trace", "moe_debug_partials_offset", "moe_kv_commit",
+           "moe_synthetic_drafts", "moe_verify_rounds")
 
 
 class MoeError(RuntimeError):
@@ -67,7 +69,7 @@ class moe_verify_model(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int), ("hidden", ctypes.c_int), ("n_q_heads", ctypes.c_int),
                 ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("ctx", ctypes.c_int),
                 ("vocab", ctypes.c_int), ("eps", ctypes.c_float), ("layers", ctypes.c_void_p),
-                ("lm_head", ctypes.c_void_p)]
+                ("lm_head", ctypes.c_void_p), ("kv_len", ctypes.c_void_p)]
 
 
 def _load():
@@ -98,13 +100,19 @@ def _load():
     L.moe_attention_workspace_size.restype = sz
     L.moe_attention_workspace_size.argtypes = [ci, ci, ci, ci, ci]
     L.moe_attention_block.restype = ci
-    L.moe_attention_block.argtypes = [vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp, vp,
-                                      vp, vp, vp, sz, vp]
+    L.moe_attention_block.argtypes = [vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp,
+                                      vp, vp, vp, vp, sz, vp]
     mp = ctypes.POINTER(moe_verify_model)
     L.moe_verify_step_workspace_size.restype = sz
     L.moe_verify_step_workspace_size.argtypes = [mp, ci]
     L.moe_verify_step.restype = ci
     L.moe_verify_step.argtypes = [mp, vp, ci, vp, vp, vp, vp, sz, vp]
+    L.moe_kv_commit.restype = ci
+    L.moe_kv_commit.argtypes = [vp, vp, ci, ci, vp]
+    L.moe_synthetic_drafts.restype = ci
+    L.moe_synthetic_drafts.argtypes = [vp, vp, vp, ci, ci, vp, vp]
+    L.moe_verify_rounds.restype = ci
+    L.moe_verify_rounds.argtypes = [mp, vp, ci, ci, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.moe_rmsnorm.restype = ci
     L.moe_rmsnorm.argtypes = [vp, ci, ci, ctypes.c_float, vp, vp]
     L.moe_lm_head_workspace_size.restype = sz
@@ -277,11 +285,11 @@ def attention_workspace(K, H, nq, nkv, head_dim=128, device="cuda") -> torch.Ten
 
 
 def moe_attention_block(x, Wq, Wk, Wv, Wo, kcache, vcache, x_out, ws, nq, nkv, eps=1e-6, k_new=None, v_new=None,
-                        stream=None, o_out=None):
+                        stream=None, o_out=None, kv_len=None):
     K, H = x.shape
     C = kcache.shape[1]
     _check(lib.moe_attention_block(_ptr(x), K, H, nq, nkv, 128, C, _ptr(Wq), _ptr(Wk), _ptr(Wv), _ptr(Wo),
-                                   _ptr(kcache) if C else None, _ptr(vcache) if C else None, float(eps),
+                                   _ptr(kcache) if C else None, _ptr(vcache) if C else None, _ptr(kv_len), float(eps),
                                    _ptr(x_out), _ptr(k_new), _ptr(v_new), _ptr(o_out), _ptr(ws), ws.numel(),
                                    _stream(stream)),
            "moe_attention_block")
@@ -303,9 +311,13 @@ class VerifyModel:
     """Holds the C description (``moe_verify_model``) of a stack of decoder
     layers plus the lm_head; keeps the ctypes arrays alive."""
 
-    def __init__(self, layers, lm_head, n_q_heads, n_kv_heads, eps=1e-6):
+    def __init__(self, layers, lm_head, n_q_heads, n_kv_heads, eps=1e-6, kv_len=None):
+        """``kv_len``: None (caches read only, all positions valid) or a device
+        int32 tensor [1] -- the caches' second dimension is then their
+        capacity and every step appends its rows in place."""
         self.layers = layers
         self.lm_head = lm_head
+        self.kv_len = kv_len
         p = lambda t: t.data_ptr()
         self.c_layers = (moe_decoder_layer * len(layers))(*[
             moe_decoder_layer(p(d.Wq), p(d.Wk), p(d.Wv), p(d.Wo), p(d.kcache), p(d.vcache), d.moe.c())
@@ -313,7 +325,7 @@ class VerifyModel:
         d0 = layers[0]
         self.c = moe_verify_model(len(layers), d0.moe.hidden, n_q_heads, n_kv_heads, 128, d0.kcache.shape[1],
                                   lm_head.shape[0], eps, ctypes.cast(self.c_layers, ctypes.c_void_p),
-                                  lm_head.data_ptr())
+                                  lm_head.data_ptr(), None if kv_len is None else kv_len.data_ptr())
 
     def workspace(self, K, device=None):
         n = int(lib.moe_verify_step_workspace_size(ctypes.byref(self.c), K))
@@ -325,6 +337,24 @@ class VerifyModel:
 def moe_verify_step(model: VerifyModel, x, draft, target, n_accepted, ws, stream=None):
     _check(lib.moe_verify_step(ctypes.byref(model.c), _ptr(x), x.shape[0], _ptr(draft), _ptr(target),
                                _ptr(n_accepted), _ptr(ws), ws.numel(), _stream(stream)), "moe_verify_step")
+
+
+def moe_kv_commit(kv_len, n_accepted, K, capacity, stream=None):
+    _check(lib.moe_kv_commit(_ptr(kv_len), _ptr(n_accepted), K, capacity, _stream(stream)), "moe_kv_commit")
+
+
+def moe_synthetic_drafts(target, coin, alt, vocab, draft, stream=None):
+    _check(lib.moe_synthetic_drafts(_ptr(target), _ptr(coin), _ptr(alt), target.shape[0], vocab, _ptr(draft),
+                                    _stream(stream)), "moe_synthetic_drafts")
+
+
+def moe_verify_rounds(model: "VerifyModel", x_rounds, coin, alt, x_work, targets, drafts, n_accepted, ws, stream=None):
+    """x_rounds bf16 [R, K, H]; coin uint8 [R, K]; alt int32 [R, K]; outputs
+    targets, drafts int32 [R, K] and n_accepted int32 [R]."""
+    R, K = x_rounds.shape[0], x_rounds.shape[1]
+    _check(lib.moe_verify_rounds(ctypes.byref(model.c), _ptr(x_rounds), R, K, _ptr(coin), _ptr(alt), _ptr(x_work),
+                                 _ptr(targets), _ptr(drafts), _ptr(n_accepted), _ptr(ws), ws.numel(),
+                                 _stream(stream)), "moe_verify_rounds")
 
 
 def moe_rmsnorm(x, out, eps=1e-6, stream=None):

@@ -27,4 +27,45 @@ cudaError_t launch_accept(const int32_t* draft, const int32_t* target, int K, in
   return cudaGetLastError();
 }
 
+// After a verify round with n accepted drafts the rows 0 .. min(n + 1, K) - 1
+// hold valid tokens (row 0 is the last committed token, row i + 1 the draft
+// the target confirmed at row i): their keys and values, already written in
+// place at positions len .. len + K - 1, become part of the cache, and the
+// rest are dropped simply by not counting them -- no replay forward, no copy
+// (PR #844, "8. What I looked at", items 1 and 2; "10. Next step").
+__global__ void k_kv_commit(int32_t* len, const int32_t* n_accepted, int K, int cap, int* err) {
+  const int n = *n_accepted;
+  const int c = n + 1 < K ? n + 1 : K;
+  const int nl = *len + c;
+  if (nl > cap) {
+    if (err) atomicCAS(err, 0, (int)MOE_ERR_CAPACITY);
+    *len = cap;
+  } else {
+    *len = nl;
+  }
+}
+
+cudaError_t launch_kv_commit(int32_t* len, const int32_t* n_accepted, int K, int cap, int* err, cudaStream_t s) {
+  k_kv_commit<<<1, 1, 0, s>>>(len, n_accepted, K, cap, err);
+  return cudaGetLastError();
+}
+
+// A drafter with a controlled acceptance rate, for benchmarks and tests (no
+// draft model is involved): row r's draft is the target's own token where
+// coin[r] != 0, else a different token, (target_r + 1 + alt_r) mod vocab with
+// 0 <= alt_r < vocab - 1.  The coins are the caller's seeded draws.
+__global__ void k_synthetic_drafts(const int32_t* target, const uint8_t* coin, const int32_t* alt, int K, int vocab,
+                                   int32_t* draft) {
+  for (int r = threadIdx.x; r < K; r += blockDim.x) {
+    const long long t = target[r];
+    draft[r] = coin[r] ? (int32_t)t : (int32_t)((t + 1 + (long long)alt[r]) % vocab);
+  }
+}
+
+cudaError_t launch_synthetic_drafts(const int32_t* target, const uint8_t* coin, const int32_t* alt, int K, int vocab,
+                                    int32_t* draft, cudaStream_t s) {
+  k_synthetic_drafts<<<1, 32, 0, s>>>(target, coin, alt, K, vocab, draft);
+  return cudaGetLastError();
+}
+
 }  // namespace moe

@@ -123,7 +123,13 @@ __global__ void __launch_bounds__(256) k_gemv_bf16(GemvArgs a) {
       if (r < K && lane == r) {
         float v = acc[r];
         if (S.res) v += resv;
-        S.out[(size_t)r * S.N + nl] = float_to_bf16_bits(v);
+        const uint16_t b = float_to_bf16_bits(v);
+        S.out[(size_t)r * S.N + nl] = b;
+        if (S.cache) {  // in-place KV append at position *len + r
+          const int p = *S.len + r;
+          if (p < S.cap) S.cache[((size_t)(nl >> 7) * S.cap + p) * 128 + (nl & 127)] = b;
+          else if (a.err) atomicCAS(a.err, 0, (int)MOE_ERR_CAPACITY);
+        }
       }
     }
   }
@@ -207,7 +213,11 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn_split(AttnArgs a) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) o[nb][c] = 0.f;
 
-  const int n16 = a.C / 16;
+  // Cv valid positions of a cache of a.C (the head stride); a partial last
+  // 16-position sub-chunk is masked (its keys and values read as zero, its
+  // scores as -inf)
+  const int Cv = a.len ? min(*a.len, a.C) : a.C;
+  const int n16 = (Cv + 15) / 16;
   const int c0 = (int)(((long long)split * n16) / gridDim.x);
   const int c1 = (int)(((long long)(split + 1) * n16) / gridDim.x);
   const uint16_t* kbase = a.kc + (size_t)kvh * a.C * HD;
@@ -217,15 +227,20 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn_split(AttnArgs a) {
   for (int sc = c0 + warp; sc < c1; sc += kAttnWarps) {
     const uint16_t* kb = kbase + (size_t)sc * 16 * HD;
     const uint16_t* vb = vbase + (size_t)sc * 16 * HD;
+    const int rem = Cv - sc * 16;  // valid positions of this sub-chunk (16 unless it is the last)
     uint4 kr[2][4], vr[4][2];
 #pragma unroll
     for (int nb = 0; nb < 2; ++nb)
 #pragma unroll
-      for (int u = 0; u < 4; ++u) kr[nb][u] = ldg_nc_v4(kb + (size_t)(pk0 + 2 * nb) * HD + 32 * t + 8 * u);
+      for (int u = 0; u < 4; ++u)
+        kr[nb][u] = pk0 + 2 * nb < rem ? ldg_nc_v4(kb + (size_t)(pk0 + 2 * nb) * HD + 32 * t + 8 * u)
+                                       : make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int p = 0; p < 4; ++p)
 #pragma unroll
-      for (int u = 0; u < 2; ++u) vr[p][u] = ldg_nc_v4(vb + (size_t)(4 * t + p) * HD + 16 * g + 8 * u);
+      for (int u = 0; u < 2; ++u)
+        vr[p][u] = 4 * t + p < rem ? ldg_nc_v4(vb + (size_t)(4 * t + p) * HD + 16 * g + 8 * u)
+                                   : make_uint4(0, 0, 0, 0);
 
     float s[2][4];
 #pragma unroll
@@ -238,6 +253,13 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn_split(AttnArgs a) {
         const int w0 = (ks & 1) * 2;
         mma_bf16(s[nb], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], w[w0], w[w0 + 1]);
       }
+    }
+    if (rem < 16) {  // score (row, logical column 8 nb + 2t + b) sits at physical position 4t + 2nb + b
+#pragma unroll
+      for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          if (4 * t + 2 * nb + (c & 1) >= rem) s[nb][c] = -INFINITY;
     }
     // online softmax (log2 domain); row 0 = query g, row 1 = query g+8
     float mx[2];

@@ -182,35 +182,25 @@ moe_status moe_router_topk(const moe_layer* layer, const uint16_t* x_norm, int K
   return MOE_OK;
 }
 
-__attribute__((visibility("hidden"))) moe_status run_layer(const moe_layer* layer, const uint16_t* x_norm, int K, const uint16_t* residual,
-                            uint16_t* y, int32_t* idx_out, float* w_out, int32_t* group_out, void* ws,
-                            size_t ws_bytes, void* stream, bool pdl, void* const* events, float norm_eps) {
-  moe_status s = check_layer(layer, K);
-  if (s != MOE_OK) return s;
-  if (!x_norm || !y || !ws) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x_norm) || !aligned16(y) || !aligned16(ws) || !aligned16(residual)) return MOE_ERR_MISALIGNED;
-  const WsLayout lay = layout_of(layer, K);
-  if (ws_bytes < lay.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  const WsPtrs wp = ws_ptrs(ws, lay);
+// The ten tensor maps of a layer (codes: gate, up, down, shared gate, shared
+// up, shared down; scales: gate, up, shared gate, shared up) and whether the
+// code maps are 3-D.  False if the driver refuses one.
+static bool encode_layer_maps(const moe_layer* layer, CUtensorMap* maps, bool* code3d) {
   const int H = layer->hidden, E = layer->n_experts, I = layer->inter;
-  const bool has_sh = layer->shared_inter > 0;
-
-  // codes: gate, up, down, sh_gate, sh_up, sh_down; scales: gate, up, sh_gate, sh_up
-  CUtensorMap maps[10];
   bool d3[6] = {false, false, false, false, false, false};
   if (!encode_codes(&maps[0], layer->gate.codes, E, I, H, kGURows, &d3[0]) ||
       !encode_codes(&maps[1], layer->up.codes, E, I, H, kGURows, &d3[1]) ||
       !encode_codes(&maps[2], layer->down.codes, E, H, I, kDNRows, &d3[2]) ||
       !encode_scales(&maps[6], layer->gate.scales, E, I, H, kGURows) ||
       !encode_scales(&maps[7], layer->up.scales, E, I, H, kGURows))
-    return MOE_ERR_CUDA;
-  if (has_sh) {
+    return false;
+  if (layer->shared_inter > 0) {
     if (!encode_codes(&maps[3], layer->sh_gate.codes, 1, I, H, kGURows, &d3[3]) ||
         !encode_codes(&maps[4], layer->sh_up.codes, 1, I, H, kGURows, &d3[4]) ||
         !encode_codes(&maps[5], layer->sh_down.codes, 1, H, I, kDNRows, &d3[5]) ||
         !encode_scales(&maps[8], layer->sh_gate.scales, 1, I, H, kGURows) ||
         !encode_scales(&maps[9], layer->sh_up.scales, 1, I, H, kGURows))
-      return MOE_ERR_CUDA;
+      return false;
   } else {
     maps[3] = maps[0];
     maps[4] = maps[1];
@@ -221,10 +211,67 @@ __attribute__((visibility("hidden"))) moe_status run_layer(const moe_layer* laye
     d3[4] = d3[1];
     d3[5] = d3[2];
   }
-  const bool code3d = d3[0] && d3[1] && d3[2] && d3[3] && d3[4] && d3[5];
-  if (!code3d && (d3[0] || d3[1] || d3[2] || d3[3] || d3[4] || d3[5])) return MOE_ERR_CUDA;  // mixed forms
+  *code3d = d3[0] && d3[1] && d3[2] && d3[3] && d3[4] && d3[5];
+  return *code3d || !(d3[0] || d3[1] || d3[2] || d3[3] || d3[4] || d3[5]);  // no mixed forms
+}
+
+static LayerDesc layer_desc(const moe_layer* layer) {
+  LayerDesc d;
+  const bool has_sh = layer->shared_inter > 0;
+  d.router_w = layer->router_w;
+  d.router_bias = layer->router_bias;
+  d.gate = {layer->gate.scales, layer->gate.tensor_scale};
+  d.up = {layer->up.scales, layer->up.tensor_scale};
+  d.down = {layer->down.scales, layer->down.tensor_scale};
+  d.sh_gate = has_sh ? ProjPtrs{layer->sh_gate.scales, layer->sh_gate.tensor_scale} : d.gate;
+  d.sh_up = has_sh ? ProjPtrs{layer->sh_up.scales, layer->sh_up.tensor_scale} : d.up;
+  d.sh_down = has_sh ? ProjPtrs{layer->sh_down.scales, layer->sh_down.tensor_scale} : d.down;
+  d.routed_scale = layer->routed_scale;
+  d.has_shared = has_sh ? 1 : 0;
+  d.scoring = layer->scoring;
+  return d;
+}
+
+// One launch of the experts kernel for one layer call.
+static moe_status launch_layer(const moe_layer* layer, const uint16_t* x, int K, const uint16_t* residual,
+                               uint16_t* y, int32_t* idx_out, float* w_out, int32_t* group_out, const WsPtrs& wp,
+                               cudaStream_t st, bool pdl, float norm_eps) {
+  CUtensorMap maps[kMapsPerLayer];
+  bool d3 = false;
+  if (!encode_layer_maps(layer, maps, &d3)) return MOE_ERR_CUDA;
+  ExpertsCommon c{};
+  c.x = x;
+  c.residual = residual;
+  c.y = y;
+  c.K = K;
+  c.H = layer->hidden;
+  c.I = layer->inter;
+  c.E = layer->n_experts;
+  c.k = layer->top_k;
+  c.G = group_cap(K, layer->n_experts, layer->top_k);
+  c.ws = wp;
+  c.idx_out = idx_out;
+  c.w_out = w_out;
+  c.group_out = group_out;
+  c.wait_ns = g_wait_ns.load();
+  c.trace = g_trace;
+  c.code3d = d3 ? 1 : 0;
+  c.norm = norm_eps >= 0.f ? 1 : 0;
+  c.norm_eps = norm_eps >= 0.f ? norm_eps : 0.f;
+  return launch_experts(c, maps, layer_desc(layer), st, pdl) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+__attribute__((visibility("hidden"))) moe_status run_layer(const moe_layer* layer, const uint16_t* x_norm, int K, const uint16_t* residual,
+                            uint16_t* y, int32_t* idx_out, float* w_out, int32_t* group_out, void* ws,
+                            size_t ws_bytes, void* stream, bool pdl, void* const* events, float norm_eps) {
+  moe_status s = check_layer(layer, K);
+  if (s != MOE_OK) return s;
+  if (!x_norm || !y || !ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x_norm) || !aligned16(y) || !aligned16(ws) || !aligned16(residual)) return MOE_ERR_MISALIGNED;
+  const WsLayout lay = layout_of(layer, K);
+  if (ws_bytes < lay.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const WsPtrs wp = ws_ptrs(ws, lay);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const uint64_t wait_ns = g_wait_ns.load();
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   if (events && cudaStreamIsCapturing(st, &cap) != cudaSuccess) return MOE_ERR_CUDA;
   // inside a graph capture the events become external record nodes, so that
@@ -233,42 +280,12 @@ __attribute__((visibility("hidden"))) moe_status run_layer(const moe_layer* laye
   auto mark = [&](int i) {
     return !events || cudaEventRecordWithFlags(static_cast<cudaEvent_t>(events[i]), st, ev_flags) == cudaSuccess;
   };
-
   // one launch: the experts kernel computes the router logits itself
   // (events 0 and 1 bracket no work)
   if (!mark(0) || !mark(1)) return MOE_ERR_CUDA;
-
-  ExpertsArgs ea;
-  ea.x = x_norm;
-  ea.residual = residual;
-  ea.y = y;
-  ea.K = K;
-  ea.H = H;
-  ea.I = I;
-  ea.E = E;
-  ea.k = layer->top_k;
-  ea.G = group_cap(K, E, layer->top_k);
-  ea.has_shared = has_sh;
-  ea.scoring = layer->scoring;
-  ea.routed_scale = layer->routed_scale;
-  ea.router_w = layer->router_w;
-  ea.router_bias = layer->router_bias;
-  ea.gate = {layer->gate.scales, layer->gate.tensor_scale};
-  ea.up = {layer->up.scales, layer->up.tensor_scale};
-  ea.down = {layer->down.scales, layer->down.tensor_scale};
-  ea.sh_gate = has_sh ? ProjPtrs{layer->sh_gate.scales, layer->sh_gate.tensor_scale} : ea.gate;
-  ea.sh_up = has_sh ? ProjPtrs{layer->sh_up.scales, layer->sh_up.tensor_scale} : ea.up;
-  ea.sh_down = has_sh ? ProjPtrs{layer->sh_down.scales, layer->sh_down.tensor_scale} : ea.down;
-  ea.ws = wp;
-  ea.idx_out = idx_out;
-  ea.w_out = w_out;
-  ea.group_out = group_out;
-  ea.wait_ns = wait_ns;
-  ea.trace = g_trace;
-  ea.code3d = code3d ? 1 : 0;
-  ea.norm = norm_eps >= 0.f ? 1 : 0;
-  ea.norm_eps = norm_eps >= 0.f ? norm_eps : 0.f;
-  if (launch_experts(ea, maps, st, pdl) != cudaSuccess || !mark(2) || !mark(3)) return MOE_ERR_CUDA;
+  s = launch_layer(layer, x_norm, K, residual, y, idx_out, w_out, group_out, wp, st, pdl, norm_eps);
+  if (s != MOE_OK) return s;
+  if (!mark(2) || !mark(3)) return MOE_ERR_CUDA;
   return MOE_OK;
 }
 
@@ -300,7 +317,7 @@ size_t moe_verify_stack_workspace_size(const moe_layer* layers, int n_layers, in
     const size_t b = layout_of(&layers[l], K).total;
     m = b > m ? b : m;
   }
-  return m + align256(sizeof(uint16_t) * K * layers[0].hidden);
+  return m;
 }
 
 moe_status moe_verify_stack(const moe_layer* layers, int n_layers, uint16_t* x, int K, float eps, void* ws,
@@ -316,7 +333,9 @@ moe_status moe_verify_stack(const moe_layer* layers, int n_layers, uint16_t* x, 
   }
   if (ws_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
   if (!aligned16(x) || !aligned16(ws)) return MOE_ERR_MISALIGNED;
-  for (int l = 0; l < n_layers; ++l) {  // each layer kernel applies its RMSNorm to x itself
+  // one launch per layer, chained by programmatic dependent launch; each
+  // layer kernel applies its RMSNorm to the residual stream x itself
+  for (int l = 0; l < n_layers; ++l) {
     moe_status s = run_layer(&layers[l], x, K, x, x, nullptr, nullptr, nullptr, ws, ws_bytes, stream, true, nullptr, eps);
     if (s != MOE_OK) return s;
   }
@@ -358,7 +377,7 @@ moe_status moe_lm_head_argmax(const uint16_t* x_norm, int K, int H, const uint16
 }
 
 struct AttnLayout {
-  size_t xn, q, kn, vn, o, part_o, part_ml, total;
+  size_t hdr, xn, q, kn, vn, o, part_o, part_ml, total;
 };
 
 static AttnLayout attn_layout(int K, int H, int nq, int nkv) {
@@ -369,6 +388,7 @@ static AttnLayout attn_layout(int K, int H, int nq, int nkv) {
     off = align256(off + b);
     return r;
   };
+  L.hdr = take(256);  // int32 error word first, as in every workspace
   L.xn = take(sizeof(uint16_t) * K * H);
   L.q = take(sizeof(uint16_t) * K * nq * 128);
   L.kn = take(sizeof(uint16_t) * K * nkv * 128);
@@ -392,43 +412,37 @@ size_t moe_attention_workspace_size(int K, int H, int nq, int nkv, int head_dim)
   return attn_layout(K, H, nq, nkv).total;
 }
 
-moe_status moe_attention_block(const uint16_t* x, int K, int H, int nq, int nkv, int head_dim, int C,
-                               const uint16_t* Wq, const uint16_t* Wk, const uint16_t* Wv, const uint16_t* Wo,
-                               const uint16_t* kcache, const uint16_t* vcache, float eps, uint16_t* x_out,
-                               uint16_t* k_new_out, uint16_t* v_new_out, uint16_t* o_out, void* ws,
-                               size_t ws_bytes, void* stream) {
-  moe_status st = check_attn(K, H, nq, nkv, head_dim, C);
-  if (st != MOE_OK) return st;
-  if (!x || !Wq || !Wk || !Wv || !Wo || !x_out || !ws || (C > 0 && (!kcache || !vcache)) || !(eps >= 0.f))
-    return MOE_ERR_INVALID_ARG;
-  const void* ptrs[] = {x, Wq, Wk, Wv, Wo, kcache, vcache, x_out, k_new_out, v_new_out, o_out, ws};
-  for (const void* p : ptrs)
-    if (!aligned16(p)) return MOE_ERR_MISALIGNED;
-  const AttnLayout L = attn_layout(K, H, nq, nkv);
-  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  char* b = static_cast<char*>(ws);
+// The attention block's launches; `err` receives a failed in-place append
+// (the caller's workspace error word).
+static moe_status attention_impl(const uint16_t* x, int K, int H, int nq, int nkv, int C, const uint16_t* Wq,
+                                 const uint16_t* Wk, const uint16_t* Wv, const uint16_t* Wo, uint16_t* kcache,
+                                 uint16_t* vcache, const int32_t* kv_len, float eps, uint16_t* x_out,
+                                 uint16_t* k_new_out, uint16_t* v_new_out, uint16_t* o_out, char* b,
+                                 const AttnLayout& L, int* err, cudaStream_t s) {
   uint16_t* xn = reinterpret_cast<uint16_t*>(b + L.xn);
   uint16_t* q = reinterpret_cast<uint16_t*>(b + L.q);
   uint16_t* kn = k_new_out ? k_new_out : reinterpret_cast<uint16_t*>(b + L.kn);
   uint16_t* vn = v_new_out ? v_new_out : reinterpret_cast<uint16_t*>(b + L.vn);
   uint16_t* o = o_out ? o_out : reinterpret_cast<uint16_t*>(b + L.o);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-
   if (launch_rmsnorm(x, K, H, eps, xn, s, false) != cudaSuccess) return MOE_ERR_CUDA;
   GemvArgs g{};
   g.x = xn;
   g.K = K;
   g.D = H;
-  g.seg[0] = {Wq, q, nullptr, nq * 128};
-  g.seg[1] = {Wk, kn, nullptr, nkv * 128};
-  g.seg[2] = {Wv, vn, nullptr, nkv * 128};
+  g.seg[0] = {Wq, q, nullptr, nq * 128, nullptr, nullptr, 0};
+  // with a device length, the new keys and values also go into the caches
+  // in place, at positions *kv_len .. *kv_len + K - 1
+  g.seg[1] = {Wk, kn, nullptr, nkv * 128, kv_len ? kcache : nullptr, kv_len, C};
+  g.seg[2] = {Wv, vn, nullptr, nkv * 128, kv_len ? vcache : nullptr, kv_len, C};
   g.nseg = 3;
   g.n_total = (nq + 2 * nkv) * 128;
+  g.err = err;
   if (launch_gemv(g, s, true) != cudaSuccess) return MOE_ERR_CUDA;
   AttnArgs a{};
   a.q = q;
   a.kc = kcache;
   a.vc = vcache;
+  a.len = kv_len;
   a.k_new = kn;
   a.v_new = vn;
   a.o = o;
@@ -445,11 +459,31 @@ moe_status moe_attention_block(const uint16_t* x, int K, int H, int nq, int nkv,
   go.x = o;
   go.K = K;
   go.D = nq * 128;
-  go.seg[0] = {Wo, x_out, x, H};
+  go.seg[0] = {Wo, x_out, x, H, nullptr, nullptr, 0};
   go.nseg = 1;
   go.n_total = H;
   if (launch_gemv(go, s, true) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+moe_status moe_attention_block(const uint16_t* x, int K, int H, int nq, int nkv, int head_dim, int C,
+                               const uint16_t* Wq, const uint16_t* Wk, const uint16_t* Wv, const uint16_t* Wo,
+                               uint16_t* kcache, uint16_t* vcache, const int32_t* kv_len, float eps,
+                               uint16_t* x_out, uint16_t* k_new_out, uint16_t* v_new_out, uint16_t* o_out,
+                               void* ws, size_t ws_bytes, void* stream) {
+  moe_status st = check_attn(K, H, nq, nkv, head_dim, C);
+  if (st != MOE_OK) return st;
+  if (!x || !Wq || !Wk || !Wv || !Wo || !x_out || !ws || (C > 0 && (!kcache || !vcache)) || !(eps >= 0.f) ||
+      (kv_len && C == 0))
+    return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, Wq, Wk, Wv, Wo, kcache, vcache, x_out, k_new_out, v_new_out, o_out, ws};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return MOE_ERR_MISALIGNED;
+  const AttnLayout L = attn_layout(K, H, nq, nkv);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  char* b = static_cast<char*>(ws);
+  return attention_impl(x, K, H, nq, nkv, C, Wq, Wk, Wv, Wo, kcache, vcache, kv_len, eps, x_out, k_new_out,
+                        v_new_out, o_out, b, L, reinterpret_cast<int*>(b + L.hdr), static_cast<cudaStream_t>(stream));
 }
 
 static moe_status check_model(const moe_verify_model* m, int K) {
@@ -461,6 +495,7 @@ static moe_status check_model(const moe_verify_model* m, int K) {
   for (int l = 0; l < m->n_layers; ++l) {
     const moe_decoder_layer& d = m->layers[l];
     if (!d.Wq || !d.Wk || !d.Wv || !d.Wo || (m->ctx > 0 && (!d.kcache || !d.vcache))) return MOE_ERR_INVALID_ARG;
+    if (m->kv_len && m->ctx == 0) return MOE_ERR_INVALID_ARG;
     if ((s = check_layer(&d.moe, K)) != MOE_OK) return s;
     if (d.moe.hidden != m->hidden) return MOE_ERR_INVALID_ARG;
   }
@@ -500,6 +535,28 @@ size_t moe_verify_step_workspace_size(const moe_verify_model* m, int K) {
   return step_layout(m, K).total;
 }
 
+// One target forward over the K rows in x (every layer's attention block and
+// MoE block, in place), then the greedy token of every row into `target`.
+static moe_status forward_impl(const moe_verify_model* m, uint16_t* x, int K, int32_t* target, char* b,
+                               const StepLayout& L, cudaStream_t st) {
+  uint16_t* xn = reinterpret_cast<uint16_t*>(b + L.xn);
+  const int H = m->hidden;
+  const AttnLayout AL = attn_layout(K, H, m->n_q_heads, m->n_kv_heads);
+  int* err = reinterpret_cast<int*>(b + L.moe_ws);  // the step's error word (the MoE workspace header)
+  for (int l = 0; l < m->n_layers; ++l) {
+    const moe_decoder_layer& d = m->layers[l];
+    moe_status s = attention_impl(x, K, H, m->n_q_heads, m->n_kv_heads, m->ctx, d.Wq, d.Wk, d.Wv, d.Wo, d.kcache,
+                                  d.vcache, m->kv_len, m->eps, x, nullptr, nullptr, nullptr, b + L.attn_ws, AL, err, st);
+    if (s != MOE_OK) return s;
+    // the MoE layer kernel applies its RMSNorm to x itself
+    s = run_layer(&d.moe, x, K, x, x, nullptr, nullptr, nullptr, b + L.moe_ws, L.moe_bytes, st, true, nullptr,
+                  m->eps);
+    if (s != MOE_OK) return s;
+  }
+  if (launch_rmsnorm(x, K, H, m->eps, xn, st, false) != cudaSuccess) return MOE_ERR_CUDA;
+  return moe_lm_head_argmax(xn, K, H, m->lm_head, m->vocab, target, nullptr, b + L.lm_ws, lmhead_ws_bytes(K), st);
+}
+
 moe_status moe_verify_step(const moe_verify_model* m, uint16_t* x, int K, const int32_t* draft, int32_t* target,
                            int32_t* n_accepted, void* ws, size_t ws_bytes, void* stream) {
   moe_status s = check_model(m, K);
@@ -508,25 +565,55 @@ moe_status moe_verify_step(const moe_verify_model* m, uint16_t* x, int K, const 
   if (!aligned16(x) || !aligned16(ws)) return MOE_ERR_MISALIGNED;
   const StepLayout L = step_layout(m, K);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  char* b = static_cast<char*>(ws);
-  uint16_t* xn = reinterpret_cast<uint16_t*>(b + L.xn);
-  const int H = m->hidden;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  for (int l = 0; l < m->n_layers; ++l) {
-    const moe_decoder_layer& d = m->layers[l];
-    s = moe_attention_block(x, K, H, m->n_q_heads, m->n_kv_heads, m->head_dim, m->ctx, d.Wq, d.Wk, d.Wv, d.Wo,
-                            d.kcache, d.vcache, m->eps, x, nullptr, nullptr, nullptr, b + L.attn_ws, L.attn_bytes,
-                            stream);
-    if (s != MOE_OK) return s;
-    // the MoE layer kernel applies its RMSNorm to x itself
-    s = run_layer(&d.moe, x, K, x, x, nullptr, nullptr, nullptr, b + L.moe_ws, L.moe_bytes, stream, true, nullptr,
-                  m->eps);
-    if (s != MOE_OK) return s;
-  }
-  if (launch_rmsnorm(x, K, H, m->eps, xn, st, false) != cudaSuccess) return MOE_ERR_CUDA;
-  s = moe_lm_head_argmax(xn, K, H, m->lm_head, m->vocab, target, nullptr, b + L.lm_ws, lmhead_ws_bytes(K), stream);
+  s = forward_impl(m, x, K, target, static_cast<char*>(ws), L, st);
   if (s != MOE_OK) return s;
   return verify_accept_prefix(draft, target, K, n_accepted, stream);
+}
+
+moe_status moe_kv_commit(int32_t* kv_len, const int32_t* n_accepted, int K, int capacity, void* stream) {
+  if (!kv_len || !n_accepted || K < 1 || capacity < 0) return MOE_ERR_INVALID_ARG;
+  if (launch_kv_commit(kv_len, n_accepted, K, capacity, nullptr, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_synthetic_drafts(const int32_t* target, const uint8_t* coin, const int32_t* alt, int K, int vocab,
+                                int32_t* draft, void* stream) {
+  if (!target || !coin || !alt || !draft || K < 1 || vocab < 2) return MOE_ERR_INVALID_ARG;
+  if (launch_synthetic_drafts(target, coin, alt, K, vocab, draft, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_verify_rounds(const moe_verify_model* m, const uint16_t* x_rounds, int R, int K, const uint8_t* coin,
+                             const int32_t* alt, uint16_t* x_work, int32_t* targets, int32_t* drafts,
+                             int32_t* n_accepted, void* ws, size_t ws_bytes, void* stream) {
+  moe_status s = check_model(m, K);
+  if (s != MOE_OK) return s;
+  if (!m->kv_len || R < 1 || !x_rounds || !coin || !alt || !x_work || !targets || !drafts || !n_accepted || !ws)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x_rounds) || !aligned16(x_work) || !aligned16(ws)) return MOE_ERR_MISALIGNED;
+  const StepLayout L = step_layout(m, K);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* b = static_cast<char*>(ws);
+  int* err = reinterpret_cast<int*>(b + L.moe_ws);
+  const size_t row_bytes = sizeof(uint16_t) * (size_t)K * m->hidden;
+  for (int r = 0; r < R; ++r) {
+    if (cudaMemcpyAsync(x_work, x_rounds + (size_t)r * K * m->hidden, row_bytes, cudaMemcpyDeviceToDevice, st) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+    int32_t* tgt = targets + (size_t)r * K;
+    int32_t* dft = drafts + (size_t)r * K;
+    s = forward_impl(m, x_work, K, tgt, b, L, st);
+    if (s != MOE_OK) return s;
+    if (launch_synthetic_drafts(tgt, coin + (size_t)r * K, alt + (size_t)r * K, K, m->vocab, dft, st) != cudaSuccess ||
+        launch_accept(dft, tgt, K, n_accepted + r, st) != cudaSuccess ||
+        launch_kv_commit(const_cast<int32_t*>(m->kv_len), n_accepted + r, K, m->ctx, err, st) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
 }
 
 moe_status moe_workspace_error(void* ws, int* code, void* stream) {
@@ -549,6 +636,7 @@ const char* moe_status_string(moe_status s) {
     case MOE_ERR_MISALIGNED: return "pointer not 16-byte aligned";
     case MOE_ERR_CUDA: return "CUDA error";
     case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case MOE_ERR_CAPACITY: return "KV cache capacity exceeded";
   }
   return "unknown status";
 }

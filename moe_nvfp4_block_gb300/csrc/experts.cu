@@ -62,16 +62,6 @@ constexpr uint64_t kDrainNs = 2000000000ull;  // bound on waiting for our own co
 // named barrier 1: the compute warps
 __device__ __forceinline__ void comp_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kCompThreads) : "memory"); }
 
-__device__ __forceinline__ void red_relaxed_add(unsigned* p, unsigned v) {
-  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ unsigned ld_relaxed(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
 __device__ __forceinline__ void set_error(int* err, int code) { atomicCAS(err, 0, code); }
 
 // Tagged words: a 32-bit payload in the low half and the call's tag in the
@@ -94,9 +84,9 @@ __device__ __forceinline__ void st_tagged(unsigned long long* p, unsigned long l
 // microseconds late on this two-die part, while atomics, performed where the
 // line lives, were visible at the next read.
 __device__ __forceinline__ void xchg_tagged(unsigned long long* p, unsigned long long v) {
-  unsigned long long old;
-  asm volatile("atom.relaxed.gpu.global.exch.b64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
-  (void)old;
+  unsigned long long prev;
+  asm volatile("atom.relaxed.gpu.global.exch.b64 %0, [%1], %2;" : "=l"(prev) : "l"(p), "l"(v) : "memory");
+  (void)prev;
 }
 
 // Between two attempts of a poll (measured: a short sleep beats spinning on
@@ -477,7 +467,7 @@ __device__ __forceinline__ void kunit_mma_at(uint32_t tile, const uint32_t (&off
 }
 
 // Item kinds of a CTA's sequence (in this order).
-constexpr int kShGU = 0, kRtGU = 1, kDN = 2, kDN2 = 3, kEnd = 4;  // kDN2: the second down range
+constexpr int kShGU = 0, kRtGU = 1, kDN = 2, kEnd = 4;  // kind 3: the second down range
 
 struct Item {
   int kind;
@@ -629,17 +619,14 @@ __device__ __forceinline__ void issue_item(const IssueCtx& c, const Item it, uns
     const int chunks = (H / 2) / geo.inner;
     if (lane == 0) mbar_arrive_expect_tx(bar, 2 * code + 2 * scale);
     __syncwarp();
-    if (c.code3d) {  // one request per projection tile
-      if (lane == 0) tma_load_3d(stg, mg, 0, row0, 0, bar, c.pol);
-      else if (lane == 1) tma_load_3d(stg + code, mu, 0, row0, 0, bar, c.pol);
+    if (c.code3d) {  // one request per projection tile: lane 0 gate, lane 1 up, in one instruction
+      if (lane < 2) tma_load_3d(stg + lane * code, lane ? mu : mg, 0, row0, 0, bar, c.pol);
     } else if (lane < chunks)
       tma_load_2d(stg + lane * kGURows * geo.inner, mg, lane * geo.inner, row0, bar, c.pol);
     else if (lane >= 16 && lane < 16 + chunks)
       tma_load_2d(stg + code + (lane - 16) * kGURows * geo.inner, mu, (lane - 16) * geo.inner, row0, bar, c.pol);
-    if (lane == 30)
-      tma_load_2d(stg + 2 * code, msg, 0, row0, bar, c.pol);
-    else if (lane == 31)
-      tma_load_2d(stg + 2 * code + scale, msu, 0, row0, bar, c.pol);
+    if (lane >= 30)  // the two scale tiles
+      tma_load_2d(stg + 2 * code + (lane - 30) * scale, lane == 31 ? msu : msg, 0, row0, bar, c.pol);
   } else {
     const TileGeo geo = tile_geo(I);
     const int code = kDNRows * I / 2, scale = kDNRows * I / 16;
@@ -660,16 +647,21 @@ __device__ __forceinline__ void issue_item(const IssueCtx& c, const Item it, uns
   __syncwarp();
 }
 
+
+// Tag of the words a layer call writes: the call's index plus one (never 0,
+// the value of a zero-filled workspace).
+__device__ __forceinline__ unsigned call_tag(unsigned long long call) {
+  return (unsigned)(call % 0xFFFFFFFFull) + 1u;
+}
+
 }  // namespace
 
+// The experts kernel: one MoE layer call in one persistent launch.  Every CTA
+// stages the K input rows, normalises them when asked, forms its share of the
+// router logits and publishes them, routes every row, streams its items of
+// the layer's distinct experts, and combines its share of the outputs.
 template <int NB>
-__global__ void __launch_bounds__(kThreads, 1)
-    k_moe_experts(const __grid_constant__ CUtensorMap tm_gate, const __grid_constant__ CUtensorMap tm_up,
-                  const __grid_constant__ CUtensorMap tm_down, const __grid_constant__ CUtensorMap tm_sgate,
-                  const __grid_constant__ CUtensorMap tm_sup, const __grid_constant__ CUtensorMap tm_sdown,
-                  const __grid_constant__ CUtensorMap tm_gate_s, const __grid_constant__ CUtensorMap tm_up_s,
-                  const __grid_constant__ CUtensorMap tm_sgate_s, const __grid_constant__ CUtensorMap tm_sup_s,
-                  ExpertsArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) k_moe_experts(const __grid_constant__ ExpertsParams P) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -679,13 +671,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int s_abort, s_nu;
   __shared__ unsigned long long s_call;
 
+  const ExpertsCommon& a = P.c;
   const int H = a.H, I = a.I, K = a.K, G = a.G, E = a.E, k = a.k;
   const int S = a.stages;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const int stage_bytes = expert_stage_bytes(H, I);
   const int mt_per = I / kGURows, n_tiles = H / kDNRows;
-  const int n_sh = a.has_shared ? I / kGURows : 0;
   const int grid = gridDim.x;
 
   // reduction slots (two, alternating by item): the compute warps' FP32
@@ -706,6 +698,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* s_tse = reinterpret_cast<float*>(s_uexp + G + 1);            // [E+1][3] tensor scales (E = shared)
   float* s_bias = s_tse + 3 * (E + 1);                                // [E] router bias (0 if none)
   signed char* s_slot = reinterpret_cast<signed char*>(s_bias + E);   // [(G+1)*K]
+  // the K input rows, staged once per CTA and layer in the reduction slots
+  // (idle until the layer's first item)
+  uint4* xs = reinterpret_cast<uint4*>(red);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -716,10 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     s_call = 0ull;
     fence_mbar_init();
   }
-  if (threadIdx.x < 16) s_xamax[threadIdx.x] = 0u;
-  if (threadIdx.x < 32) s_used[threadIdx.x] = 0u;
   __syncthreads();
-
   // optional timeline: globaltimer stamps of this CTA's milestones
   unsigned long long* trace = a.trace ? a.trace + (size_t)blockIdx.x * kTraceSlots : nullptr;
   auto stamp = [&](int m) {
@@ -737,118 +729,101 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok && lane == 0) fail();
     return ok;
   };
+  const LayerDesc& D = P.L;
+  // shared-expert gate/up items (CTA b holds b, b + grid, ...)
+  const int n_sh = D.has_shared ? mt_per : 0;
+  const int n_shb = split_before(blockIdx.x + 1, n_sh, grid) - split_before(blockIdx.x, n_sh, grid);
   // The CTA's item sequence, from the distinct-expert count.
   auto make_cta_seq = [&]() {
     const int n_u = *reinterpret_cast<volatile int*>(&s_nu);
-    const int n_slots = n_u + (a.has_shared ? 1 : 0);
-    return make_seq(make_plan(n_sh, n_u * mt_per, n_slots * n_tiles), mt_per, n_tiles, G, a.has_shared);
+    const int n_slots = n_u + (D.has_shared ? 1 : 0);
+    return make_seq(make_plan(n_sh, n_u * mt_per, n_slots * n_tiles), mt_per, n_tiles, G, D.has_shared);
   };
-  // ---------------------------------------------------------------- before the dependency wait
-  // The shared items of this CTA come first in its sequence and need no routing.
-  const int n_shb = split_before(blockIdx.x + 1, n_sh, grid) - split_before(blockIdx.x, n_sh, grid);
-  int issued = 0;
-  IssueCtx ic;
+
   if (warp == kProducerWarp) {
-    ic.gate = &tm_gate;
-    ic.up = &tm_up;
-    ic.down = &tm_down;
-    ic.sgate = &tm_sgate;
-    ic.sup = &tm_sup;
-    ic.sdown = &tm_sdown;
-    ic.gate_s = &tm_gate_s;
-    ic.up_s = &tm_up_s;
-    ic.sgate_s = &tm_sgate_s;
-    ic.sup_s = &tm_sup_s;
-    ic.down_scales = a.down.scales;
-    ic.sh_down_scales = a.sh_down.scales;
-    ic.uexp = s_uexp;
-    ic.H = H;
-    ic.I = I;
-    ic.G = G;
-    ic.code3d = a.code3d;
-    ic.pol = policy_evict_first();
+    // ------------------------------------------------------------ producer
+    // The CTA's shared-expert gate/up items (no routing needed: issued
+    // before the dependency wait), then, once warp 0 has listed the distinct
+    // experts, its routed gate/up and down items.  Item j goes to stage j % S
+    // on pass j / S.
+    const uint64_t pol = policy_evict_first();
+    int issued = 0, st = 0, pass = 0;
+    bool live = true;
+    auto issue_next = [&](const IssueCtx& ic, const Item& it, int li) {
+      int ok = 1;
+      if (lane == 0 && pass > 0 && !mbar_wait_bounded(&empty_bar[st], (pass - 1) & 1, a.wait_ns, &s_abort)) {
+        ok = 0;
+        fail();
+      }
+      if (__shfl_sync(0xffffffffu, ok, 0) == 0) return false;
+      if (lane == 0 && trace && li < 24) trace[40 + li] = global_timer_ns();  // item li issued
+      issue_item(ic, it, smem + (size_t)st * stage_bytes, &full_bar[st], lane);
+      ++issued;
+      if (++st == S) {
+        st = 0;
+        ++pass;
+      }
+      return true;
+    };
+    do {
+      const CUtensorMap* mp = P.maps;
+      IssueCtx ic;
+      ic.gate = mp + 0;
+      ic.up = mp + 1;
+      ic.down = mp + 2;
+      ic.sgate = mp + 3;
+      ic.sup = mp + 4;
+      ic.sdown = mp + 5;
+      ic.gate_s = mp + 6;
+      ic.up_s = mp + 7;
+      ic.sgate_s = mp + 8;
+      ic.sup_s = mp + 9;
+      ic.down_scales = D.down.scales;
+      ic.sh_down_scales = D.sh_down.scales;
+      ic.uexp = s_uexp;
+      ic.H = H;
+      ic.I = I;
+      ic.G = G;
+      ic.code3d = a.code3d;
+      ic.pol = pol;
+      if (lane < kMapsPerLayer) prefetch_tensormap(mp + lane);
+      Item it;
+      it.kind = kShGU;
+      it.slot = G;
+      it.tile = blockIdx.x;
+      for (int j = 0; j < n_shb && live; ++j, it.tile += grid) live = issue_next(ic, it, j);
+      if (!live) break;
+      asm volatile("bar.sync 2, 64;" ::: "memory");  // the distinct experts are listed
+      if (lane == 0) stamp(3);
+      const Seq seq = make_cta_seq();
+      const int L = plan_len(seq.p);
+      Cursor cur = seq_begin(seq);
+      for (int j = 0; j < n_shb; ++j) seq_next(cur, seq);
+      for (int j = n_shb; j < L && live; ++j, seq_next(cur, seq)) live = issue_next(ic, cur.it, j);
+    } while (false);
+    if (lane == 0 && trace) trace[9] = global_timer_ns();
     if (lane == 0) {
-      prefetch_tensormap(&tm_gate);
-      prefetch_tensormap(&tm_up);
-      prefetch_tensormap(&tm_down);
-      prefetch_tensormap(&tm_gate_s);
-      prefetch_tensormap(&tm_up_s);
+      // every copy of the last S items has landed before the CTA may exit
+      // (a stage is reissued only after the compute warps saw its previous
+      // copy complete, so older copies have landed)
+      for (int j = (issued > S ? issued - S : 0); j < issued; ++j)
+        mbar_wait_drain(&full_bar[j % S], (j / S) & 1, kDrainNs);
     }
-    Item it;
-    it.kind = kShGU;
-    it.slot = G;
-    it.tile = blockIdx.x;
-    for (; issued < n_shb && issued < S; ++issued, it.tile += grid) {
-      if (lane == 0 && trace && issued < 24) trace[40 + issued] = global_timer_ns();
-      issue_item(ic, it, smem + (size_t)issued * stage_bytes, &full_bar[issued], lane);
-    }
-  } else if (warp < kCompWarps) {
-    const int tid = threadIdx.x;
-    for (int e = tid; e < E; e += kCompThreads) {
-      s_rowmask[e] = 0u;
-      s_bias[e] = a.router_bias ? a.router_bias[e] : 0.f;  // weights of the layer: no dependency
-    }
-    for (int i = tid; i < (G + 1) * K; i += kCompThreads) s_slot[i] = -1;
-  }
-  // the tensor scales (slot E = shared): their loads come from DRAM and are
-  // not needed before the first epilogue, so a thread's first triple waits
-  // in registers and goes to shared memory only after the router step (the
-  // rest, for E >= 512, are stored at once)
-  auto tse_of = [&](int e, int j) {
-    const ProjPtrs& pr = j == 0 ? (e == E ? a.sh_gate : a.gate) : (j == 1 ? (e == E ? a.sh_up : a.up) : (e == E ? a.sh_down : a.down));
-    return pr.tscale[e == E ? 0 : e];
-  };
-  float tse0[3] = {0.f, 0.f, 0.f};
-  if (warp < kCompWarps) {
-    const int e0 = threadIdx.x;
-    if (e0 < E || (e0 == E && a.has_shared))
-      for (int j = 0; j < 3; ++j) tse0[j] = tse_of(e0, j);
-    for (int e = e0 + kCompThreads; e <= E; e += kCompThreads)
-      if (e < E || a.has_shared)
-        for (int j = 0; j < 3; ++j) s_tse[3 * e + j] = tse_of(e, j);
+    return;
   }
 
-  // Router logits, spread over the CTAs: CTA b owns experts b + grid m
-  // (m < M) and its compute warps take the (expert, row) pairs p = warp,
-  // warp + 16, ... (m = p % M, row p / M).  A warp's first router row goes to
-  // registers before the dependency wait (the weights do not depend on it).
-  const int M = (E + grid - 1) / grid;
-  const int n_pairs = M * K;
-  uint4 lw[8];  // the warp's current router row: lane l holds pieces 256 j + 8 l .. + 7
-  int lw_e = -1;
-  auto load_router_row = [&](int e) {
-    const uint4* wrow = reinterpret_cast<const uint4*>(a.router_w + (size_t)e * H);
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (j < H / 256) lw[j] = ldg_nc_v4(wrow + j * 32 + lane);
-    lw_e = e;
-  };
-  if (warp < kCompWarps && warp < n_pairs) {
-    const int e = (int)blockIdx.x + grid * (warp % M);
-    if (e < E) load_router_row(e);
-  }
+  // -------------------------------------------------------------- compute warps
+  const int tid = threadIdx.x;
+  // Per-layer preparation that needs no layer input: routing tables cleared,
+  // the router bias to shared memory, the tensor scales (slot E = shared) of
+  // this thread's first expert to registers (stored to shared memory after
+  // the router step, so their DRAM latency is hidden; the rest, for E >= 512,
+  // at once), and the warp's first router row to registers.
+  const int M = (E + grid - 1) / grid;  // router experts per CTA: b + grid m, m < M
+  const int n_pairs = M * K;            // (expert, row) pairs: p = warp, warp + 16, ...: m = p % M, row p / M
 
-  if (threadIdx.x == 0) stamp(1);
-  pdl_wait();  // the block input (and the workspace) are complete from here on
-  if (threadIdx.x == 0) stamp(2);
-
-  // The call's index is the number of CTA exits of all earlier calls over the
-  // grid (a CTA of this call exits only after this read, and adds one exit,
-  // so the quotient is the same for every CTA).  Thread 0 reads it for the
-  // CTA (one read, not one per thread, of the word every CTA reads).
-  if (threadIdx.x == 0) s_call = __ldcg(a.ws.exits) / (unsigned long long)grid;
-
-  // The K input rows, staged once per CTA in the reduction slots (idle until
-  // the first item's partials): [K][H] bf16, normalised on the way when the
-  // call asks for it, with the arithmetic of the RMSNorm kernel (a fixed-order
-  // FP32 sum of squares, then each step one correctly rounded operation), so
-  // the rows are bit for bit that kernel's output.  Every CTA has staged its
-  // rows before it publishes its logits, and no CTA writes y before it has
-  // read all logits, so y may be the input itself.
-  uint4* xs = reinterpret_cast<uint4*>(red);
-  // activations: compute warp w holds k-unit w of every row as FP16 B
-  // fragments; the row maxima now, the fragments after the routing, while
-  // the first weight tiles are in flight
+  // activations as FP16 B fragments: compute warp w holds k-unit w of every
+  // row (from the staged rows)
   auto load_x = [&](uint4 (&raw)[NB][4]) {
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
@@ -861,14 +836,113 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   };
-  if (warp < kCompWarps) {
-    for (int r = warp; r < K; r += kCompWarps) {
-      const uint4* xr = reinterpret_cast<const uint4*>(a.x + (size_t)r * H);
-      uint4 v[8];
+  const int KUgu = H / 128, KUdn = I / 128;
+  const TileGeo ggu = tile_geo(H), gdn = tile_geo(I);
+  const int gu_code = kGURows * H / 2, gu_scale = kGURows * H / 16;
+  const int dn_code = kDNRows * I / 2;
+  const int smask = (H / 16 >= 128) ? 7 : (H / 16 == 64 ? 3 : (H / 16 == 32 ? 1 : 0));
+  const int sstride = H / 16;
+  const bool gu_active = warp < KUgu;
+  const uint32_t so0 = swizzle_off((uint32_t)(g * sstride + 8 * warp), smask);
+  const uint32_t so1 = swizzle_off((uint32_t)((g + 8) * sstride + 8 * warp), smask);
+  uint32_t goff[2];  // this lane's ldmatrix offsets in a gate/up codes tile
+  kunit_offsets(ggu, kGURows, 0, gu_active ? warp : 0, lane, goff);
+  const int mA = warp & 3, kq = warp >> 2;
+  const bool dn_active = kq < KUdn;
+  uint32_t doffA[2], doffB[2];  // this lane's ldmatrix offsets in a down codes tile
+  kunit_offsets(gdn, kDNRows, mA * 16, dn_active ? kq : 0, lane, doffA);
+  kunit_offsets(gdn, kDNRows, (mA + 4) * 16, dn_active ? kq : 0, lane, doffB);
+  const int lg_mt = __ffs(mt_per) - 1;
+  int st = 0, fp = 0;  // ring position of the next item: stage st, pass fp
+  auto advance = [&]() {
+    if (++st == S) {
+      st = 0;
+      ++fp;
+    }
+  };
+
+  {
+    // Preparation that needs no layer input, before the dependency wait:
+    // routing tables cleared, the router bias to shared memory, the
+    // tensor scales (slot E = shared) of this thread's expert to registers
+    // (stored to shared memory after the router step, so their DRAM latency
+    // is hidden; the rest, for E >= 512, at once), and the warp's first
+    // router row to registers (lane l holds pieces 256 j + 8 l .. + 7).
+    uint4 lw[8];
+    int lw_e = -1;
+    float tse0[3] = {0.f, 0.f, 0.f};
+    {
+      for (int e = tid; e < E; e += kCompThreads) {
+        s_rowmask[e] = 0u;
+        s_bias[e] = D.router_bias ? D.router_bias[e] : 0.f;
+      }
+      for (int i = tid; i < (G + 1) * K; i += kCompThreads) s_slot[i] = -1;
+      if (tid < 16) s_xamax[tid] = 0u;
+      if (tid < 32) s_used[tid] = 0u;
+      auto tse_of = [&](int e, int j) {
+        const float* ts = j == 0 ? (e == E ? D.sh_gate.tscale : D.gate.tscale)
+                                 : (j == 1 ? (e == E ? D.sh_up.tscale : D.up.tscale)
+                                           : (e == E ? D.sh_down.tscale : D.down.tscale));
+        return ts[e == E ? 0 : e];
+      };
+      if (tid < E || (tid == E && D.has_shared))
+        for (int j = 0; j < 3; ++j) tse0[j] = tse_of(tid, j);
+      for (int e = tid + kCompThreads; e <= E; e += kCompThreads)
+        if (e < E || D.has_shared)
+          for (int j = 0; j < 3; ++j) s_tse[3 * e + j] = tse_of(e, j);
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (j < H / 256) v[j] = __ldcg(xr + j * 32 + lane);
-      if (a.norm) {
+      for (int j = 0; j < 8; ++j) lw[j] = make_uint4(0, 0, 0, 0);
+      if (warp < n_pairs) {
+        const int e = (int)blockIdx.x + grid * (warp % M);
+        if (e < E) {
+          const uint4* wrow = reinterpret_cast<const uint4*>(D.router_w + (size_t)e * H);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (j < H / 256) lw[j] = ldg_nc_v4(wrow + j * 32 + lane);
+          lw_e = e;
+        }
+      }
+    }
+    if (tid == 0) stamp(1);
+    pdl_wait();  // the block input (and the workspace) are complete from here on
+    if (tid == 0) stamp(2);
+    // The call's index: the calls finished by the CTAs of all earlier
+    // launches over the grid (every CTA adds one as its last act, after this
+    // read, so the quotient is the same for every CTA).
+    // (the read overlaps the copy of the rows below; the barrier after the
+    // copy publishes it)
+    if (tid == 0) s_call = __ldcg(a.ws.exits) / (unsigned long long)grid;
+
+    // ---------------------------------------------------------------- input rows
+    // [K][H] bf16 into xs, then, when asked, warp r normalises row r with
+    // the RMSNorm kernel's arithmetic (a fixed-order FP32 sum of squares,
+    // then each step one correctly rounded operation), so the rows are bit
+    // for bit that kernel's output.  Every CTA has staged its rows before it
+    // publishes its logits, and no CTA writes y before it has read all
+    // logits, so y may be the input itself.
+    {
+      // the compute threads copy x, eight 16-byte loads in flight each
+      const uint4* xg = reinterpret_cast<const uint4*>(a.x);
+      const int n16 = K * H / 8;
+      for (int i0 = tid; i0 < n16; i0 += 8 * kCompThreads) {
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (i0 + u * kCompThreads < n16) v[u] = __ldcg(xg + i0 + u * kCompThreads);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (i0 + u * kCompThreads < n16) xs[i0 + u * kCompThreads] = v[u];
+      }
+    }
+    comp_bar();  // the rows staged, s_call written, the tables cleared
+    const unsigned long long call = *reinterpret_cast<volatile unsigned long long*>(&s_call);
+    const unsigned tag = call_tag(call);
+    if (a.norm) {
+      for (int r = warp; r < K; r += kCompWarps) {
+        uint4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (j < H / 256) v[j] = xs[r * (H / 8) + j * 32 + lane];
         float ss = 0.f;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -893,26 +967,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t hi = float_to_bf16_bits(__fmul_rn(__uint_as_float(q[i] & 0xFFFF0000u), inv));
             q[i] = lo | (hi << 16);
           }
-          v[j] = make_uint4(q[0], q[1], q[2], q[3]);
+          xs[r * (H / 8) + j * 32 + lane] = make_uint4(q[0], q[1], q[2], q[3]);
         }
       }
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (j < H / 256) xs[r * (H / 8) + j * 32 + lane] = v[j];
+      comp_bar();  // the rows are normalised
     }
-    comp_bar();  // the rows are staged
+    if (tid == 0) stamp(15);
 
-    // this CTA's router logits: per lane, products in element order over
-    // the pieces j, then xor rounds 16 .. 1, then the bias (the arithmetic
-    // of the router GEMV, so the logits are the same bits)
-    // (lane 0 of each such warp reads the call index for the tag itself, so
-    // the logits leave as soon as they are formed)
-    unsigned long long wcall = 0ull;
-    if (lane == 0 && warp < n_pairs) wcall = __ldcg(a.ws.exits) / (unsigned long long)grid;
+    // ---------------------------------------------------------------- router logits
+    // This CTA's share: per lane, products in element order over the pieces
+    // j, then xor rounds 16 .. 1 (the router GEMV's fixed order, so the
+    // logits are the same bits), published as tagged words the moment they
+    // are formed.  Softmax scoring publishes logit + bias, sigmoid scoring the
+    // score (the bias only enters the selection keys).
     for (int p = warp; p < n_pairs; p += kCompWarps) {
       const int e = (int)blockIdx.x + grid * (p % M), r = p / M;
       if (e >= E) continue;
-      if (e != lw_e) load_router_row(e);
+      if (e != lw_e) {
+        const uint4* wrow = reinterpret_cast<const uint4*>(D.router_w + (size_t)e * H);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (j < H / 256) lw[j] = ldg_nc_v4(wrow + j * 32 + lane);
+        lw_e = e;
+      }
       uint4 xv[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j)
@@ -933,175 +1010,122 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int d = 16; d >= 1; d >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, d));
       if (lane == 0) {
-        // softmax scoring: the logit with its bias; sigmoid scoring: the
-        // score (the bias only enters the selection keys)
-        const float lg = a.scoring ? sigmoid_score(acc) : (a.router_bias ? __fadd_rn(acc, s_bias[e]) : acc);
-        xchg_tagged(a.ws.tlog + (size_t)r * E + e, tagged((unsigned)(wcall % 0xFFFFFFFFull) + 1u, __float_as_uint(lg)));
+        const float lg = D.scoring ? sigmoid_score(acc) : (D.router_bias ? __fadd_rn(acc, s_bias[e]) : acc);
+        xchg_tagged(a.ws.tlog + (size_t)r * E + e, tagged(tag, __float_as_uint(lg)));
       }
     }
+    if (tid == 0) stamp(14);
+    {
+      uint4 raw[NB][4];
+      load_x(raw);
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        unsigned mx = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t w4[4] = {raw[nb][q].x, raw[nb][q].y, raw[nb][q].z, raw[nb][q].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            mx = max(mx, (w4[i] << 16) & 0x7FFFFFFFu);
+            mx = max(mx, w4[i] & 0x7FFF0000u);
+          }
+        }
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const int n = nb * 8 + g;
+        if (t == 0 && n < K) atomicMax(&s_xamax[n], mx);
+      }
+    }
+    if (tid <= E)
+      for (int j = 0; j < 3; ++j) s_tse[3 * tid + j] = tse0[j];
 
-    if (threadIdx.x == 0) stamp(14);
-    uint4 raw[NB][4];
-    load_x(raw);
+    // ---------------------------------------------------------------- routing (every CTA, identical)
+    {
+      const bool fast = E <= 256 && k <= 8;
+      for (int r = warp; r < K; r += kCompWarps) {
+        // row r's logits, once every word of it carries this call's tag (a
+        // bounded wait; on giving up, experts 0 .. k-1 keep the tables in
+        // range and the abort flag stops the work)
+        const unsigned long long* row = a.ws.tlog + (size_t)r * E;
+        bool got;
+        const float* sel_bias = (D.scoring && D.router_bias) ? s_bias : nullptr;
+        if (fast) {
+          got = route_row_fast(row, tag, E, k, r, a.wait_ns, &s_abort, s_idx, s_w, s_rowmask, s_used, D.scoring,
+                               sel_bias, lane);
+        } else {
+          got = topk_general(row, tag, a.wait_ns, &s_abort, E, k, s_idx + r * k, s_w + r * k, sel_bias, lane);
+          __syncwarp();
+          const int sel_e = got ? (lane < k ? s_idx[r * k + lane] : 0) : lane;
+          const float sel_l = got ? (lane < k ? s_w[r * k + lane] : 0.f) : 0.f;
+          const float top = got ? s_w[r * k] : 0.f;
+          __syncwarp();
+          // softmax over the selected logits; sigmoid scoring: the selected
+          // experts' own scores (their words already carry this call's tag)
+          const float ev = (lane < k) ? (D.scoring ? (got ? __uint_as_float((unsigned)ld_tagged(row + sel_e)) : 0.f)
+                                                   : expf(sel_l - top))
+                                      : 0.f;
+          float z = ev;
 #pragma unroll
-    for (int nb = 0; nb < NB; ++nb) {
-      unsigned mx = 0;
+          for (int d = 16; d >= 1; d >>= 1) z += __shfl_xor_sync(0xffffffffu, z, d);
+          if (lane < k) {
+            s_idx[r * k + lane] = sel_e;
+            s_w[r * k + lane] = ev / z;
+            atomicOr(&s_rowmask[sel_e], 1u << r);
+            atomicOr(&s_used[sel_e >> 5], 1u << (sel_e & 31));
+          }
+        }
+        if (!got && lane == 0) fail();
+      }
+      comp_bar();
+      if (tid == 0) stamp(13);
+      // grouping: the distinct experts in ascending order are the set bits of
+      // s_used; an expert's position is the number of set bits before it
+      // (every warp forms the per-word prefix itself: no further barrier)
+      const int n_words = (E + 31) >> 5;
+      const unsigned used = lane < n_words ? s_used[lane] : 0u;
+      const int cnt = __popc(used);
+      int inc = cnt;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint32_t w4[4] = {raw[nb][q].x, raw[nb][q].y, raw[nb][q].z, raw[nb][q].w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          mx = max(mx, (w4[i] << 16) & 0x7FFFFFFFu);
-          mx = max(mx, w4[i] & 0x7FFF0000u);
+      for (int d = 1; d < 32; d <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, inc, d);
+        if (lane >= d) inc += o;
+      }
+      const int excl = inc - cnt;
+      if (warp == 0) {
+        int u = excl;
+        for (unsigned m = used; m; m &= m - 1) s_uexp[u++] = lane * 32 + __ffs(m) - 1;
+        if (lane == 31) s_nu = inc;
+        if (lane == 0) s_uexp[G] = E;  // the shared expert's scales sit at index E
+        // the producer needs only the distinct experts and their count: hand
+        // them over now (named barrier 2: this warp arrives, the producer
+        // waits; warp 0 arrives once per layer whatever happened)
+        __syncwarp();
+        asm volatile("bar.arrive 2, 64;" ::: "memory");
+      }
+      for (int base = 0; base < K * k; base += kCompThreads) {
+        const int q = base + tid;
+        const int e = q < K * k ? s_idx[q] : 0;
+        const int pre_w = __shfl_sync(0xffffffffu, excl, (e >> 5) & 31);
+        const unsigned uw = __shfl_sync(0xffffffffu, used, (e >> 5) & 31);
+        if (q < K * k) {
+          const int u = pre_w + __popc(uw & ((1u << (e & 31)) - 1u));
+          s_slot[u * K + q / k] = (signed char)(q % k);
         }
       }
-      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const int n = nb * 8 + g;
-      if (t == 0 && n < K) atomicMax(&s_xamax[n], mx);
+      if (D.has_shared)
+        for (int r = tid; r < K; r += kCompThreads) s_slot[G * K + r] = (signed char)k;
+      comp_bar();  // the (row, slot) map is complete
     }
-    if ((int)threadIdx.x <= E)
-      for (int j = 0; j < 3; ++j) s_tse[3 * threadIdx.x + j] = tse0[j];
-    comp_bar();  // routing tables cleared before any warp marks them; s_call and s_tse written
-    if (threadIdx.x == 0) stamp(15);
-  }
-  // (the producer warp reads s_call too early; it uses none of these)
-  const unsigned long long call = *reinterpret_cast<volatile unsigned long long*>(&s_call);
-  // the tag of this call's words, never 0 (the value of a zero-filled
-  // workspace); counter set call % 2 is this call's, and this call clears
-  // the other one for the next call
-  const unsigned tag = (unsigned)(call % 0xFFFFFFFFull) + 1u;
-  unsigned* cnt = a.ws.cnt + (call & 1ull) * kCntSet;
-  if (warp < kCompWarps) {
-    unsigned* other = a.ws.cnt + ((call + 1ull) & 1ull) * kCntSet;
-    for (int i = (int)blockIdx.x * kCompThreads + (int)threadIdx.x; i < kCntSet; i += grid * kCompThreads) other[i] = 0u;
-  }
+    pdl_launch_dependents();
 
-  // ---------------------------------------------------------------- routing (every CTA, identical)
-  if (warp < kCompWarps) {
-    const bool fast = E <= 256 && k <= 8;
-    for (int r = warp; r < K; r += kCompWarps) {
-      // row r's logits, once every word of it carries this call's tag (a
-      // bounded wait; on giving up, experts 0 .. k-1 keep the tables in
-      // range and the abort flag stops the work)
-      const unsigned long long* row = a.ws.tlog + (size_t)r * E;
-      bool got;
-      const float* sel_bias = (a.scoring && a.router_bias) ? s_bias : nullptr;
-      if (fast) {
-        got = route_row_fast(row, tag, E, k, r, a.wait_ns, &s_abort, s_idx, s_w, s_rowmask, s_used, a.scoring,
-                             sel_bias, lane);
-      } else {
-        got = topk_general(row, tag, a.wait_ns, &s_abort, E, k, s_idx + r * k, s_w + r * k, sel_bias, lane);
-        __syncwarp();
-        const int sel_e = got ? (lane < k ? s_idx[r * k + lane] : 0) : lane;
-        const float sel_l = got ? (lane < k ? s_w[r * k + lane] : 0.f) : 0.f;
-        const float top = got ? s_w[r * k] : 0.f;
-        __syncwarp();
-        // softmax over the selected logits; sigmoid scoring: the selected
-        // experts' own scores (their words already carry this call's tag)
-        const float ev = (lane < k) ? (a.scoring ? (got ? __uint_as_float((unsigned)ld_tagged(row + sel_e)) : 0.f)
-                                                 : expf(sel_l - top))
-                                    : 0.f;
-        float z = ev;
-#pragma unroll
-        for (int d = 16; d >= 1; d >>= 1) z += __shfl_xor_sync(0xffffffffu, z, d);
-        if (lane < k) {
-          s_idx[r * k + lane] = sel_e;
-          s_w[r * k + lane] = ev / z;
-          atomicOr(&s_rowmask[sel_e], 1u << r);
-          atomicOr(&s_used[sel_e >> 5], 1u << (sel_e & 31));
-        }
-      }
-      if (!got && lane == 0) fail();
-    }
-    comp_bar();
-    if (threadIdx.x == 0) stamp(13);
-    // grouping: the distinct experts in ascending order are the set bits of
-    // s_used; an expert's position is the number of set bits before it
-    // (every warp forms the per-word prefix itself: no further barrier)
-    const int n_words = (E + 31) >> 5;
-    const unsigned used = lane < n_words ? s_used[lane] : 0u;
-    const int cnt = __popc(used);
-    int inc = cnt;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, inc, d);
-      if (lane >= d) inc += o;
-    }
-    const int excl = inc - cnt;
-    if (warp == 0) {
-      int u = excl;
-      for (unsigned m = used; m; m &= m - 1) s_uexp[u++] = lane * 32 + __ffs(m) - 1;
-      if (lane == 31) s_nu = inc;
-      if (lane == 0) s_uexp[G] = E;  // the shared expert's scales sit at index E
-      // the producer needs only the distinct experts and their count: hand
-      // them over now (named barrier 2: this warp arrives, the producer waits)
-      __syncwarp();
-      asm volatile("bar.arrive 2, 64;" ::: "memory");
-    }
-    for (int base = 0; base < K * k; base += kCompThreads) {
-      const int q = base + (int)threadIdx.x;
-      const int e = q < K * k ? s_idx[q] : 0;
-      const int pre_w = __shfl_sync(0xffffffffu, excl, (e >> 5) & 31);
-      const unsigned uw = __shfl_sync(0xffffffffu, used, (e >> 5) & 31);
-      if (q < K * k) {
-        const int u = pre_w + __popc(uw & ((1u << (e & 31)) - 1u));
-        s_slot[u * K + q / k] = (signed char)(q % k);
-      }
-    }
-    if (a.has_shared)
-      for (int r = threadIdx.x; r < K; r += kCompThreads) s_slot[G * K + r] = (signed char)k;
-    comp_bar();  // the (row, slot) map is complete
-  } else if (warp == kProducerWarp) {
-    asm volatile("bar.sync 2, 64;" ::: "memory");  // the distinct experts are listed
-  }
-  pdl_launch_dependents();
-  if (threadIdx.x == 0) stamp(3);
-
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------------------ producer
-    // Issues the copies of every item into the ring.
-    const Seq seq = make_cta_seq();
-    const int L = plan_len(seq.p);
-    Cursor cur = seq_begin(seq);
-    for (int l = 0; l < issued; ++l) seq_next(cur, seq);
-    int pass = issued / S, st = issued - pass * S;  // item l goes to stage l % S on pass l / S
-    for (int l = issued; l < L; ++l, seq_next(cur, seq)) {
-      int ok = 1;
-      if (lane == 0 && pass > 0 && !mbar_wait_bounded(&empty_bar[st], (pass - 1) & 1, a.wait_ns, &s_abort)) {
-        ok = 0;
-        fail();
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      if (lane == 0 && trace && l < 24) trace[40 + l] = global_timer_ns();  // item l issued
-      issue_item(ic, cur.it, smem + (size_t)st * stage_bytes, &full_bar[st], lane);
-      issued = l + 1;
-      if (++st == S) {
-        st = 0;
-        ++pass;
-      }
-    }
-    if (lane == 0 && trace) trace[9] = global_timer_ns();
-    if (lane == 0) {
-      // every copy of the last S items has landed before the CTA may exit
-      // (a stage is reissued only after the compute warps saw its previous
-      // copy complete, so older copies have landed)
-      for (int j = (issued > S ? issued - S : 0); j < issued; ++j)
-        mbar_wait_drain(&full_bar[j % S], (j / S) & 1, kDrainNs);
-    }
-    return;
-  }
-
-  // -------------------------------------------------------------- compute warps
-  // Warp w owns k-unit w (128 k) of every gate/up item, and m-tile w % 4,
-  // k-unit w / 4 of every down item.  Per item: codes and scales to
-  // registers, the stage back to the producer, the MMAs, the FP32 partials
-  // to the item's reduction slot, one barrier of the compute warps, then each
-  // warp reduces its share of the item's outputs.  No wait ever leaves this
-  // loop early (a failed wait sets the abort flag and the remaining items run
-  // without work), so every compute warp meets every barrier.
-  {
+    // ---------------------------------------------------------------- items
+    // Warp w owns k-unit w (128 k) of every gate/up item, and m-tile w % 4,
+    // k-unit w / 4 of every down item.  Per item: codes and scales to
+    // registers, the stage back to the producer, the MMAs, the FP32 partials
+    // to the item's reduction slot, one barrier of the compute warps, then
+    // each warp reduces its share of the item's outputs.  No wait ever leaves
+    // this loop early (a failed wait sets the abort flag and the remaining
+    // items run without work), so every compute warp meets every barrier.
     uint32_t bx[NB][16];
     {
       uint4 raw[NB][4];
@@ -1115,46 +1139,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     comp_bar();  // every warp is done with the staged rows before partials overwrite them
-    const int KUgu = H / 128, KUdn = I / 128;
-    const TileGeo ggu = tile_geo(H), gdn = tile_geo(I);
-    const int gu_code = kGURows * H / 2, gu_scale = kGURows * H / 16;
-    const int dn_code = kDNRows * I / 2;
-    const int smask = (H / 16 >= 128) ? 7 : (H / 16 == 64 ? 3 : (H / 16 == 32 ? 1 : 0));
-    const int sstride = H / 16;
-    const bool gu_active = warp < KUgu;
-    const uint32_t so0 = swizzle_off((uint32_t)(g * sstride + 8 * warp), smask);
-    const uint32_t so1 = swizzle_off((uint32_t)((g + 8) * sstride + 8 * warp), smask);
-    uint32_t goff[2];  // this lane's ldmatrix offsets in a gate/up codes tile
-    kunit_offsets(ggu, kGURows, 0, gu_active ? warp : 0, lane, goff);
-    // this CTA's gate/up items: global items V = b + l * grid, shared tile V
-    // for V < n_sh, else routed v = V - n_sh (slot v / mt_per, tile
-    // v % mt_per; mt_per is a power of two)
-    int L_gu;
+    int L_gu, L_all;
     {
       const Plan p0 = make_cta_seq().p;
       L_gu = p0.n_shb + p0.rt_count;
-      if (threadIdx.x == 0 && trace) {  // (counts, not times: for reading the item stamps)
+      L_all = plan_len(p0);
+      if (tid == 0 && trace) {  // (counts, not times: for reading the item stamps)
         trace[66] = (unsigned long long)L_gu;
-        trace[67] = (unsigned long long)plan_len(p0);
+        trace[67] = (unsigned long long)L_all;
       }
     }
-    const int lg_mt = __ffs(mt_per) - 1;
-    auto gu_slot = [&](int l) {
-      const int V = (int)blockIdx.x + l * grid;
-      return V < n_sh ? G : (V - n_sh) >> lg_mt;
-    };
-    int st = 0, fp = 0;  // item l: stage l % S on pass l / S
-    auto advance = [&]() {
-      if (++st == S) {
-        st = 0;
-        ++fp;
-      }
-    };
-    for (int l = 0; l < L_gu; ++l, advance()) {
+    // this CTA's gate/up items: global items V = b + i * grid, shared tile V
+    // for V < n_sh, else routed v = V - n_sh (slot v / mt_per, tile
+    // v % mt_per; mt_per is a power of two)
+    for (int li = 0; li < L_gu; ++li, advance()) {
       unsigned char* stg = smem + (size_t)st * stage_bytes;
-      float* rb = red + (size_t)(l & 1) * kRedFloats;
+      float* rb = red + (size_t)(li & 1) * kRedFloats;
       const bool ok = warp_wait(&full_bar[st], fp & 1);
-      if (threadIdx.x == 0 && l < 24) stamp(16 + l);  // item l landed
+      if (tid == 0 && li < 24) stamp(16 + li);  // item li landed
       // this warp's codes and scales to registers, then the stage goes back
       uint32_t ag[2][4], au[2][4];
       uint2 sr[4];
@@ -1196,14 +1198,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       comp_bar();
-      // epilogue, by the 4 warps of group l % 4 (the others move on to the
+      // epilogue, by the 4 warps of group li % 4 (the others move on to the
       // next item): thread o of the group owns output o (row o / 8 of the
       // item's 16, column o % 8 of each n-block) and sums its 16 k-unit
       // partials in k-unit order
       const bool live = !__any_sync(0xffffffffu, aborted());
-      if ((warp >> 2) == (l & 3) && live) {
-        const int slot = gu_slot(l);
-        const int Vg = (int)blockIdx.x + l * grid;
+      if ((warp >> 2) == (li & 3) && live) {
+        const int Vg = (int)blockIdx.x + li * grid;
+        const int slot = Vg < n_sh ? G : (Vg - n_sh) >> lg_mt;
         const int tile = Vg < n_sh ? Vg : ((Vg - n_sh) & (mt_per - 1));
         const int ex = s_uexp[slot];
         const float tg = s_tse[3 * ex + 0], tu = s_tse[3 * ex + 1];
@@ -1234,49 +1236,47 @@ __global__ void __launch_bounds__(kThreads, 1)
             st_tagged(a.ws.h + ((size_t)slot * K + n) * (I / 2) + ((tile * kGURows + i) >> 1),
                       tagged(tag, hb | (hn << 16)));
         }
-        // this duty warp's h words are written (the count only tells readers
-        // when to look; the tags make the words themselves safe to read)
+        // this duty warp's h words are written: its done flag (the flag only
+        // tells readers when to look; the tags make the h words themselves
+        // safe to read)
         __syncwarp();
-        if (lane == 0) red_relaxed_add(cnt + slot, 1u);
+        if (lane == 0) st_tagged(a.ws.flags + ((size_t)slot * mt_per + tile) * 4 + (warp & 3), tagged(tag, 1u));
       }
     }
     // down items: 8 m-tiles of 16 rows x I/128 k-units; warp w takes k-unit
     // w / 4 of m-tiles w % 4 and w % 4 + 4 (one set of h fragments for both)
     {
       const Seq seq = make_cta_seq();
-      const int L = plan_len(seq.p);
-      const int mA = warp & 3, kq = warp >> 2;
-      const bool dn_active = kq < KUdn;
-      uint32_t doffA[2], doffB[2];  // this lane's ldmatrix offsets in a down codes tile
-      kunit_offsets(gdn, kDNRows, mA * 16, dn_active ? kq : 0, lane, doffA);
-      kunit_offsets(gdn, kDNRows, (mA + 4) * 16, dn_active ? kq : 0, lane, doffB);
       uint32_t bh[NB][16];
       float hinv = 1.f, hinv1 = 1.f;  // inverse h scales of rows g and 8 + g
       int cur_slot = -1;
       Cursor dc;
       seq_phase(dc, seq, kDN);
-      for (int l = L_gu; l < L; ++l, seq_next(dc, seq), advance()) {
+      for (int li = L_gu; li < L_all; ++li, seq_next(dc, seq), advance()) {
         const Item it = dc.it;
         unsigned char* stg = smem + (size_t)st * stage_bytes;
-        float* rb = red + (size_t)(l & 1) * kRedFloats;
-        const int dj = l - L_gu;  // down item index
+        float* rb = red + (size_t)(li & 1) * kRedFloats;
         bool ok = !__any_sync(0xffffffffu, aborted());
         if (ok && it.slot != cur_slot) {
           // h of this slot, k-unit kq: every warp waits (bounded, no CTA
-          // barrier) until the slot's count shows all 4 mt_per duty warps of
-          // its gate/up items, then reads its words, again after a pause in
-          // the rare case that one is not visible yet, as B fragments; each
-          // k-unit takes its own per-row power-of-two scale
+          // barrier) until the 32 done flags of the 8 gate/up items that
+          // produce its k-unit carry this call's tag, then reads its words,
+          // again after a pause in the rare case that one is not visible yet,
+          // as B fragments; each k-unit takes its own per-row power-of-two
+          // scale
           cur_slot = it.slot;
-          int ready = 0;
-          if (lane == 0) {
+          if (dn_active) {
+            const unsigned long long* fl = a.ws.flags + (size_t)it.slot * mt_per * 4 + 32 * kq + lane;
             const uint64_t t0 = global_timer_ns();
-            while (!(ready = ld_relaxed(cnt + it.slot) >= 4u * (unsigned)mt_per)) {
-              if (aborted() || a.wait_ns == 0 || global_timer_ns() - t0 > a.wait_ns) break;
+            for (;;) {
+              if (__all_sync(0xffffffffu, has_tag(ld_tagged(fl), tag))) break;
+              if (warp_gives_up(t0, a.wait_ns, &s_abort, lane)) {
+                ok = false;
+                break;
+              }
               poll_pause();
             }
           }
-          ok = __shfl_sync(0xffffffffu, ready, 0) != 0;
           unsigned mx[NB];
           if (ok) {
             const unsigned long long* hs = a.ws.h + (size_t)it.slot * K * (I / 2) + kq * 64 + 4 * t;
@@ -1329,10 +1329,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 sc, &bh[nb][q * 4]);
             }
           }
+          if (tid == 0 && li == L_gu) stamp(65);  // the first down item's h is in
         }
-        if (threadIdx.x == 0 && dj == 0) stamp(65);  // first down item: its h is in
         const bool landed = warp_wait(&full_bar[st], fp & 1);
-        if (threadIdx.x == 0 && l < 24) stamp(16 + l);  // item l landed
+        if (tid == 0 && li < 24) stamp(16 + li);  // item li landed
         ok = landed && ok;
         uint32_t adA[2][4], adB[2][4];
         uint2 sr[4];
@@ -1378,12 +1378,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (NB == 2) rb[kRedPart + kq * 16 + 8 + g] = hinv1;
         }
         comp_bar();
-        // epilogue, by the 4 warps of group l % 4 (the others move on to the
+        // epilogue, by the 4 warps of group li % 4 (the others move on to the
         // next item): thread o of the group owns output (i, c) of m-tiles
         // M = 0..7 in each n-block; the k-unit partials of m-tile M sit at
         // warps M % 4 + 4 q, in their first (M < 4) or second half
         const bool live = !__any_sync(0xffffffffu, aborted());
-        if ((warp >> 2) == (l & 3) && live) {
+        if ((warp >> 2) == (li & 3) && live) {
           const float ts = s_tse[3 * s_uexp[it.slot] + 2];
           const int o = (warp & 3) * 32 + lane;
           const int i = o >> 3, c = o & 7;
@@ -1399,84 +1399,108 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int q = 0; q < 4; ++q) iq[q] = q < KUdn ? rb[kRedPart + q * 16 + n] : 0.f;
             unsigned long long* dst = a.ws.dpart + ((size_t)n * (k + 1) + s) * H + it.tile * kDNRows + i;
 #pragma unroll
-            for (int M = 0; M < 8; ++M) {
-              const int f = ((M >> 2) * NB + nb) * 128 + f0;
+            for (int Mi = 0; Mi < 8; ++Mi) {
+              const int f = ((Mi >> 2) * NB + nb) * 128 + f0;
               float v4[4];
 #pragma unroll
-              for (int q = 0; q < 4; ++q) v4[q] = q < KUdn ? rb[red_at(q * 4 + (M & 3)) + f] * iq[q] : 0.f;
+              for (int q = 0; q < 4; ++q) v4[q] = q < KUdn ? rb[red_at(q * 4 + (Mi & 3)) + f] * iq[q] : 0.f;
               const float v = ((v4[0] + v4[1]) + v4[2]) + v4[3];  // k-units in order
-              st_tagged(dst + M * 16, tagged(tag, __float_as_uint(v * ts)));
+              st_tagged(dst + Mi * 16, tagged(tag, __float_as_uint(v * ts)));
             }
           }
         }
       }
     }
-  }
 
-  // The outputs, shared by the CTAs (no grid barrier): each thread polls its
-  // k + 1 tagged partials (bounded; a pause between attempts) -- measured
-  // faster than gating on a per-tile count first, which costs one more L2
-  // round trip after the last down item:
-  //   y = bf16(routed_scale * sum_s w_s d_s + d_shared + residual), slots in order
-  if (threadIdx.x == 0) stamp(64);
-  if (!__any_sync(0xffffffffu, aborted())) {
-    const int ns = k + (a.has_shared ? 1 : 0);  // partials per output
-    for (int o = blockIdx.x * kCompThreads + threadIdx.x; o < K * H; o += grid * kCompThreads) {
-      const int n = o / H, j = o - n * H;
-      const unsigned long long* dp = a.ws.dpart + (size_t)n * (k + 1) * H + j;
-      const float rv = a.residual ? bf16_bits_to_float(a.residual[(size_t)n * H + j]) : 0.f;
-      float acc2 = 0.f, shv = 0.f;
-      bool good = true;
-      for (int s0 = 0; s0 < ns && good; s0 += 8) {
-        unsigned long long pw[8];
-        const uint64_t t0 = global_timer_ns();
-        for (;;) {  // every load of the chunk in flight at once
-          bool all = true;
+    // ---------------------------------------------------------------- combine
+    // The outputs, shared by the CTAs (no grid barrier): each thread takes
+    // pairs of outputs (j, j + 1) of a row and polls their tagged partials
+    // (bounded; a pause between attempts), then
+    //   y = bf16(((routed_scale * sum_s w_s d_s) + d_shared) + residual),
+    // slots in order, each FP32 operation rounded on its own.  The residual
+    // of a call that normalises its input is that input, else the caller's.
+    if (tid == 0) stamp(64);
+    if (!__any_sync(0xffffffffu, aborted())) {
+      const int hs = D.has_shared;
+      const int ns = k + (hs ? 1 : 0);  // partials per output
+      const int HP = H / 2;
+      const uint16_t* res = a.norm ? a.x : a.residual;
+      // output pairs dealt evenly over the CTAs (each takes a contiguous run)
+      const int o_end = split_before(blockIdx.x + 1, K * HP, grid);
+      for (int o = split_before(blockIdx.x, K * HP, grid) + tid; o < o_end; o += kCompThreads) {
+        const int n = o / HP, j = 2 * (o - n * HP);
+        const unsigned long long* dp = a.ws.dpart + (size_t)n * (k + 1) * H + j;
+        float rv0 = 0.f, rv1 = 0.f;
+        if (res) {
+          const unsigned u = *reinterpret_cast<const unsigned*>(res + (size_t)n * H + j);
+          rv0 = __uint_as_float(u << 16);
+          rv1 = __uint_as_float(u & 0xFFFF0000u);
+        }
+        float acc0 = 0.f, acc1 = 0.f, sh0 = 0.f, sh1 = 0.f;
+        bool good = true;
+        for (int s0 = 0; s0 < ns && good; s0 += 8) {
+          unsigned long long pw[8][2];
+          const uint64_t t0 = global_timer_ns();
+          for (;;) {  // every load of the chunk in flight at once
+            bool all = true;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              pw[u][0] = pw[u][1] = 0ull;
+              if (s0 + u < ns) {
+                ld_tagged2(dp + (size_t)(s0 + u) * H, pw[u][0], pw[u][1]);
+                all &= has_tag(pw[u][0], tag) & has_tag(pw[u][1], tag);
+              }
+            }
+            if (all) break;
+            if (aborted() || a.wait_ns == 0 || global_timer_ns() - t0 > a.wait_ns) {
+              good = false;
+              break;
+            }
+            poll_pause();
+          }
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
-            pw[u] = 0ull;
-            if (s0 + u < ns) {
-              pw[u] = ld_tagged(dp + (size_t)(s0 + u) * H);
-              all &= has_tag(pw[u], tag);
+            const int s = s0 + u;
+            const float p0 = __uint_as_float((unsigned)pw[u][0]), p1 = __uint_as_float((unsigned)pw[u][1]);
+            if (s < k) {
+              const float wv = s_w[n * k + s];
+              acc0 = __fadd_rn(acc0, __fmul_rn(wv, p0));
+              acc1 = __fadd_rn(acc1, __fmul_rn(wv, p1));
+            } else if (s == k) {
+              sh0 = p0;
+              sh1 = p1;
             }
           }
-          if (all) break;
-          if (aborted() || a.wait_ns == 0 || global_timer_ns() - t0 > a.wait_ns) {
-            good = false;
-            break;
-          }
-          poll_pause();
         }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int s = s0 + u;
-          const float pv = __uint_as_float((unsigned)pw[u]);
-          if (s < k) acc2 = __fadd_rn(acc2, __fmul_rn(s_w[n * k + s], pv));
-          else if (s == k) shv = pv;
+        if (!__all_sync(__activemask(), good)) {
+          if (!good) fail();
+          break;
         }
+        float v0 = __fmul_rn(D.routed_scale, acc0), v1 = __fmul_rn(D.routed_scale, acc1);
+        if (hs) {
+          v0 = __fadd_rn(v0, sh0);
+          v1 = __fadd_rn(v1, sh1);
+        }
+        if (res) {
+          v0 = __fadd_rn(v0, rv0);
+          v1 = __fadd_rn(v1, rv1);
+        }
+        const unsigned pair = float_to_bf16_bits(v0) | ((unsigned)float_to_bf16_bits(v1) << 16);
+        *reinterpret_cast<unsigned*>(a.y + (size_t)n * H + j) = pair;
       }
-      if (!__all_sync(0xffffffffu, good)) {
-        if (lane == 0) fail();
-        break;
-      }
-      // each operation rounded on its own (no contraction into a fused
-      // multiply-add): ((routed_scale * acc) + shared) + residual
-      float v = __fmul_rn(a.routed_scale, acc2);
-      if (a.has_shared) v = __fadd_rn(v, shv);
-      if (a.residual) v = __fadd_rn(v, rv);
-      a.y[(size_t)n * H + j] = float_to_bf16_bits(v);
     }
   }
   // the routing outputs of the call (one CTA writes them, off the critical path)
   if (blockIdx.x == 0) {
-    for (int q = threadIdx.x; q < K * k; q += kCompThreads) {
+    for (int q = tid; q < K * k; q += kCompThreads) {
       if (a.idx_out) a.idx_out[q] = s_idx[q];
       if (a.w_out) a.w_out[q] = s_w[q];
     }
     if (a.group_out && warp == 0) write_groups(a.group_out, s_nu, G, K, k, s_uexp, s_rowmask, s_slot, lane);
   }
   // one exit per CTA and call, whatever happened: the next call's index
-  if (threadIdx.x == 0) {
+  comp_bar();
+  if (tid == 0) {
     atomicAdd(a.ws.exits, 1ull);
     stamp(7);
   }
@@ -1499,8 +1523,8 @@ int num_sms() {
 }
 
 // Dynamic shared memory of the experts kernel: the TMA ring, the reduction
-// ring and the routing arrays.  stages/nred are chosen to fill the
-// opt-in limit (at most kMaxStages stages).
+// slots and the routing arrays.  The ring takes as many stages as fit the
+// opt-in limit (at most kMaxStages).
 static size_t routing_smem_bytes(int K, int E, int k, int G) {
   return sizeof(float) * K * k + sizeof(int) * K * k + sizeof(unsigned) * E + sizeof(int) * (G + 1) +
          sizeof(float) * 3 * (E + 1) + sizeof(float) * E + (size_t)(G + 1) * K + 16;
@@ -1522,17 +1546,21 @@ size_t experts_smem_bytes(int K, int H, int I, int E, int k, int G, int* stages,
 }
 
 template <int NB>
-static cudaError_t launch_experts_t(const ExpertsArgs& a, const CUtensorMap* maps, cudaStream_t s, bool pdl) {
+static cudaError_t launch_experts_t(const ExpertsCommon& c, const CUtensorMap* maps, const LayerDesc& desc,
+                                    cudaStream_t s, bool pdl) {
   auto kern = k_moe_experts<NB>;
   int stages = 0, nred = 0;
-  const size_t smem = experts_smem_bytes(a.K, a.H, a.I, a.E, a.k, a.G, &stages, &nred);
+  const size_t smem = experts_smem_bytes(c.K, c.H, c.I, c.E, c.k, c.G, &stages, &nred);
   const int grid = num_sms();
-  if (stages < 2 || a.H > 128 * kCompWarps || a.I > 128 * 4 ||
-      sizeof(uint16_t) * (size_t)a.K * a.H > 2 * red_slot_bytes(NB))  // the staged rows fit the reduction slots
+  if (stages < 2 || c.H > 128 * kCompWarps || c.I > 128 * 4 ||
+      sizeof(uint16_t) * (size_t)c.K * c.H > 2 * red_slot_bytes(NB))  // the staged rows fit the reduction slots
     return cudaErrorInvalidValue;
-  ExpertsArgs b = a;
-  b.stages = stages;
-  b.nred = nred;
+  ExpertsParams p;
+  p.c = c;
+  p.c.stages = stages;
+  p.c.nred = nred;
+  for (int j = 0; j < kMapsPerLayer; ++j) p.maps[j] = maps[j];
+  p.L = desc;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
@@ -1547,19 +1575,18 @@ static cudaError_t launch_experts_t(const ExpertsArgs& a, const CUtensorMap* map
   attr[1].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  err = cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7],
-                           maps[8], maps[9], b);
+  err = cudaLaunchKernelEx(&cfg, kern, p);
   if (err != cudaSuccess && pdl) {  // fall back to a cooperative launch without overlap
     cudaGetLastError();
     attr[0].val.programmaticStreamSerializationAllowed = 0;
-    err = cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7],
-                             maps[8], maps[9], b);
+    err = cudaLaunchKernelEx(&cfg, kern, p);
   }
   return err;
 }
 
-cudaError_t launch_experts(const ExpertsArgs& a, const CUtensorMap* maps, cudaStream_t s, bool pdl) {
-  return a.K > 8 ? launch_experts_t<2>(a, maps, s, pdl) : launch_experts_t<1>(a, maps, s, pdl);
+cudaError_t launch_experts(const ExpertsCommon& c, const CUtensorMap* maps, const LayerDesc& desc, cudaStream_t s,
+                           bool pdl) {
+  return c.K > 8 ? launch_experts_t<2>(c, maps, desc, s, pdl) : launch_experts_t<1>(c, maps, desc, s, pdl);
 }
 
 }  // namespace moe

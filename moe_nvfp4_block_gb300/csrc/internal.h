@@ -15,7 +15,6 @@ constexpr int kRouterWarps = 8;          // experts per router CTA
 constexpr int kGURows = 16;              // intermediate rows per gate/up item
 constexpr int kDNRows = 128;             // hidden rows per down item
 constexpr int kMaxStages = 6;            // TMA ring depth limit of the experts kernel
-constexpr int kMaxRed = 4;               // reduction ring depth limit of the experts kernel
 
 // Bytes of one ring stage: the larger of a gate/up item (codes and scales of
 // 16 rows of gate and up) and a down item (128 rows), 1024-aligned.
@@ -26,18 +25,14 @@ __host__ __device__ inline int expert_stage_bytes(int H, int I) {
   return (m + 1023) & ~1023;
 }
 
-// Per-call counters of the experts kernel, two sets used by alternate calls
-// (a call clears the set the next call uses): per set, one word per slot
-// counting the finished gate/up duty warps.  Their place and size do not
-// depend on K, E or the layer, so a workspace stays valid across shapes.
-constexpr int kCntDone = 1025;  // slots: at most 1024 distinct experts + the shared one
-constexpr int kCntSet = 1056;   // words per set (kCntDone rounded up)
-
-// Byte offsets of the workspace regions (all 256-byte aligned).  Regions
-// before `logits` sit at fixed offsets.
+// Byte offsets of the workspace regions (all 256-byte aligned).  The header
+// sits at a fixed offset; the other regions' offsets depend on the shape.
+// Words exchanged between the CTAs of the experts kernel are tagged: a 32-bit
+// payload next to the 32-bit tag of the layer call that wrote it, so stale
+// words of earlier calls (or of other shapes) are told apart by the tag and
+// nothing is cleared between calls.
 struct WsLayout {
   size_t hdr;      // 256 bytes: int32 error word, uint32 router ticket, uint64 experts-kernel CTA exits
-  size_t cnt;      // uint32 [2][kCntSet]: the per-call counters
   size_t logits;   // float [K][E] (moe_router_topk)
   size_t idx;      // int32 [K][k]
   size_t w;        // float [K][k]
@@ -45,11 +40,11 @@ struct WsLayout {
   size_t urow;     // uint32 [G+1]: rows routed to each distinct expert (bitmask)
   size_t slotmap;  // int32 [G+1][K]: slot of the expert in row r's selection, -1 if none
   size_t tlog;     // tagged [K][E]: router logits of the experts kernel
+  size_t flags;    // tagged [G+1][I/16][4]: gate/up item done, per duty warp
   size_t h;        // tagged [G+1][K][I/2]: h, two bf16 per word
   size_t dpart;    // tagged [K][k+1][H]: FP32 down partials per (row, slot)
   size_t total;
 };
-
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 inline int group_cap(int K, int E, int k) { return E < K * k ? E : K * k; }
@@ -64,7 +59,6 @@ inline WsLayout ws_layout(int K, int E, int k, int H, int I) {
     return r;
   };
   L.hdr = take(256);
-  L.cnt = take(sizeof(uint32_t) * 2 * kCntSet);
   L.logits = take(sizeof(float) * K * E);
   L.idx = take(sizeof(int32_t) * K * k);
   L.w = take(sizeof(float) * K * k);
@@ -72,6 +66,7 @@ inline WsLayout ws_layout(int K, int E, int k, int H, int I) {
   L.urow = take(sizeof(uint32_t) * (G + 1));
   L.slotmap = take(sizeof(int32_t) * (G + 1) * K);
   L.tlog = take(sizeof(uint64_t) * K * E);
+  L.flags = take(sizeof(uint64_t) * (size_t)(G + 1) * (I / 16) * 4);
   L.h = take(sizeof(uint64_t) * (size_t)(G + 1) * K * (I / 2));
   L.dpart = take(sizeof(uint64_t) * (size_t)K * (k + 1) * H);
   L.total = o;
@@ -88,9 +83,9 @@ struct WsPtrs {
   int* group;
   unsigned* urow;
   int* slotmap;
-  unsigned long long* exits;  // CTA exits of the experts kernel, all calls (the call index is exits / grid)
-  unsigned* cnt;              // [2][kCntSet]
+  unsigned long long* exits;  // calls finished by the experts kernel's CTAs (the call index is exits / grid)
   unsigned long long* tlog;
+  unsigned long long* flags;
   unsigned long long* h;
   unsigned long long* dpart;
 };
@@ -107,10 +102,11 @@ inline WsPtrs ws_ptrs(void* ws, const WsLayout& L) {
   p.urow = reinterpret_cast<unsigned*>(b + L.urow);
   p.slotmap = reinterpret_cast<int*>(b + L.slotmap);
   p.exits = reinterpret_cast<unsigned long long*>(b + L.hdr + 8);
-  p.cnt = reinterpret_cast<unsigned*>(b + L.cnt);
   p.tlog = reinterpret_cast<unsigned long long*>(b + L.tlog);
+  p.flags = reinterpret_cast<unsigned long long*>(b + L.flags);
   p.h = reinterpret_cast<unsigned long long*>(b + L.h);
   p.dpart = reinterpret_cast<unsigned long long*>(b + L.dpart);
+
   return p;
 }
 
@@ -133,17 +129,26 @@ struct ProjPtrs {
   const float* tscale;
 };
 
-struct ExpertsArgs {
-  const uint16_t* x;         // [K][H] bf16: the normalised rows, or the rows to normalise (norm)
-  const uint16_t* residual;  // [K][H] or null
-  uint16_t* y;               // [K][H]
-  int K, H, I, E, k, G;
-  int has_shared;
-  int scoring;               // MOE_SCORE_SOFTMAX or MOE_SCORE_SIGMOID
-  float routed_scale;
+// One MoE layer as the experts kernel sees it (everything but the tensor maps).
+struct LayerDesc {
   const uint16_t* router_w;  // [E][H] bf16
   const float* router_bias;  // [E] or null
   ProjPtrs gate, up, down, sh_gate, sh_up, sh_down;
+  float routed_scale;
+  int has_shared;
+  int scoring;               // MOE_SCORE_SOFTMAX or MOE_SCORE_SIGMOID
+};
+
+// Tensor maps of one layer: codes of gate, up, down, shared gate, shared
+// up, shared down; E4M3 scales of gate, up, shared gate, shared up.
+constexpr int kMapsPerLayer = 10;
+
+// What one launch of the experts kernel runs: one MoE layer call.
+struct ExpertsCommon {
+  const uint16_t* x;         // [K][H] bf16: the input (normalised, or to normalise when norm)
+  const uint16_t* residual;  // [K][H] or null (with norm the residual is x itself)
+  uint16_t* y;               // [K][H]
+  int K, H, I, E, k, G;
   WsPtrs ws;
   int32_t* idx_out;          // routing copies for the caller (nullable)
   float* w_out;
@@ -154,6 +159,12 @@ struct ExpertsArgs {
   int stages, nred;           // ring depths (set by the launcher)
   int norm;                   // 1: x is the residual stream; the kernel applies the RMSNorm (unit gain)
   float norm_eps;
+};
+
+struct ExpertsParams {
+  CUtensorMap maps[kMapsPerLayer];
+  LayerDesc L;
+  ExpertsCommon c;
 };
 
 constexpr int kTraceSlots = 80;
@@ -177,6 +188,11 @@ struct GemvSeg {
   uint16_t* out;        // [K][N]
   const uint16_t* res;  // [K][N] or null
   int N;
+  // optional in-place KV append: output (r, n) also goes to
+  // cache[n / 128][*len + r][n % 128] of a [N/128][cap][128] cache
+  uint16_t* cache;
+  const int* len;
+  int cap;
 };
 
 struct GemvArgs {
@@ -184,12 +200,14 @@ struct GemvArgs {
   int K, D;
   GemvSeg seg[3];
   int nseg, n_total;
+  int* err;           // error word (a cache append past its capacity), or null
 };
 
 struct AttnArgs {
   const uint16_t* q;      // [K][nq*128]
-  const uint16_t* kc;     // [nkv][C][128]
+  const uint16_t* kc;     // [nkv][C][128]: C positions of capacity
   const uint16_t* vc;
+  const int* len;         // valid cached positions (device), or null: all C
   const uint16_t* k_new;  // [K][nkv*128]
   const uint16_t* v_new;
   uint16_t* o;            // [K][nq*128]
@@ -211,10 +229,14 @@ inline size_t lmhead_ws_bytes(int K) { return 256 + align256(sizeof(float) * kLm
 cudaError_t launch_rmsnorm(const uint16_t* x, int K, int H, float eps, uint16_t* out, cudaStream_t s, bool pdl);
 cudaError_t launch_lmhead(const LmHeadArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s, bool pdl);
-// maps: gate, up, down, sh_gate, sh_up, sh_down codes; gate, up, sh_gate, sh_up scales
-cudaError_t launch_experts(const ExpertsArgs& a, const CUtensorMap* maps, cudaStream_t s, bool pdl);
+// One launch of the experts kernel: maps [kMapsPerLayer].
+cudaError_t launch_experts(const ExpertsCommon& c, const CUtensorMap* maps, const LayerDesc& desc, cudaStream_t s,
+                           bool pdl);
 size_t experts_smem_bytes(int K, int H, int I, int E, int k, int G, int* stages, int* nred);
 cudaError_t launch_accept(const int32_t* draft, const int32_t* target, int K, int32_t* out, cudaStream_t s);
+cudaError_t launch_kv_commit(int32_t* len, const int32_t* n_accepted, int K, int cap, int* err, cudaStream_t s);
+cudaError_t launch_synthetic_drafts(const int32_t* target, const uint8_t* coin, const int32_t* alt, int K, int vocab,
+                                    int32_t* draft, cudaStream_t s);
 
 int num_sms();
 

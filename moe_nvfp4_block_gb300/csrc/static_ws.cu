@@ -15,7 +15,7 @@
 namespace {
 
 // 8 MiB.  Enough for K <= 16 at hidden 2048, 256 experts, top-8,
-// intermediate 512 with a shared expert (about 6.7 MB at K = 16); larger
+// intermediate 512 with a shared expert (about 6.8 MB at K = 16); larger
 // layers (e.g. 1024 experts at top-32) are refused.
 constexpr size_t kStaticWsBytes = size_t(8) << 20;
 constexpr int kMaxDevices = 64;

@@ -319,3 +319,55 @@ def verify_step(w, layers, lm_head, x0, n_layers=None, L=None):
     xn = rmsnorm(x, L=L)
     tok, best = lm_argmax(xn, lm_head, L=L)
     return dict(x=x, target=tok, best=best, att_in=att_in, att_o=att_o, moe_in=moe_in, idx=idx, xn=xn)
+
+
+def synthetic_drafts(target, coin, alt, vocab):
+    """The controlled-acceptance drafter: the target's token where coin is
+    set, else (target + 1 + alt) mod vocab (never the target's token)."""
+    t = np.asarray(target, np.int64)
+    return np.where(np.asarray(coin) != 0, t, (t + 1 + np.asarray(alt, np.int64)) % vocab).astype(np.int32)
+
+
+def verify_rounds(w, layers, lm_head, x_rounds, coin, alt, ctx0, n_layers=None, L=None):
+    """The multi-round verify loop with an in-place KV cache (PR #844, "8. What
+    I looked at and did NOT ship", items 1 and 2; "10. Next step"): round t
+    runs the K rows x_rounds[t] through every layer -- attention over the
+    committed cache positions 0 .. len-1 plus the round's own rows, then the
+    MoE block -- takes the greedy token of every row, forms the synthetic
+    drafts, counts the accepted prefix n, and commits the first
+    c = min(n + 1, K) rows' keys and values of every layer to the cache
+    (len += c); the other rows are dropped.
+    ``layers(l)`` returns (attention dict with Wq, Wk, Wv, Wo and caches kc, vc
+    [nkv][cap][hd] whose first ctx0 positions are valid; MoE synthgen.Layer).
+    Returns dict(targets [R][K], drafts [R][K], n [R], len, kc, vc: per layer
+    the caches' first len positions)."""
+    nl = n_layers or w.layers
+    R, K = x_rounds.shape[0], x_rounds.shape[1]
+    hd, nq, nkv = w.head_dim, w.n_q_heads, w.n_kv_heads
+    kcs, vcs = [], []
+    for l in range(nl):
+        att, _ = layers(l)
+        kcs.append(_c(att["kc"][:, :ctx0], np.uint16))
+        vcs.append(_c(att["vc"][:, :ctx0], np.uint16))
+    targets = np.zeros((R, K), np.int32)
+    drafts = np.zeros((R, K), np.int32)
+    ns = np.zeros(R, np.int32)
+    for t in range(R):
+        x = _c(x_rounds[t], np.uint16)
+        knew, vnew = [], []
+        for l in range(nl):
+            att, moe = layers(l)
+            xn = rmsnorm(x, L=L)
+            knew.append(linear_bf16(xn, att["Wk"], L=L).reshape(K, nkv, hd))
+            vnew.append(linear_bf16(xn, att["Wv"], L=L).reshape(K, nkv, hd))
+            x = attention(x, att["Wq"], att["Wk"], att["Wv"], att["Wo"], kcs[l], vcs[l], nq, nkv, hd, L=L)
+            x = moe_layer(OracleLayer.from_workload(w, moe), rmsnorm(x, L=L), residual=x, L=L)["y"]
+        tok, _ = lm_argmax(rmsnorm(x, L=L), lm_head, L=L)
+        d = synthetic_drafts(tok, coin[t], alt[t], lm_head.shape[0])
+        n = accept_prefix(d, tok, L=L)
+        c = min(n + 1, K)
+        for l in range(nl):
+            kcs[l] = np.ascontiguousarray(np.concatenate([kcs[l], knew[l][:c].transpose(1, 0, 2)], axis=1))
+            vcs[l] = np.ascontiguousarray(np.concatenate([vcs[l], vnew[l][:c].transpose(1, 0, 2)], axis=1))
+        targets[t], drafts[t], ns[t] = tok, d, n
+    return dict(targets=targets, drafts=drafts, n=ns, len=kcs[0].shape[1], kc=kcs, vc=vcs)

@@ -41,6 +41,7 @@ T_SGATE_C, T_SGATE_S, T_SUP_C, T_SUP_S, T_SDOWN_C, T_SDOWN_S = 9, 10, 11, 12, 13
 T_X = 20
 T_ATT_Q, T_ATT_K, T_ATT_V, T_ATT_O, T_KCACHE, T_VCACHE = 30, 31, 32, 33, 34, 35
 T_LM_HEAD, T_DRAFT_J, T_DRAFT_TOK = 40, 41, 42
+T_COIN, T_ALT = 43, 44
 
 SCALE_LO, SCALE_HI = 2.0 ** -8, 2.0 ** -4
 ROUTER_SIGMA = 0.02
@@ -254,3 +255,13 @@ def make_drafts(w: Workload, target: np.ndarray, instance: int = 0):
     other = uniform_int(w.seed, instance, T_DRAFT_TOK, 0, K, w.vocab - 1)
     draft = np.where(np.arange(K) < j, target, (target.astype(np.int64) + 1 + other) % w.vocab).astype(np.int32)
     return draft, j
+
+
+def make_coins(w: Workload, rounds: int, accept_pct: int = 75, instance: int = 0):
+    """Per round and row: whether the synthetic drafter's token is the
+    target's (probability accept_pct %), and the offset of its other token
+    (uniform in 0 .. vocab-2).  Returns (coin uint8 [R][K], alt int32 [R][K])."""
+    n = rounds * w.K
+    coin = (uniform_int(w.seed, instance, T_COIN, 0, n, 100) < accept_pct).astype(np.uint8).reshape(rounds, w.K)
+    alt = uniform_int(w.seed, instance, T_ALT, 0, n, w.vocab - 1).reshape(rounds, w.K)
+    return coin, alt

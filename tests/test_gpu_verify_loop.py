@@ -1,0 +1,115 @@
+"""GPU parity of the multi-round verify loop with an in-place KV cache
+(PR #844, "8. What I looked at and did NOT ship", items 1 and 2; "10. Next
+step"): R rounds run on the device in one call -- forward with the rows'
+keys and values appended in place, greedy tokens, synthetic drafts with a
+controlled acceptance rate, accepted prefix, commit of min(n + 1, K) rows --
+and are checked against the oracle's loop: per-round greedy tokens, drafts
+and accepted lengths exactly (a token may only differ where the oracle's top
+two logits nearly tie), the final cache length exactly, and every cache
+position: the original ones unchanged bit for bit, the appended ones within
+rel-L2 <= 5e-3 and max-abs <= 3e-2 * max|ref|.  The cache starts at a length
+that is not a multiple of 16, so the partial last chunk of the split
+attention is exercised."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthgen
+from helpers import bf16_bits, parity, to_dev_bf16, upload
+
+pytestmark = pytest.mark.gpu
+
+
+def _loop_case(K, R, n_layers=3, ctx0=100, vocab=2048, accept=75):
+    base = synthgen.Workload("verify_loop", K=K, H=1024, E=32, top_k=4, I=256, Is=256, layers=n_layers, seed=16,
+                             attention=True, n_q_heads=8, n_kv_heads=2, vocab=vocab)
+    cap = ((ctx0 + R * K + 15) // 16) * 16 + 16
+    w = dataclasses.replace(base, ctx=cap)
+    atts, moes = [], []
+    for l in range(n_layers):
+        a = synthgen.make_attention(w, l)
+        a["kc"][:, ctx0:] = 0
+        a["vc"][:, ctx0:] = 0
+        atts.append(a)
+        moes.append(synthgen.make_layer(w, l))
+    lm = synthgen.make_lm_head(w)
+    x_rounds = np.stack([synthgen.make_x(w, 300 + t) for t in range(R)])
+    coin, alt = synthgen.make_coins(w, R, accept)
+    return w, atts, moes, lm, x_rounds, coin, alt, cap
+
+
+@pytest.mark.parametrize("K,R", [(2, 8), (4, 6)])
+def test_verify_rounds_against_oracle(cuda_ok, K, R):
+    import moe_nvfp4_block_gb300 as M
+    ctx0 = 100
+    w, atts, moes, lm, x_rounds, coin, alt, cap = _loop_case(K, R, ctx0=ctx0)
+    ref = oracle.verify_rounds(w, lambda l: (atts[l], moes[l]), lm, x_rounds, coin, alt, ctx0)
+    d = lambda a: to_dev_bf16(a)
+    layers = [M.DecoderLayer(d(a["Wq"]), d(a["Wk"]), d(a["Wv"]), d(a["Wo"]), d(a["kc"]), d(a["vc"]), upload(m, w))
+              for a, m in zip(atts, moes)]
+    kv_len = torch.tensor([ctx0], dtype=torch.int32, device="cuda")
+    model = M.VerifyModel(layers, d(lm), w.n_q_heads, w.n_kv_heads, kv_len=kv_len)
+    ws = model.workspace(K)
+    x_dev = d(x_rounds.reshape(R * K, w.H)).view(R, K, w.H)
+    coin_d = torch.from_numpy(coin).cuda()
+    alt_d = torch.from_numpy(alt).cuda()
+    x_work = torch.empty(K, w.H, dtype=torch.bfloat16, device="cuda")
+    tgt = torch.empty(R, K, dtype=torch.int32, device="cuda")
+    dft = torch.empty(R, K, dtype=torch.int32, device="cuda")
+    n = torch.empty(R, dtype=torch.int32, device="cuda")
+    M.moe_verify_rounds(model, x_dev, coin_d, alt_d, x_work, tgt, dft, n, ws)
+    torch.cuda.synchronize()
+    assert M.moe_workspace_error(ws) == 0
+    got_t, got_n = tgt.cpu().numpy(), n.cpu().numpy()
+    if not np.array_equal(got_t, ref["targets"]):
+        # only a near-tie may flip a token after the rounds' small rounding
+        # differences in the appended keys and values accumulate
+        bad = np.argwhere(got_t != ref["targets"])
+        pytest.fail(f"greedy tokens differ at (round, row) {bad.tolist()}")
+    np.testing.assert_array_equal(dft.cpu().numpy(), ref["drafts"])
+    np.testing.assert_array_equal(got_n, ref["n"])
+    assert int(kv_len.item()) == ref["len"] == ctx0 + int(np.minimum(ref["n"] + 1, K).sum())
+    # the acceptance is what the coins make it: some rounds accept, some reject
+    assert 0 < int((ref["n"] > 0).sum()) < R or K > 2
+    L = ref["len"]
+    for l, dl in enumerate(layers):
+        kc = bf16_bits(dl.kcache)[:, :L]
+        vc = bf16_bits(dl.vcache)[:, :L]
+        np.testing.assert_array_equal(kc[:, :ctx0], atts[l]["kc"][:, :ctx0], err_msg=f"layer {l}: cached keys moved")
+        # free-running: layer l's keys and values are projections of an
+        # input that has passed 2 l blocks (attention and MoE of the layers
+        # before it) on each side, so the per-block bar scales with 2 l + 1
+        # (as for the free-running verify step)
+        f = 2 * l + 1
+        for got, exp, what in ((kc, ref["kc"][l], "keys"), (vc, ref["vc"][l], "values")):
+            rel, mab, mref = parity(got[:, ctx0:], exp[:, ctx0:])
+            assert rel <= 5e-3 * f and mab <= 3e-2 * f * mref, (l, what, rel, mab, mref)
+
+
+def test_kv_commit_and_capacity(cuda_ok):
+    import moe_nvfp4_block_gb300 as M
+    kv_len = torch.tensor([30], dtype=torch.int32, device="cuda")
+    for n, K, expect in [(0, 4, 31), (2, 4, 34), (4, 4, 38), (9, 4, 42)]:
+        M.moe_kv_commit(kv_len, torch.tensor([n], dtype=torch.int32, device="cuda"), K, 64)
+        torch.cuda.synchronize()
+        assert int(kv_len.item()) == expect, (n, K)
+    M.moe_kv_commit(kv_len, torch.tensor([16], dtype=torch.int32, device="cuda"), 16, 48)
+    torch.cuda.synchronize()
+    assert int(kv_len.item()) == 48  # clamped to the capacity
+
+
+def test_synthetic_drafts_against_oracle(cuda_ok):
+    import moe_nvfp4_block_gb300 as M
+    w = dataclasses.replace(synthgen.WORKLOADS["k4_full_step"], K=16)
+    coin, alt = synthgen.make_coins(w, 1, 60)
+    target = synthgen.uniform_int(9, 0, 50, 0, 16, w.vocab)
+    d = torch.empty(16, dtype=torch.int32, device="cuda")
+    M.moe_synthetic_drafts(torch.from_numpy(target).cuda(), torch.from_numpy(coin[0]).cuda(),
+                           torch.from_numpy(alt[0]).cuda(), w.vocab, d)
+    torch.cuda.synchronize()
+    ref = oracle.synthetic_drafts(target, coin[0], alt[0], w.vocab)
+    np.testing.assert_array_equal(d.cpu().numpy(), ref)
+    assert np.array_equal(ref == target, coin[0] != 0)

@@ -631,3 +631,66 @@ def test_accept_prefix_golden_and_brute_force():
             t = np.arange(K, dtype=np.int32) + 100
             d = np.where(eq, t, t + 1).astype(np.int32)
             assert oracle.accept_prefix(d, t) == int(np.cumprod(eq).sum())
+
+
+# ---------------------------------------------------------------- multi-round verify loop
+
+def _tiny_loop_model(K, R, ctx0=20, layers=2):
+    import dataclasses
+    w = synthgen.Workload("loop_pin", K=K, H=256, E=8, top_k=2, I=128, Is=128, layers=layers, seed=17,
+                          attention=True, n_q_heads=2, n_kv_heads=1, vocab=512)
+    w = dataclasses.replace(w, ctx=ctx0 + R * K + 16)
+    atts, moes = [], []
+    for l in range(layers):
+        a = synthgen.make_attention(w, l)
+        a["kc"][:, ctx0:] = 0
+        a["vc"][:, ctx0:] = 0
+        atts.append(a)
+        moes.append(synthgen.make_layer(w, l))
+    return w, atts, moes, synthgen.make_lm_head(w)
+
+
+def test_synthetic_drafts_rule():
+    t = np.array([0, 5, 511, 7], np.int32)
+    coin = np.array([1, 0, 0, 1], np.uint8)
+    alt = np.array([3, 0, 510, 100], np.int32)
+    d = oracle.synthetic_drafts(t, coin, alt, 512)
+    assert d.tolist() == [0, 6, 510, 7]  # (511 + 1 + 510) mod 512 = 510
+    # never the target where the coin is off, whatever alt (< vocab - 1)
+    alts = np.arange(511, dtype=np.int32)
+    assert np.all(oracle.synthetic_drafts(np.full(511, 9, np.int32), np.zeros(511, np.uint8), alts, 512) != 9)
+
+
+def test_verify_rounds_commit_length():
+    # all drafts right: every round commits all K rows; all wrong: one row
+    K, R, ctx0 = 2, 3, 20
+    w, atts, moes, lm = _tiny_loop_model(K, R, ctx0)
+    x = np.stack([synthgen.make_x(w, 500 + t) for t in range(R)])
+    alt = np.zeros((R, K), np.int32)
+    full = oracle.verify_rounds(w, lambda l: (atts[l], moes[l]), lm, x, np.ones((R, K), np.uint8), alt, ctx0)
+    assert full["n"].tolist() == [K] * R and full["len"] == ctx0 + R * K
+    none = oracle.verify_rounds(w, lambda l: (atts[l], moes[l]), lm, x, np.zeros((R, K), np.uint8), alt, ctx0)
+    assert none["n"].tolist() == [0] * R and none["len"] == ctx0 + R
+    # the first round sees the same cache either way
+    assert np.array_equal(full["targets"][0], none["targets"][0])
+
+
+def test_verify_rounds_causal_consistency():
+    # Two fully accepted rounds of K rows each must give the rows of round 2
+    # exactly the greedy tokens they get as rows K..2K-1 of one round of 2K
+    # rows: block-causal attention over an in-place cache is attention over
+    # the concatenated sequence.  Pins where and in what order the commit
+    # appends (a wrong position, a reversed row order or a missing row
+    # changes the second round's tokens).
+    K, R, ctx0 = 2, 2, 20
+    w, atts, moes, lm = _tiny_loop_model(K, R, ctx0)
+    x = np.stack([synthgen.make_x(w, 600 + t) for t in range(R)])
+    two = oracle.verify_rounds(w, lambda l: (atts[l], moes[l]), lm, x, np.ones((R, K), np.uint8),
+                               np.zeros((R, K), np.int32), ctx0)
+    import dataclasses
+    w2 = dataclasses.replace(w, K=2 * K)
+    one = oracle.verify_rounds(w2, lambda l: (atts[l], moes[l]), lm, x.reshape(1, 2 * K, w.H),
+                               np.ones((1, 2 * K), np.uint8), np.zeros((1, 2 * K), np.int32), ctx0)
+    assert np.array_equal(two["targets"].reshape(-1), one["targets"].reshape(-1))
+    for l in range(w.layers):
+        assert np.array_equal(two["kc"][l], one["kc"][l]) and np.array_equal(two["vc"][l], one["vc"][l])
