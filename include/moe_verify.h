@@ -263,6 +263,31 @@ moe_status moe_lm_head_argmax(const uint16_t* x_norm, int K, int H, const uint16
                               float* best_logit, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Position handling of an attention block (README, "Why this challenge
+ * exists": Laguna alternates three sliding-window layers -- 512-token
+ * window, plain RoPE at theta 10000 -- with one full-attention layer per
+ * block of four -- YaRN rotary with a 0.5 partial-rotary factor).
+ *   window       a row at position p sees positions p - window + 1 .. p
+ *                (0: every position); at least 16 when set
+ *   rotary_dim   RoPE on the first rotary_dim dims of every q and new-key
+ *                head (pairs i, i + rotary_dim/2, "rotate half"), at
+ *                positions C .. C+K-1 (C = the valid cache length); 0 = none
+ *   rope_theta   RoPE base: pair i turns by p * theta^(-2i/rotary_dim)
+ *   yarn_factor  > 1: YaRN frequencies (NTK-by-parts ramp between 1 and 32
+ *                rotations over yarn_orig_ctx positions, interpolation by
+ *                yarn_factor below it) and logits scaled by
+ *                (0.1 ln yarn_factor + 1)^2; <= 1: plain RoPE
+ * The cached keys are taken as already rotated (a cache stores rotated keys).
+ */
+typedef struct {
+  int window;
+  int rotary_dim;
+  float rope_theta;
+  float yarn_factor;
+  int yarn_orig_ctx;
+} moe_attn_pos;
+
+/*
  * GQA attention block of the verify step (README, "Why this challenge
  * exists": GQA with 8 KV heads at head_dim 128; the verify forward runs all
  * K drafted rows at once):
@@ -281,18 +306,33 @@ moe_status moe_lm_head_argmax(const uint16_t* x_norm, int K, int H, const uint16
  *     of capacity; an append past C is refused and recorded as
  *     MOE_ERR_CAPACITY in the workspace error word).  The length itself is
  *     not changed here: moe_kv_commit counts the accepted rows in.
- *   k_new_out, v_new_out: optional [K][nkv*128] copies of the new keys and
- *   values; o_out: optional [K][nq*128] copy of the attention output o
- *   (before the o-projection).
- * Envelope: head_dim 128, nq even, nq % nkv == 0, K * nq/nkv <= 16, H a
- * multiple of 256 up to 4096, nq*128 <= 4096, C a multiple of 16.
+ *   pos: NULL, or the window / rotary embedding of the block (moe_attn_pos).
+ *   k_new_out, v_new_out: optional [K][nkv*128] copies of the new (rotated)
+ *   keys and values; o_out: optional [K][nq*128] copy of the attention
+ *   output o (before the o-projection).
+ * Envelope: head_dim 128, nq even, nq % nkv == 0, K * nq/nkv <= 64, H a
+ * multiple of 256 up to 4096, nq*128 <= 8192, K * nq <= 768, C a multiple
+ * of 16.
  */
 size_t moe_attention_workspace_size(int K, int H, int nq, int nkv, int head_dim);
 moe_status moe_attention_block(const uint16_t* x, int K, int H, int nq, int nkv, int head_dim, int C,
                                const uint16_t* Wq, const uint16_t* Wk, const uint16_t* Wv, const uint16_t* Wo,
-                               uint16_t* kcache, uint16_t* vcache, const int32_t* kv_len, float eps,
-                               uint16_t* x_out, uint16_t* k_new_out, uint16_t* v_new_out, uint16_t* o_out,
-                               void* ws, size_t ws_bytes, void* stream);
+                               uint16_t* kcache, uint16_t* vcache, const int32_t* kv_len, const moe_attn_pos* pos,
+                               float eps, uint16_t* x_out, uint16_t* k_new_out, uint16_t* v_new_out,
+                               uint16_t* o_out, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * The dense SwiGLU MLP block of Laguna's layer 0 (README, "Why this
+ * challenge exists": layer 0 has a dense MLP, intermediate 8192, bf16):
+ *   xn = rmsnorm(x);  h = bf16( silu(xn . Wg^T) * (xn . Wu^T) )
+ *   x_out = bf16( x + h . Wd^T )      (FP32 accumulation)
+ *   x, x_out bf16 [K][H] (may alias); Wg, Wu [I][H]; Wd [H][I]; I a
+ *   multiple of 256, K * I <= 98304.
+ */
+size_t moe_dense_mlp_workspace_size(int K, int H, int I);
+moe_status moe_dense_mlp_block(const uint16_t* x, int K, int H, int I, const uint16_t* Wg, const uint16_t* Wu,
+                               const uint16_t* Wd, float eps, uint16_t* x_out, void* ws, size_t ws_bytes,
+                               void* stream);
 
 /*
  * The full verify step of a decoder with GQA attention and MoE blocks:
@@ -308,6 +348,12 @@ typedef struct {
   const uint16_t *Wq, *Wk, *Wv, *Wo;  /* bf16 attention projections (see moe_attention_block) */
   uint16_t *kcache, *vcache;          /* bf16 [nkv][ctx][128] */
   moe_layer moe;                      /* the MoE block of the layer */
+  int n_q_heads;                      /* 0: the model's n_q_heads */
+  moe_attn_pos pos;                   /* all zero: no window, no rotary embedding */
+  const uint16_t *mlp_gate, *mlp_up, *mlp_down;  /* non-NULL: a dense SwiGLU MLP block
+                                         (moe_dense_mlp_block, intermediate mlp_inter)
+                                         instead of the MoE block */
+  int mlp_inter;
 } moe_decoder_layer;
 
 typedef struct {

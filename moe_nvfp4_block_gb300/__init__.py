@@ -35,7 +35,7 @@ EXPORTS = ("moe_verify_layer_workspace_size", "moe_router_topk", "moe_group_ints
            "moe_attention_workspace_size", "moe_attention_block", "moe_verify_layer_static",
            "moe_verify_step_workspace_size", "moe_verify_step", "moe_workspace_error", "moe_status_string",
            "moe_debug_set_wait_limit_ns", "moe_debug_set_trace", "moe_debug_partials_offset", "moe_kv_commit",
-           "moe_synthetic_drafts", "moe_verify_rounds")
+           "moe_synthetic_drafts", "moe_verify_rounds", "moe_dense_mlp_workspace_size", "moe_dense_mlp_block")
 
 
 class MoeError(RuntimeError):
@@ -60,9 +60,16 @@ MOE_SCORE_SOFTMAX = 0
 MOE_SCORE_SIGMOID = 1
 
 
+class moe_attn_pos(ctypes.Structure):
+    _fields_ = [("window", ctypes.c_int), ("rotary_dim", ctypes.c_int), ("rope_theta", ctypes.c_float),
+                ("yarn_factor", ctypes.c_float), ("yarn_orig_ctx", ctypes.c_int)]
+
+
 class moe_decoder_layer(ctypes.Structure):
     _fields_ = [("Wq", ctypes.c_void_p), ("Wk", ctypes.c_void_p), ("Wv", ctypes.c_void_p), ("Wo", ctypes.c_void_p),
-                ("kcache", ctypes.c_void_p), ("vcache", ctypes.c_void_p), ("moe", moe_layer)]
+                ("kcache", ctypes.c_void_p), ("vcache", ctypes.c_void_p), ("moe", moe_layer),
+                ("n_q_heads", ctypes.c_int), ("pos", moe_attn_pos), ("mlp_gate", ctypes.c_void_p),
+                ("mlp_up", ctypes.c_void_p), ("mlp_down", ctypes.c_void_p), ("mlp_inter", ctypes.c_int)]
 
 
 class moe_verify_model(ctypes.Structure):
@@ -100,8 +107,12 @@ def _load():
     L.moe_attention_workspace_size.restype = sz
     L.moe_attention_workspace_size.argtypes = [ci, ci, ci, ci, ci]
     L.moe_attention_block.restype = ci
-    L.moe_attention_block.argtypes = [vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp,
-                                      vp, vp, vp, vp, sz, vp]
+    L.moe_attention_block.argtypes = [vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float,
+                                      vp, vp, vp, vp, vp, sz, vp]
+    L.moe_dense_mlp_workspace_size.restype = sz
+    L.moe_dense_mlp_workspace_size.argtypes = [ci, ci, ci]
+    L.moe_dense_mlp_block.restype = ci
+    L.moe_dense_mlp_block.argtypes = [vp, ci, ci, ci, vp, vp, vp, ctypes.c_float, vp, vp, sz, vp]
     mp = ctypes.POINTER(moe_verify_model)
     L.moe_verify_step_workspace_size.restype = sz
     L.moe_verify_step_workspace_size.argtypes = [mp, ci]
@@ -284,27 +295,51 @@ def attention_workspace(K, H, nq, nkv, head_dim=128, device="cuda") -> torch.Ten
     return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
+def attn_pos(window=0, rotary_dim=0, rope_theta=10000.0, yarn_factor=1.0, yarn_orig_ctx=0) -> moe_attn_pos:
+    return moe_attn_pos(window, rotary_dim, rope_theta, yarn_factor, yarn_orig_ctx)
+
+
 def moe_attention_block(x, Wq, Wk, Wv, Wo, kcache, vcache, x_out, ws, nq, nkv, eps=1e-6, k_new=None, v_new=None,
-                        stream=None, o_out=None, kv_len=None):
+                        stream=None, o_out=None, kv_len=None, pos: moe_attn_pos | None = None):
     K, H = x.shape
     C = kcache.shape[1]
     _check(lib.moe_attention_block(_ptr(x), K, H, nq, nkv, 128, C, _ptr(Wq), _ptr(Wk), _ptr(Wv), _ptr(Wo),
-                                   _ptr(kcache) if C else None, _ptr(vcache) if C else None, _ptr(kv_len), float(eps),
+                                   _ptr(kcache) if C else None, _ptr(vcache) if C else None, _ptr(kv_len),
+                                   None if pos is None else ctypes.byref(pos), float(eps),
                                    _ptr(x_out), _ptr(k_new), _ptr(v_new), _ptr(o_out), _ptr(ws), ws.numel(),
                                    _stream(stream)),
            "moe_attention_block")
 
 
+def dense_mlp_workspace(K, H, I, device="cuda") -> torch.Tensor:
+    n = int(lib.moe_dense_mlp_workspace_size(K, H, I))
+    if n == 0:
+        raise MoeError(MOE_ERR_INVALID_ARG, "dense MLP workspace size")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def moe_dense_mlp_block(x, Wg, Wu, Wd, x_out, ws, eps=1e-6, stream=None):
+    K, H = x.shape
+    _check(lib.moe_dense_mlp_block(_ptr(x), K, H, Wg.shape[0], _ptr(Wg), _ptr(Wu), _ptr(Wd), float(eps), _ptr(x_out),
+                                   _ptr(ws), ws.numel(), _stream(stream)), "moe_dense_mlp_block")
+
+
 @dataclass
 class DecoderLayer:
-    """Device tensors of one decoder layer: attention weights, KV cache, MoE."""
+    """Device tensors of one decoder layer: attention weights, KV cache, and
+    the MoE block -- or, with ``mlp`` = (Wg, Wu, Wd), a dense SwiGLU MLP.
+    ``n_q_heads`` 0 takes the model's; ``pos`` (moe_attn_pos) the window and
+    rotary embedding of the attention."""
     Wq: torch.Tensor
     Wk: torch.Tensor
     Wv: torch.Tensor
     Wo: torch.Tensor
     kcache: torch.Tensor
     vcache: torch.Tensor
-    moe: Layer
+    moe: Layer | None
+    n_q_heads: int = 0
+    pos: moe_attn_pos | None = None
+    mlp: tuple | None = None
 
 
 class VerifyModel:
@@ -319,11 +354,17 @@ class VerifyModel:
         self.lm_head = lm_head
         self.kv_len = kv_len
         p = lambda t: t.data_ptr()
-        self.c_layers = (moe_decoder_layer * len(layers))(*[
-            moe_decoder_layer(p(d.Wq), p(d.Wk), p(d.Wv), p(d.Wo), p(d.kcache), p(d.vcache), d.moe.c())
-            for d in layers])
+
+        def c_layer(d):
+            mg, mu, md = (p(d.mlp[0]), p(d.mlp[1]), p(d.mlp[2])) if d.mlp else (None, None, None)
+            return moe_decoder_layer(p(d.Wq), p(d.Wk), p(d.Wv), p(d.Wo), p(d.kcache), p(d.vcache),
+                                     d.moe.c() if d.moe is not None else moe_layer(), d.n_q_heads,
+                                     d.pos if d.pos is not None else moe_attn_pos(), mg, mu, md,
+                                     d.mlp[0].shape[0] if d.mlp else 0)
+
+        self.c_layers = (moe_decoder_layer * len(layers))(*[c_layer(d) for d in layers])
         d0 = layers[0]
-        self.c = moe_verify_model(len(layers), d0.moe.hidden, n_q_heads, n_kv_heads, 128, d0.kcache.shape[1],
+        self.c = moe_verify_model(len(layers), d0.Wq.shape[1], n_q_heads, n_kv_heads, 128, d0.kcache.shape[1],
                                   lm_head.shape[0], eps, ctypes.cast(self.c_layers, ctypes.c_void_p),
                                   lm_head.data_ptr(), None if kv_len is None else kv_len.data_ptr())
 

@@ -55,7 +55,10 @@ __device__ __forceinline__ uint4 ldg_v4(const void* p) { return *reinterpret_cas
 }  // namespace
 
 // ------------------------------------------------------------------ bf16 GEMV
-template <int KR, int NJ>
+// One warp per output row; the reduction runs over D in chunks of 2048 (8
+// pieces of 256 per lane, 16-byte loads), so D may be any multiple of 256
+// that the staged rows fit in shared memory.
+template <int KR>
 __global__ void __launch_bounds__(256) k_gemv_bf16(GemvArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -75,40 +78,35 @@ __global__ void __launch_bounds__(256) k_gemv_bf16(GemvArgs a) {
       ++sg;
     }
   };
-  auto load_row = [&](int n, uint4 (&w)[NJ]) {
-    int sg, nl;
-    locate(n, sg, nl);
-    const uint4* wrow = reinterpret_cast<const uint4*>(a.seg[sg].W + (size_t)nl * D);
-#pragma unroll
-    for (int j = 0; j < NJ; ++j)
-      if (j < nj) w[j] = ldg_nc_v4(wrow + j * 32 + lane);
-  };
-  // (loading the next row's weights ahead of this row's products measured
-  // slower in the full verify step)
-  uint4 wv[NJ];
   for (int n = blockIdx.x * (blockDim.x >> 5) + warp; n < a.n_total; n += nw) {
     int sg, nl;
     locate(n, sg, nl);
     const GemvSeg& S = a.seg[sg];
-    load_row(n, wv);
+    const uint4* wrow = reinterpret_cast<const uint4*>(S.W + (size_t)nl * D);
     // lane r < K: row r's residual, issued with the weights
     const float resv = (S.res && lane < K) ? bf_lo(S.res[(size_t)lane * S.N + nl]) : 0.f;
     float acc[KR];
 #pragma unroll
     for (int r = 0; r < KR; ++r) acc[r] = 0.f;
+    for (int j0 = 0; j0 < nj; j0 += 8) {
+      uint4 wv[8];
 #pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      if (j >= nj) break;
-      const uint32_t wq[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
+      for (int j = 0; j < 8; ++j)
+        if (j0 + j < nj) wv[j] = ldg_nc_v4(wrow + (j0 + j) * 32 + lane);
 #pragma unroll
-      for (int r = 0; r < KR; ++r) {
-        if (r < K) {
-          const uint4 xv = xs[r * (D / 8) + j * 32 + lane];
-          const uint32_t xq[4] = {xv.x, xv.y, xv.z, xv.w};
+      for (int j = 0; j < 8; ++j) {
+        if (j0 + j >= nj) break;
+        const uint32_t wq[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            acc[r] = __fmaf_rn(bf_lo(xq[i]), bf_lo(wq[i]), acc[r]);
-            acc[r] = __fmaf_rn(bf_hi(xq[i]), bf_hi(wq[i]), acc[r]);
+        for (int r = 0; r < KR; ++r) {
+          if (r < K) {
+            const uint4 xv = xs[r * (D / 8) + (j0 + j) * 32 + lane];
+            const uint32_t xq[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              acc[r] = __fmaf_rn(bf_lo(xq[i]), bf_lo(wq[i]), acc[r]);
+              acc[r] = __fmaf_rn(bf_hi(xq[i]), bf_hi(wq[i]), acc[r]);
+            }
           }
         }
       }
@@ -135,25 +133,158 @@ __global__ void __launch_bounds__(256) k_gemv_bf16(GemvArgs a) {
   }
 }
 
+template <typename Kern, typename Args>
+static cudaError_t launch_rows_kernel(Kern kern, const Args& a, size_t sm, cudaStream_t s, bool pdl) {
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * num_sms());
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = sm;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t s, bool pdl) {
   const size_t sm = sizeof(uint16_t) * a.K * a.D;
-  auto run = [&](auto kern) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * num_sms());
-    cfg.blockDim = dim3(256);
-    cfg.dynamicSmemBytes = sm;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a);
-  };
-  if (a.D <= 2048) return a.K <= 4 ? run(k_gemv_bf16<4, 8>) : (a.K <= 8 ? run(k_gemv_bf16<8, 8>) : run(k_gemv_bf16<16, 8>));
-  return a.K <= 4 ? run(k_gemv_bf16<4, 16>) : (a.K <= 8 ? run(k_gemv_bf16<8, 16>) : run(k_gemv_bf16<16, 16>));
+  if (a.K <= 4) return launch_rows_kernel(k_gemv_bf16<4>, a, sm, s, pdl);
+  if (a.K <= 8) return launch_rows_kernel(k_gemv_bf16<8>, a, sm, s, pdl);
+  return launch_rows_kernel(k_gemv_bf16<16>, a, sm, s, pdl);
+}
+
+// ------------------------------------------------------------------ dense SwiGLU rows
+// One warp per intermediate row i: the gate and up rows' dot products with
+// every staged row x_r (the GEMV's order), then h = bf16(silu(g) * u).
+template <int KR>
+__global__ void __launch_bounds__(256) k_swiglu_rows(SwigluArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int K = a.K, D = a.D, nj = D / 256;
+  pdl_wait();
+  pdl_launch_dependents();
+  uint4* xs = reinterpret_cast<uint4*>(smem);
+  block_copy_g2s(xs, reinterpret_cast<const uint4*>(a.x), K * D / 8);
+  __syncthreads();
+  const int nw = gridDim.x * (blockDim.x >> 5);
+  for (int n = blockIdx.x * (blockDim.x >> 5) + warp; n < a.N; n += nw) {
+    const uint4* grow = reinterpret_cast<const uint4*>(a.Wg + (size_t)n * D);
+    const uint4* urow = reinterpret_cast<const uint4*>(a.Wu + (size_t)n * D);
+    float ag[KR], au[KR];
+#pragma unroll
+    for (int r = 0; r < KR; ++r) ag[r] = au[r] = 0.f;
+    for (int j0 = 0; j0 < nj; j0 += 4) {
+      uint4 gv[4], uv[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (j0 + j < nj) {
+          gv[j] = ldg_nc_v4(grow + (j0 + j) * 32 + lane);
+          uv[j] = ldg_nc_v4(urow + (j0 + j) * 32 + lane);
+        }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (j0 + j >= nj) break;
+        const uint32_t gq[4] = {gv[j].x, gv[j].y, gv[j].z, gv[j].w};
+        const uint32_t uq[4] = {uv[j].x, uv[j].y, uv[j].z, uv[j].w};
+#pragma unroll
+        for (int r = 0; r < KR; ++r) {
+          if (r < K) {
+            const uint4 xv = xs[r * (D / 8) + (j0 + j) * 32 + lane];
+            const uint32_t xq[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              ag[r] = __fmaf_rn(bf_lo(xq[i]), bf_lo(gq[i]), ag[r]);
+              ag[r] = __fmaf_rn(bf_hi(xq[i]), bf_hi(gq[i]), ag[r]);
+              au[r] = __fmaf_rn(bf_lo(xq[i]), bf_lo(uq[i]), au[r]);
+              au[r] = __fmaf_rn(bf_hi(xq[i]), bf_hi(uq[i]), au[r]);
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < KR; ++r) {
+#pragma unroll
+      for (int d = 16; d >= 1; d >>= 1) {
+        ag[r] += __shfl_xor_sync(0xffffffffu, ag[r], d);
+        au[r] += __shfl_xor_sync(0xffffffffu, au[r], d);
+      }
+      if (r < K && lane == r) a.h[(size_t)r * a.N + n] = float_to_bf16_bits(ag[r] * __frcp_rn(1.f + expf(-ag[r])) * au[r]);
+    }
+  }
+}
+
+cudaError_t launch_swiglu(const SwigluArgs& a, cudaStream_t s, bool pdl) {
+  const size_t sm = sizeof(uint16_t) * a.K * a.D;
+  if (a.K <= 4) return launch_rows_kernel(k_swiglu_rows<4>, a, sm, s, pdl);
+  if (a.K <= 8) return launch_rows_kernel(k_swiglu_rows<8>, a, sm, s, pdl);
+  return launch_rows_kernel(k_swiglu_rows<16>, a, sm, s, pdl);
+}
+
+// ------------------------------------------------------------------ rotary embedding
+// One block.  The K x rd/2 angles (pos0 + r) * freq[i] -- shared by all heads
+// -- and their sines and cosines are taken in double (positions reach the
+// cache length, where an FP32 product would lose the angle); then one thread
+// per (row, head, pair) rotates (v[i], v[i + rd/2]) in FP32 and rounds to
+// bf16.  With caches given, the rotated keys and the values then go to
+// positions pos0 + r (bounded by the capacity).
+__global__ void __launch_bounds__(1024) k_rope(RopeArgs a) {
+  __shared__ float s_cos[16 * 64], s_sin[16 * 64];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int half = a.rd / 2;
+  const int pos0 = a.len ? *a.len : a.C;
+  for (int t = threadIdx.x; t < a.K * half; t += blockDim.x) {
+    const int r = t / half, i = t - r * half;
+    double sn, cs;
+    sincos((double)(pos0 + r) * a.freq[i], &sn, &cs);
+    s_cos[t] = (float)cs;
+    s_sin[t] = (float)sn;
+  }
+  __syncthreads();
+  const int per_row = (a.nq + a.nkv) * half;
+  const int total = a.K * per_row;
+  for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
+    const int r = idx / per_row, rem = idx - r * per_row;
+    const int hh = rem / half, i = rem - hh * half;
+    uint16_t* base = hh < a.nq ? a.q + (size_t)r * a.nq * 128 + (size_t)hh * 128
+                               : a.k + (size_t)r * a.nkv * 128 + (size_t)(hh - a.nq) * 128;
+    const float x0 = bf16_bits_to_float(base[i]), x1 = bf16_bits_to_float(base[i + half]);
+    const float c = s_cos[r * half + i], s = s_sin[r * half + i];
+    base[i] = float_to_bf16_bits(__fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, s)));
+    base[i + half] = float_to_bf16_bits(__fadd_rn(__fmul_rn(x1, c), __fmul_rn(x0, s)));
+  }
+  if (!a.kc) return;
+  __syncthreads();  // the rotated keys are in place
+  const int nkv_el = a.K * a.nkv * 128;
+  for (int idx = threadIdx.x; idx < nkv_el; idx += blockDim.x) {
+    const int r = idx / (a.nkv * 128), rem = idx - r * a.nkv * 128;
+    const int kvh = rem >> 7, d = rem & 127;
+    const int p = pos0 + r;
+    if (p >= a.C) {
+      if (a.err) atomicCAS(a.err, 0, (int)MOE_ERR_CAPACITY);
+      continue;
+    }
+    a.kc[((size_t)kvh * a.C + p) * 128 + d] = a.k[idx];
+    a.vc[((size_t)kvh * a.C + p) * 128 + d] = a.v[idx];
+  }
+}
+
+cudaError_t launch_rope(const RopeArgs& a, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(1024);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_rope, a);
 }
 
 // ------------------------------------------------------------------ split-KV attention
@@ -170,19 +301,20 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn_split(AttnArgs a) {
   __shared__ float s_o[kAttnWarps][16][129];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  const int kvh = blockIdx.y, split = blockIdx.x;
+  const int kvh = blockIdx.y, split = blockIdx.x, tile = blockIdx.z;
   const int HD = 128;
   pdl_wait();
   pdl_launch_dependents();
 
-  // Q fragments: thread t holds head dims [32t, 32t+32) of rows g and g+8
+  // Q fragments: thread t holds head dims [32t, 32t+32) of the tile's rows g
+  // and g+8 (query rows 16 tile + g, + 8 of the KV head)
   uint32_t qa[8][4];
+  const int nrow = a.K * a.group;
   {
-    const int nrow = a.K * a.group;
     uint4 rg[4], rh[4];
 #pragma unroll
     for (int hrow = 0; hrow < 2; ++hrow) {
-      const int i = g + 8 * hrow;
+      const int i = 16 * tile + g + 8 * hrow;
       uint4* dst = hrow ? rh : rg;
       if (i < nrow) {
         const int r = i / a.group, hh = i % a.group;
@@ -215,11 +347,26 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn_split(AttnArgs a) {
 
   // Cv valid positions of a cache of a.C (the head stride); a partial last
   // 16-position sub-chunk is masked (its keys and values read as zero, its
-  // scores as -inf)
+  // scores as -inf).  With a window W, query row i (verify row r = i / group,
+  // at position Cv + r) sees the cached positions from Cv + r - W + 1 on:
+  // the splits walk the sub-chunks from the lowest row's start, and scores
+  // before a row's own start are masked.
   const int Cv = a.len ? min(*a.len, a.C) : a.C;
   const int n16 = (Cv + 15) / 16;
-  const int c0 = (int)(((long long)split * n16) / gridDim.x);
-  const int c1 = (int)(((long long)(split + 1) * n16) / gridDim.x);
+  const int lo = a.window > 0 ? max(0, Cv - a.window + 1) : 0;
+  const int s16 = lo / 16;
+  const int c0 = s16 + (int)(((long long)split * (n16 - s16)) / gridDim.x);
+  const int c1 = s16 + (int)(((long long)(split + 1) * (n16 - s16)) / gridDim.x);
+  // the window start of this thread's two score rows (g and g + 8 of the tile)
+  int rs[2] = {0, 0};
+  if (a.window > 0) {
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int i = 16 * tile + g + 8 * hr;
+      rs[hr] = Cv + (i < nrow ? i / a.group : 0) - a.window + 1;
+    }
+  }
+  const int rs_max = max(rs[0], rs[1]);
   const uint16_t* kbase = a.kc + (size_t)kvh * a.C * HD;
   const uint16_t* vbase = a.vc + (size_t)kvh * a.C * HD;
   const int pk0 = 4 * (g >> 1) + (g & 1);  // physical row of logical column g (n-block 0); +2 for n-block 1
@@ -254,12 +401,16 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn_split(AttnArgs a) {
         mma_bf16(s[nb], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], w[w0], w[w0 + 1]);
       }
     }
-    if (rem < 16) {  // score (row, logical column 8 nb + 2t + b) sits at physical position 4t + 2nb + b
+    if (rem < 16 || sc * 16 < rs_max) {
+      // score (row g + 8 (c >> 1), logical column 8 nb + 2t + b) sits at
+      // physical position 4t + 2nb + b
 #pragma unroll
       for (int nb = 0; nb < 2; ++nb)
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          if (4 * t + 2 * nb + (c & 1) >= rem) s[nb][c] = -INFINITY;
+        for (int c = 0; c < 4; ++c) {
+          const int pp = 4 * t + 2 * nb + (c & 1);
+          if (pp >= rem || sc * 16 + pp < rs[c >> 1]) s[nb][c] = -INFINITY;
+        }
     }
     // online softmax (log2 domain); row 0 = query g, row 1 = query g+8
     float mx[2];
@@ -332,8 +483,9 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn_split(AttnArgs a) {
   }
   __syncthreads();
   const int d = threadIdx.x;  // 128 threads = head dims
-  float* po = a.part_o + ((size_t)(kvh * gridDim.x + split) * 16) * HD;
-  float* pml = a.part_ml + (size_t)(kvh * gridDim.x + split) * 32;
+  const int TR = a.tiles * 16;  // query rows per KV head in the partial buffers
+  float* po = a.part_o + ((size_t)(kvh * gridDim.x + split) * TR + 16 * tile) * HD;
+  float* pml = a.part_ml + ((size_t)(kvh * gridDim.x + split) * TR + 16 * tile) * 2;
   for (int i = 0; i < 16; ++i) {
     float M = -INFINITY;
     for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, s_m[w][i]);
@@ -368,17 +520,18 @@ __global__ void __launch_bounds__(128) k_attn_combine(AttnArgs a, int splits) {
   const int i = r * a.group + hh;
   pdl_wait();
   pdl_launch_dependents();
-  const float* pml = a.part_ml + (size_t)kvh * splits * 32 + 2 * i;
-  const float* po = a.part_o + ((size_t)kvh * splits * 16 + i) * HD + d;
+  const int TR = a.tiles * 16;
+  const float* pml = a.part_ml + (size_t)kvh * splits * TR * 2 + 2 * i;
+  const float* po = a.part_o + ((size_t)kvh * splits * TR + i) * HD + d;
   if (d < splits) {
-    s_ms[d] = __ldcg(pml + (size_t)d * 32);
-    s_ls[d] = __ldcg(pml + (size_t)d * 32 + 1);
+    s_ms[d] = __ldcg(pml + (size_t)d * TR * 2);
+    s_ls[d] = __ldcg(pml + (size_t)d * TR * 2 + 1);
   }
   float ov[2][32];  // this thread's split outputs (splits <= 64)
 #pragma unroll
   for (int c = 0; c < 2; ++c)
 #pragma unroll
-    for (int u = 0; u < 32; ++u) ov[c][u] = 32 * c + u < splits ? __ldcg(po + (size_t)(32 * c + u) * 16 * HD) : 0.f;
+    for (int u = 0; u < 32; ++u) ov[c][u] = 32 * c + u < splits ? __ldcg(po + (size_t)(32 * c + u) * TR * HD) : 0.f;
   const float qd = bf_lo(a.q[(size_t)r * a.nq * HD + (size_t)h * HD + d]);
   float kd[16], vd[16];  // the new positions j <= r (r < K <= 16)
 #pragma unroll
@@ -428,18 +581,22 @@ __global__ void __launch_bounds__(128) k_attn_combine(AttnArgs a, int splits) {
   a.o[(size_t)r * a.nq * HD + (size_t)h * HD + d] = float_to_bf16_bits(O / L);
 }
 
-int attn_splits(int nkv) {
-  int s = (2 * num_sms() + nkv - 1) / nkv;
+// Splits per (KV head, tile): about two CTAs per SM in all, no more than
+// there are 16-position sub-chunks to walk.
+int attn_splits(int nkv, int tiles, int max_chunks) {
+  int s = (2 * num_sms() + nkv * tiles - 1) / (nkv * tiles);
+  if (s > max_chunks) s = max_chunks;
   return s < 1 ? 1 : (s > kAttnMaxSplits ? kAttnMaxSplits : s);
 }
 
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s, bool pdl) {
-  const int splits = attn_splits(a.nkv);
+  const int chunks = (a.window > 0 ? (a.window + 31) / 16 : (a.C + 15) / 16);
+  const int splits = attn_splits(a.nkv, a.tiles, chunks);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(splits, a.nkv);
+  cfg.gridDim = dim3(splits, a.nkv, a.tiles);
   cfg.blockDim = dim3(kAttnWarps * 32);
   cfg.stream = s;
   cfg.attrs = attr;

@@ -394,17 +394,48 @@ static AttnLayout attn_layout(int K, int H, int nq, int nkv) {
   L.kn = take(sizeof(uint16_t) * K * nkv * 128);
   L.vn = take(sizeof(uint16_t) * K * nkv * 128);
   L.o = take(sizeof(uint16_t) * K * nq * 128);
-  L.part_o = take(sizeof(float) * (size_t)nkv * kAttnMaxSplits * 16 * 128);
-  L.part_ml = take(sizeof(float) * (size_t)nkv * kAttnMaxSplits * 32);
+  const int tiles = (K * (nq / nkv) + 15) / 16;
+  L.part_o = take(sizeof(float) * (size_t)nkv * kAttnMaxSplits * tiles * 16 * 128);
+  L.part_ml = take(sizeof(float) * (size_t)nkv * kAttnMaxSplits * tiles * 32);
   L.total = off;
   return L;
 }
 
 static moe_status check_attn(int K, int H, int nq, int nkv, int hd, int C) {
   if (K < 1 || K > MOE_MAX_ROWS || nq < 1 || nkv < 1 || C < 0) return MOE_ERR_INVALID_ARG;
-  if (hd != 128 || nq % nkv != 0 || K * (nq / nkv) > 16) return MOE_ERR_UNSUPPORTED_SHAPE;
-  if (H % 256 != 0 || H > 4096 || nq % 2 != 0 || nq * 128 > 4096 || C % 16 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (hd != 128 || nq % nkv != 0 || K * (nq / nkv) > 16 * kAttnMaxTiles) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (H % 256 != 0 || H > 4096 || nq % 2 != 0 || nq * 128 > 8192 || K * nq > 768 || C % 16 != 0)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
   return MOE_OK;
+}
+
+static moe_status check_pos(const moe_attn_pos* p) {
+  if (!p) return MOE_OK;
+  if (p->window < 0 || (p->window > 0 && p->window < 16)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (p->rotary_dim < 0 || p->rotary_dim > 128 || p->rotary_dim % 2 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (p->rotary_dim > 0 && !(p->rope_theta > 1.f)) return MOE_ERR_INVALID_ARG;
+  if (p->rotary_dim > 0 && p->yarn_factor > 1.f && p->yarn_orig_ctx < 1) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+// Angle per position of each rotary pair (YaRN-scaled when asked) and the
+// logit temperature.
+static void rope_freqs(const moe_attn_pos& p, double* f, double* temp) {
+  const double two_pi = 6.283185307179586476925286766559;
+  const int rd = p.rotary_dim;
+  const bool yarn = p.yarn_factor > 1.f;
+  for (int i = 0; i < rd / 2; ++i) {
+    double fi = std::pow((double)p.rope_theta, -2.0 * i / rd);
+    if (yarn) {
+      const double r = (double)p.yarn_orig_ctx * fi / two_pi;
+      double g = (r - 1.0) / (32.0 - 1.0);
+      g = g < 0.0 ? 0.0 : (g > 1.0 ? 1.0 : g);
+      fi = (1.0 - g) * fi / (double)p.yarn_factor + g * fi;
+    }
+    f[i] = fi;
+  }
+  const double m = yarn ? 0.1 * std::log((double)p.yarn_factor) + 1.0 : 1.0;
+  *temp = m * m;
 }
 
 size_t moe_attention_workspace_size(int K, int H, int nq, int nkv, int head_dim) {
@@ -416,7 +447,8 @@ size_t moe_attention_workspace_size(int K, int H, int nq, int nkv, int head_dim)
 // (the caller's workspace error word).
 static moe_status attention_impl(const uint16_t* x, int K, int H, int nq, int nkv, int C, const uint16_t* Wq,
                                  const uint16_t* Wk, const uint16_t* Wv, const uint16_t* Wo, uint16_t* kcache,
-                                 uint16_t* vcache, const int32_t* kv_len, float eps, uint16_t* x_out,
+                                 uint16_t* vcache, const int32_t* kv_len, const moe_attn_pos* pos, float eps,
+                                 uint16_t* x_out,
                                  uint16_t* k_new_out, uint16_t* v_new_out, uint16_t* o_out, char* b,
                                  const AttnLayout& L, int* err, cudaStream_t s) {
   uint16_t* xn = reinterpret_cast<uint16_t*>(b + L.xn);
@@ -429,15 +461,36 @@ static moe_status attention_impl(const uint16_t* x, int K, int H, int nq, int nk
   g.x = xn;
   g.K = K;
   g.D = H;
+  const bool rope = pos && pos->rotary_dim > 0;
   g.seg[0] = {Wq, q, nullptr, nq * 128, nullptr, nullptr, 0};
   // with a device length, the new keys and values also go into the caches
-  // in place, at positions *kv_len .. *kv_len + K - 1
-  g.seg[1] = {Wk, kn, nullptr, nkv * 128, kv_len ? kcache : nullptr, kv_len, C};
-  g.seg[2] = {Wv, vn, nullptr, nkv * 128, kv_len ? vcache : nullptr, kv_len, C};
+  // in place, at positions *kv_len .. *kv_len + K - 1 (with a rotary
+  // embedding the rotation kernel appends the rotated keys instead)
+  const bool gemv_append = kv_len && !rope;
+  g.seg[1] = {Wk, kn, nullptr, nkv * 128, gemv_append ? kcache : nullptr, kv_len, C};
+  g.seg[2] = {Wv, vn, nullptr, nkv * 128, gemv_append ? vcache : nullptr, kv_len, C};
   g.nseg = 3;
   g.n_total = (nq + 2 * nkv) * 128;
   g.err = err;
   if (launch_gemv(g, s, true) != cudaSuccess) return MOE_ERR_CUDA;
+  double temp = 1.0;
+  if (rope) {
+    RopeArgs ra{};
+    ra.q = q;
+    ra.k = kn;
+    ra.v = vn;
+    ra.K = K;
+    ra.nq = nq;
+    ra.nkv = nkv;
+    ra.rd = pos->rotary_dim;
+    rope_freqs(*pos, ra.freq, &temp);
+    ra.len = kv_len;
+    ra.C = C;
+    ra.kc = kv_len ? kcache : nullptr;
+    ra.vc = kv_len ? vcache : nullptr;
+    ra.err = err;
+    if (launch_rope(ra, s) != cudaSuccess) return MOE_ERR_CUDA;
+  }
   AttnArgs a{};
   a.q = q;
   a.kc = kcache;
@@ -451,7 +504,9 @@ static moe_status attention_impl(const uint16_t* x, int K, int H, int nq, int nk
   a.nkv = nkv;
   a.C = C;
   a.group = nq / nkv;
-  a.scale_log2 = 1.4426950408889634f / sqrtf(128.f);
+  a.tiles = (K * a.group + 15) / 16;
+  a.window = pos ? pos->window : 0;
+  a.scale_log2 = (float)(1.4426950408889634 * temp / std::sqrt(128.0));
   a.part_o = reinterpret_cast<float*>(b + L.part_o);
   a.part_ml = reinterpret_cast<float*>(b + L.part_ml);
   if (launch_attention(a, s, true) != cudaSuccess) return MOE_ERR_CUDA;
@@ -468,11 +523,12 @@ static moe_status attention_impl(const uint16_t* x, int K, int H, int nq, int nk
 
 moe_status moe_attention_block(const uint16_t* x, int K, int H, int nq, int nkv, int head_dim, int C,
                                const uint16_t* Wq, const uint16_t* Wk, const uint16_t* Wv, const uint16_t* Wo,
-                               uint16_t* kcache, uint16_t* vcache, const int32_t* kv_len, float eps,
-                               uint16_t* x_out, uint16_t* k_new_out, uint16_t* v_new_out, uint16_t* o_out,
-                               void* ws, size_t ws_bytes, void* stream) {
+                               uint16_t* kcache, uint16_t* vcache, const int32_t* kv_len, const moe_attn_pos* pos,
+                               float eps, uint16_t* x_out, uint16_t* k_new_out, uint16_t* v_new_out,
+                               uint16_t* o_out, void* ws, size_t ws_bytes, void* stream) {
   moe_status st = check_attn(K, H, nq, nkv, head_dim, C);
   if (st != MOE_OK) return st;
+  if ((st = check_pos(pos)) != MOE_OK) return st;
   if (!x || !Wq || !Wk || !Wv || !Wo || !x_out || !ws || (C > 0 && (!kcache || !vcache)) || !(eps >= 0.f) ||
       (kv_len && C == 0))
     return MOE_ERR_INVALID_ARG;
@@ -482,44 +538,124 @@ moe_status moe_attention_block(const uint16_t* x, int K, int H, int nq, int nkv,
   const AttnLayout L = attn_layout(K, H, nq, nkv);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   char* b = static_cast<char*>(ws);
-  return attention_impl(x, K, H, nq, nkv, C, Wq, Wk, Wv, Wo, kcache, vcache, kv_len, eps, x_out, k_new_out,
+  return attention_impl(x, K, H, nq, nkv, C, Wq, Wk, Wv, Wo, kcache, vcache, kv_len, pos, eps, x_out, k_new_out,
                         v_new_out, o_out, b, L, reinterpret_cast<int*>(b + L.hdr), static_cast<cudaStream_t>(stream));
+}
+
+struct MlpLayout {
+  size_t hdr, xn, h, total;
+};
+
+static MlpLayout mlp_layout(int K, int H, int I) {
+  MlpLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t b) {
+    size_t r = off;
+    off = align256(off + b);
+    return r;
+  };
+  L.hdr = take(256);
+  L.xn = take(sizeof(uint16_t) * K * H);
+  L.h = take(sizeof(uint16_t) * K * I);
+  L.total = off;
+  return L;
+}
+
+static moe_status check_mlp(int K, int H, int I) {
+  if (K < 1 || K > MOE_MAX_ROWS || I < 1) return MOE_ERR_INVALID_ARG;
+  if (H % 256 != 0 || H > 4096 || I % 256 != 0 || K * I > 98304) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+size_t moe_dense_mlp_workspace_size(int K, int H, int I) {
+  if (check_mlp(K, H, I) != MOE_OK) return 0;
+  return mlp_layout(K, H, I).total;
+}
+
+static moe_status dense_mlp_impl(const uint16_t* x, int K, int H, int I, const uint16_t* Wg, const uint16_t* Wu,
+                                 const uint16_t* Wd, float eps, uint16_t* x_out, char* b, const MlpLayout& L,
+                                 cudaStream_t s) {
+  uint16_t* xn = reinterpret_cast<uint16_t*>(b + L.xn);
+  uint16_t* h = reinterpret_cast<uint16_t*>(b + L.h);
+  if (launch_rmsnorm(x, K, H, eps, xn, s, false) != cudaSuccess) return MOE_ERR_CUDA;
+  SwigluArgs sa{xn, Wg, Wu, h, K, H, I};
+  if (launch_swiglu(sa, s, true) != cudaSuccess) return MOE_ERR_CUDA;
+  GemvArgs gd{};
+  gd.x = h;
+  gd.K = K;
+  gd.D = I;
+  gd.seg[0] = {Wd, x_out, x, H, nullptr, nullptr, 0};
+  gd.nseg = 1;
+  gd.n_total = H;
+  if (launch_gemv(gd, s, true) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_dense_mlp_block(const uint16_t* x, int K, int H, int I, const uint16_t* Wg, const uint16_t* Wu,
+                               const uint16_t* Wd, float eps, uint16_t* x_out, void* ws, size_t ws_bytes,
+                               void* stream) {
+  moe_status st = check_mlp(K, H, I);
+  if (st != MOE_OK) return st;
+  if (!x || !Wg || !Wu || !Wd || !x_out || !ws || !(eps >= 0.f)) return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, Wg, Wu, Wd, x_out, ws};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return MOE_ERR_MISALIGNED;
+  const MlpLayout L = mlp_layout(K, H, I);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return dense_mlp_impl(x, K, H, I, Wg, Wu, Wd, eps, x_out, static_cast<char*>(ws), L,
+                        static_cast<cudaStream_t>(stream));
+}
+
+static int layer_nq(const moe_verify_model* m, const moe_decoder_layer& d) {
+  return d.n_q_heads > 0 ? d.n_q_heads : m->n_q_heads;
 }
 
 static moe_status check_model(const moe_verify_model* m, int K) {
   if (!m || !m->layers || !m->lm_head || m->n_layers < 1 || m->vocab < 1 || !(m->eps >= 0.f))
     return MOE_ERR_INVALID_ARG;
-  moe_status s = check_attn(K, m->hidden, m->n_q_heads, m->n_kv_heads, m->head_dim, m->ctx);
-  if (s != MOE_OK) return s;
+  moe_status s;
   if (m->hidden > 2048) return MOE_ERR_UNSUPPORTED_SHAPE;  // lm_head and MoE envelope
+  if (m->kv_len && m->ctx == 0) return MOE_ERR_INVALID_ARG;
   for (int l = 0; l < m->n_layers; ++l) {
     const moe_decoder_layer& d = m->layers[l];
+    if ((s = check_attn(K, m->hidden, layer_nq(m, d), m->n_kv_heads, m->head_dim, m->ctx)) != MOE_OK) return s;
+    if ((s = check_pos(&d.pos)) != MOE_OK) return s;
     if (!d.Wq || !d.Wk || !d.Wv || !d.Wo || (m->ctx > 0 && (!d.kcache || !d.vcache))) return MOE_ERR_INVALID_ARG;
-    if (m->kv_len && m->ctx == 0) return MOE_ERR_INVALID_ARG;
-    if ((s = check_layer(&d.moe, K)) != MOE_OK) return s;
-    if (d.moe.hidden != m->hidden) return MOE_ERR_INVALID_ARG;
+    if (d.mlp_gate) {
+      if (!d.mlp_up || !d.mlp_down) return MOE_ERR_INVALID_ARG;
+      if ((s = check_mlp(K, m->hidden, d.mlp_inter)) != MOE_OK) return s;
+    } else {
+      if ((s = check_layer(&d.moe, K)) != MOE_OK) return s;
+      if (d.moe.hidden != m->hidden) return MOE_ERR_INVALID_ARG;
+    }
   }
   return MOE_OK;
 }
 
 struct StepLayout {
-  size_t moe_ws, attn_ws, xn, lm_ws, total;
-  size_t moe_bytes, attn_bytes;
+  size_t moe_ws, attn_ws, mlp_ws, xn, lm_ws, total;
+  size_t moe_bytes, attn_bytes, mlp_bytes;
 };
 
 static StepLayout step_layout(const moe_verify_model* m, int K) {
   StepLayout L{};
-  size_t mb = 0;
+  size_t mb = 256, ab = 0, pb = 0;  // (the MoE workspace's header holds the step's error word)
   for (int l = 0; l < m->n_layers; ++l) {
-    const size_t b = layout_of(&m->layers[l].moe, K).total;
-    mb = b > mb ? b : mb;
+    const moe_decoder_layer& d = m->layers[l];
+    const size_t b = d.mlp_gate ? mlp_layout(K, m->hidden, d.mlp_inter).total : 0;
+    pb = b > pb ? b : pb;
+    const size_t e = d.mlp_gate ? 0 : layout_of(&d.moe, K).total;
+    mb = e > mb ? e : mb;
+    const size_t a = attn_layout(K, m->hidden, layer_nq(m, d), m->n_kv_heads).total;
+    ab = a > ab ? a : ab;
   }
-  const size_t ab = attn_layout(K, m->hidden, m->n_q_heads, m->n_kv_heads).total;
   size_t off = 0;
   L.moe_ws = off;
   off = align256(off + mb);
   L.attn_ws = off;
   off = align256(off + ab);
+  L.mlp_ws = off;
+  off = align256(off + pb);
   L.xn = off;
   off = align256(off + sizeof(uint16_t) * K * m->hidden);
   L.lm_ws = off;
@@ -527,6 +663,7 @@ static StepLayout step_layout(const moe_verify_model* m, int K) {
   L.total = off;
   L.moe_bytes = mb;
   L.attn_bytes = ab;
+  L.mlp_bytes = pb;
   return L;
 }
 
@@ -541,16 +678,20 @@ static moe_status forward_impl(const moe_verify_model* m, uint16_t* x, int K, in
                                const StepLayout& L, cudaStream_t st) {
   uint16_t* xn = reinterpret_cast<uint16_t*>(b + L.xn);
   const int H = m->hidden;
-  const AttnLayout AL = attn_layout(K, H, m->n_q_heads, m->n_kv_heads);
   int* err = reinterpret_cast<int*>(b + L.moe_ws);  // the step's error word (the MoE workspace header)
   for (int l = 0; l < m->n_layers; ++l) {
     const moe_decoder_layer& d = m->layers[l];
-    moe_status s = attention_impl(x, K, H, m->n_q_heads, m->n_kv_heads, m->ctx, d.Wq, d.Wk, d.Wv, d.Wo, d.kcache,
-                                  d.vcache, m->kv_len, m->eps, x, nullptr, nullptr, nullptr, b + L.attn_ws, AL, err, st);
+    const int nq = layer_nq(m, d);
+    const AttnLayout AL = attn_layout(K, H, nq, m->n_kv_heads);
+    moe_status s = attention_impl(x, K, H, nq, m->n_kv_heads, m->ctx, d.Wq, d.Wk, d.Wv, d.Wo, d.kcache, d.vcache,
+                                  m->kv_len, &d.pos, m->eps, x, nullptr, nullptr, nullptr, b + L.attn_ws, AL, err, st);
     if (s != MOE_OK) return s;
-    // the MoE layer kernel applies its RMSNorm to x itself
-    s = run_layer(&d.moe, x, K, x, x, nullptr, nullptr, nullptr, b + L.moe_ws, L.moe_bytes, st, true, nullptr,
-                  m->eps);
+    if (d.mlp_gate)  // a dense SwiGLU MLP block (Laguna's layer 0)
+      s = dense_mlp_impl(x, K, H, d.mlp_inter, d.mlp_gate, d.mlp_up, d.mlp_down, m->eps, x, b + L.mlp_ws,
+                         mlp_layout(K, H, d.mlp_inter), st);
+    else  // the MoE layer kernel applies its RMSNorm to x itself
+      s = run_layer(&d.moe, x, K, x, x, nullptr, nullptr, nullptr, b + L.moe_ws, L.moe_bytes, st, true, nullptr,
+                    m->eps);
     if (s != MOE_OK) return s;
   }
   if (launch_rmsnorm(x, K, H, m->eps, xn, st, false) != cudaSuccess) return MOE_ERR_CUDA;

@@ -212,16 +212,45 @@ struct AttnArgs {
   const uint16_t* v_new;
   uint16_t* o;            // [K][nq*128]
   int K, nq, nkv, C, group;
-  float scale_log2;       // log2(e) / sqrt(128)
-  float* part_o;          // [nkv][splits][16][128]
-  float* part_ml;         // [nkv][splits][16][2]
+  int tiles;              // 16-row query tiles per KV head: ceil(K * group / 16)
+  int window;             // sliding window (positions a row sees, itself included), 0 = all
+  float scale_log2;       // log2(e) * temperature / sqrt(128)
+  float* part_o;          // [nkv][splits][tiles * 16][128]
+  float* part_ml;         // [nkv][splits][tiles * 16][2]
 };
 
 constexpr int kAttnMaxSplits = 64;
+constexpr int kAttnMaxTiles = 4;  // K * group <= 64 query rows per KV head
+
+// Rotary position embedding of the new rows (in place), at positions
+// pos0 + r with pos0 = *len (or C when len is null); optionally the rotated
+// keys and the values appended to the caches at those positions.
+struct RopeArgs {
+  uint16_t* q;            // [K][nq*128]
+  uint16_t* k;            // [K][nkv*128]
+  const uint16_t* v;      // [K][nkv*128] (for the append)
+  int K, nq, nkv, rd;     // rd: rotary dims per head (pairs i, i + rd/2)
+  double freq[64];        // angle per position of pair i
+  const int* len;
+  int C;                  // cache capacity (head stride)
+  uint16_t *kc, *vc;      // caches to append to, or null
+  int* err;
+};
+cudaError_t launch_rope(const RopeArgs& a, cudaStream_t s);
+
+// Dense SwiGLU rows: h[r][i] = bf16(silu(x_r . Wg_i) * (x_r . Wu_i)).
+struct SwigluArgs {
+  const uint16_t* x;   // [K][D]
+  const uint16_t* Wg;  // [N][D]
+  const uint16_t* Wu;  // [N][D]
+  uint16_t* h;         // [K][N]
+  int K, D, N;
+};
+cudaError_t launch_swiglu(const SwigluArgs& a, cudaStream_t s, bool pdl);
 
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s, bool pdl);
-int attn_splits(int nkv);
+int attn_splits(int nkv, int tiles, int max_chunks);
 
 inline size_t lmhead_ws_bytes(int K) { return 256 + align256(sizeof(float) * kLmMaxGrid * K) + sizeof(int) * kLmMaxGrid * K; }
 

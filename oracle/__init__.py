@@ -81,6 +81,11 @@ def _bind(L):
     L.orc_linear_bf16.argtypes = [vp, vp, ci, ci, ci, vp]
     L.orc_attention.argtypes = [vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, vp, vp, vp, cd, vp, vp]
     L.orc_lm_argmax.argtypes = [vp, vp, ci, ci, ci, vp, vp]
+    L.orc_rope_freqs.argtypes = [ci, cd, cd, ci, vp]
+    L.orc_rope_vec.argtypes = [vp, ci, vp, cd]
+    L.orc_attention_ex.argtypes = [vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, vp, vp, vp, cd, ci, ci, cd, cd, ci, vp, vp,
+                                   vp, vp]
+    L.orc_dense_mlp.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, vp]
     L.orc_accept_prefix.restype = ci
     L.orc_accept_prefix.argtypes = [vp, vp, ci]
     return L
@@ -270,6 +275,51 @@ def attention(x, Wq, Wk, Wv, Wo, kc, vc, nq, nkv, hd, eps=RMS_EPS, L=None, with_
     return (out, o) if with_o else out
 
 
+def rope_freqs(rd, theta=10000.0, yarn_factor=1.0, yarn_orig=0, L=None):
+    """Per rotary pair i < rd/2 the angle per position (YaRN-scaled when
+    yarn_factor > 1)."""
+    f = np.empty(rd // 2, np.float64)
+    (L or lib()).orc_rope_freqs(rd, theta, yarn_factor, yarn_orig, _p(f))
+    return f
+
+
+def rope_vec(v, rd, freqs, pos, L=None):
+    """One head vector (float64) rotated at position pos (no rounding)."""
+    v = np.array(v, np.float64)
+    f = _c(freqs, np.float64)
+    (L or lib()).orc_rope_vec(_p(v), rd, _p(f), float(pos))
+    return v
+
+
+def attention_ex(x, Wq, Wk, Wv, Wo, kc, vc, nq, nkv, hd, window=0, rotary_dim=0, theta=10000.0, yarn_factor=1.0,
+                 yarn_orig=0, eps=RMS_EPS, L=None):
+    """A Laguna attention block (RoPE / YaRN, sliding window); returns dict
+    (x=block output, k_new, v_new (the rotated new keys and the values), o)."""
+    x = _c(x, np.uint16)
+    K, H = x.shape
+    C = kc.shape[1]
+    arrs = [_c(a, np.uint16) for a in (Wq, Wk, Wv, Wo, kc, vc)]
+    out = np.empty_like(x)
+    kn = np.empty((K, nkv * hd), np.uint16)
+    vn = np.empty((K, nkv * hd), np.uint16)
+    o = np.empty((K, nq * hd), np.uint16)
+    (L or lib()).orc_attention_ex(_p(x), K, H, nq, nkv, hd, C, *[_p(a) for a in arrs], eps, window, rotary_dim,
+                                  theta, yarn_factor, yarn_orig, _p(out), _p(kn), _p(vn), _p(o))
+    return dict(x=out, k_new=kn, v_new=vn, o=o)
+
+
+def dense_mlp(x_norm, residual, Wg, Wu, Wd, L=None):
+    """Laguna's layer-0 dense SwiGLU MLP: bf16 [K][H]."""
+    x_norm = _c(x_norm, np.uint16)
+    K, H = x_norm.shape
+    I = Wg.shape[0]
+    res = None if residual is None else _c(residual, np.uint16)
+    y = np.empty_like(x_norm)
+    (L or lib()).orc_dense_mlp(_p(x_norm), _p(res), _p(_c(Wg, np.uint16)), _p(_c(Wu, np.uint16)),
+                               _p(_c(Wd, np.uint16)), K, H, I, _p(y))
+    return y
+
+
 def lm_argmax(x_norm, W, L=None):
     x_norm, W = _c(x_norm, np.uint16), _c(W, np.uint16)
     K, H = x_norm.shape
@@ -371,3 +421,29 @@ def verify_rounds(w, layers, lm_head, x_rounds, coin, alt, ctx0, n_layers=None, 
             vcs[l] = np.ascontiguousarray(np.concatenate([vcs[l], vnew[l][:c].transpose(1, 0, 2)], axis=1))
         targets[t], drafts[t], ns[t] = tok, d, n
     return dict(targets=targets, drafts=drafts, n=ns, len=kcs[0].shape[1], kc=kcs, vc=vcs)
+
+
+def laguna_step(w, layers, lm_head, x0, n_layers=None, L=None):
+    """The verify step of the Laguna layer schedule: per layer the attention
+    block with its window / rotary embedding, then its dense MLP (layer 0) or
+    MoE block, then the lm_head argmax of every row.  ``layers(l)`` returns
+    (attention dict with Wq, Wk, Wv, Wo, kc, vc; configuration dict of
+    synthgen.laguna_layer_kind; MLP dict (dense) or MoE synthgen.Layer).
+    Returns dict(x, target, att_in, mlp_in, att_o)."""
+    x = _c(x0, np.uint16)
+    att_in, mlp_in, att_o = [], [], []
+    for l in range(n_layers or w.layers):
+        att, cfg, mlp = layers(l)
+        att_in.append(x.copy())
+        r = attention_ex(x, att["Wq"], att["Wk"], att["Wv"], att["Wo"], att["kc"], att["vc"], cfg["n_q_heads"],
+                         w.n_kv_heads, w.head_dim, window=cfg["window"], rotary_dim=cfg["rotary_dim"],
+                         theta=cfg["rope_theta"], yarn_factor=cfg["yarn_factor"], yarn_orig=cfg["yarn_orig"], L=L)
+        x = r["x"]
+        att_o.append(r["o"])
+        mlp_in.append(x.copy())
+        if cfg["dense"]:
+            x = dense_mlp(rmsnorm(x, L=L), x, mlp["Wg"], mlp["Wu"], mlp["Wd"], L=L)
+        else:
+            x = moe_layer(OracleLayer.from_workload(w, mlp), rmsnorm(x, L=L), residual=x, L=L)["y"]
+    tok, best = lm_argmax(rmsnorm(x, L=L), lm_head, L=L)
+    return dict(x=x, target=tok, best=best, att_in=att_in, mlp_in=mlp_in, att_o=att_o)

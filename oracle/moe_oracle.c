@@ -549,6 +549,165 @@ void orc_attention(const uint16_t* x, int K, int H, int nq, int nkv, int hd, int
   free(xn); free(q); free(kn); free(vn); free(o);
 }
 
+/* ------------------------------------------------------------------ */
+/* Rotary position embedding (RoPE) with YaRN frequency scaling         */
+/* ------------------------------------------------------------------ */
+/*
+ * README, "Why this challenge exists": sliding-window layers use plain RoPE
+ * at theta 10000, full-attention layers YaRN rotary with a 0.5
+ * partial-rotary factor.  Rotary dims: the first rd of a head; pair i < rd/2
+ * is (v[i], v[i + rd/2]) ("rotate half"), rotated by angle p * f_i at
+ * position p, f_i = theta^(-2i/rd).  YaRN (Peng et al., "YaRN: Efficient
+ * Context Window Extension of Large Language Models", NTK-by-parts) with
+ * factor s > 1 and original context L0: r_i = L0 * f_i / (2 pi) (rotations
+ * of pair i over L0 positions), ramp g_i = clamp((r_i - 1) / (32 - 1), 0, 1),
+ * f_i <- (1 - g_i) f_i / s + g_i f_i; and the attention logits are scaled by
+ * (0.1 ln s + 1)^2 (the temperature applied to both q and k).
+ */
+void orc_rope_freqs(int rd, double theta, double yarn_s, int yarn_l0, double* f) {
+  const double two_pi = 6.283185307179586476925286766559;
+  for (int i = 0; i < rd / 2; ++i) {
+    double fi = pow(theta, -2.0 * i / rd);
+    if (yarn_s > 1.0) {
+      double r = (double)yarn_l0 * fi / two_pi;
+      double g = (r - 1.0) / (32.0 - 1.0);
+      if (g < 0.0) g = 0.0;
+      if (g > 1.0) g = 1.0;
+      fi = (1.0 - g) * fi / yarn_s + g * fi;
+    }
+    f[i] = fi;
+  }
+}
+
+/* Rotates one head vector v[hd] (double, in place) at position p. */
+void orc_rope_vec(double* v, int rd, const double* f, double p) {
+  for (int i = 0; i < rd / 2; ++i) {
+    double a = p * f[i], c = cos(a), s = sin(a);
+    double x0 = v[i], x1 = v[i + rd / 2];
+    v[i] = x0 * c - x1 * s;
+    v[i + rd / 2] = x1 * c + x0 * s;
+  }
+}
+
+/* The rows [K][n_heads * hd] (bf16) rotated at positions pos0 + r, rounded
+ * to bf16 again. */
+static void rope_rows_bf16(uint16_t* x, int K, int n_heads, int hd, int rd, const double* f, int pos0) {
+  double* v = (double*)malloc(sizeof(double) * hd);
+  for (int r = 0; r < K; ++r)
+    for (int h = 0; h < n_heads; ++h) {
+      uint16_t* xv = x + (size_t)r * n_heads * hd + (size_t)h * hd;
+      for (int c = 0; c < hd; ++c) v[c] = orc_bf16(xv[c]);
+      orc_rope_vec(v, rd, f, (double)(pos0 + r));
+      for (int c = 0; c < hd; ++c) xv[c] = orc_round_bf16(v[c]);
+    }
+  free(v);
+}
+
+/*
+ * The attention block of a Laguna layer: as orc_attention, with RoPE / YaRN
+ * on q and the new keys (rd = 0: none), the rows at positions C .. C+K-1, and
+ * a sliding window of `window` positions (0: none): row r at position
+ * p = C + r sees positions max(0, p - window + 1) .. p.
+ *   k_new_out, v_new_out [K][nkv*hd] (optional): the (rotated) new keys and
+ *   the new values; o_out [K][nq*hd] (optional).
+ */
+void orc_attention_ex(const uint16_t* x, int K, int H, int nq, int nkv, int hd, int C, const uint16_t* Wq,
+                      const uint16_t* Wk, const uint16_t* Wv, const uint16_t* Wo, const uint16_t* kc,
+                      const uint16_t* vc, double eps, int window, int rd, double theta, double yarn_s, int yarn_l0,
+                      uint16_t* x_out, uint16_t* k_new_out, uint16_t* v_new_out, uint16_t* o_out) {
+  int QD = nq * hd, KD = nkv * hd, grp = nq / nkv;
+  uint16_t* xn = (uint16_t*)malloc(2 * (size_t)K * H);
+  uint16_t* q = (uint16_t*)malloc(2 * (size_t)K * QD);
+  uint16_t* kn = (uint16_t*)malloc(2 * (size_t)K * KD);
+  uint16_t* vn = (uint16_t*)malloc(2 * (size_t)K * KD);
+  uint16_t* o = (uint16_t*)malloc(2 * (size_t)K * QD);
+  double f[256];
+  orc_rmsnorm(x, K, H, eps, xn);
+  orc_linear_bf16(xn, Wq, K, H, QD, q);
+  orc_linear_bf16(xn, Wk, K, H, KD, kn);
+  orc_linear_bf16(xn, Wv, K, H, KD, vn);
+  double temp = 1.0;
+  if (rd > 0) {
+    orc_rope_freqs(rd, theta, yarn_s, yarn_l0, f);
+    rope_rows_bf16(q, K, nq, hd, rd, f, C);
+    rope_rows_bf16(kn, K, nkv, hd, rd, f, C);
+    if (yarn_s > 1.0) temp = (0.1 * log(yarn_s) + 1.0) * (0.1 * log(yarn_s) + 1.0);
+  }
+  double scale = temp / sqrt((double)hd);
+  #pragma omp parallel for collapse(2) schedule(dynamic, 1)
+  for (int r = 0; r < K; ++r)
+    for (int h = 0; h < nq; ++h) {
+      int kvh = h / grp;
+      int p_row = C + r;
+      int lo = (window > 0 && p_row - window + 1 > 0) ? p_row - window + 1 : 0;
+      int n = C + r + 1;
+      double* sc = (double*)malloc(sizeof(double) * n);
+      const uint16_t* qv = q + (size_t)r * QD + (size_t)h * hd;
+      double mx = -INFINITY;
+      for (int p = 0; p < n; ++p) {
+        if (p < lo) { sc[p] = -INFINITY; continue; }
+        const uint16_t* kv = (p < C) ? kc + ((size_t)kvh * C + p) * hd
+                                     : kn + (size_t)(p - C) * KD + (size_t)kvh * hd;
+        double s = 0.0;
+        for (int c = 0; c < hd; ++c) s += orc_bf16(qv[c]) * orc_bf16(kv[c]);
+        sc[p] = s * scale;
+        if (sc[p] > mx) mx = sc[p];
+      }
+      double z = 0.0;
+      for (int p = 0; p < n; ++p) { sc[p] = (p < lo) ? 0.0 : exp(sc[p] - mx); z += sc[p]; }
+      for (int c = 0; c < hd; ++c) {
+        double acc = 0.0;
+        for (int p = lo; p < n; ++p) {
+          const uint16_t* vv = (p < C) ? vc + ((size_t)kvh * C + p) * hd
+                                       : vn + (size_t)(p - C) * KD + (size_t)kvh * hd;
+          acc += (sc[p] / z) * orc_bf16(vv[c]);
+        }
+        o[(size_t)r * QD + (size_t)h * hd + c] = orc_round_bf16(acc);
+      }
+      free(sc);
+    }
+  for (int r = 0; r < K; ++r)
+    for (int j = 0; j < H; ++j) {
+      double s = 0.0;
+      for (int c = 0; c < QD; ++c) s += orc_bf16(o[(size_t)r * QD + c]) * orc_bf16(Wo[(size_t)j * QD + c]);
+      x_out[(size_t)r * H + j] = orc_round_bf16(orc_bf16(x[(size_t)r * H + j]) + s);
+    }
+  if (k_new_out) memcpy(k_new_out, kn, 2 * (size_t)K * KD);
+  if (v_new_out) memcpy(v_new_out, vn, 2 * (size_t)K * KD);
+  if (o_out) memcpy(o_out, o, 2 * (size_t)K * QD);
+  free(xn); free(q); free(kn); free(vn); free(o);
+}
+
+/* The dense bf16 SwiGLU MLP of Laguna's layer 0 (README, "Why this
+ * challenge exists": layer 0 has a dense MLP, intermediate 8192):
+ *   h = bf16( silu(x_norm . Wg^T) * (x_norm . Wu^T) )   [K][I]
+ *   y = bf16( residual + h . Wd^T )                      [K][H]
+ * dot products in double, the same rounding points as the experts. */
+void orc_dense_mlp(const uint16_t* x_norm, const uint16_t* residual, const uint16_t* Wg, const uint16_t* Wu,
+                   const uint16_t* Wd, int K, int H, int I, uint16_t* y) {
+  double* h = (double*)malloc(sizeof(double) * (size_t)K * I);
+  #pragma omp parallel for schedule(static)
+  for (int i = 0; i < I; ++i)
+    for (int r = 0; r < K; ++r) {
+      double g = 0.0, u = 0.0;
+      for (int c = 0; c < H; ++c) {
+        double xv = orc_bf16(x_norm[(size_t)r * H + c]);
+        g += xv * orc_bf16(Wg[(size_t)i * H + c]);
+        u += xv * orc_bf16(Wu[(size_t)i * H + c]);
+      }
+      h[(size_t)r * I + i] = orc_bf16(orc_round_bf16(silu(g) * u));
+    }
+  #pragma omp parallel for schedule(static)
+  for (int j = 0; j < H; ++j)
+    for (int r = 0; r < K; ++r) {
+      double s = 0.0;
+      for (int i = 0; i < I; ++i) s += h[(size_t)r * I + i] * orc_bf16(Wd[(size_t)j * I + i]);
+      double v = s + (residual ? orc_bf16(residual[(size_t)r * H + j]) : 0.0);
+      y[(size_t)r * H + j] = orc_round_bf16(v);
+    }
+  free(h);
+}
+
 /* lm_head greedy token per row: argmax over V of the fixed-order FP32
  * logits of x_norm[r] . W[v]; an exact tie goes to the lower index.
  * best_logit (optional) receives the winning FP32 logit. */

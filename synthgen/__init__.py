@@ -42,6 +42,7 @@ T_X = 20
 T_ATT_Q, T_ATT_K, T_ATT_V, T_ATT_O, T_KCACHE, T_VCACHE = 30, 31, 32, 33, 34, 35
 T_LM_HEAD, T_DRAFT_J, T_DRAFT_TOK = 40, 41, 42
 T_COIN, T_ALT = 43, 44
+T_MLP_G, T_MLP_U, T_MLP_D = 45, 46, 47
 
 SCALE_LO, SCALE_HI = 2.0 ** -8, 2.0 ** -4
 ROUTER_SIGMA = 0.02
@@ -265,3 +266,34 @@ def make_coins(w: Workload, rounds: int, accept_pct: int = 75, instance: int = 0
     coin = (uniform_int(w.seed, instance, T_COIN, 0, n, 100) < accept_pct).astype(np.uint8).reshape(rounds, w.K)
     alt = uniform_int(w.seed, instance, T_ALT, 0, n, w.vocab - 1).reshape(rounds, w.K)
     return coin, alt
+
+
+# The Laguna layer schedule (README, "Why this challenge exists"): blocks of
+# four layers, three sliding-window (512 positions, 64 q heads, RoPE theta
+# 10000) then one full-attention (48 q heads, YaRN rotary on half the head
+# dims); layer 0 a dense bf16 SwiGLU MLP of intermediate 8192, every other
+# layer the MoE block.  YaRN factor and original context are readings:
+# factor 4 over an original 4,096 positions (the workloads' 16,384-position
+# context is four times that).
+LAGUNA_WINDOW, LAGUNA_THETA = 512, 10000.0
+LAGUNA_SLIDING_HEADS, LAGUNA_FULL_HEADS = 64, 48
+LAGUNA_YARN_FACTOR, LAGUNA_YARN_ORIG = 4.0, 4096
+LAGUNA_DENSE_INTER = 8192
+
+
+def laguna_layer_kind(layer: int) -> dict:
+    """Attention configuration of layer `layer`: n_q_heads, window,
+    rotary_dim, rope_theta, yarn_factor, yarn_orig; and whether its MLP is
+    the dense one."""
+    full = layer % 4 == 3
+    return dict(n_q_heads=LAGUNA_FULL_HEADS if full else LAGUNA_SLIDING_HEADS,
+                window=0 if full else LAGUNA_WINDOW, rotary_dim=64 if full else 128, rope_theta=LAGUNA_THETA,
+                yarn_factor=LAGUNA_YARN_FACTOR if full else 1.0, yarn_orig=LAGUNA_YARN_ORIG if full else 0,
+                dense=layer == 0)
+
+
+def make_dense_mlp(w: Workload, layer: int, inter: int = LAGUNA_DENSE_INTER) -> dict:
+    s, H = w.seed, w.H
+    return dict(Wg=normal_bf16(s, layer, T_MLP_G, 0, inter * H, 0.0, ROUTER_SIGMA).reshape(inter, H),
+                Wu=normal_bf16(s, layer, T_MLP_U, 0, inter * H, 0.0, ROUTER_SIGMA).reshape(inter, H),
+                Wd=normal_bf16(s, layer, T_MLP_D, 0, H * inter, 0.0, ROUTER_SIGMA).reshape(H, inter))

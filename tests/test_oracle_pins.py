@@ -694,3 +694,108 @@ def test_verify_rounds_causal_consistency():
     assert np.array_equal(two["targets"].reshape(-1), one["targets"].reshape(-1))
     for l in range(w.layers):
         assert np.array_equal(two["kc"][l], one["kc"][l]) and np.array_equal(two["vc"][l], one["vc"][l])
+
+
+# ---------------------------------------------------------------- Laguna layer schedule: RoPE / YaRN, window, dense MLP
+
+def test_rope_identity_norm_and_relative_position():
+    rng = np.random.default_rng(3)
+    rd, hd = 64, 128
+    f = oracle.rope_freqs(rd, 10000.0)
+    q, k = rng.standard_normal(hd), rng.standard_normal(hd)
+    assert np.array_equal(oracle.rope_vec(q, rd, f, 0), q)  # position 0 rotates by nothing
+    r = oracle.rope_vec(q, rd, f, 12345)
+    assert np.array_equal(r[rd:], q[rd:])  # dims past the rotary ones untouched
+    pn = lambda v: v[: rd // 2] ** 2 + v[rd // 2: rd] ** 2
+    assert np.allclose(pn(r), pn(q), rtol=1e-12)  # each pair keeps its length
+    # q_m . k_n depends only on m - n
+    d1 = oracle.rope_vec(q, rd, f, 700) @ oracle.rope_vec(k, rd, f, 650)
+    d2 = oracle.rope_vec(q, rd, f, 16400) @ oracle.rope_vec(k, rd, f, 16350)
+    assert abs(d1 - d2) <= 1e-9 * (abs(d1) + 1.0)
+    # rotate-half pairing: pair 0 is (dim 0, dim rd/2), angle = position * 1
+    e = np.zeros(hd)
+    e[0] = 1.0
+    v = oracle.rope_vec(e, rd, f, 1.0)
+    assert abs(v[0] - math.cos(1.0)) < 1e-15 and abs(v[rd // 2] - math.sin(1.0)) < 1e-15
+
+
+def test_yarn_frequencies_closed_form():
+    rd, s, L0 = 64, 4.0, 4096
+    base = 10000.0 ** (-2.0 * np.arange(rd // 2) / rd)
+    assert np.allclose(oracle.rope_freqs(rd, 10000.0, 1.0, L0), base, rtol=1e-15, atol=0)
+    f = oracle.rope_freqs(rd, 10000.0, s, L0)
+    r = L0 * base / (2 * math.pi)
+    g = np.clip((r - 1.0) / 31.0, 0.0, 1.0)
+    assert np.allclose(f, (1 - g) * base / s + g * base, rtol=1e-15)
+    assert abs(f[0] - base[0]) < 1e-15 and abs(f[-1] - base[-1] / s) < 1e-18  # fast pairs kept, slow ones interpolated
+    assert np.all(f <= base * (1 + 1e-15)) and np.all(f >= base / s * (1 - 1e-15))
+
+
+def _att_case(K, H, nq, nkv, C, seed):
+    hd = 128
+    g = lambda t, n, sd: synthgen.normal_bf16(seed, 0, t, 0, n, 0.0, sd)
+    return (g(36, K * H, 1.0).reshape(K, H), g(30, nq * hd * H, 0.05).reshape(nq * hd, H),
+            g(31, nkv * hd * H, 0.05).reshape(nkv * hd, H), g(32, nkv * hd * H, 0.05).reshape(nkv * hd, H),
+            g(33, H * nq * hd, 0.05).reshape(H, nq * hd), g(34, nkv * C * hd, 1.0).reshape(nkv, C, hd),
+            g(35, nkv * C * hd, 1.0).reshape(nkv, C, hd))
+
+
+def _torch_rope(x, rd, f, pos):  # independent restatement: rotate-half pairs, double
+    x = x.clone()
+    ang = torch.tensor(pos, dtype=torch.float64)[:, None] * torch.from_numpy(f)[None, :]
+    c, s = torch.cos(ang), torch.sin(ang)
+    a, b = x[..., : rd // 2].clone(), x[..., rd // 2: rd].clone()
+    x[..., : rd // 2] = a * c[:, None, :] - b * s[:, None, :]
+    x[..., rd // 2: rd] = b * c[:, None, :] + a * s[:, None, :]
+    return x
+
+
+@pytest.mark.parametrize("window,rd,yarn", [(0, 0, 1.0), (24, 128, 1.0), (40, 64, 4.0)])
+def test_attention_ex_against_library_sdpa(window, rd, yarn):
+    K, H, nq, nkv, C, hd = 3, 256, 4, 2, 37, 128
+    x, Wq, Wk, Wv, Wo, kc, vc = _att_case(K, H, nq, nkv, C, 31)
+    got = oracle.attention_ex(x, Wq, Wk, Wv, Wo, kc, vc, nq, nkv, hd, window=window, rotary_dim=rd,
+                              yarn_factor=yarn, yarn_orig=16)
+    xn = _bf(oracle.rmsnorm(x))
+    q = _bf16_round_t(xn @ _bf(Wq).T).view(K, nq, hd)
+    kn = _bf16_round_t(xn @ _bf(Wk).T).view(K, nkv, hd)
+    vn = _bf16_round_t(xn @ _bf(Wv).T).view(K, nkv, hd)
+    temp = 1.0
+    if rd:
+        base = 10000.0 ** (-2.0 * np.arange(rd // 2) / rd)
+        if yarn > 1:
+            g = np.clip((16 * base / (2 * math.pi) - 1.0) / 31.0, 0.0, 1.0)
+            base = (1 - g) * base / yarn + g * base
+            temp = (0.1 * math.log(yarn) + 1.0) ** 2
+        pos = [C + r for r in range(K)]
+        q = _bf16_round_t(_torch_rope(q, rd, base, pos))
+        kn = _bf16_round_t(_torch_rope(kn, rd, base, pos))
+    assert np.array_equal(got["k_new"], kn.reshape(K, -1).to(torch.float32).to(torch.bfloat16).view(torch.int16)
+                          .numpy().view(np.uint16))
+    kk = torch.cat([_bf(kc.reshape(-1, hd)).view(nkv, C, hd), kn.transpose(0, 1)], 1).repeat_interleave(nq // nkv, 0)
+    vv = torch.cat([_bf(vc.reshape(-1, hd)).view(nkv, C, hd), vn.transpose(0, 1)], 1).repeat_interleave(nq // nkv, 0)
+    mask = torch.zeros(K, C + K, dtype=torch.bool)
+    for r in range(K):
+        lo = max(0, C + r - window + 1) if window else 0
+        mask[r, lo: C + r + 1] = True
+    o = torch.nn.functional.scaled_dot_product_attention(q.transpose(0, 1), kk, vv, attn_mask=mask,
+                                                         scale=temp / math.sqrt(hd))
+    o = _bf16_round_t(o.transpose(0, 1).reshape(K, nq * hd))
+    assert np.allclose(synthgen.bf16_to_f32(got["o"]), o.numpy(), rtol=2.0 ** -7, atol=2e-3)
+    ref = _bf(x) + o @ _bf(Wo).T
+    assert np.allclose(synthgen.bf16_to_f32(got["x"]), ref.numpy(), rtol=2.0 ** -7, atol=2e-3)
+    if window == 0 and rd == 0:  # the plain block is the original attention function
+        assert np.array_equal(got["x"], oracle.attention(x, Wq, Wk, Wv, Wo, kc, vc, nq, nkv, hd))
+
+
+def test_dense_mlp_against_library():
+    K, H, I = 3, 256, 512
+    g = lambda t, n, sd: synthgen.normal_bf16(32, 0, t, 0, n, 0.0, sd)
+    xn = oracle.rmsnorm(g(1, K * H, 1.0).reshape(K, H))
+    res = g(2, K * H, 1.0).reshape(K, H)
+    Wg, Wu, Wd = g(3, I * H, 0.05).reshape(I, H), g(4, I * H, 0.05).reshape(I, H), g(5, H * I, 0.05).reshape(H, I)
+    y = oracle.dense_mlp(xn, res, Wg, Wu, Wd)
+    x64 = _bf(xn)
+    h = _bf16_round_t(torch.nn.functional.silu(x64 @ _bf(Wg).T) * (x64 @ _bf(Wu).T))
+    ref = _bf(res) + h @ _bf(Wd).T
+    assert np.allclose(synthgen.bf16_to_f32(y), ref.numpy(), rtol=2.0 ** -8, atol=1e-6)
