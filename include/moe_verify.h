@@ -247,7 +247,9 @@ moe_status verify_accept_prefix(const int32_t* draft, const int32_t* target, int
 moe_status moe_rmsnorm(const uint16_t* x, int K, int H, float eps, uint16_t* out, void* stream);
 
 /* Bytes of workspace moe_lm_head_argmax needs for K rows (zero-filled once
- * before first use; calls leave it ready for the next call). */
+ * before first use; calls leave it ready for the next call).  Its first
+ * int32 is the error word that moe_workspace_error reads (a device-side wait
+ * that ran out: MOE_ERR_DEVICE_TIMEOUT). */
 size_t moe_lm_head_workspace_size(int K);
 
 /*

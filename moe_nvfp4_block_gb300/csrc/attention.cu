@@ -151,6 +151,12 @@ static cudaError_t launch_rows_kernel(Kern kern, const Args& a, size_t sm, cudaS
 }
 
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t s, bool pdl) {
+  if (gemv_stream_fits(a, num_sms())) {
+    GemvArgs b = a;
+    b.rows_per_stage = gemv_rows_per_stage(a.D);
+    return launch_gemv_stream(b, s, pdl);
+  }
+  if (a.norm_eps > 0.f) return cudaErrorInvalidValue;  // the row kernel takes normalised rows only
   const size_t sm = sizeof(uint16_t) * a.K * a.D;
   if (a.K <= 4) return launch_rows_kernel(k_gemv_bf16<4>, a, sm, s, pdl);
   if (a.K <= 8) return launch_rows_kernel(k_gemv_bf16<8>, a, sm, s, pdl);
@@ -603,10 +609,20 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s, bool pdl) {
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, k_attn_split, a);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t c2 = cfg;
-  c2.gridDim = dim3(a.nq, a.K);
-  c2.blockDim = dim3(128);
-  return cudaLaunchKernelEx(&c2, k_attn_combine, a, splits);
+  return launch_attn_combine(a, splits, s);
+}
+
+cudaError_t launch_attn_combine(const AttnArgs& a, int splits, cudaStream_t s) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.nq, a.K);
+  cfg.blockDim = dim3(128);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_attn_combine, a, splits);
 }
 
 }  // namespace moe

@@ -98,6 +98,24 @@ bool encode_scales(CUtensorMap* m, const uint8_t* scales, int n_exp, int rows, i
   return r == CUDA_SUCCESS;
 }
 
+}  // namespace
+
+// 2-D map over a KV cache [nkv][C][128] bf16 seen as nkv * C rows of 128
+// dims; box 64 dims x 128 rows, 128-byte swizzle, zero fill past the end.
+bool moe::encode_kv_map(CUtensorMap* m, const uint16_t* cache, int nkv, int C) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {128, (cuuint64_t)nkv * (cuuint64_t)C};
+  cuuint64_t strides[1] = {256};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(cache), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 moe_status check_proj(const moe_nvfp4& p) {
@@ -354,8 +372,10 @@ size_t moe_lm_head_workspace_size(int K) {
   return lmhead_ws_bytes(K);
 }
 
-moe_status moe_lm_head_argmax(const uint16_t* x_norm, int K, int H, const uint16_t* W, int V, int32_t* tok,
-                              float* best_logit, void* ws, size_t ws_bytes, void* stream) {
+// lm_head argmax of x (normalised first, in the kernel, when norm_eps > 0).
+static moe_status lm_head_impl(const uint16_t* x_norm, int K, int H, const uint16_t* W, int V, int32_t* tok,
+                               float* best_logit, void* ws, size_t ws_bytes, float norm_eps, bool pdl,
+                               int* err, void* stream) {
   if (!x_norm || !W || !tok || !ws || K < 1 || K > MOE_MAX_ROWS || V < 1) return MOE_ERR_INVALID_ARG;
   if (H < 256 || H % 256 != 0 || H > 2048) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(x_norm) || !aligned16(W) || !aligned16(ws)) return MOE_ERR_MISALIGNED;
@@ -369,11 +389,25 @@ moe_status moe_lm_head_argmax(const uint16_t* x_norm, int K, int H, const uint16
   a.V = V;
   a.tok = tok;
   a.best = best_logit;
-  a.ticket = reinterpret_cast<unsigned*>(b);
+  a.err = err ? err : reinterpret_cast<int*>(b);
+  a.ticket = reinterpret_cast<unsigned*>(b + 4);
   a.part_v = reinterpret_cast<float*>(b + 256);
   a.part_i = reinterpret_cast<int*>(b + 256 + align256(sizeof(float) * kLmMaxGrid * K));
-  if (launch_lmhead(a, static_cast<cudaStream_t>(stream), false) != cudaSuccess) return MOE_ERR_CUDA;
-  return MOE_OK;
+  a.norm_eps = norm_eps;
+  a.wait_ns = g_wait_ns.load();
+  cudaError_t e;
+  if (lmhead_stream_fits(K, H)) {
+    e = launch_lmhead_stream(a, static_cast<cudaStream_t>(stream), pdl);
+  } else {
+    if (norm_eps > 0.f) return MOE_ERR_UNSUPPORTED_SHAPE;  // the row kernel takes normalised rows
+    e = launch_lmhead(a, static_cast<cudaStream_t>(stream), pdl);
+  }
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_lm_head_argmax(const uint16_t* x_norm, int K, int H, const uint16_t* W, int V, int32_t* tok,
+                              float* best_logit, void* ws, size_t ws_bytes, void* stream) {
+  return lm_head_impl(x_norm, K, H, W, V, tok, best_logit, ws, ws_bytes, 0.f, false, nullptr, stream);
 }
 
 struct AttnLayout {
@@ -456,11 +490,12 @@ static moe_status attention_impl(const uint16_t* x, int K, int H, int nq, int nk
   uint16_t* kn = k_new_out ? k_new_out : reinterpret_cast<uint16_t*>(b + L.kn);
   uint16_t* vn = v_new_out ? v_new_out : reinterpret_cast<uint16_t*>(b + L.vn);
   uint16_t* o = o_out ? o_out : reinterpret_cast<uint16_t*>(b + L.o);
-  if (launch_rmsnorm(x, K, H, eps, xn, s, false) != cudaSuccess) return MOE_ERR_CUDA;
   GemvArgs g{};
-  g.x = xn;
+  g.x = x;
   g.K = K;
   g.D = H;
+  g.norm_eps = eps;  // the streamed GEMV normalises the rows itself
+  g.wait_ns = g_wait_ns.load();
   const bool rope = pos && pos->rotary_dim > 0;
   g.seg[0] = {Wq, q, nullptr, nq * 128, nullptr, nullptr, 0};
   // with a device length, the new keys and values also go into the caches
@@ -472,6 +507,11 @@ static moe_status attention_impl(const uint16_t* x, int K, int H, int nq, int nk
   g.nseg = 3;
   g.n_total = (nq + 2 * nkv) * 128;
   g.err = err;
+  if (!gemv_stream_fits(g, num_sms())) {  // the row kernel takes normalised rows
+    if (launch_rmsnorm(x, K, H, eps, xn, s, false) != cudaSuccess) return MOE_ERR_CUDA;
+    g.x = xn;
+    g.norm_eps = 0.f;
+  }
   if (launch_gemv(g, s, true) != cudaSuccess) return MOE_ERR_CUDA;
   double temp = 1.0;
   if (rope) {
@@ -509,7 +549,15 @@ static moe_status attention_impl(const uint16_t* x, int K, int H, int nq, int nk
   a.scale_log2 = (float)(1.4426950408889634 * temp / std::sqrt(128.0));
   a.part_o = reinterpret_cast<float*>(b + L.part_o);
   a.part_ml = reinterpret_cast<float*>(b + L.part_ml);
-  if (launch_attention(a, s, true) != cudaSuccess) return MOE_ERR_CUDA;
+  a.err = err;
+  a.wait_ns = g_wait_ns.load();
+  AttnStreamArgs sa;
+  sa.a = a;
+  if (encode_kv_map(&sa.km, kcache, nkv, C) && encode_kv_map(&sa.vm, vcache, nkv, C)) {
+    if (launch_attention_stream(sa, s, true) != cudaSuccess) return MOE_ERR_CUDA;
+  } else if (launch_attention(a, s, true) != cudaSuccess) {
+    return MOE_ERR_CUDA;
+  }
   GemvArgs go{};
   go.x = o;
   go.K = K;
@@ -517,6 +565,8 @@ static moe_status attention_impl(const uint16_t* x, int K, int H, int nq, int nk
   go.seg[0] = {Wo, x_out, x, H, nullptr, nullptr, 0};
   go.nseg = 1;
   go.n_total = H;
+  go.err = err;
+  go.wait_ns = g_wait_ns.load();
   if (launch_gemv(go, s, true) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }
@@ -574,7 +624,7 @@ size_t moe_dense_mlp_workspace_size(int K, int H, int I) {
 
 static moe_status dense_mlp_impl(const uint16_t* x, int K, int H, int I, const uint16_t* Wg, const uint16_t* Wu,
                                  const uint16_t* Wd, float eps, uint16_t* x_out, char* b, const MlpLayout& L,
-                                 cudaStream_t s) {
+                                 int* err, cudaStream_t s) {
   uint16_t* xn = reinterpret_cast<uint16_t*>(b + L.xn);
   uint16_t* h = reinterpret_cast<uint16_t*>(b + L.h);
   if (launch_rmsnorm(x, K, H, eps, xn, s, false) != cudaSuccess) return MOE_ERR_CUDA;
@@ -587,6 +637,8 @@ static moe_status dense_mlp_impl(const uint16_t* x, int K, int H, int I, const u
   gd.seg[0] = {Wd, x_out, x, H, nullptr, nullptr, 0};
   gd.nseg = 1;
   gd.n_total = H;
+  gd.err = err;
+  gd.wait_ns = g_wait_ns.load();
   if (launch_gemv(gd, s, true) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }
@@ -603,7 +655,7 @@ moe_status moe_dense_mlp_block(const uint16_t* x, int K, int H, int I, const uin
   const MlpLayout L = mlp_layout(K, H, I);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   return dense_mlp_impl(x, K, H, I, Wg, Wu, Wd, eps, x_out, static_cast<char*>(ws), L,
-                        static_cast<cudaStream_t>(stream));
+                        reinterpret_cast<int*>(static_cast<char*>(ws) + L.hdr), static_cast<cudaStream_t>(stream));
 }
 
 static int layer_nq(const moe_verify_model* m, const moe_decoder_layer& d) {
@@ -688,12 +740,15 @@ static moe_status forward_impl(const moe_verify_model* m, uint16_t* x, int K, in
     if (s != MOE_OK) return s;
     if (d.mlp_gate)  // a dense SwiGLU MLP block (Laguna's layer 0)
       s = dense_mlp_impl(x, K, H, d.mlp_inter, d.mlp_gate, d.mlp_up, d.mlp_down, m->eps, x, b + L.mlp_ws,
-                         mlp_layout(K, H, d.mlp_inter), st);
+                         mlp_layout(K, H, d.mlp_inter), err, st);
     else  // the MoE layer kernel applies its RMSNorm to x itself
       s = run_layer(&d.moe, x, K, x, x, nullptr, nullptr, nullptr, b + L.moe_ws, L.moe_bytes, st, true, nullptr,
                     m->eps);
     if (s != MOE_OK) return s;
   }
+  if (lmhead_stream_fits(K, H))  // the final RMSNorm inside the lm_head kernel
+    return lm_head_impl(x, K, H, m->lm_head, m->vocab, target, nullptr, b + L.lm_ws, lmhead_ws_bytes(K), m->eps,
+                        true, err, st);
   if (launch_rmsnorm(x, K, H, m->eps, xn, st, false) != cudaSuccess) return MOE_ERR_CUDA;
   return moe_lm_head_argmax(xn, K, H, m->lm_head, m->vocab, target, nullptr, b + L.lm_ws, lmhead_ws_bytes(K), st);
 }

@@ -171,7 +171,7 @@ constexpr int kTraceSlots = 80;
 extern unsigned long long* g_trace;  // debug timeline buffer (null = off)
 
 struct LmHeadArgs {
-  const uint16_t* x;  // [K][H] normalised rows
+  const uint16_t* x;  // [K][H] normalised rows (raw rows when norm_eps > 0)
   const uint16_t* W;  // [V][H]
   int K, H, V;
   int32_t* tok;       // [K] out
@@ -179,6 +179,10 @@ struct LmHeadArgs {
   float* part_v;      // [grid][K]
   int* part_i;        // [grid][K]
   unsigned* ticket;
+  float norm_eps;     // streamed kernel: > 0 normalises x while staged
+  int rows_per_stage; // streamed kernel (set by its launcher)
+  int* err;           // streamed kernel: a ring wait that ran out, or null
+  uint64_t wait_ns;
 };
 
 constexpr int kLmMaxGrid = 1024;
@@ -200,7 +204,10 @@ struct GemvArgs {
   int K, D;
   GemvSeg seg[3];
   int nseg, n_total;
-  int* err;           // error word (a cache append past its capacity), or null
+  int* err;           // error word (a cache append past its capacity, a wait that ran out), or null
+  float norm_eps;     // > 0: x is RMS-normalised first (streamed kernel only)
+  int rows_per_stage; // streamed kernel: weight rows per ring stage (set by the launcher)
+  uint64_t wait_ns;   // streamed kernel: limit of each ring wait
 };
 
 struct AttnArgs {
@@ -217,6 +224,15 @@ struct AttnArgs {
   float scale_log2;       // log2(e) * temperature / sqrt(128)
   float* part_o;          // [nkv][splits][tiles * 16][128]
   float* part_ml;         // [nkv][splits][tiles * 16][2]
+  int* err;               // error word (a ring wait that ran out), or null
+  uint64_t wait_ns;       // limit of each ring wait (streamed kernel)
+};
+
+// The streamed split kernel's arguments: the caches as 2-D bf16 tensor maps
+// over [nkv * C rows][128 dims], box 64 dims x 128 rows, 128-byte swizzle.
+struct AttnStreamArgs {
+  AttnArgs a;
+  CUtensorMap km, vm;
 };
 
 constexpr int kAttnMaxSplits = 64;
@@ -249,7 +265,16 @@ struct SwigluArgs {
 cudaError_t launch_swiglu(const SwigluArgs& a, cudaStream_t s, bool pdl);
 
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t s, bool pdl);
+// The streamed GEMV (csrc/gemv.cu): whether it takes `a` on `grid` CTAs, and
+// its launch (rows_per_stage filled in by launch_gemv).
+bool gemv_stream_fits(const GemvArgs& a, int grid);
+int gemv_rows_per_stage(int D);
+cudaError_t launch_gemv_stream(const GemvArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s, bool pdl);
+cudaError_t launch_attention_stream(const AttnStreamArgs& p, cudaStream_t s, bool pdl);
+cudaError_t launch_attn_combine(const AttnArgs& a, int splits, cudaStream_t s);
+int attn_stream_splits(int nkv, int tiles, int C, int window);
+bool encode_kv_map(CUtensorMap* m, const uint16_t* cache, int nkv, int C);
 int attn_splits(int nkv, int tiles, int max_chunks);
 
 inline size_t lmhead_ws_bytes(int K) { return 256 + align256(sizeof(float) * kLmMaxGrid * K) + sizeof(int) * kLmMaxGrid * K; }
@@ -257,6 +282,8 @@ inline size_t lmhead_ws_bytes(int K) { return 256 + align256(sizeof(float) * kLm
 // Launchers (return cudaGetLastError()).
 cudaError_t launch_rmsnorm(const uint16_t* x, int K, int H, float eps, uint16_t* out, cudaStream_t s, bool pdl);
 cudaError_t launch_lmhead(const LmHeadArgs& a, cudaStream_t s, bool pdl);
+bool lmhead_stream_fits(int K, int H);
+cudaError_t launch_lmhead_stream(const LmHeadArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s, bool pdl);
 // One launch of the experts kernel: maps [kMapsPerLayer].
 cudaError_t launch_experts(const ExpertsCommon& c, const CUtensorMap* maps, const LayerDesc& desc, cudaStream_t s,

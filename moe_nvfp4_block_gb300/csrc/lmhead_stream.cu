@@ -1,0 +1,301 @@
+// lmhead_stream.cu -- the lm_head greedy argmax with the vocab rows streamed
+// into shared memory by bulk copies.
+//
+// Logit (r, v) = fixed-order FP32 dot product of the normalised row x_r with
+// vocab row v: lane l of a warp owns elements 256 j + 8 l + i and
+// accumulates them in element order, the 32 lane sums are added in xor
+// rounds 16, 8, 4, 2, 1.  An exact tie goes to the lower vocab index.  The
+// order is the same as the row kernel's in stack.cu, so both give the same
+// logits bit for bit.
+//
+// One CTA per SM owns a contiguous range of vocab rows.  Stages of R rows
+// (R = min(8, 16384 / H), at most 32 KB) go through five ring slots; warp
+// pair p owns slot p and takes the stages p, p + 5, ...; each of its two
+// warps reduces R / 2 rows of a stage, so every 16-byte load of x from shared
+// memory serves R / 2 rows.  The weights do not depend on the previous
+// kernel, so the first five stages are issued before the dependency wait.
+// Optionally the rows of x are RMS-normalised while staged (the RMSNorm
+// kernel's fixed order and rounding, so bit-identical to normalising first).
+#include <cfloat>
+#include <climits>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kLsPairs = 5;
+constexpr int kLsWarps = 2 * kLsPairs;
+constexpr int kLsSlotBytes = 32768;
+constexpr int kLsRowsPerWarp = 4;
+
+__device__ __forceinline__ float lbf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float lbf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ float lsum_xor(float v) {
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, d));
+  return v;
+}
+
+__device__ __forceinline__ bool l_before(float la, int a, float lb, int b) {
+  return (la > lb) || (la == lb && a < b);
+}
+
+struct LsTable {
+  uint64_t full[kLsPairs];
+  uint64_t empty[kLsPairs];
+  int abort;
+  int last;
+  float inv[16];
+  float bv[kLsWarps][16];
+  int bi[kLsWarps][16];
+};
+
+}  // namespace
+
+template <int KR>
+__global__ void __launch_bounds__(kLsWarps * 32, 1) k_lmhead_stream(const __grid_constant__ LmHeadArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int K = a.K, H = a.H, V = a.V;
+  uint4* xs = reinterpret_cast<uint4*>(smem + kLsPairs * kLsSlotBytes);
+  LsTable& T = *reinterpret_cast<LsTable*>(smem + kLsPairs * kLsSlotBytes + (size_t)K * H * 2);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int p = warp >> 1, hw = warp & 1;
+  const int R = a.rows_per_stage;
+  const int v0 = (int)((long long)blockIdx.x * V / gridDim.x);
+  const int v1 = (int)((long long)(blockIdx.x + 1) * V / gridDim.x);
+  const int nst = (v1 - v0 + R - 1) / R;
+  const uint32_t row_bytes = (uint32_t)H * 2u;
+  auto issue = [&](int s, uint64_t pol) {
+    const int slot = s % kLsPairs;
+    const int vb = v0 + s * R;
+    const uint32_t bytes = (uint32_t)min(R, v1 - vb) * row_bytes;
+    mbar_arrive_expect_tx(&T.full[slot], bytes);
+    bulk_load(smem + (size_t)slot * kLsSlotBytes, a.W + (size_t)vb * H, bytes, &T.full[slot], pol);
+  };
+  if (threadIdx.x == 0) {
+    T.abort = 0;
+    for (int i = 0; i < kLsPairs; ++i) {
+      mbar_init(&T.full[i], 1);
+      mbar_init(&T.empty[i], 2);
+    }
+    fence_mbar_init();
+    const uint64_t pol = policy_evict_first();
+    for (int s = 0; s < min(nst, kLsPairs); ++s) issue(s, pol);
+  }
+  __syncthreads();
+  pdl_wait();
+  pdl_launch_dependents();
+  block_copy_g2s(xs, reinterpret_cast<const uint4*>(a.x), K * H / 8);
+  __syncthreads();
+  if (a.norm_eps > 0.f) {
+    for (int r = warp; r < K; r += kLsWarps) {
+      float acc = 0.f;
+      for (int j = 0; j < H / 256; ++j) {
+        const uint4 xv = xs[r * (H / 8) + j * 32 + lane];
+        const uint32_t q[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float f = (i & 1) ? lbf_hi(q[i >> 1]) : lbf_lo(q[i >> 1]);
+          acc = __fmaf_rn(f, f, acc);
+        }
+      }
+      acc = lsum_xor(acc);
+      const float mean = __fdiv_rn(acc, (float)H);
+      if (lane == 0) T.inv[r] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, a.norm_eps)));
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < K * H / 8; i += blockDim.x) {
+      const float inv = T.inv[i / (H / 8)];
+      uint4 v = xs[i];
+      uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t lo = float_to_bf16_bits(__fmul_rn(lbf_lo(w[u]), inv));
+        const uint32_t hi = float_to_bf16_bits(__fmul_rn(lbf_hi(w[u]), inv));
+        w[u] = lo | (hi << 16);
+      }
+      xs[i] = v;
+    }
+    __syncthreads();
+  }
+
+  float bv[KR];
+  int bi[KR];
+#pragma unroll
+  for (int r = 0; r < KR; ++r) {
+    bv[r] = -INFINITY;
+    bi[r] = INT_MAX;
+  }
+  const int nj = H / 256;
+  const int rpw = R / 2;  // rows per warp (<= 4)
+  volatile int* abort = &T.abort;
+  uint64_t pol = 0;
+  if (hw == 0 && lane == 0) pol = policy_evict_first();
+  int issued = (p < nst) ? 1 : 0;  // this slot's copies (lane 0 of the pair's first warp)
+  for (int s = p, k = 0; s < nst; s += kLsPairs, ++k) {
+    const uint32_t par = (uint32_t)k & 1u;
+    bool ok = !*abort && mbar_wait_bounded(&T.full[p], par, a.wait_ns, abort);
+    ok = __all_sync(0xffffffffu, ok);
+    const int vb = v0 + s * R;
+    const int nr = min(R, v1 - vb);
+    float acc[kLsRowsPerWarp][KR];
+#pragma unroll
+    for (int q = 0; q < kLsRowsPerWarp; ++q)
+#pragma unroll
+      for (int r = 0; r < KR; ++r) acc[q][r] = 0.f;
+    if (!ok) {
+      *abort = 1;
+    } else {
+      const uint4* ws = reinterpret_cast<const uint4*>(smem + (size_t)p * kLsSlotBytes);
+      for (int j = 0; j < nj; ++j) {
+        uint32_t wq[kLsRowsPerWarp][4];
+#pragma unroll
+        for (int q = 0; q < kLsRowsPerWarp; ++q) {
+          const int row = hw * rpw + q;
+          if (q < rpw && row < nr) {
+            const uint4 v = ws[row * (H / 8) + j * 32 + lane];
+            wq[q][0] = v.x;
+            wq[q][1] = v.y;
+            wq[q][2] = v.z;
+            wq[q][3] = v.w;
+          } else {
+            wq[q][0] = wq[q][1] = wq[q][2] = wq[q][3] = 0u;
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < KR; ++r) {
+          if (r < K) {
+            const uint4 xv = xs[r * (H / 8) + j * 32 + lane];
+            const uint32_t xq[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float xf = (i & 1) ? lbf_hi(xq[i >> 1]) : lbf_lo(xq[i >> 1]);
+#pragma unroll
+              for (int q = 0; q < kLsRowsPerWarp; ++q) {
+                const float wf = (i & 1) ? lbf_hi(wq[q][i >> 1]) : lbf_lo(wq[q][i >> 1]);
+                acc[q][r] = __fmaf_rn(xf, wf, acc[q][r]);
+              }
+            }
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&T.empty[p]);
+    if (hw == 0 && lane == 0 && s + kLsPairs < nst) {
+      // refill this pair's slot once both warps have read it
+      if (!*abort && mbar_wait_bounded(&T.empty[p], par, a.wait_ns, abort)) {
+        issue(s + kLsPairs, pol);
+        ++issued;
+      } else {
+        *abort = 1;
+      }
+    }
+    __syncwarp();
+    if (ok) {
+#pragma unroll
+      for (int q = 0; q < kLsRowsPerWarp; ++q) {
+        const int row = hw * rpw + q;
+        if (q < rpw && row < nr) {
+#pragma unroll
+          for (int r = 0; r < KR; ++r) {
+            if (r < K) {
+              const float l = lsum_xor(acc[q][r]);
+              if (bi[r] == INT_MAX || l > bv[r]) {  // this warp's rows arrive in increasing order
+                bv[r] = l;
+                bi[r] = vb + row;
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (*abort) {
+    // no copy may land in a finished CTA; the ticket is still taken (the
+    // tokens of this call are undefined, the next call starts clean)
+    if (hw == 0 && lane == 0 && issued > 0) mbar_wait_drain(&T.full[p], (uint32_t)(issued - 1) & 1u, a.wait_ns);
+    if (threadIdx.x == 0 && a.err) atomicCAS(a.err, 0, (int)MOE_ERR_DEVICE_TIMEOUT);
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int r = 0; r < KR; ++r) {
+      T.bv[warp][r] = bv[r];
+      T.bi[warp][r] = bi[r];
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < K) {
+    const int r = threadIdx.x;
+    float b = -INFINITY;
+    int i = INT_MAX;
+    for (int w = 0; w < kLsWarps; ++w)
+      if (T.bi[w][r] != INT_MAX && (i == INT_MAX || l_before(T.bv[w][r], T.bi[w][r], b, i))) {
+        b = T.bv[w][r];
+        i = T.bi[w][r];
+      }
+    a.part_v[blockIdx.x * K + r] = b;
+    a.part_i[blockIdx.x * K + r] = i;
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) T.last = (atomicAdd(a.ticket, 1u) == gridDim.x - 1);
+  __syncthreads();
+  if (!T.last) return;
+  __threadfence();
+  if (threadIdx.x < K) {
+    const int r = threadIdx.x;
+    float b = -INFINITY;
+    int i = INT_MAX;
+    for (int c = 0; c < (int)gridDim.x; ++c) {
+      const float cv = __ldcg(a.part_v + c * K + r);
+      const int ci = __ldcg(a.part_i + c * K + r);
+      if (ci != INT_MAX && (i == INT_MAX || l_before(cv, ci, b, i))) {
+        b = cv;
+        i = ci;
+      }
+    }
+    a.tok[r] = i;
+    if (a.best) a.best[r] = b;
+  }
+  if (threadIdx.x == 0) *a.ticket = 0u;
+}
+
+size_t lmhead_stream_smem(int K, int H) {
+  return (size_t)kLsPairs * kLsSlotBytes + (size_t)K * H * 2 + sizeof(LsTable);
+}
+
+bool lmhead_stream_fits(int K, int H) {
+  return K <= 16 && H % 256 == 0 && H <= 8192 && lmhead_stream_smem(K, H) <= 227 * 1024;
+}
+
+cudaError_t launch_lmhead_stream(const LmHeadArgs& a0, cudaStream_t s, bool pdl) {
+  LmHeadArgs a = a0;
+  a.rows_per_stage = kLsSlotBytes / (2 * a.H) < 2 * kLsRowsPerWarp ? kLsSlotBytes / (2 * a.H) : 2 * kLsRowsPerWarp;
+  const size_t sm = lmhead_stream_smem(a.K, a.H);
+  auto run = [&](auto kern) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms());
+    cfg.blockDim = dim3(kLsWarps * 32);
+    cfg.dynamicSmemBytes = sm;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+  };
+  if (a.K <= 4) return run(k_lmhead_stream<4>);
+  if (a.K <= 8) return run(k_lmhead_stream<8>);
+  return run(k_lmhead_stream<16>);
+}
+
+}  // namespace moe
