@@ -64,6 +64,10 @@ def parse(argv=None):
     p.add_argument("--no-full-step", action="store_true", help="skip the full verify step (attention + MoE)")
     p.add_argument("--only-full-step", action="store_true",
                    help="run only the full verify step and print its JSON object (for profiling its launches)")
+    p.add_argument("--kernel-case", choices=["attention", "lm_head"], default=None,
+                   help="run only one attention block (K=4, H=2048, 32/8 heads, 16,384 cached positions) or one "
+                        "lm_head argmax (151,936 x 2048) a few times and print its time (a small case for ncu)")
+    p.add_argument("--case-iters", type=int, default=20)
     p.add_argument("--oracle-sample", type=float, default=None,
                    help="(internal) time the CPU oracle for this many seconds and print bytes/s as JSON")
     return p.parse_args(argv)
@@ -290,6 +294,9 @@ def run_gpu(args):
         dist.init_process_group("nccl", init_method="env://")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if args.kernel_case:
+        print(json.dumps(kernel_case(M, torch, dev, args.kernel_case, args.case_iters)), flush=True)
+        return
     if args.only_full_step:
         hbm, _ = peaks()
         stream = torch.cuda.Stream(device=dev)
@@ -626,6 +633,45 @@ def full_step(M, torch, synthgen, dev, stream, hbm, steps):
     del layers, model
     torch.cuda.empty_cache()
     return res
+
+
+def kernel_case(M, torch, dev, which, iters):
+    """One attention block of the full-step shape or one lm_head argmax,
+    launched `iters` times back to back on one stream (no graph), random bf16
+    operands; µs per call and algorithmic GB/s.  Sized for an ncu capture
+    (about 0.1 / 0.6 GB on the device)."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    r = lambda *s, sd=0.02: (torch.randn(*s, device=dev, generator=g) * sd).to(torch.bfloat16)
+    K, H, nq, nkv, C, V = 4, 2048, 32, 8, 16384, 151936
+    st = torch.cuda.Stream(device=dev)
+    if which == "attention":
+        Wq, Wk, Wv, Wo = r(nq * 128, H), r(nkv * 128, H), r(nkv * 128, H), r(H, nq * 128)
+        kc, vc = r(nkv, C, 128, sd=1.0), r(nkv, C, 128, sd=1.0)
+        x = r(K, H, sd=1.0)
+        ws = M.attention_workspace(K, H, nq, nkv, device=dev)
+        call = lambda: M.moe_attention_block(x, Wq, Wk, Wv, Wo, kc, vc, x, ws, nq, nkv, stream=st)
+        nbytes = 2 * ((nq + 2 * nkv) * 128 * H + H * nq * 128 + 2 * nkv * C * 128 + 2 * K * H)
+    else:
+        lm = r(V, H)
+        xn = r(K, H, sd=1.0)
+        tok = torch.empty(K, dtype=torch.int32, device=dev)
+        ws = M.lm_head_workspace(K, device=dev)
+        call = lambda: M.moe_lm_head_argmax(xn, lm, tok, ws, stream=st)
+        nbytes = 2 * (V * H + K * H)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    with torch.cuda.stream(st):
+        for _ in range(3):
+            call()
+        ev[0].record(st)
+        for _ in range(iters):
+            call()
+        ev[1].record(st)
+    st.synchronize()
+    us = ev[0].elapsed_time(ev[1]) * 1e3 / iters
+    assert M.moe_workspace_error(ws, st) == 0
+    return {"kernel_case": which, "us_per_call": round(us, 2), "GBps": round(nbytes / (us * 1e-6) / 1e9, 1),
+            "bytes": nbytes, "iters": iters}
 
 
 def verify_loop(M, torch, synthgen, dev, stream, model, w, steps, rounds=16, accept_pct=75):

@@ -23,6 +23,7 @@ __global__ void __launch_bounds__(32) k_accept(const int32_t* __restrict__ draft
 }
 
 cudaError_t launch_accept(const int32_t* draft, const int32_t* target, int K, int32_t* out, cudaStream_t s) {
+  max_carveout(k_accept);
   k_accept<<<1, 32, 0, s>>>(draft, target, K, out);
   return cudaGetLastError();
 }
@@ -46,6 +47,7 @@ __global__ void k_kv_commit(int32_t* len, const int32_t* n_accepted, int K, int 
 }
 
 cudaError_t launch_kv_commit(int32_t* len, const int32_t* n_accepted, int K, int cap, int* err, cudaStream_t s) {
+  max_carveout(k_kv_commit);
   k_kv_commit<<<1, 1, 0, s>>>(len, n_accepted, K, cap, err);
   return cudaGetLastError();
 }
@@ -64,6 +66,7 @@ __global__ void k_synthetic_drafts(const int32_t* target, const uint8_t* coin, c
 
 cudaError_t launch_synthetic_drafts(const int32_t* target, const uint8_t* coin, const int32_t* alt, int K, int vocab,
                                     int32_t* draft, cudaStream_t s) {
+  max_carveout(k_synthetic_drafts);
   k_synthetic_drafts<<<1, 32, 0, s>>>(target, coin, alt, K, vocab, draft);
   return cudaGetLastError();
 }

@@ -136,6 +136,7 @@ __global__ void __launch_bounds__(256) k_gemv_bf16(GemvArgs a) {
 template <typename Kern, typename Args>
 static cudaError_t launch_rows_kernel(Kern kern, const Args& a, size_t sm, cudaStream_t s, bool pdl) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e == cudaSuccess) e = max_carveout(kern);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * num_sms());
@@ -290,6 +291,7 @@ cudaError_t launch_rope(const RopeArgs& a, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  max_carveout(k_rope);
   return cudaLaunchKernelEx(&cfg, k_rope, a);
 }
 
@@ -607,6 +609,7 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s, bool pdl) {
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  max_carveout(k_attn_split);
   cudaError_t e = cudaLaunchKernelEx(&cfg, k_attn_split, a);
   if (e != cudaSuccess) return e;
   return launch_attn_combine(a, splits, s);
@@ -622,6 +625,7 @@ cudaError_t launch_attn_combine(const AttnArgs& a, int splits, cudaStream_t s) {
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  max_carveout(k_attn_combine);
   return cudaLaunchKernelEx(&cfg, k_attn_combine, a, splits);
 }
 

@@ -2,8 +2,9 @@
 // keys and values streamed into shared memory by TMA.
 //
 // CTA (split, KV head, query tile) walks a contiguous range of 128-position
-// chunks of its KV head.  Each chunk is four 16 KB boxes (keys, values; head
-// dims 0-63 and 64-127), 128-byte swizzled, in a ring of three 64 KB stages.
+// chunks of its KV head.  A chunk's keys and its values are each one 32 KB
+// box (128 rows x head dims 0-63 and 64-127, 128-byte swizzled), in a ring of
+// three 64 KB stages.
 // The cache below the valid length does not depend on the previous kernel
 // (the new rows' projection), so the first ring-full is issued before the
 // dependency wait.  Warp w takes positions [16w, 16w + 16) of every chunk:
@@ -98,10 +99,15 @@ __global__ void __launch_bounds__(kAsWarps * 32, 1) k_attn_stream(const __grid_c
     unsigned char* st = smem + (size_t)slot * kAsStageBytes;
     const int row = kvh * a.C + (c0 + s) * kAsPos;
     mbar_arrive_expect_tx(&T.full[slot], kAsStageBytes);
-    tma_load_2d(st, &P.km, 0, row, &T.full[slot], pol);
-    tma_load_2d(st + kAsHalf, &P.km, 64, row, &T.full[slot], pol);
-    tma_load_2d(st + 2 * kAsHalf, &P.vm, 0, row, &T.full[slot], pol);
-    tma_load_2d(st + 3 * kAsHalf, &P.vm, 64, row, &T.full[slot], pol);
+    if (P.kv3d) {  // one box per chunk: [half][row][64 dims]
+      tma_load_3d(st, &P.km, 0, row, 0, &T.full[slot], pol);
+      tma_load_3d(st + 2 * kAsHalf, &P.vm, 0, row, 0, &T.full[slot], pol);
+    } else {
+      tma_load_2d(st, &P.km, 0, row, &T.full[slot], pol);
+      tma_load_2d(st + kAsHalf, &P.km, 64, row, &T.full[slot], pol);
+      tma_load_2d(st + 2 * kAsHalf, &P.vm, 0, row, &T.full[slot], pol);
+      tma_load_2d(st + 3 * kAsHalf, &P.vm, 64, row, &T.full[slot], pol);
+    }
   };
   if (threadIdx.x == 0) {
     T.abort = 0;
@@ -317,6 +323,7 @@ cudaError_t launch_attention_stream(const AttnStreamArgs& P, cudaStream_t s, boo
   const int splits = attn_stream_splits(a.nkv, a.tiles, a.C, a.window);
   const size_t sm = attn_stream_smem();
   cudaError_t e = cudaFuncSetAttribute(k_attn_stream, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e == cudaSuccess) e = max_carveout(k_attn_stream);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

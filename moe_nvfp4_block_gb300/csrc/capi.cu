@@ -100,15 +100,30 @@ bool encode_scales(CUtensorMap* m, const uint8_t* scales, int n_exp, int rows, i
 
 }  // namespace
 
-// 2-D map over a KV cache [nkv][C][128] bf16 seen as nkv * C rows of 128
-// dims; box 64 dims x 128 rows, 128-byte swizzle, zero fill past the end.
-bool moe::encode_kv_map(CUtensorMap* m, const uint16_t* cache, int nkv, int C) {
+// Map over a KV cache [nkv][C][128] bf16 seen as nkv * C rows of 128 dims,
+// 128-byte swizzle, zero fill past the end.  Preferred: 3-D (64 dims, rows,
+// 2 dim halves), one 32 KB box = 128 rows x both halves laid out as
+// [half][row][64 dims]; else 2-D with a box of one half (64 dims x 128 rows).
+bool moe::encode_kv_map(CUtensorMap* m, const uint16_t* cache, int nkv, int C, bool* is3d) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
+  {
+    cuuint64_t dims[3] = {64, (cuuint64_t)nkv * (cuuint64_t)C, 2};
+    cuuint64_t strides[2] = {256, 128};
+    cuuint32_t box[3] = {64, 128, 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(cache), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS) {
+      *is3d = true;
+      return true;
+    }
+  }
   cuuint64_t dims[2] = {128, (cuuint64_t)nkv * (cuuint64_t)C};
   cuuint64_t strides[1] = {256};
   cuuint32_t box[2] = {64, 128};
   cuuint32_t estr[2] = {1, 1};
+  *is3d = false;
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(cache), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -553,7 +568,9 @@ static moe_status attention_impl(const uint16_t* x, int K, int H, int nq, int nk
   a.wait_ns = g_wait_ns.load();
   AttnStreamArgs sa;
   sa.a = a;
-  if (encode_kv_map(&sa.km, kcache, nkv, C) && encode_kv_map(&sa.vm, vcache, nkv, C)) {
+  bool k3 = false, v3 = false;
+  if (encode_kv_map(&sa.km, kcache, nkv, C, &k3) && encode_kv_map(&sa.vm, vcache, nkv, C, &v3) && k3 == v3) {
+    sa.kv3d = k3 ? 1 : 0;
     if (launch_attention_stream(sa, s, true) != cudaSuccess) return MOE_ERR_CUDA;
   } else if (launch_attention(a, s, true) != cudaSuccess) {
     return MOE_ERR_CUDA;

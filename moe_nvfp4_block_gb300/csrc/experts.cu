@@ -1562,6 +1562,7 @@ static cudaError_t launch_experts_t(const ExpertsCommon& c, const CUtensorMap* m
   for (int j = 0; j < kMapsPerLayer; ++j) p.maps[j] = maps[j];
   p.L = desc;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err == cudaSuccess) err = max_carveout(kern);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);

@@ -289,6 +289,7 @@ cudaError_t launch_gemv_stream(const GemvArgs& a, cudaStream_t s, bool pdl) {
   if (!kern) return cudaErrorInvalidValue;
   const size_t sm = (size_t)kGsStages * kGsStageBytes + kGsTail;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e == cudaSuccess) e = max_carveout(kern);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms());

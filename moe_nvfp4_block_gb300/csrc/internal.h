@@ -228,11 +228,12 @@ struct AttnArgs {
   uint64_t wait_ns;       // limit of each ring wait (streamed kernel)
 };
 
-// The streamed split kernel's arguments: the caches as 2-D bf16 tensor maps
-// over [nkv * C rows][128 dims], box 64 dims x 128 rows, 128-byte swizzle.
+// The streamed split kernel's arguments: the caches as bf16 tensor maps over
+// [nkv * C rows][128 dims] with the 128-byte swizzle (encode_kv_map).
 struct AttnStreamArgs {
   AttnArgs a;
   CUtensorMap km, vm;
+  int kv3d;  // the maps are 3-D (one box per chunk) rather than 2-D (one per dim half)
 };
 
 constexpr int kAttnMaxSplits = 64;
@@ -274,7 +275,7 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_attention_stream(const AttnStreamArgs& p, cudaStream_t s, bool pdl);
 cudaError_t launch_attn_combine(const AttnArgs& a, int splits, cudaStream_t s);
 int attn_stream_splits(int nkv, int tiles, int C, int window);
-bool encode_kv_map(CUtensorMap* m, const uint16_t* cache, int nkv, int C);
+bool encode_kv_map(CUtensorMap* m, const uint16_t* cache, int nkv, int C, bool* is3d);
 int attn_splits(int nkv, int tiles, int max_chunks);
 
 inline size_t lmhead_ws_bytes(int K) { return 256 + align256(sizeof(float) * kLmMaxGrid * K) + sizeof(int) * kLmMaxGrid * K; }
@@ -295,6 +296,15 @@ cudaError_t launch_synthetic_drafts(const int32_t* target, const uint8_t* coin, 
                                     int32_t* draft, cudaStream_t s);
 
 int num_sms();
+
+// Every kernel of the library asks for the same L1/shared-memory split (all
+// shared): an SM that runs one kernel's CTAs can then take the next kernel's
+// CTAs (programmatic dependent launch) without first draining to change it.
+template <typename Kern>
+inline cudaError_t max_carveout(Kern kern) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              (int)cudaSharedmemCarveoutMaxShared);
+}
 
 }  // namespace moe
 

@@ -280,6 +280,7 @@ cudaError_t launch_lmhead_stream(const LmHeadArgs& a0, cudaStream_t s, bool pdl)
   const size_t sm = lmhead_stream_smem(a.K, a.H);
   auto run = [&](auto kern) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e == cudaSuccess) e = max_carveout(kern);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_sms());

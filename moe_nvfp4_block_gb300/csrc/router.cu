@@ -287,6 +287,7 @@ template <int KR>
 static cudaError_t launch_router_t(const RouterArgs& a, cudaStream_t s, bool pdl) {
   const size_t sm = router_smem(a);
   cudaError_t err = cudaFuncSetAttribute(k_router<KR>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (err == cudaSuccess) err = max_carveout(k_router<KR>);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((a.E + kRouterWarps - 1) / kRouterWarps);

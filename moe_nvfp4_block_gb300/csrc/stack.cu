@@ -100,6 +100,7 @@ cudaError_t launch_rmsnorm(const uint16_t* x, int K, int H, float eps, uint16_t*
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  max_carveout(k_rmsnorm);
   return cudaLaunchKernelEx(&cfg, k_rmsnorm, x, K, H, eps, out);
 }
 
@@ -233,6 +234,7 @@ cudaError_t launch_lmhead(const LmHeadArgs& a, cudaStream_t s, bool pdl) {
   const size_t sm = sizeof(uint16_t) * a.K * a.H;
   auto run = [&](auto kern) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e == cudaSuccess) e = max_carveout(kern);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(lmhead_grid());
