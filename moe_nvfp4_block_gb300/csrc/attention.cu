@@ -516,24 +516,36 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn_split(AttnArgs a) {
 // One CTA per (query head h, row r); 128 threads = head dims.  Merges the
 // splits of KV head h/group in split order with the row's visible new
 // positions 0..r and writes o = bf16(O / L).  Every global load is issued up
-// front (the split maxima and sums to shared memory, this thread's split
-// outputs, q and the new keys and values to registers), so the kernel waits
-// for about one memory round trip instead of one per split or position.
+// front (warp 0: the splits' maxima and sums; every thread: its dims of the
+// splits' outputs, q and the new keys and values), then warp 0 forms the
+// split weights exp2(m_s - M) and L with shuffles, so the CTA waits for
+// about one memory round trip and does no serial pass over the splits but
+// the in-order accumulation of O.  The dependent kernel (the o-projection,
+// which reads only its weights before its own wait) is released at once.
 __global__ void __launch_bounds__(128) k_attn_combine(AttnArgs a, int splits) {
   __shared__ float s_red[4][16];
-  __shared__ float s_sc[16];
-  __shared__ float s_ms[kAttnMaxSplits], s_ls[kAttnMaxSplits];
+  __shared__ float s_f[kAttnMaxSplits];
+  __shared__ float s_fj[16];
+  __shared__ float s_L;
   const int h = blockIdx.x, r = blockIdx.y, d = threadIdx.x;
+  const int warp = d >> 5, lane = d & 31;
   const int HD = 128, kvh = h / a.group, hh = h % a.group;
   const int i = r * a.group + hh;
-  pdl_wait();
   pdl_launch_dependents();
+  pdl_wait();
   const int TR = a.tiles * 16;
   const float* pml = a.part_ml + (size_t)kvh * splits * TR * 2 + 2 * i;
   const float* po = a.part_o + ((size_t)kvh * splits * TR + i) * HD + d;
-  if (d < splits) {
-    s_ms[d] = __ldcg(pml + (size_t)d * TR * 2);
-    s_ls[d] = __ldcg(pml + (size_t)d * TR * 2 + 1);
+  float ms[2] = {-INFINITY, -INFINITY}, ls[2] = {0.f, 0.f};
+  if (warp == 0) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int sp = lane + 32 * u;
+      if (sp < splits) {
+        ms[u] = __ldcg(pml + (size_t)sp * TR * 2);
+        ls[u] = __ldcg(pml + (size_t)sp * TR * 2 + 1);
+      }
+    }
   }
   float ov[2][32];  // this thread's split outputs (splits <= 64)
 #pragma unroll
@@ -558,35 +570,54 @@ __global__ void __launch_bounds__(128) k_attn_combine(AttnArgs a, int splits) {
     float p = qd * kd[j];
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
-    if ((d & 31) == 0) s_red[d >> 5][j] = p;
+    if (lane == 0) s_red[warp][j] = p;
   }
   __syncthreads();
-  if (d <= r) s_sc[d] = ((s_red[0][d] + s_red[1][d]) + (s_red[2][d] + s_red[3][d])) * a.scale_log2;
+  if (warp == 0) {
+    // M over the splits (xor rounds) and the new positions; the weights
+    // f_s = exp2(m_s - M) (0 for an empty split) and f_j; L = the
+    // l-weighted sum of the f_s in xor rounds plus the f_j in order
+    const float sc = lane <= r && lane < 16
+                         ? ((s_red[0][lane] + s_red[1][lane]) + (s_red[2][lane] + s_red[3][lane])) * a.scale_log2
+                         : -INFINITY;
+    float M = fmaxf(fmaxf(ms[0], ms[1]), sc);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float L = 0.f;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const float f = ms[u] == -INFINITY ? 0.f : exp2f(ms[u] - M);
+      if (lane + 32 * u < splits) s_f[lane + 32 * u] = f;
+      L += ls[u] * f;
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    const float fj = lane <= r && lane < 16 ? exp2f(sc - M) : 0.f;
+    if (lane < 16) s_fj[lane] = fj;
+    float Lj = fj;  // the new positions' weights in order 0..r
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) {
+      const float v = __shfl_up_sync(0xffffffffu, Lj, o);
+      if (lane >= o) Lj += v;
+    }
+    if (lane == 15) s_L = L + Lj;
+  }
   __syncthreads();
-  float M = -INFINITY;
-  for (int s = 0; s < splits; ++s) M = fmaxf(M, s_ms[s]);
-  for (int j = 0; j <= r; ++j) M = fmaxf(M, s_sc[j]);
-  float L = 0.f, O = 0.f;
+  float O = 0.f;
 #pragma unroll
   for (int c = 0; c < 2; ++c)
 #pragma unroll
     for (int u = 0; u < 32; ++u) {
       const int s = 32 * c + u;
       if (s >= splits) break;
-      const float ms = s_ms[s];
-      if (ms == -INFINITY) continue;
-      const float f = exp2f(ms - M);
-      L += s_ls[s] * f;
-      O += ov[c][u] * f;
+      O += ov[c][u] * s_f[s];
     }
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     if (j > r) break;
-    const float f = exp2f(s_sc[j] - M);
-    L += f;
-    O += f * vd[j];
+    O += s_fj[j] * vd[j];
   }
-  a.o[(size_t)r * a.nq * HD + (size_t)h * HD + d] = float_to_bf16_bits(O / L);
+  a.o[(size_t)r * a.nq * HD + (size_t)h * HD + d] = float_to_bf16_bits(O / s_L);
 }
 
 // Splits per (KV head, tile): about two CTAs per SM in all, no more than
