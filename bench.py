@@ -281,9 +281,9 @@ def combine_ranks(dist, torch, world, ms, total_bytes, device):
 def run_gpu(args):
     import torch
     import synthgen
-    import moe_nvfp4_block_gb300 as M
     import __graft_entry__
     __graft_entry__.build()
+    import moe_nvfp4_block_gb300 as M
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
