@@ -9,11 +9,11 @@
 // logits bit for bit.
 //
 // One CTA per SM owns a contiguous range of vocab rows.  Stages of R rows
-// (R = min(8, 16384 / H), at most 32 KB) go through five ring slots; warp
-// pair p owns slot p and takes the stages p, p + 5, ...; each of its two
+// (a 24 or 32 KB slot's worth, at most 8) go through the ring slots; warp
+// pair p owns slot p and takes the stages p, p + P, ...; each of its two
 // warps reduces R / 2 rows of a stage, so every 16-byte load of x from shared
 // memory serves R / 2 rows.  The weights do not depend on the previous
-// kernel, so the first five stages are issued before the dependency wait.
+// kernel, so the first stage of every slot is issued before the dependency wait.
 // Optionally the rows of x are RMS-normalised while staged (the RMSNorm
 // kernel's fixed order and rounding, so bit-identical to normalising first).
 #include <cfloat>
@@ -26,9 +26,7 @@ namespace moe {
 
 namespace {
 
-constexpr int kLsPairs = 5;
-constexpr int kLsWarps = 2 * kLsPairs;
-constexpr int kLsSlotBytes = 32768;
+constexpr int kLsMaxPairs = 8;
 constexpr int kLsRowsPerWarp = 4;
 
 __device__ __forceinline__ float lbf_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -45,19 +43,28 @@ __device__ __forceinline__ bool l_before(float la, int a, float lb, int b) {
 }
 
 struct LsTable {
-  uint64_t full[kLsPairs];
-  uint64_t empty[kLsPairs];
+  uint64_t full[kLsMaxPairs];
+  uint64_t empty[kLsMaxPairs];
   int abort;
   int last;
   float inv[16];
-  float bv[kLsWarps][16];
-  int bi[kLsWarps][16];
+  float bv[2 * kLsMaxPairs][16];
+  int bi[2 * kLsMaxPairs][16];
+};
+
+// Ring shape by K: eight pairs of warps on 24 KB slots while x is small
+// (K <= 8; more warps in flight for an issue-bound loop), five pairs on
+// 32 KB slots at K = 16 (x takes 64 KB of shared memory).
+template <int KR> struct LsShape {
+  static constexpr int pairs = KR <= 8 ? 8 : 5;
+  static constexpr int slot = KR <= 8 ? 24576 : 32768;
 };
 
 }  // namespace
 
 template <int KR>
-__global__ void __launch_bounds__(kLsWarps * 32, 1) k_lmhead_stream(const __grid_constant__ LmHeadArgs a) {
+__global__ void __launch_bounds__(2 * LsShape<KR>::pairs * 32, 1) k_lmhead_stream(const __grid_constant__ LmHeadArgs a) {
+  constexpr int kLsPairs = LsShape<KR>::pairs, kLsWarps = 2 * kLsPairs, kLsSlotBytes = LsShape<KR>::slot;
   extern __shared__ __align__(128) unsigned char smem[];
   const int K = a.K, H = a.H, V = a.V;
   uint4* xs = reinterpret_cast<uint4*>(smem + kLsPairs * kLsSlotBytes);
@@ -266,8 +273,13 @@ __global__ void __launch_bounds__(kLsWarps * 32, 1) k_lmhead_stream(const __grid
   if (threadIdx.x == 0) *a.ticket = 0u;
 }
 
-size_t lmhead_stream_smem(int K, int H) {
-  return (size_t)kLsPairs * kLsSlotBytes + (size_t)K * H * 2 + sizeof(LsTable);
+template <int KR>
+static size_t lmhead_stream_smem_t(int K, int H) {
+  return (size_t)LsShape<KR>::pairs * LsShape<KR>::slot + (size_t)K * H * 2 + sizeof(LsTable);
+}
+
+static size_t lmhead_stream_smem(int K, int H) {
+  return K <= 4 ? lmhead_stream_smem_t<4>(K, H) : K <= 8 ? lmhead_stream_smem_t<8>(K, H) : lmhead_stream_smem_t<16>(K, H);
 }
 
 bool lmhead_stream_fits(int K, int H) {
@@ -275,16 +287,16 @@ bool lmhead_stream_fits(int K, int H) {
 }
 
 cudaError_t launch_lmhead_stream(const LmHeadArgs& a0, cudaStream_t s, bool pdl) {
-  LmHeadArgs a = a0;
-  a.rows_per_stage = kLsSlotBytes / (2 * a.H) < 2 * kLsRowsPerWarp ? kLsSlotBytes / (2 * a.H) : 2 * kLsRowsPerWarp;
-  const size_t sm = lmhead_stream_smem(a.K, a.H);
-  auto run = [&](auto kern) {
+  auto run = [&](auto kern, int pairs, int slot) {
+    LmHeadArgs a = a0;
+    a.rows_per_stage = slot / (2 * a.H) < 2 * kLsRowsPerWarp ? slot / (2 * a.H) : 2 * kLsRowsPerWarp;
+    const size_t sm = lmhead_stream_smem(a.K, a.H);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e == cudaSuccess) e = max_carveout(kern);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_sms());
-    cfg.blockDim = dim3(kLsWarps * 32);
+    cfg.blockDim = dim3(2 * pairs * 32);
     cfg.dynamicSmemBytes = sm;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -294,9 +306,9 @@ cudaError_t launch_lmhead_stream(const LmHeadArgs& a0, cudaStream_t s, bool pdl)
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, a);
   };
-  if (a.K <= 4) return run(k_lmhead_stream<4>);
-  if (a.K <= 8) return run(k_lmhead_stream<8>);
-  return run(k_lmhead_stream<16>);
+  if (a0.K <= 4) return run(k_lmhead_stream<4>, LsShape<4>::pairs, LsShape<4>::slot);
+  if (a0.K <= 8) return run(k_lmhead_stream<8>, LsShape<8>::pairs, LsShape<8>::slot);
+  return run(k_lmhead_stream<16>, LsShape<16>::pairs, LsShape<16>::slot);
 }
 
 }  // namespace moe

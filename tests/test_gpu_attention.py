@@ -72,6 +72,15 @@ def test_attention_block_small(M, K, H, nq, nkv, C):
     _check_all(run(M, K, H, nq, nkv, C, seed=K * 7 + C, wsig=0.05), f"attention K={K} C={C}", term_tol=3e-2)
 
 
+@pytest.mark.parametrize("K,nq,nkv,C", [(16, 32, 8, 304), (8, 16, 4, 1008), (1, 48, 8, 144), (2, 64, 8, 1024),
+                                        (2, 32, 8, 0)])
+def test_attention_block_streamed_shapes(M, K, nq, nkv, C):
+    # H = 2048: the streamed projection (x fragments of rows 8..15 when K > 8;
+    # o-projections 2048 .. 8192 wide), several 16-row query tiles per KV head,
+    # caches ending inside a 128-position chunk, and an empty cache
+    _check_all(run(M, K, 2048, nq, nkv, C, seed=K * 11 + C, wsig=0.02), f"attention K={K} nq={nq} C={C}")
+
+
 def test_attention_block_full_step_shape(M):
     # the full verify step's attention: K=4, 32 q heads, 8 kv heads, 16,384 cached positions
     _check_all(run(M, 4, 2048, 32, 8, 16384, seed=4), "attention full-step shape")
