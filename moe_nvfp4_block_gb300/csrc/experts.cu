@@ -802,6 +802,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_experts(const __grid_consta
       for (int j = n_shb; j < L && live; ++j, seq_next(cur, seq)) live = issue_next(ic, cur.it, j);
     } while (false);
     if (lane == 0 && trace) trace[9] = global_timer_ns();
+    if (lane == 0 && live) l2_prefetch_list(a.pf, blockIdx.x, grid);  // the next kernel's first bytes
     if (lane == 0) {
       // every copy of the last S items has landed before the CTA may exit
       // (a stage is reissued only after the compute warps saw its previous

@@ -130,6 +130,14 @@ struct ProjPtrs {
 };
 
 // One MoE layer as the experts kernel sees it (everything but the tensor maps).
+// Byte ranges a kernel prefetches into L2 for the kernel that follows it,
+// once its own stream is issued (each CTA its share); n = 0: none.
+struct L2Prefetch {
+  const void* p[4];
+  uint64_t bytes[4];  // multiples of 16, p 16-byte aligned
+  int n;
+};
+
 struct LayerDesc {
   const uint16_t* router_w;  // [E][H] bf16
   const float* router_bias;  // [E] or null
@@ -159,6 +167,7 @@ struct ExpertsCommon {
   int stages, nred;           // ring depths (set by the launcher)
   int norm;                   // 1: x is the residual stream; the kernel applies the RMSNorm (unit gain)
   float norm_eps;
+  L2Prefetch pf;              // the next kernel's first bytes, prefetched once the producer is done
 };
 
 struct ExpertsParams {
@@ -314,4 +323,4 @@ inline cudaError_t max_carveout(Kern kern) {
 extern "C" __attribute__((visibility("hidden"))) moe_status run_layer(const moe_layer* layer, const uint16_t* x_norm, int K, const uint16_t* residual,
                                 uint16_t* y, int32_t* idx_out, float* w_out, int32_t* group_out, void* ws,
                                 size_t ws_bytes, void* stream, bool pdl, void* const* events,
-                                float norm_eps = -1.f);
+                                float norm_eps = -1.f, const moe::L2Prefetch* pf = nullptr);

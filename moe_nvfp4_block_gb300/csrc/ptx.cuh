@@ -126,6 +126,30 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// Bulk prefetch of [p, p + bytes) into L2 (p 16-byte aligned, bytes a
+// multiple of 16), issued in pieces of at most 64 KB.
+__device__ __forceinline__ void l2_prefetch_span(const void* p, uint64_t bytes) {
+  const char* c = static_cast<const char*>(p);
+  while (bytes > 0) {
+    const uint32_t n = bytes > 65536u ? 65536u : (uint32_t)bytes;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(c), "r"(n) : "memory");
+    c += n;
+    bytes -= n;
+  }
+}
+
+// Share `part` of `nparts` of every range of a prefetch list (each range cut
+// at 16-byte boundaries into nparts slices).
+template <typename List>
+__device__ __forceinline__ void l2_prefetch_list(const List& pf, int part, int nparts) {
+  for (int i = 0; i < pf.n; ++i) {
+    const uint64_t total = pf.bytes[i];
+    const uint64_t a = (total * (uint64_t)part / (uint64_t)nparts) & ~(uint64_t)15;
+    const uint64_t b = part + 1 == nparts ? total : (total * (uint64_t)(part + 1) / (uint64_t)nparts) & ~(uint64_t)15;
+    if (b > a) l2_prefetch_span(static_cast<const char*>(pf.p[i]) + a, b - a);
+  }
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
