@@ -516,17 +516,16 @@ __global__ void __launch_bounds__(kAttnWarps * 32) k_attn_split(AttnArgs a) {
 // One CTA per (query head h, row r); 128 threads = head dims.  Merges the
 // splits of KV head h/group in split order with the row's visible new
 // positions 0..r and writes o = bf16(O / L).  Every global load is issued up
-// front (warp 0: the splits' maxima and sums; every thread: its dims of the
-// splits' outputs, q and the new keys and values), then warp 0 forms the
-// split weights exp2(m_s - M) and L with shuffles, so the CTA waits for
-// about one memory round trip and does no serial pass over the splits but
-// the in-order accumulation of O.  The dependent kernel (the o-projection,
-// which reads only its weights before its own wait) is released at once.
+// front (every warp: the splits' maxima and sums; every thread: its dim of
+// the splits' outputs, q and the new keys and values).  Every warp forms the
+// split weights exp2(m_s - Ms) with shuffles and each thread accumulates its
+// dim over the splits at once (so the loads are consumed as they land); the
+// new positions then join with the usual rescaling to the row's maximum.
+// The dependent kernel (the o-projection, which reads only its weights
+// before its own wait) is released at once.
+template <int MAXS>
 __global__ void __launch_bounds__(128) k_attn_combine(AttnArgs a, int splits) {
   __shared__ float s_red[4][16];
-  __shared__ float s_f[kAttnMaxSplits];
-  __shared__ float s_fj[16];
-  __shared__ float s_L;
   const int h = blockIdx.x, r = blockIdx.y, d = threadIdx.x;
   const int warp = d >> 5, lane = d & 31;
   const int HD = 128, kvh = h / a.group, hh = h % a.group;
@@ -536,20 +535,20 @@ __global__ void __launch_bounds__(128) k_attn_combine(AttnArgs a, int splits) {
   const int TR = a.tiles * 16;
   const float* pml = a.part_ml + (size_t)kvh * splits * TR * 2 + 2 * i;
   const float* po = a.part_o + ((size_t)kvh * splits * TR + i) * HD + d;
+  // every load first: lane s of every warp the (m, l) of splits s and s + 32,
+  // every thread its dim of the splits' outputs, q, the new keys and values
   float ms[2] = {-INFINITY, -INFINITY}, ls[2] = {0.f, 0.f};
-  if (warp == 0) {
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int sp = lane + 32 * u;
-      if (sp < splits) {
-        ms[u] = __ldcg(pml + (size_t)sp * TR * 2);
-        ls[u] = __ldcg(pml + (size_t)sp * TR * 2 + 1);
-      }
+  for (int u = 0; u < 2; ++u) {
+    const int sp = lane + 32 * u;
+    if (sp < splits) {
+      ms[u] = __ldcg(pml + (size_t)sp * TR * 2);
+      ls[u] = __ldcg(pml + (size_t)sp * TR * 2 + 1);
     }
   }
-  float ov[2][32];  // this thread's split outputs (splits <= 64)
+  float ov[MAXS / 32][32];  // this thread's split outputs (splits <= MAXS)
 #pragma unroll
-  for (int c = 0; c < 2; ++c)
+  for (int c = 0; c < MAXS / 32; ++c)
 #pragma unroll
     for (int u = 0; u < 32; ++u) ov[c][u] = 32 * c + u < splits ? __ldcg(po + (size_t)(32 * c + u) * TR * HD) : 0.f;
   const float qd = bf_lo(a.q[(size_t)r * a.nq * HD + (size_t)h * HD + d]);
@@ -562,6 +561,27 @@ __global__ void __launch_bounds__(128) k_attn_combine(AttnArgs a, int splits) {
       vd[j] = bf_lo(a.v_new[(size_t)j * a.nkv * HD + (size_t)kvh * HD + d]);
     }
   }
+  // the splits, in every warp alike: Ms = max m_s (xor rounds), weights
+  // f_s = exp2(m_s - Ms) (0 for an empty split), Ls = sum l_s f_s (xor
+  // rounds), and this thread's Os = sum over s in order of f_s O_s
+  float Ms = fmaxf(ms[0], ms[1]);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) Ms = fmaxf(Ms, __shfl_xor_sync(0xffffffffu, Ms, o));
+  float f[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) f[u] = ms[u] == -INFINITY ? 0.f : exp2f(ms[u] - Ms);
+  float Ls = f[0] * ls[0] + f[1] * ls[1];
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
+  float Os = 0.f;
+#pragma unroll
+  for (int c = 0; c < MAXS / 32; ++c)
+#pragma unroll
+    for (int u = 0; u < 32; ++u) {
+      const int s = 32 * c + u;
+      const float fs = __shfl_sync(0xffffffffu, f[c < 2 ? c : 1], u);
+      if (s < splits) Os += ov[c][u] * fs;
+    }
   // scores of the new positions (log2 domain): per warp a xor sum, then the
   // four warps in a fixed order
 #pragma unroll
@@ -573,51 +593,28 @@ __global__ void __launch_bounds__(128) k_attn_combine(AttnArgs a, int splits) {
     if (lane == 0) s_red[warp][j] = p;
   }
   __syncthreads();
-  if (warp == 0) {
-    // M over the splits (xor rounds) and the new positions; the weights
-    // f_s = exp2(m_s - M) (0 for an empty split) and f_j; L = the
-    // l-weighted sum of the f_s in xor rounds plus the f_j in order
-    const float sc = lane <= r && lane < 16
-                         ? ((s_red[0][lane] + s_red[1][lane]) + (s_red[2][lane] + s_red[3][lane])) * a.scale_log2
-                         : -INFINITY;
-    float M = fmaxf(fmaxf(ms[0], ms[1]), sc);
+  float sc[16];
+  float M = Ms;
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float L = 0.f;
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const float f = ms[u] == -INFINITY ? 0.f : exp2f(ms[u] - M);
-      if (lane + 32 * u < splits) s_f[lane + 32 * u] = f;
-      L += ls[u] * f;
+  for (int j = 0; j < 16; ++j) {
+    sc[j] = -INFINITY;
+    if (j <= r) {
+      sc[j] = ((s_red[0][j] + s_red[1][j]) + (s_red[2][j] + s_red[3][j])) * a.scale_log2;
+      M = fmaxf(M, sc[j]);
     }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-    const float fj = lane <= r && lane < 16 ? exp2f(sc - M) : 0.f;
-    if (lane < 16) s_fj[lane] = fj;
-    float Lj = fj;  // the new positions' weights in order 0..r
-#pragma unroll
-    for (int o = 1; o < 16; o <<= 1) {
-      const float v = __shfl_up_sync(0xffffffffu, Lj, o);
-      if (lane >= o) Lj += v;
-    }
-    if (lane == 15) s_L = L + Lj;
   }
-  __syncthreads();
-  float O = 0.f;
-#pragma unroll
-  for (int c = 0; c < 2; ++c)
-#pragma unroll
-    for (int u = 0; u < 32; ++u) {
-      const int s = 32 * c + u;
-      if (s >= splits) break;
-      O += ov[c][u] * s_f[s];
-    }
+  // the splits' sums rescaled to the row's maximum, then the new positions
+  // in order 0..r
+  const float cs = Ms == -INFINITY ? 0.f : exp2f(Ms - M);
+  float O = Os * cs, L = Ls * cs;
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     if (j > r) break;
-    O += s_fj[j] * vd[j];
+    const float fj = exp2f(sc[j] - M);
+    L += fj;
+    O += fj * vd[j];
   }
-  a.o[(size_t)r * a.nq * HD + (size_t)h * HD + d] = float_to_bf16_bits(O / s_L);
+  a.o[(size_t)r * a.nq * HD + (size_t)h * HD + d] = float_to_bf16_bits(O / L);
 }
 
 // Splits per (KV head, tile): about two CTAs per SM in all, no more than
@@ -656,8 +653,14 @@ cudaError_t launch_attn_combine(const AttnArgs& a, int splits, cudaStream_t s) {
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  max_carveout(k_attn_combine);
-  return cudaLaunchKernelEx(&cfg, k_attn_combine, a, splits);
+  // at most 32 splits: a smaller register footprint, so a merge CTA fits on
+  // an SM beside the attention and the o-projection CTAs
+  if (splits <= 32) {
+    max_carveout(k_attn_combine<32>);
+    return cudaLaunchKernelEx(&cfg, k_attn_combine<32>, a, splits);
+  }
+  max_carveout(k_attn_combine<64>);
+  return cudaLaunchKernelEx(&cfg, k_attn_combine<64>, a, splits);
 }
 
 }  // namespace moe

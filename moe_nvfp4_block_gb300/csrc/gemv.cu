@@ -194,12 +194,13 @@ __global__ void __launch_bounds__(kGsWarps * 32, 1) k_gemv_stream(const __grid_c
     if (!ok) {
       *abort = 1;
     } else {
-      const int nr = T.n[s];
-      const int row = g < nr ? g : g % nr;  // rows past the stage's own: repeated, results unused
-      const unsigned char* wp = smem + (size_t)slot * kGsStageBytes + ((size_t)row * D + cb) * 2;
+      // lanes of rows past the stage's own (R < 8, or a short last stage)
+      // read nothing: their n columns are zero and unused
+      const bool live = g < T.n[s];
+      const unsigned char* wp = smem + (size_t)slot * kGsStageBytes + ((size_t)(live ? g : 0) * D + cb) * 2;
 #pragma unroll
       for (int kp = 0; kp < KPW / 2; ++kp) {
-        const uint4 w = *reinterpret_cast<const uint4*>(wp + 64 * kp);
+        const uint4 w = live ? *reinterpret_cast<const uint4*>(wp + 64 * kp) : make_uint4(0, 0, 0, 0);
         if constexpr (KH > 1) {
           mma_bf16_gs(acc[s], xa[2 * kp][0], xa[2 * kp][2], xa[2 * kp][1], xa[2 * kp][3], w.x, w.y);
           mma_bf16_gs(acc[s], xa[2 * kp + 1][0], xa[2 * kp + 1][2], xa[2 * kp + 1][1], xa[2 * kp + 1][3], w.z, w.w);
