@@ -33,6 +33,9 @@ constexpr int kAsPos = 128;                     // positions per chunk
 constexpr int kAsHalf = kAsPos * 128;           // one box: 128 rows x 64 dims x 2 B
 constexpr int kAsStageBytes = 4 * kAsHalf;      // K lo, K hi, V lo, V hi
 constexpr int kAsStages = 3;
+// Bound on waiting for the CTA's own copies before it exits (independent of
+// the caller's wait limit, which may be 0 in a test of the give-up path).
+constexpr uint64_t kAsDrainNs = 2000000000ull;
 
 struct AsTable {
   uint64_t full[kAsStages];
@@ -254,7 +257,7 @@ __global__ void __launch_bounds__(kAsWarps * 32, 1) k_attn_stream(const __grid_c
     if (threadIdx.x == 0) {
       if (a.err) atomicCAS(a.err, 0, (int)MOE_ERR_DEVICE_TIMEOUT);
       for (int s = max(0, issued - kAsStages); s < issued; ++s)
-        mbar_wait_drain(&T.full[s % kAsStages], (uint32_t)(s / kAsStages) & 1u, a.wait_ns);
+        mbar_wait_drain(&T.full[s % kAsStages], (uint32_t)(s / kAsStages) & 1u, kAsDrainNs);
     }
     return;
   }

@@ -35,6 +35,9 @@ constexpr int kGsStages = 6;
 constexpr int kGsStageBytes = 32768;
 constexpr int kGsMaxBlocks = 8;  // stages per CTA (one accumulator set each)
 constexpr int kGsTail = 1024;    // barriers and the stage table after the ring
+// Bound on waiting for the CTA's own copies before it exits (independent of
+// the caller's wait limit, which may be 0 in a test of the give-up path).
+constexpr uint64_t kGsDrainNs = 2000000000ull;
 
 __device__ __forceinline__ float bfl(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bfh(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -229,7 +232,7 @@ __global__ void __launch_bounds__(kGsWarps * 32, 1) k_gemv_stream(const __grid_c
       if (a.err) atomicCAS(a.err, 0, (int)MOE_ERR_DEVICE_TIMEOUT);
       // no copy may land in the shared memory of a finished CTA
       for (int s = max(0, issued - kGsStages); s < issued; ++s)
-        mbar_wait_drain(&T.full[s % kGsStages], (uint32_t)(s / kGsStages) & 1u, a.wait_ns);
+        mbar_wait_drain(&T.full[s % kGsStages], (uint32_t)(s / kGsStages) & 1u, kGsDrainNs);
     }
     return;
   }

@@ -28,6 +28,9 @@ namespace {
 
 constexpr int kLsMaxPairs = 8;
 constexpr int kLsRowsPerWarp = 4;
+// Bound on waiting for the CTA's own copies before it exits (independent of
+// the caller's wait limit, which may be 0 in a test of the give-up path).
+constexpr uint64_t kLsDrainNs = 2000000000ull;
 
 __device__ __forceinline__ float lbf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float lbf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -226,7 +229,7 @@ __global__ void __launch_bounds__(2 * LsShape<KR>::pairs * 32, 1) k_lmhead_strea
   if (*abort) {
     // no copy may land in a finished CTA; the ticket is still taken (the
     // tokens of this call are undefined, the next call starts clean)
-    if (hw == 0 && lane == 0 && issued > 0) mbar_wait_drain(&T.full[p], (uint32_t)(issued - 1) & 1u, a.wait_ns);
+    if (hw == 0 && lane == 0 && issued > 0) mbar_wait_drain(&T.full[p], (uint32_t)(issued - 1) & 1u, kLsDrainNs);
     if (threadIdx.x == 0 && a.err) atomicCAS(a.err, 0, (int)MOE_ERR_DEVICE_TIMEOUT);
   }
   if (lane == 0) {

@@ -84,3 +84,37 @@ def test_attention_block_streamed_shapes(M, K, nq, nkv, C):
 def test_attention_block_full_step_shape(M):
     # the full verify step's attention: K=4, 32 q heads, 8 kv heads, 16,384 cached positions
     _check_all(run(M, 4, 2048, 32, 8, 16384, seed=4), "attention full-step shape")
+
+
+def test_streamed_kernels_wait_timeout_reports_error_and_recovers(M):
+    # a zero wait limit makes every ring wait of the streamed projection,
+    # split attention and lm_head give up at once: the calls return, report
+    # MOE_ERR_DEVICE_TIMEOUT, drain their own copies, and the next calls (at
+    # the default limit) are correct
+    K, H, nq, nkv, C, V = 4, 2048, 32, 8, 1024, 4096
+    x, Wq, Wk, Wv, Wo, kc, vc = make(K, H, nq, nkv, C, seed=77)
+    d = [to_dev_bf16(a) for a in (x, Wq, Wk, Wv, Wo, kc, vc)]
+    ws = M.attention_workspace(K, H, nq, nkv)
+    lm = synthgen.normal_bf16(77, 0, synthgen.T_LM_HEAD, 0, V * H, 0.0, 0.02).reshape(V, H)
+    xn = oracle.rmsnorm(x)
+    lmd, xnd = to_dev_bf16(lm), to_dev_bf16(xn)
+    tok = torch.empty(K, dtype=torch.int32, device="cuda")
+    lws = M.lm_head_workspace(K)
+    out = torch.empty_like(d[0])
+    try:
+        M.moe_debug_set_wait_limit_ns(0)
+        M.moe_attention_block(d[0], *d[1:5], d[5], d[6], out, ws, nq, nkv)
+        M.moe_lm_head_argmax(xnd, lmd, tok, lws)
+        torch.cuda.synchronize()
+    finally:
+        M.moe_debug_set_wait_limit_ns(2_000_000_000)
+    assert M.moe_workspace_error(ws) == M.MOE_ERR_DEVICE_TIMEOUT
+    assert M.moe_workspace_error(lws) == M.MOE_ERR_DEVICE_TIMEOUT
+    M.moe_attention_block(d[0], *d[1:5], d[5], d[6], out, ws, nq, nkv)
+    M.moe_lm_head_argmax(xnd, lmd, tok, lws)
+    torch.cuda.synchronize()
+    assert M.moe_workspace_error(ws) == 0 and M.moe_workspace_error(lws) == 0
+    ref = oracle.attention(x, Wq, Wk, Wv, Wo, kc, vc, nq, nkv, 128)
+    assert_parity(bf16_bits(out), ref, "attention block after the timeout")
+    ref_tok, _ = oracle.lm_argmax(xn, lm)
+    np.testing.assert_array_equal(tok.cpu().numpy(), ref_tok)
