@@ -27,7 +27,6 @@ namespace moe {
 namespace {
 
 constexpr int kLsMaxPairs = 8;
-constexpr int kLsRowsPerWarp = 4;
 // Bound on waiting for the CTA's own copies before it exits (independent of
 // the caller's wait limit, which may be 0 in a test of the give-up path).
 constexpr uint64_t kLsDrainNs = 2000000000ull;
@@ -61,6 +60,8 @@ struct LsTable {
 template <int KR> struct LsShape {
   static constexpr int pairs = KR <= 8 ? 8 : 5;
   static constexpr int slot = KR <= 8 ? 24576 : 32768;
+  static constexpr int rpw = KR <= 8 ? 3 : 4;  // vocab rows per warp and stage
+  static constexpr bool xf32 = KR <= 4;         // x held as floats (no unpacking per use)
 };
 
 }  // namespace
@@ -68,10 +69,15 @@ template <int KR> struct LsShape {
 template <int KR>
 __global__ void __launch_bounds__(2 * LsShape<KR>::pairs * 32, 1) k_lmhead_stream(const __grid_constant__ LmHeadArgs a) {
   constexpr int kLsPairs = LsShape<KR>::pairs, kLsWarps = 2 * kLsPairs, kLsSlotBytes = LsShape<KR>::slot;
+  constexpr int RPW = LsShape<KR>::rpw;
+  constexpr bool XF32 = LsShape<KR>::xf32;
   extern __shared__ __align__(128) unsigned char smem[];
   const int K = a.K, H = a.H, V = a.V;
-  uint4* xs = reinterpret_cast<uint4*>(smem + kLsPairs * kLsSlotBytes);
-  LsTable& T = *reinterpret_cast<LsTable*>(smem + kLsPairs * kLsSlotBytes + (size_t)K * H * 2);
+  // x: bf16 rows, or (XF32) floats, the bf16 rows staged in the upper half
+  // of the region first
+  unsigned char* xreg = smem + kLsPairs * kLsSlotBytes;
+  uint4* xs = reinterpret_cast<uint4*>(xreg + (XF32 ? (size_t)K * H * 2 : 0));
+  LsTable& T = *reinterpret_cast<LsTable*>(xreg + (size_t)K * H * (XF32 ? 4 : 2));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int p = warp >> 1, hw = warp & 1;
   const int R = a.rows_per_stage;
@@ -132,6 +138,28 @@ __global__ void __launch_bounds__(2 * LsShape<KR>::pairs * 32, 1) k_lmhead_strea
     }
     __syncthreads();
   }
+  if constexpr (XF32) {
+    // the rows to floats (exact), over the region's lower half: every thread
+    // holds its pieces before any is overwritten
+    const int n16 = K * H / 8;
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = threadIdx.x + u * (int)blockDim.x;
+      if (i < n16) v[u] = xs[i];
+    }
+    __syncthreads();
+    float4* xf = reinterpret_cast<float4*>(xreg);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = threadIdx.x + u * (int)blockDim.x;
+      if (i < n16) {
+        xf[2 * i] = make_float4(lbf_lo(v[u].x), lbf_hi(v[u].x), lbf_lo(v[u].y), lbf_hi(v[u].y));
+        xf[2 * i + 1] = make_float4(lbf_lo(v[u].z), lbf_hi(v[u].z), lbf_lo(v[u].w), lbf_hi(v[u].w));
+      }
+    }
+    __syncthreads();
+  }
 
   float bv[KR];
   int bi[KR];
@@ -152,44 +180,49 @@ __global__ void __launch_bounds__(2 * LsShape<KR>::pairs * 32, 1) k_lmhead_strea
     ok = __all_sync(0xffffffffu, ok);
     const int vb = v0 + s * R;
     const int nr = min(R, v1 - vb);
-    float acc[kLsRowsPerWarp][KR];
+    float acc[RPW][KR];
 #pragma unroll
-    for (int q = 0; q < kLsRowsPerWarp; ++q)
+    for (int q = 0; q < RPW; ++q)
 #pragma unroll
       for (int r = 0; r < KR; ++r) acc[q][r] = 0.f;
     if (!ok) {
       *abort = 1;
     } else {
       const uint4* ws = reinterpret_cast<const uint4*>(smem + (size_t)p * kLsSlotBytes);
-      for (int j = 0; j < nj; ++j) {
-        uint32_t wq[kLsRowsPerWarp][4];
+      const float4* xf4 = reinterpret_cast<const float4*>(xreg);
 #pragma unroll
-        for (int q = 0; q < kLsRowsPerWarp; ++q) {
+      for (int j = 0; j < 8; ++j) {  // H / 256 <= 8 pieces
+        if (j >= nj) break;
+        // this lane's 8 weights of each of the warp's rows, as floats
+        float wf[RPW][8];
+#pragma unroll
+        for (int q = 0; q < RPW; ++q) {
           const int row = hw * rpw + q;
-          if (q < rpw && row < nr) {
-            const uint4 v = ws[row * (H / 8) + j * 32 + lane];
-            wq[q][0] = v.x;
-            wq[q][1] = v.y;
-            wq[q][2] = v.z;
-            wq[q][3] = v.w;
-          } else {
-            wq[q][0] = wq[q][1] = wq[q][2] = wq[q][3] = 0u;
-          }
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (q < rpw && row < nr) v = ws[row * (H / 8) + j * 32 + lane];
+          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) wf[q][i] = (i & 1) ? lbf_hi(w4[i >> 1]) : lbf_lo(w4[i >> 1]);
         }
 #pragma unroll
         for (int r = 0; r < KR; ++r) {
           if (r < K) {
-            const uint4 xv = xs[r * (H / 8) + j * 32 + lane];
-            const uint32_t xq[4] = {xv.x, xv.y, xv.z, xv.w};
+            float xf[8];
+            if constexpr (XF32) {  // x held as floats
+              const float4 a0 = xf4[(r * H + j * 256 + 8 * lane) / 4];
+              const float4 a1 = xf4[(r * H + j * 256 + 8 * lane) / 4 + 1];
+              xf[0] = a0.x; xf[1] = a0.y; xf[2] = a0.z; xf[3] = a0.w;
+              xf[4] = a1.x; xf[5] = a1.y; xf[6] = a1.z; xf[7] = a1.w;
+            } else {
+              const uint4 xv = xs[r * (H / 8) + j * 32 + lane];
+              const uint32_t xq[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float xf = (i & 1) ? lbf_hi(xq[i >> 1]) : lbf_lo(xq[i >> 1]);
-#pragma unroll
-              for (int q = 0; q < kLsRowsPerWarp; ++q) {
-                const float wf = (i & 1) ? lbf_hi(wq[q][i >> 1]) : lbf_lo(wq[q][i >> 1]);
-                acc[q][r] = __fmaf_rn(xf, wf, acc[q][r]);
-              }
+              for (int i = 0; i < 8; ++i) xf[i] = (i & 1) ? lbf_hi(xq[i >> 1]) : lbf_lo(xq[i >> 1]);
             }
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+              for (int q = 0; q < RPW; ++q) acc[q][r] = __fmaf_rn(xf[i], wf[q][i], acc[q][r]);
           }
         }
       }
@@ -208,7 +241,7 @@ __global__ void __launch_bounds__(2 * LsShape<KR>::pairs * 32, 1) k_lmhead_strea
     __syncwarp();
     if (ok) {
 #pragma unroll
-      for (int q = 0; q < kLsRowsPerWarp; ++q) {
+      for (int q = 0; q < RPW; ++q) {
         const int row = hw * rpw + q;
         if (q < rpw && row < nr) {
 #pragma unroll
@@ -278,7 +311,8 @@ __global__ void __launch_bounds__(2 * LsShape<KR>::pairs * 32, 1) k_lmhead_strea
 
 template <int KR>
 static size_t lmhead_stream_smem_t(int K, int H) {
-  return (size_t)LsShape<KR>::pairs * LsShape<KR>::slot + (size_t)K * H * 2 + sizeof(LsTable);
+  return (size_t)LsShape<KR>::pairs * LsShape<KR>::slot + (size_t)K * H * (LsShape<KR>::xf32 ? 4 : 2) +
+         sizeof(LsTable);
 }
 
 static size_t lmhead_stream_smem(int K, int H) {
@@ -290,9 +324,9 @@ bool lmhead_stream_fits(int K, int H) {
 }
 
 cudaError_t launch_lmhead_stream(const LmHeadArgs& a0, cudaStream_t s, bool pdl) {
-  auto run = [&](auto kern, int pairs, int slot) {
+  auto run = [&](auto kern, int pairs, int slot, int rpw) {
     LmHeadArgs a = a0;
-    a.rows_per_stage = slot / (2 * a.H) < 2 * kLsRowsPerWarp ? slot / (2 * a.H) : 2 * kLsRowsPerWarp;
+    a.rows_per_stage = slot / (2 * a.H) < 2 * rpw ? slot / (2 * a.H) : 2 * rpw;
     const size_t sm = lmhead_stream_smem(a.K, a.H);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e == cudaSuccess) e = max_carveout(kern);
@@ -309,9 +343,9 @@ cudaError_t launch_lmhead_stream(const LmHeadArgs& a0, cudaStream_t s, bool pdl)
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, a);
   };
-  if (a0.K <= 4) return run(k_lmhead_stream<4>, LsShape<4>::pairs, LsShape<4>::slot);
-  if (a0.K <= 8) return run(k_lmhead_stream<8>, LsShape<8>::pairs, LsShape<8>::slot);
-  return run(k_lmhead_stream<16>, LsShape<16>::pairs, LsShape<16>::slot);
+  if (a0.K <= 4) return run(k_lmhead_stream<4>, LsShape<4>::pairs, LsShape<4>::slot, LsShape<4>::rpw);
+  if (a0.K <= 8) return run(k_lmhead_stream<8>, LsShape<8>::pairs, LsShape<8>::slot, LsShape<8>::rpw);
+  return run(k_lmhead_stream<16>, LsShape<16>::pairs, LsShape<16>::slot, LsShape<16>::rpw);
 }
 
 }  // namespace moe
