@@ -149,13 +149,20 @@ __global__ void __launch_bounds__(2 * LsShape<KR>::pairs * 32, 1) k_lmhead_strea
       if (i < n16) v[u] = xs[i];
     }
     __syncthreads();
+    // layout [row][piece j][half][lane][4]: lane l's elements 256 j + 8 l + 0..3
+    // and + 4..7 are each one float4, lanes of a half consecutive (no bank
+    // conflict when a warp reads them)
     float4* xf = reinterpret_cast<float4*>(xreg);
+    const int nj8 = H / 256;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int i = threadIdx.x + u * (int)blockDim.x;
       if (i < n16) {
-        xf[2 * i] = make_float4(lbf_lo(v[u].x), lbf_hi(v[u].x), lbf_lo(v[u].y), lbf_hi(v[u].y));
-        xf[2 * i + 1] = make_float4(lbf_lo(v[u].z), lbf_hi(v[u].z), lbf_lo(v[u].w), lbf_hi(v[u].w));
+        const int r = i / (H / 8), c = i - r * (H / 8);  // 16-byte piece c of row r
+        const int j = c >> 5, l = c & 31;
+        const int b = ((r * nj8 + j) * 2) * 32 + l;
+        xf[b] = make_float4(lbf_lo(v[u].x), lbf_hi(v[u].x), lbf_lo(v[u].y), lbf_hi(v[u].y));
+        xf[b + 32] = make_float4(lbf_lo(v[u].z), lbf_hi(v[u].z), lbf_lo(v[u].w), lbf_hi(v[u].w));
       }
     }
     __syncthreads();
@@ -209,8 +216,8 @@ __global__ void __launch_bounds__(2 * LsShape<KR>::pairs * 32, 1) k_lmhead_strea
           if (r < K) {
             float xf[8];
             if constexpr (XF32) {  // x held as floats
-              const float4 a0 = xf4[(r * H + j * 256 + 8 * lane) / 4];
-              const float4 a1 = xf4[(r * H + j * 256 + 8 * lane) / 4 + 1];
+              const float4 a0 = xf4[((r * nj + j) * 2) * 32 + lane];
+              const float4 a1 = xf4[((r * nj + j) * 2 + 1) * 32 + lane];
               xf[0] = a0.x; xf[1] = a0.y; xf[2] = a0.z; xf[3] = a0.w;
               xf[4] = a1.x; xf[5] = a1.y; xf[6] = a1.z; xf[7] = a1.w;
             } else {
