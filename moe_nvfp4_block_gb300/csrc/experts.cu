@@ -1439,13 +1439,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_experts(const __grid_consta
         }
         float acc0 = 0.f, acc1 = 0.f, sh0 = 0.f, sh1 = 0.f;
         bool good = true;
-        for (int s0 = 0; s0 < ns && good; s0 += 8) {
-          unsigned long long pw[8][2];
+        constexpr int kChunk = 12;  // top-8 and the shared expert: one round
+        for (int s0 = 0; s0 < ns && good; s0 += kChunk) {
+          unsigned long long pw[kChunk][2];
           const uint64_t t0 = global_timer_ns();
           for (;;) {  // every load of the chunk in flight at once
             bool all = true;
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
+            for (int u = 0; u < kChunk; ++u) {
               pw[u][0] = pw[u][1] = 0ull;
               if (s0 + u < ns) {
                 ld_tagged2(dp + (size_t)(s0 + u) * H, pw[u][0], pw[u][1]);
@@ -1460,7 +1461,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_experts(const __grid_consta
             poll_pause();
           }
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
+          for (int u = 0; u < kChunk; ++u) {
             const int s = s0 + u;
             const float p0 = __uint_as_float((unsigned)pw[u][0]), p1 = __uint_as_float((unsigned)pw[u][1]);
             if (s < k) {
