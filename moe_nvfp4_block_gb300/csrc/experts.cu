@@ -1259,29 +1259,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_experts(const __grid_consta
         float* rb = red + (size_t)(li & 1) * kRedFloats;
         bool ok = !__any_sync(0xffffffffu, aborted());
         if (ok && it.slot != cur_slot) {
-          // h of this slot, k-unit kq: every warp waits (bounded, no CTA
-          // barrier) until the 32 done flags of the 8 gate/up items that
-          // produce its k-unit carry this call's tag, then reads its words,
-          // again after a pause in the rare case that one is not visible yet,
-          // as B fragments; each k-unit takes its own per-row power-of-two
-          // scale
+          // h of this slot, k-unit kq, as B fragments: every warp reads its
+          // words at once (they usually carry this call's tag already: one
+          // round trip); if some do not, it waits (bounded, no CTA barrier)
+          // until the 32 done flags of the 8 gate/up items that produce its
+          // k-unit carry the tag -- one word per lane and attempt -- and
+          // reads the words again, after a pause in the rare case that one
+          // is not visible yet; each k-unit takes its own per-row
+          // power-of-two scale
           cur_slot = it.slot;
-          if (dn_active) {
-            const unsigned long long* fl = a.ws.flags + (size_t)it.slot * mt_per * 4 + 32 * kq + lane;
-            const uint64_t t0 = global_timer_ns();
-            for (;;) {
-              if (__all_sync(0xffffffffu, has_tag(ld_tagged(fl), tag))) break;
-              if (warp_gives_up(t0, a.wait_ns, &s_abort, lane)) {
-                ok = false;
-                break;
-              }
-              poll_pause();
-            }
-          }
           unsigned mx[NB];
           if (ok) {
             const unsigned long long* hs = a.ws.h + (size_t)it.slot * K * (I / 2) + kq * 64 + 4 * t;
+            const unsigned long long* fl = a.ws.flags + (size_t)it.slot * mt_per * 4 + 32 * kq + lane;
             const uint64_t t0 = global_timer_ns();
+            bool flagged = false;
             for (;;) {
               bool mine = true;
 #pragma unroll
@@ -1310,7 +1302,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_experts(const __grid_consta
                 ok = false;
                 break;
               }
-              poll_pause();
+              if (!flagged) {  // not all there yet: the done flags first
+                flagged = true;
+                for (;;) {
+                  if (__all_sync(0xffffffffu, has_tag(ld_tagged(fl), tag))) break;
+                  if (warp_gives_up(t0, a.wait_ns, &s_abort, lane)) {
+                    ok = false;
+                    break;
+                  }
+                  poll_pause();
+                }
+                if (!ok) break;
+              } else {
+                poll_pause();
+              }
             }
           }
           if (!ok && lane == 0) fail();
