@@ -161,6 +161,14 @@ size_t moe_group_ints(int K, int n_experts, int top_k);
  *             moe_router_topk); NULL to skip
  * Accumulation is FP32; activations enter the tensor cores as FP16 after an
  * exact per-row power-of-two rescaling, so no bf16 value overflows.
+ *
+ * The call is one grid of one CTA per SM whose CTAs wait on one another
+ * (every wait bounded, MOE_ERR_DEVICE_TIMEOUT when it runs out).  It needs
+ * all SMs of the GPU within that bound: work that holds SMs briefly
+ * (another kernel finishing) only delays it, but two layer calls (this one,
+ * moe_verify_stack or moe_verify_step) running at the same time on one GPU,
+ * e.g. on two streams, can each hold part of the SMs and both time out.
+ * Serialise them (one stream, or events between the streams).
  */
 moe_status moe_verify_layer(const moe_layer* layer, const uint16_t* x_norm, int K,
                             const uint16_t* residual, uint16_t* y, int32_t* idx_out, float* w_out,
