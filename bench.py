@@ -20,6 +20,11 @@ roofline  = the experts kernel's algorithmic bytes per launch over its mean
             around each launch), against the measured HBM copy bandwidth.
 stack_sweep = 40-layer verify steps at K = 1, 2, 4, 8, 16 (and the Zipf-biased
             K = 16 stack): verified tokens/s = K / step time.
+laguna_router_layer = the k2_layer call with the Laguna router tail (sigmoid
+            scores, selection-only bias, routed scale 2.5), GB/s as the headline.
+full_step.laguna_schedule = the full step with the Laguna layer schedule
+            (dense layer 0; sliding-window and full-attention layers with
+            their head counts and rotary embeddings) over the same caches.
 cpu_baseline = the CPU oracle on a bounded sample of the same workload.
 
 ``--impl reference`` times the CPU oracle alone on the same workload (the
@@ -478,6 +483,7 @@ def run_gpu(args):
         "setup_s": round(t_gen, 1),
     }
     if not args.no_sweep:
+        out["laguna_router_layer"] = laguna_router_layer(M, torch, synthgen, dev, stream, hbm, args.steps)
         out["stack_sweep"] = stack_sweep(M, torch, synthgen, dev, stream, hbm, args.sweep_steps)
     if not args.no_full_step:
         out["full_step"] = full_step(M, torch, synthgen, dev, stream, hbm, max(10, args.sweep_steps))
@@ -622,6 +628,7 @@ def full_step(M, torch, synthgen, dev, stream, hbm, steps):
     acc = int(n.item())
     gbs = step_bytes / (ms * 1e-3) / 1e9
     loop = verify_loop(M, torch, synthgen, dev, stream, model, w, steps)
+    laguna = laguna_step(M, torch, synthgen, dev, stream, hbm, steps, layers, model.lm_head, w)
     res = {"workload": "k4_full_step", "K": K, "layers": w.layers, "ctx": w.ctx, "vocab": w.vocab,
            "ms_per_step": round(ms, 4), "verified_tokens_per_s": round(K / (ms * 1e-3), 1),
            "accepted": acc, "accepted_expected": j,
@@ -629,7 +636,150 @@ def full_step(M, torch, synthgen, dev, stream, hbm, steps):
            "GBps": round(gbs, 1), "pct_of_peak": round(100 * gbs / hbm, 1),
            "step_bytes": step_bytes, "distinct_experts_mean": round(float(np.mean(n_u)), 2), "steps": steps,
            "ms_median": round(dist_["median"], 4), "ms_p10": round(dist_["p10"], 4), "ms_p90": round(dist_["p90"], 4),
-           "verify_loop": loop}
+           "verify_loop": loop, "laguna_schedule": laguna}
+    del layers, model
+    torch.cuda.empty_cache()
+    return res
+
+
+def laguna_router_layer(M, torch, synthgen, dev, stream, hbm, steps, R=4):
+    """The k2_layer shape with the Laguna router tail: sigmoid scores, a
+    selection-only bias of 0.05 N(0, 1) per expert (the size of a trained
+    correction bias next to scores in (0, 1)), routed scale 2.5.  A ring of R
+    layers replayed from a CUDA graph, algorithmic GB/s as in the headline
+    (plus the bias's E * 4 bytes)."""
+    w = synthgen.WORKLOADS["k2_layer"]
+    t = lambda p: (p.codes, p.scales, p.tscale)
+    layers, xs, ys = [], [], []
+    for l in range(R):
+        L = synthgen.make_layer(w, 40 + l)
+        bias = (synthgen.bf16_to_f32(synthgen.normal_bf16(31 + l, 0, synthgen.T_ROUTER_B, 0, w.E)) * 0.05)
+        sh = (t(L.sh_gate), t(L.sh_up), t(L.sh_down))
+        layers.append(M.layer_from_arrays(L.router_w, bias.astype(np.float32), t(L.gate), t(L.up), t(L.down), sh,
+                                          top_k=w.top_k, routed_scale=2.5, device=dev,
+                                          scoring=M.MOE_SCORE_SIGMOID))
+        xs.append(torch.from_numpy(synthgen.make_x(w, 1100 + l)).view(torch.bfloat16).to(dev))
+        ys.append(torch.empty_like(xs[-1]))
+        del L
+    cl = [lay.c() for lay in layers]
+    ws = M.workspace(layers[0], w.K, device=dev)
+    grp = torch.empty(M.moe_group_ints(w.K, w.E, w.top_k), dtype=torch.int32, device=dev)
+    n_u = []
+    with torch.cuda.stream(stream):
+        for i in range(R):
+            M.moe_verify_layer(layers[i], xs[i], None, ys[i], ws, group_out=grp, stream=stream, c_layer=cl[i])
+            stream.synchronize()
+            n_u.append(int(grp[0].item()))
+    nbytes = [kernel_bytes(w, n)["layer"] + w.E * 4 for n in n_u]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(R):
+            M.moe_verify_layer(layers[i], xs[i], None, ys[i], ws, stream=stream, c_layer=cl[i])
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g.replay()
+    stream.synchronize()
+    n_rep = max(200, steps // R)
+    per, tot = timed_replays(torch, stream, g, n_rep)
+    assert M.moe_workspace_error(ws, stream) == 0
+    ms = tot / (n_rep * R)
+    gbs = sum(nbytes) / R / (ms * 1e-3) / 1e9
+    dist_ = pctl([p / R for p in per])
+    res = {"workload": "k2_layer with the Laguna router tail (sigmoid scores, selection bias, routed scale 2.5)",
+           "K": w.K, "ms_per_call": round(ms, 5), "GBps": round(gbs, 1), "pct_of_peak": round(100 * gbs / hbm, 1),
+           "distinct_experts_mean": round(float(np.mean(n_u)), 2), "calls": n_rep * R,
+           "ms_median": round(dist_["median"], 5), "ms_p10": round(dist_["p10"], 5), "ms_p90": round(dist_["p90"], 5)}
+    del layers
+    torch.cuda.empty_cache()
+    return res
+
+
+def laguna_step(M, torch, synthgen, dev, stream, hbm, steps, base, lm_head, w):
+    """The Laguna layer schedule at the full-step shape (K=4, 40 layers over
+    16,384 cached positions, lm_head over 151,936 rows): layer 0 a dense
+    SwiGLU MLP (intermediate 8,192), layers 1..39 the full step's MoE layers;
+    per four layers three sliding-window ones (512 positions, 64 q heads,
+    RoPE on all 128 dims) then a full-attention one (48 q heads, YaRN x4 over
+    a 4,096 original context on 64 of the 128 dims); 8 KV heads (the full
+    step's caches).  The new q/o projections and the MLP are bf16
+    N(0, 0.02) drawn on the GPU.  One moe_verify_step per step, replayed from
+    a CUDA graph; bytes from a teacher pass (distinct experts per layer)."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    r = lambda *sz: (torch.randn(*sz, device=dev, generator=g) * 0.02).to(torch.bfloat16)
+    H, K, nkv = w.H, w.K, w.n_kv_heads
+    layers, cfgs = [], []
+    for l, b in enumerate(base):
+        cfg = synthgen.laguna_layer_kind(l)
+        nq = cfg["n_q_heads"]
+        pos = M.attn_pos(cfg["window"], cfg["rotary_dim"], cfg["rope_theta"], cfg["yarn_factor"], cfg["yarn_orig"])
+        mlp = None
+        if cfg["dense"]:
+            inter = synthgen.LAGUNA_DENSE_INTER
+            mlp = (r(inter, H), r(inter, H), r(H, inter))
+        layers.append(M.DecoderLayer(r(nq * 128, H), b.Wk, b.Wv, r(H, nq * 128), b.kcache, b.vcache,
+                                     None if cfg["dense"] else b.moe, nq, pos, mlp))
+        cfgs.append(cfg)
+    model = M.VerifyModel(layers, lm_head, synthgen.LAGUNA_SLIDING_HEADS, nkv)
+    x0 = torch.from_numpy(synthgen.make_x(w, 17)).view(torch.bfloat16).to(dev)
+    x = x0.clone()
+    ws = model.workspace(K, device=dev)
+    tgt = torch.empty(K, dtype=torch.int32, device=dev)
+    n = torch.empty(1, dtype=torch.int32, device=dev)
+    draft = torch.zeros(K, dtype=torch.int32, device=dev)
+    with torch.cuda.stream(stream):
+        M.moe_verify_step(model, x, draft, tgt, n, ws, stream=stream)
+    stream.synchronize()
+    dr, j = synthgen.make_drafts(w, tgt.cpu().numpy())
+    draft.copy_(torch.from_numpy(dr))
+    # teacher pass: each layer's block by itself, the MoE routing recorded
+    x.copy_(x0)
+    xn = torch.empty_like(x)
+    wl = M.workspace(layers[1].moe, K, device=dev)
+    grp = torch.empty(M.moe_group_ints(K, w.E, w.top_k), dtype=torch.int32, device=dev)
+    mws = M.dense_mlp_workspace(K, H, synthgen.LAGUNA_DENSE_INTER, device=dev)
+    n_u, step_bytes = [], 0
+    act = K * H * 2
+    with torch.cuda.stream(stream):
+        for l, (dl, cfg) in enumerate(zip(layers, cfgs)):
+            nq = cfg["n_q_heads"]
+            aws = M.attention_workspace(K, H, nq, nkv, device=dev)
+            M.moe_attention_block(x, dl.Wq, dl.Wk, dl.Wv, dl.Wo, dl.kcache, dl.vcache, x, aws, nq, nkv,
+                                  stream=stream, pos=dl.pos)
+            seen = min(w.ctx, cfg["window"]) if cfg["window"] else w.ctx
+            step_bytes += 2 * (nq + 2 * nkv) * 128 * H + 2 * H * nq * 128 + 2 * 2 * nkv * seen * 128 + 2 * act
+            if cfg["dense"]:
+                M.moe_dense_mlp_block(x, dl.mlp[0], dl.mlp[1], dl.mlp[2], x, mws, stream=stream)
+                step_bytes += 3 * 2 * dl.mlp[0].shape[0] * H + 3 * act
+            else:
+                M.moe_rmsnorm(x, xn, stream=stream)
+                M.moe_verify_layer(dl.moe, xn, x, x, wl, group_out=grp, stream=stream)
+                stream.synchronize()
+                n_u.append(int(grp[0].item()))
+                step_bytes += kernel_bytes(w, n_u[-1], residual=True, K=K)["layer"]
+            stream.synchronize()
+    step_bytes += w.vocab * H * 2 + 2 * act
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream):
+        x.copy_(x0)
+        M.moe_verify_step(model, x, draft, tgt, n, ws, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            gr.replay()
+    stream.synchronize()
+    per, tot = timed_replays(torch, stream, gr, steps)
+    assert M.moe_workspace_error(ws, stream) == 0
+    ms = tot / steps
+    dist_ = pctl(per)
+    acc = int(n.item())
+    gbs = step_bytes / (ms * 1e-3) / 1e9
+    res = {"workload": "Laguna schedule at the k4_full_step shape (dense layer 0, 3 sliding : 1 full attention, "
+                       "64 / 48 q heads, RoPE / YaRN)",
+           "K": K, "layers": len(layers), "ctx": w.ctx, "vocab": w.vocab, "ms_per_step": round(ms, 4),
+           "verified_tokens_per_s": round(K / (ms * 1e-3), 1), "accepted": acc, "accepted_expected": j,
+           "GBps": round(gbs, 1), "pct_of_peak": round(100 * gbs / hbm, 1), "step_bytes": step_bytes,
+           "distinct_experts_mean": round(float(np.mean(n_u)), 2), "steps": steps,
+           "ms_median": round(dist_["median"], 4), "ms_p10": round(dist_["p10"], 4), "ms_p90": round(dist_["p90"], 4)}
     del layers, model
     torch.cuda.empty_cache()
     return res
