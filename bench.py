@@ -69,6 +69,9 @@ def parse(argv=None):
     p.add_argument("--no-full-step", action="store_true", help="skip the full verify step (attention + MoE)")
     p.add_argument("--only-full-step", action="store_true",
                    help="run only the full verify step and print its JSON object (for profiling its launches)")
+    p.add_argument("--only-laguna", action="store_true",
+                   help="run only the Laguna-schedule step at the full-step shape and print its JSON object "
+                        "(for profiling its launches)")
     p.add_argument("--kernel-case", choices=["attention", "lm_head"], default=None,
                    help="run only one attention block (K=4, H=2048, 32/8 heads, 16,384 cached positions) or one "
                         "lm_head argmax (151,936 x 2048) a few times and print its time (a small case for ncu)")
@@ -302,11 +305,11 @@ def run_gpu(args):
     if args.kernel_case:
         print(json.dumps(kernel_case(M, torch, dev, args.kernel_case, args.case_iters)), flush=True)
         return
-    if args.only_full_step:
+    if args.only_full_step or args.only_laguna:
         hbm, _ = peaks()
         stream = torch.cuda.Stream(device=dev)
-        print(json.dumps({"full_step": full_step(M, torch, synthgen, dev, stream, hbm, max(3, args.sweep_steps))}),
-              flush=True)
+        res = full_step(M, torch, synthgen, dev, stream, hbm, max(3, args.sweep_steps), args.only_laguna)
+        print(json.dumps({"full_step": res}), flush=True)
         return
     w = synthgen.WORKLOADS[args.workload]
     R = args.ring
@@ -564,10 +567,11 @@ def stack_sweep(M, torch, synthgen, dev, stream, hbm, steps):
     return res
 
 
-def full_step(M, torch, synthgen, dev, stream, hbm, steps):
+def full_step(M, torch, synthgen, dev, stream, hbm, steps, only_laguna=False):
     """The k4_full_step workload: 40 x (GQA attention over a 16,384-position
     bf16 cache + MoE block), lm_head argmax over 151,936 rows, accepted
-    prefix; one native moe_verify_step per step, replayed from a CUDA graph."""
+    prefix; one native moe_verify_step per step, replayed from a CUDA graph.
+    only_laguna: build the same layers but time only the Laguna schedule."""
     w = synthgen.WORKLOADS["k4_full_step"]
     t = lambda p: (p.codes, p.scales, p.tscale)
     d = lambda a: torch.from_numpy(a).view(torch.bfloat16).to(dev)
@@ -580,6 +584,11 @@ def full_step(M, torch, synthgen, dev, stream, hbm, steps):
         layers.append(M.DecoderLayer(d(A["Wq"]), d(A["Wk"]), d(A["Wv"]), d(A["Wo"]), d(A["kc"]), d(A["vc"]), moe))
         del A, L
     model = M.VerifyModel(layers, d(synthgen.make_lm_head(w)), w.n_q_heads, w.n_kv_heads)
+    if only_laguna:
+        res = {"laguna_schedule": laguna_step(M, torch, synthgen, dev, stream, hbm, steps, layers, model.lm_head, w)}
+        del layers, model
+        torch.cuda.empty_cache()
+        return res
     K = w.K
     x0 = d(synthgen.make_x(w, 11))
     x = x0.clone()

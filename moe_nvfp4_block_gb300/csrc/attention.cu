@@ -233,58 +233,72 @@ cudaError_t launch_swiglu(const SwigluArgs& a, cudaStream_t s, bool pdl) {
 }
 
 // ------------------------------------------------------------------ rotary embedding
-// One block.  The K x rd/2 angles (pos0 + r) * freq[i] -- shared by all heads
-// -- and their sines and cosines are taken in double (positions reach the
-// cache length, where an FP32 product would lose the angle); then one thread
-// per (row, head, pair) rotates (v[i], v[i + rd/2]) in FP32 and rounds to
-// bf16.  With caches given, the rotated keys and the values then go to
-// positions pos0 + r (bounded by the capacity).
-__global__ void __launch_bounds__(1024) k_rope(RopeArgs a) {
-  __shared__ float s_cos[16 * 64], s_sin[16 * 64];
+// Grid (K, units / 4): CTA (r, j) serves row r.  Its threads first take the
+// rd/2 angles (pos0 + r) * freq[i] of that row and their sines and cosines
+// in double (positions reach the cache length, where an FP32 product would
+// lose the angle).  Then each warp takes one unit of the row: a q head, a k
+// head or (with caches given) a v head.  For a q or k head, lane l rotates
+// the pairs (v[i], v[i + rd/2]) with i = l, l + 32 in FP32 and rounds to
+// bf16, in place; a k head's warp then writes its whole rotated head to
+// the key cache at position pos0 + r, and a v head's warp copies the value
+// head to the value cache (both bounded by the capacity).  No warp reads
+// what another one writes.
+constexpr int kRopeWarps = 4;
+
+__global__ void __launch_bounds__(kRopeWarps * 32) k_rope(RopeArgs a) {
+  __shared__ float s_cos[64], s_sin[64];
   pdl_wait();
   pdl_launch_dependents();
+  const int r = blockIdx.x;
   const int half = a.rd / 2;
   const int pos0 = a.len ? *a.len : a.C;
-  for (int t = threadIdx.x; t < a.K * half; t += blockDim.x) {
-    const int r = t / half, i = t - r * half;
+  const int p = pos0 + r;
+  for (int i = threadIdx.x; i < half; i += blockDim.x) {
     double sn, cs;
-    sincos((double)(pos0 + r) * a.freq[i], &sn, &cs);
-    s_cos[t] = (float)cs;
-    s_sin[t] = (float)sn;
+    sincos((double)p * a.freq[i], &sn, &cs);
+    s_cos[i] = (float)cs;
+    s_sin[i] = (float)sn;
   }
   __syncthreads();
-  const int per_row = (a.nq + a.nkv) * half;
-  const int total = a.K * per_row;
-  for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
-    const int r = idx / per_row, rem = idx - r * per_row;
-    const int hh = rem / half, i = rem - hh * half;
-    uint16_t* base = hh < a.nq ? a.q + (size_t)r * a.nq * 128 + (size_t)hh * 128
-                               : a.k + (size_t)r * a.nkv * 128 + (size_t)(hh - a.nq) * 128;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int u = blockIdx.y * kRopeWarps + warp;
+  const int nunit = a.nq + a.nkv + (a.kc ? a.nkv : 0);
+  if (u >= nunit) return;
+  const bool room = p < a.C;
+  if (a.kc && !room && u == 0 && lane == 0 && a.err) atomicCAS(a.err, 0, (int)MOE_ERR_CAPACITY);
+  if (u >= a.nq + a.nkv) {  // value head: cache append only
+    if (!room) return;
+    const int kvh = u - a.nq - a.nkv;
+    const uint16_t* src = a.v + ((size_t)r * a.nkv + kvh) * 128;
+    uint16_t* dst = a.vc + ((size_t)kvh * a.C + p) * 128;
+    for (int d = lane; d < 128; d += 32) dst[d] = src[d];
+    return;
+  }
+  const bool isk = u >= a.nq;
+  const int kvh = u - a.nq;
+  uint16_t* base = isk ? a.k + ((size_t)r * a.nkv + kvh) * 128 : a.q + ((size_t)r * a.nq + u) * 128;
+  uint16_t* dst = (isk && a.kc && room) ? a.kc + ((size_t)kvh * a.C + p) * 128 : nullptr;
+  for (int i = lane; i < half; i += 32) {
     const float x0 = bf16_bits_to_float(base[i]), x1 = bf16_bits_to_float(base[i + half]);
-    const float c = s_cos[r * half + i], s = s_sin[r * half + i];
-    base[i] = float_to_bf16_bits(__fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, s)));
-    base[i + half] = float_to_bf16_bits(__fadd_rn(__fmul_rn(x1, c), __fmul_rn(x0, s)));
-  }
-  if (!a.kc) return;
-  __syncthreads();  // the rotated keys are in place
-  const int nkv_el = a.K * a.nkv * 128;
-  for (int idx = threadIdx.x; idx < nkv_el; idx += blockDim.x) {
-    const int r = idx / (a.nkv * 128), rem = idx - r * a.nkv * 128;
-    const int kvh = rem >> 7, d = rem & 127;
-    const int p = pos0 + r;
-    if (p >= a.C) {
-      if (a.err) atomicCAS(a.err, 0, (int)MOE_ERR_CAPACITY);
-      continue;
+    const float c = s_cos[i], s = s_sin[i];
+    const uint16_t y0 = float_to_bf16_bits(__fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, s)));
+    const uint16_t y1 = float_to_bf16_bits(__fadd_rn(__fmul_rn(x1, c), __fmul_rn(x0, s)));
+    base[i] = y0;
+    base[i + half] = y1;
+    if (dst) {
+      dst[i] = y0;
+      dst[i + half] = y1;
     }
-    a.kc[((size_t)kvh * a.C + p) * 128 + d] = a.k[idx];
-    a.vc[((size_t)kvh * a.C + p) * 128 + d] = a.v[idx];
   }
+  if (dst)  // the dims past the rotary ones, unchanged
+    for (int d = a.rd + lane; d < 128; d += 32) dst[d] = base[d];
 }
 
 cudaError_t launch_rope(const RopeArgs& a, cudaStream_t s) {
+  const int nunit = a.nq + a.nkv + (a.kc ? a.nkv : 0);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(1);
-  cfg.blockDim = dim3(1024);
+  cfg.gridDim = dim3(a.K, (nunit + kRopeWarps - 1) / kRopeWarps);
+  cfg.blockDim = dim3(kRopeWarps * 32);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -33,7 +33,10 @@ namespace {
 constexpr int kGsWarps = 16;
 constexpr int kGsStages = 6;
 constexpr int kGsStageBytes = 32768;
-constexpr int kGsMaxBlocks = 8;  // stages per CTA (one accumulator set each)
+constexpr int kGsMaxBlocks = 12;  // stages per CTA (one accumulator set each), at most
+// Accumulator sets: 8, or 12 where x's fragments (KPW * 2 * KH registers)
+// leave room; the 8-set form runs whenever it suffices.
+constexpr int gs_max_sets(int kpw, int kh) { return kpw * kh <= 16 ? 12 : 8; }
 constexpr int kGsTail = 1024;    // barriers and the stage table after the ring
 // Bound on waiting for the CTA's own copies before it exits (independent of
 // the caller's wait limit, which may be 0 in a test of the give-up path).
@@ -67,10 +70,12 @@ struct GsTable {
   float inv[16];
 };
 static_assert(sizeof(GsTable) <= kGsTail, "stage table");
+// the partial sums of every set fit the ring once it is free
+static_assert(kGsMaxBlocks * kGsWarps * 128 * 4 <= kGsStages * kGsStageBytes, "reduction area");
 
 }  // namespace
 
-template <int KPW, int KH>
+template <int KPW, int KH, int NB>
 __global__ void __launch_bounds__(kGsWarps * 32, 1) k_gemv_stream(const __grid_constant__ GemvArgs a) {
   extern __shared__ __align__(1024) unsigned char smem[];
   GsTable& T = *reinterpret_cast<GsTable*>(smem + kGsStages * kGsStageBytes);
@@ -80,6 +85,7 @@ __global__ void __launch_bounds__(kGsWarps * 32, 1) k_gemv_stream(const __grid_c
   int issued = 0;  // thread 0: stages whose copy was issued
   uint64_t pol = 0;
 
+  static_assert(NB <= kGsMaxBlocks, "accumulator sets");
   auto issue = [&](int s) {
     const int slot = s % kGsStages;
     const uint32_t bytes = (uint32_t)T.n[s] * (uint32_t)D * 2u;
@@ -96,7 +102,7 @@ __global__ void __launch_bounds__(kGsWarps * 32, 1) k_gemv_stream(const __grid_c
     T.abort = 0;
     while (cur < r1) {
       while (cur >= base + a.seg[sg].N) base += a.seg[sg++].N;
-      if (ns == kGsMaxBlocks) {  // more stages than accumulator sets: refused by the launcher
+      if (ns == NB) {  // more stages than accumulator sets: refused by the launcher
         T.abort = 1;
         break;
       }
@@ -180,15 +186,15 @@ __global__ void __launch_bounds__(kGsWarps * 32, 1) k_gemv_stream(const __grid_c
     }
   }
 
-  float acc[kGsMaxBlocks][4];
+  float acc[NB][4];
 #pragma unroll
-  for (int s = 0; s < kGsMaxBlocks; ++s)
+  for (int s = 0; s < NB; ++s)
 #pragma unroll
     for (int c = 0; c < 4; ++c) acc[s][c] = 0.f;
   const int ns = T.nst;
   volatile int* abort = &T.abort;
 #pragma unroll
-  for (int s = 0; s < kGsMaxBlocks; ++s) {
+  for (int s = 0; s < NB; ++s) {
     if (s >= ns) break;
     const int slot = s % kGsStages;
     const uint32_t par = (uint32_t)(s / kGsStages) & 1u;
@@ -240,7 +246,7 @@ __global__ void __launch_bounds__(kGsWarps * 32, 1) k_gemv_stream(const __grid_c
   // partial sums to the (now free) ring: red[s][w][m][n], m < 16, n < 8
   float* red = reinterpret_cast<float*>(smem);
 #pragma unroll
-  for (int s = 0; s < kGsMaxBlocks; ++s) {
+  for (int s = 0; s < NB; ++s) {
     if (s >= ns) break;
     float* p = red + ((size_t)s * kGsWarps + warp) * 128;
     p[g * 8 + 2 * t] = acc[s][0];
@@ -272,24 +278,31 @@ int gemv_rows_per_stage(int D) { return kGsStageBytes / (2 * D) < 8 ? kGsStageBy
 
 // Whether the streamed kernel takes this GEMV: x's fragments must fit the
 // registers and no CTA may need more stages than it has accumulator sets.
+static int gemv_stream_sets(const GemvArgs& a, int grid) {
+  const int R = gemv_rows_per_stage(a.D);
+  const int rows_max = (a.n_total + grid - 1) / grid;
+  return (rows_max + R - 1) / R + (a.nseg - 1);
+}
+
 bool gemv_stream_fits(const GemvArgs& a, int grid) {
   if (a.K < 1 || a.K > 16 || a.D % 512 != 0) return false;
   const int kpw = a.D / 256;
   if (kpw != 8 && kpw != 16 && kpw != 24 && kpw != 32) return false;
   if (a.K > 8 && kpw > 16) return false;
-  const int R = gemv_rows_per_stage(a.D);
-  const int rows_max = (a.n_total + grid - 1) / grid;
-  return (rows_max + R - 1) / R + (a.nseg - 1) <= kGsMaxBlocks;
+  return gemv_stream_sets(a, grid) <= gs_max_sets(kpw, a.K > 8 ? 2 : 1);
 }
 
 cudaError_t launch_gemv_stream(const GemvArgs& a, cudaStream_t s, bool pdl) {
   const int kpw = a.D / 256;
   const bool two = a.K > 8;
+  const bool wide = gemv_stream_sets(a, num_sms()) > 8;
   void (*kern)(GemvArgs) = nullptr;
-  if (kpw == 8) kern = two ? k_gemv_stream<8, 2> : k_gemv_stream<8, 1>;
-  else if (kpw == 16) kern = two ? k_gemv_stream<16, 2> : k_gemv_stream<16, 1>;
-  else if (kpw == 24 && !two) kern = k_gemv_stream<24, 1>;
-  else if (kpw == 32 && !two) kern = k_gemv_stream<32, 1>;
+  if (kpw == 8 && wide) kern = two ? k_gemv_stream<8, 2, 12> : k_gemv_stream<8, 1, 12>;
+  else if (kpw == 8) kern = two ? k_gemv_stream<8, 2, 8> : k_gemv_stream<8, 1, 8>;
+  else if (kpw == 16 && wide && !two) kern = k_gemv_stream<16, 1, 12>;
+  else if (kpw == 16 && !wide) kern = two ? k_gemv_stream<16, 2, 8> : k_gemv_stream<16, 1, 8>;
+  else if (kpw == 24 && !two && !wide) kern = k_gemv_stream<24, 1, 8>;
+  else if (kpw == 32 && !two && !wide) kern = k_gemv_stream<32, 1, 8>;
   if (!kern) return cudaErrorInvalidValue;
   const size_t sm = (size_t)kGsStages * kGsStageBytes + kGsTail;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
