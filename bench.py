@@ -76,6 +76,8 @@ def parse(argv=None):
                    help="run only one attention block (K=4, H=2048, 32/8 heads, 16,384 cached positions) or one "
                         "lm_head argmax (151,936 x 2048) a few times and print its time (a small case for ncu)")
     p.add_argument("--case-iters", type=int, default=20)
+    p.add_argument("--case-heads", type=int, default=32,
+                   help="q heads of the attention kernel case (64: the Laguna sliding-window layers' projections)")
     p.add_argument("--oracle-sample", type=float, default=None,
                    help="(internal) time the CPU oracle for this many seconds and print bytes/s as JSON")
     return p.parse_args(argv)
@@ -303,7 +305,7 @@ def run_gpu(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     if args.kernel_case:
-        print(json.dumps(kernel_case(M, torch, dev, args.kernel_case, args.case_iters)), flush=True)
+        print(json.dumps(kernel_case(M, torch, dev, args.kernel_case, args.case_iters, args.case_heads)), flush=True)
         return
     if args.only_full_step or args.only_laguna:
         hbm, _ = peaks()
@@ -794,15 +796,15 @@ def laguna_step(M, torch, synthgen, dev, stream, hbm, steps, base, lm_head, w):
     return res
 
 
-def kernel_case(M, torch, dev, which, iters):
-    """One attention block of the full-step shape or one lm_head argmax,
+def kernel_case(M, torch, dev, which, iters, nq=32):
+    """One attention block of the full-step shape (nq q heads) or one lm_head argmax,
     launched `iters` times back to back on one stream (no graph), random bf16
     operands; µs per call and algorithmic GB/s.  Sized for an ncu capture
     (about 0.1 / 0.6 GB on the device)."""
     g = torch.Generator(device=dev)
     g.manual_seed(7)
     r = lambda *s, sd=0.02: (torch.randn(*s, device=dev, generator=g) * sd).to(torch.bfloat16)
-    K, H, nq, nkv, C, V = 4, 2048, 32, 8, 16384, 151936
+    K, H, nkv, C, V = 4, 2048, 8, 16384, 151936
     st = torch.cuda.Stream(device=dev)
     if which == "attention":
         Wq, Wk, Wv, Wo = r(nq * 128, H), r(nkv * 128, H), r(nkv * 128, H), r(H, nq * 128)
@@ -829,7 +831,7 @@ def kernel_case(M, torch, dev, which, iters):
     st.synchronize()
     us = ev[0].elapsed_time(ev[1]) * 1e3 / iters
     assert M.moe_workspace_error(ws, st) == 0
-    return {"kernel_case": which, "us_per_call": round(us, 2), "GBps": round(nbytes / (us * 1e-6) / 1e9, 1),
+    return {"kernel_case": which, "q_heads": nq, "us_per_call": round(us, 2), "GBps": round(nbytes / (us * 1e-6) / 1e9, 1),
             "bytes": nbytes, "iters": iters}
 
 

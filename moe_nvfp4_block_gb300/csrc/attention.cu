@@ -152,11 +152,7 @@ static cudaError_t launch_rows_kernel(Kern kern, const Args& a, size_t sm, cudaS
 }
 
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t s, bool pdl) {
-  if (gemv_stream_fits(a, num_sms())) {
-    GemvArgs b = a;
-    b.rows_per_stage = gemv_rows_per_stage(a.D);
-    return launch_gemv_stream(b, s, pdl);
-  }
+  if (gemv_stream_fits(a, num_sms())) return launch_gemv_stream(a, s, pdl);
   if (a.norm_eps > 0.f) return cudaErrorInvalidValue;  // the row kernel takes normalised rows only
   const size_t sm = sizeof(uint16_t) * a.K * a.D;
   if (a.K <= 4) return launch_rows_kernel(k_gemv_bf16<4>, a, sm, s, pdl);

@@ -7,19 +7,22 @@
 // exactly those weight rows -- each byte once -- through a ring of shared-
 // memory stages filled by bulk copies.  The weights do not depend on the
 // previous kernel, so the first ring-full is issued before the dependency
-// wait and lands while that kernel finishes.  A stage holds up to
-// R = min(8, 16384 / D) consecutive rows of one matrix (at most 32 KB).
+// wait and lands while that kernel finishes.
 //
-// The 16 warps split the reduction dimension: warp w owns columns
-// [w D/16, (w+1) D/16) and keeps its fragments of x in registers for the
-// whole kernel.  Per stage and 16-column step a warp issues one
-// mma.sync m16n8k16 (A = the K rows of x, B = the stage's rows as the n
-// dimension, FP32 accumulate).  After the last stage the 16 warps' partial
-// sums of each output are added in warp order.
+// The CTA's rows are cut into groups of up to 8 consecutive rows of one
+// matrix, and each group into D / 2048 column blocks: a stage holds one
+// block of one group (8 x 4 KB; rows 4160 bytes apart in shared memory, so
+// that a warp's reads of the 8 rows fall on all 32 banks).  The 16 warps
+// split the reduction dimension: warp w owns columns [128 w, 128 w + 128)
+// of every block and keeps its fragments of x in registers for the whole
+// kernel.  Per stage and 16-column step a warp issues one mma.sync m16n8k16
+// (A = the K rows of x, B = the group's rows as the n dimension, FP32
+// accumulate) into the group's accumulators.  After the last stage the 16
+// warps' partial sums of each output are added in warp order.
 //
-// Column order inside a warp's 32-column blocks: thread t of a quad reads
+// Column order inside a warp's 32-column pieces: thread t of a quad reads
 // the 8 consecutive columns [8t, 8t+8).  Its first four are its logical
-// k = 2t, 2t+1, 2t+8, 2t+9 of the block's even 16-column step, the last four
+// k = 2t, 2t+1, 2t+8, 2t+9 of the piece's even 16-column step, the last four
 // those of the odd step.  x and W use the same order, so every product is
 // x[r][c] * W[n][c]; only the order of the FP32 sum differs from a plain
 // dot product.
@@ -32,15 +35,18 @@ namespace {
 
 constexpr int kGsWarps = 16;
 constexpr int kGsStages = 6;
-constexpr int kGsStageBytes = 32768;
-constexpr int kGsMaxBlocks = 12;  // stages per CTA (one accumulator set each), at most
-// Accumulator sets: 8, or 12 where x's fragments (KPW * 2 * KH registers)
-// leave room; the 8-set form runs whenever it suffices.
-constexpr int gs_max_sets(int kpw, int kh) { return kpw * kh <= 16 ? 12 : 8; }
-constexpr int kGsTail = 1024;    // barriers and the stage table after the ring
+constexpr int kGsRows = 8;                 // rows per group (the mma's n dimension)
+constexpr int kGsCols = 2048;              // columns per block: 4 KB of a row
+constexpr int kGsPitch = kGsCols * 2 + 64; // bytes between a stage's rows
+constexpr int kGsStageBytes = kGsRows * kGsPitch;
+constexpr int kGsMaxGroups = 12;  // row groups per CTA (one accumulator set each), at most
+constexpr int kGsTail = 1024;     // barriers and the group table after the ring
 // Bound on waiting for the CTA's own copies before it exits (independent of
 // the caller's wait limit, which may be 0 in a test of the give-up path).
 constexpr uint64_t kGsDrainNs = 2000000000ull;
+// Accumulator sets (row groups) of an instantiation: x's fragments take
+// KPW * 2 * KH registers, so the narrow ones have room for more sets.
+constexpr int gs_max_groups(int kpw, int kh) { return kpw * kh <= 16 ? 12 : (kpw <= 16 ? 8 : 4); }
 
 __device__ __forceinline__ float bfl(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bfh(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -64,84 +70,96 @@ __device__ __forceinline__ uint32_t scale_pair(uint32_t w, float inv) {
 struct GsTable {
   uint64_t full[kGsStages];
   uint64_t empty[kGsStages];
-  int seg[kGsMaxBlocks], row[kGsMaxBlocks], n[kGsMaxBlocks];
-  int nst;
+  int seg[kGsMaxGroups], row[kGsMaxGroups], n[kGsMaxGroups];
+  int ng;
   int abort;
   float inv[16];
 };
-static_assert(sizeof(GsTable) <= kGsTail, "stage table");
-// the partial sums of every set fit the ring once it is free
-static_assert(kGsMaxBlocks * kGsWarps * 128 * 4 <= kGsStages * kGsStageBytes, "reduction area");
+static_assert(sizeof(GsTable) <= kGsTail, "group table");
+// the partial sums of every group fit the ring once it is free
+static_assert(kGsMaxGroups * kGsWarps * 128 * 4 <= kGsStages * kGsStageBytes, "reduction area");
+static_assert(kGsPitch % 16 == 0 && kGsStageBytes % 16 == 0, "bulk copy alignment");
 
 }  // namespace
 
-template <int KPW, int KH, int NB>
+template <int KPW, int KH, int NG>
 __global__ void __launch_bounds__(kGsWarps * 32, 1) k_gemv_stream(const __grid_constant__ GemvArgs a) {
+  static_assert(NG <= kGsMaxGroups && KPW % 8 == 0, "accumulator sets, column blocks");
+  constexpr int NCB = KPW / 8;  // column blocks of 2048
   extern __shared__ __align__(1024) unsigned char smem[];
   GsTable& T = *reinterpret_cast<GsTable*>(smem + kGsStages * kGsStageBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const int D = a.D, K = a.K;
-  int issued = 0;  // thread 0: stages whose copy was issued
+  int issued = 0;  // warp 0: stages whose copies were issued
   uint64_t pol = 0;
 
-  static_assert(NB <= kGsMaxBlocks, "accumulator sets");
+  // stage s = block s % NCB of group s / NCB, issued by warp 0: lane 0 posts
+  // the stage's bytes, then lane i copies row i (4 KB)
   auto issue = [&](int s) {
-    const int slot = s % kGsStages;
-    const uint32_t bytes = (uint32_t)T.n[s] * (uint32_t)D * 2u;
-    mbar_arrive_expect_tx(&T.full[slot], bytes);
-    bulk_load(smem + (size_t)slot * kGsStageBytes, a.seg[T.seg[s]].W + (size_t)T.row[s] * D, bytes,
-              &T.full[slot], pol);
+    const int slot = s % kGsStages, gr = s / NCB, cb = s - gr * NCB;
+    const int nr = T.n[gr];
+    if (lane == 0) mbar_arrive_expect_tx(&T.full[slot], (uint32_t)nr * (kGsCols * 2));
+    __syncwarp();
+    if (lane < nr)
+      bulk_load(smem + (size_t)slot * kGsStageBytes + (size_t)lane * kGsPitch,
+                a.seg[T.seg[gr]].W + (size_t)(T.row[gr] + lane) * D + (size_t)cb * kGsCols, kGsCols * 2,
+                &T.full[slot], pol);
   };
 
   if (threadIdx.x == 0) {
-    // this CTA's output rows [r0, r1), cut into stages at matrix ends
+    // this CTA's output rows [r0, r1), cut into groups at matrix ends
     const int r0 = (int)((long long)blockIdx.x * a.n_total / gridDim.x);
     const int r1 = (int)((long long)(blockIdx.x + 1) * a.n_total / gridDim.x);
-    int ns = 0, cur = r0, base = 0, sg = 0;
+    int ng = 0, cur = r0, base = 0, sg = 0;
     T.abort = 0;
     while (cur < r1) {
       while (cur >= base + a.seg[sg].N) base += a.seg[sg++].N;
-      if (ns == NB) {  // more stages than accumulator sets: refused by the launcher
+      if (ng == NG) {  // more groups than accumulator sets: refused by the launcher
         T.abort = 1;
         break;
       }
-      const int nr = min(a.rows_per_stage, min(r1, base + a.seg[sg].N) - cur);
-      T.seg[ns] = sg;
-      T.row[ns] = cur - base;
-      T.n[ns] = nr;
-      ++ns;
+      const int nr = min(kGsRows, min(r1, base + a.seg[sg].N) - cur);
+      T.seg[ng] = sg;
+      T.row[ng] = cur - base;
+      T.n[ng] = nr;
+      ++ng;
       cur += nr;
     }
-    T.nst = T.abort ? 0 : ns;
+    T.ng = T.abort ? 0 : ng;
     for (int i = 0; i < kGsStages; ++i) {
       mbar_init(&T.full[i], 1);
       mbar_init(&T.empty[i], kGsWarps);
     }
     fence_mbar_init();
+  }
+  if (warp == 0) {
+    __syncwarp();
     pol = policy_evict_first();
-    for (; issued < min(T.nst, kGsStages); ++issued) issue(issued);
+    const int first = min(T.ng * NCB, kGsStages);
+    for (; issued < first; ++issued) issue(issued);
   }
   __syncthreads();
   pdl_wait();
   pdl_launch_dependents();
   if (T.abort && threadIdx.x == 0 && a.err) atomicCAS(a.err, 0, (int)MOE_ERR_UNSUPPORTED_SHAPE);
 
-  // x fragments of this warp's columns: xa[k][0], xa[k][1] = a0, a2 (row g);
-  // xa[k][2], xa[k][3] = a1, a3 (row g + 8)
-  const int cb = warp * (D / kGsWarps) + 8 * t;
+  // x fragments of this warp's columns, piece p (32 columns) at column
+  // 2048 (p / 4) + 128 warp + 32 (p % 4) + 8t: xa[2p], xa[2p + 1] hold
+  // [0], [1] = a0, a2 (row g) and [2], [3] = a1, a3 (row g + 8)
+  const int cw = warp * 128 + 8 * t;
   uint32_t xa[KPW][2 * KH];
 #pragma unroll
-  for (int kp = 0; kp < KPW / 2; ++kp)
+  for (int p = 0; p < KPW / 2; ++p)
 #pragma unroll
     for (int h = 0; h < KH; ++h) {
       const int r = g + 8 * h;
       uint4 v = make_uint4(0, 0, 0, 0);
-      if (r < K) v = *reinterpret_cast<const uint4*>(a.x + (size_t)r * D + cb + 32 * kp);
-      xa[2 * kp][2 * h] = v.x;
-      xa[2 * kp][2 * h + 1] = v.y;
-      xa[2 * kp + 1][2 * h] = v.z;
-      xa[2 * kp + 1][2 * h + 1] = v.w;
+      if (r < K) v = *reinterpret_cast<const uint4*>(a.x + (size_t)r * D + (p >> 2) * kGsCols + cw + 32 * (p & 3));
+      xa[2 * p][2 * h] = v.x;
+      xa[2 * p][2 * h + 1] = v.y;
+      xa[2 * p + 1][2 * h] = v.z;
+      xa[2 * p + 1][2 * h + 1] = v.w;
     }
   if (a.norm_eps > 0.f) {
     // RMSNorm of row `warp` in the fixed order of the RMSNorm kernel: lane l
@@ -186,51 +204,59 @@ __global__ void __launch_bounds__(kGsWarps * 32, 1) k_gemv_stream(const __grid_c
     }
   }
 
-  float acc[NB][4];
+  float acc[NG][4];
 #pragma unroll
-  for (int s = 0; s < NB; ++s)
+  for (int gr = 0; gr < NG; ++gr)
 #pragma unroll
-    for (int c = 0; c < 4; ++c) acc[s][c] = 0.f;
-  const int ns = T.nst;
+    for (int c = 0; c < 4; ++c) acc[gr][c] = 0.f;
+  const int ng = T.ng, nst = T.ng * NCB;
   volatile int* abort = &T.abort;
 #pragma unroll
-  for (int s = 0; s < NB; ++s) {
-    if (s >= ns) break;
-    const int slot = s % kGsStages;
-    const uint32_t par = (uint32_t)(s / kGsStages) & 1u;
-    bool ok = !*abort && mbar_wait_bounded(&T.full[slot], par, a.wait_ns, abort);
-    ok = __all_sync(0xffffffffu, ok);  // converged for mma.sync; one verdict per warp
-    if (!ok) {
-      *abort = 1;
-    } else {
-      // lanes of rows past the stage's own (R < 8, or a short last stage)
-      // read nothing: their n columns are zero and unused
-      const bool live = g < T.n[s];
-      const unsigned char* wp = smem + (size_t)slot * kGsStageBytes + ((size_t)(live ? g : 0) * D + cb) * 2;
+  for (int gr = 0; gr < NG; ++gr) {
+    if (gr >= ng) break;
+    // lanes of rows past the group's own (a short group) read nothing:
+    // their n columns are zero and unused
+    const bool live = g < T.n[gr];
 #pragma unroll
-      for (int kp = 0; kp < KPW / 2; ++kp) {
-        const uint4 w = live ? *reinterpret_cast<const uint4*>(wp + 64 * kp) : make_uint4(0, 0, 0, 0);
-        if constexpr (KH > 1) {
-          mma_bf16_gs(acc[s], xa[2 * kp][0], xa[2 * kp][2], xa[2 * kp][1], xa[2 * kp][3], w.x, w.y);
-          mma_bf16_gs(acc[s], xa[2 * kp + 1][0], xa[2 * kp + 1][2], xa[2 * kp + 1][1], xa[2 * kp + 1][3], w.z, w.w);
-        } else {
-          mma_bf16_gs(acc[s], xa[2 * kp][0], 0u, xa[2 * kp][1], 0u, w.x, w.y);
-          mma_bf16_gs(acc[s], xa[2 * kp + 1][0], 0u, xa[2 * kp + 1][1], 0u, w.z, w.w);
+    for (int cb = 0; cb < NCB; ++cb) {
+      const int s = gr * NCB + cb;
+      const int slot = s % kGsStages;
+      const uint32_t par = (uint32_t)(s / kGsStages) & 1u;
+      bool ok = !*abort && mbar_wait_bounded(&T.full[slot], par, a.wait_ns, abort);
+      ok = __all_sync(0xffffffffu, ok);  // converged for mma.sync; one verdict per warp
+      if (!ok) {
+        *abort = 1;
+      } else {
+        const unsigned char* wp = smem + (size_t)slot * kGsStageBytes + (size_t)(live ? g : 0) * kGsPitch + cw * 2;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int p = 4 * cb + q;
+          const uint4 w = live ? *reinterpret_cast<const uint4*>(wp + 64 * q) : make_uint4(0, 0, 0, 0);
+          if constexpr (KH > 1) {
+            mma_bf16_gs(acc[gr], xa[2 * p][0], xa[2 * p][2], xa[2 * p][1], xa[2 * p][3], w.x, w.y);
+            mma_bf16_gs(acc[gr], xa[2 * p + 1][0], xa[2 * p + 1][2], xa[2 * p + 1][1], xa[2 * p + 1][3], w.z, w.w);
+          } else {
+            mma_bf16_gs(acc[gr], xa[2 * p][0], 0u, xa[2 * p][1], 0u, w.x, w.y);
+            mma_bf16_gs(acc[gr], xa[2 * p + 1][0], 0u, xa[2 * p + 1][1], 0u, w.z, w.w);
+          }
         }
       }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&T.empty[slot]);
-    if (threadIdx.x == 0 && issued < ns && issued == s + kGsStages) {
-      // refill this slot once every warp has read it
-      if (!*abort && mbar_wait_bounded(&T.empty[slot], par, a.wait_ns, abort)) {
-        issue(issued);
-        ++issued;
-      } else {
-        *abort = 1;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&T.empty[slot]);
+      if (warp == 0 && issued < nst && issued == s + kGsStages) {
+        // refill this slot once every warp has read it
+        bool go = false;
+        if (lane == 0) {
+          go = !*abort && mbar_wait_bounded(&T.empty[slot], par, a.wait_ns, abort);
+          if (!go) *abort = 1;
+        }
+        if (__shfl_sync(0xffffffffu, go, 0)) {
+          issue(issued);
+          ++issued;
+        }
       }
+      __syncwarp();
     }
-    __syncwarp();
   }
   __syncthreads();  // every warp is done with the ring
   if (*abort) {
@@ -243,26 +269,26 @@ __global__ void __launch_bounds__(kGsWarps * 32, 1) k_gemv_stream(const __grid_c
     return;
   }
 
-  // partial sums to the (now free) ring: red[s][w][m][n], m < 16, n < 8
+  // partial sums to the (now free) ring: red[gr][w][m][n], m < 16, n < 8
   float* red = reinterpret_cast<float*>(smem);
 #pragma unroll
-  for (int s = 0; s < NB; ++s) {
-    if (s >= ns) break;
-    float* p = red + ((size_t)s * kGsWarps + warp) * 128;
-    p[g * 8 + 2 * t] = acc[s][0];
-    p[g * 8 + 2 * t + 1] = acc[s][1];
-    p[(g + 8) * 8 + 2 * t] = acc[s][2];
-    p[(g + 8) * 8 + 2 * t + 1] = acc[s][3];
+  for (int gr = 0; gr < NG; ++gr) {
+    if (gr >= ng) break;
+    float* p = red + ((size_t)gr * kGsWarps + warp) * 128;
+    p[g * 8 + 2 * t] = acc[gr][0];
+    p[g * 8 + 2 * t + 1] = acc[gr][1];
+    p[(g + 8) * 8 + 2 * t] = acc[gr][2];
+    p[(g + 8) * 8 + 2 * t + 1] = acc[gr][3];
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < ns * 128; idx += blockDim.x) {
-    const int s = idx >> 7, m = (idx >> 3) & 15, n = idx & 7;
-    if (m >= K || n >= T.n[s]) continue;
+  for (int idx = threadIdx.x; idx < ng * 128; idx += blockDim.x) {
+    const int gr = idx >> 7, m = (idx >> 3) & 15, n = idx & 7;
+    if (m >= K || n >= T.n[gr]) continue;
     float v = 0.f;
 #pragma unroll
-    for (int w = 0; w < kGsWarps; ++w) v += red[((size_t)s * kGsWarps + w) * 128 + m * 8 + n];
-    const GemvSeg& S = a.seg[T.seg[s]];
-    const int nl = T.row[s] + n;
+    for (int w = 0; w < kGsWarps; ++w) v += red[((size_t)gr * kGsWarps + w) * 128 + m * 8 + n];
+    const GemvSeg& S = a.seg[T.seg[gr]];
+    const int nl = T.row[gr] + n;
     if (S.res) v += bfl(S.res[(size_t)m * S.N + nl]);
     const uint16_t b = float_to_bf16_bits(v);
     S.out[(size_t)m * S.N + nl] = b;
@@ -274,35 +300,37 @@ __global__ void __launch_bounds__(kGsWarps * 32, 1) k_gemv_stream(const __grid_c
   }
 }
 
-int gemv_rows_per_stage(int D) { return kGsStageBytes / (2 * D) < 8 ? kGsStageBytes / (2 * D) : 8; }
-
-// Whether the streamed kernel takes this GEMV: x's fragments must fit the
-// registers and no CTA may need more stages than it has accumulator sets.
-static int gemv_stream_sets(const GemvArgs& a, int grid) {
-  const int R = gemv_rows_per_stage(a.D);
+// Row groups a CTA of the grid needs (at most): its rows in groups of 8,
+// plus one per matrix end inside its range.
+static int gemv_stream_groups(const GemvArgs& a, int grid) {
   const int rows_max = (a.n_total + grid - 1) / grid;
-  return (rows_max + R - 1) / R + (a.nseg - 1);
+  return (rows_max + kGsRows - 1) / kGsRows + (a.nseg - 1);
 }
 
+// Whether the streamed kernel takes this GEMV: D a whole number of column
+// blocks, x's fragments within the registers, and no CTA needing more row
+// groups than an instantiation has accumulator sets.
 bool gemv_stream_fits(const GemvArgs& a, int grid) {
-  if (a.K < 1 || a.K > 16 || a.D % 512 != 0) return false;
+  if (a.K < 1 || a.K > 16 || a.D % kGsCols != 0) return false;
   const int kpw = a.D / 256;
   if (kpw != 8 && kpw != 16 && kpw != 24 && kpw != 32) return false;
   if (a.K > 8 && kpw > 16) return false;
-  return gemv_stream_sets(a, grid) <= gs_max_sets(kpw, a.K > 8 ? 2 : 1);
+  return gemv_stream_groups(a, grid) <= gs_max_groups(kpw, a.K > 8 ? 2 : 1);
 }
 
 cudaError_t launch_gemv_stream(const GemvArgs& a, cudaStream_t s, bool pdl) {
   const int kpw = a.D / 256;
   const bool two = a.K > 8;
-  const bool wide = gemv_stream_sets(a, num_sms()) > 8;
+  const int ng = gemv_stream_groups(a, num_sms());
   void (*kern)(GemvArgs) = nullptr;
-  if (kpw == 8 && wide) kern = two ? k_gemv_stream<8, 2, 12> : k_gemv_stream<8, 1, 12>;
+  // the smallest set count that suffices (fewer accumulator registers)
+  if (kpw == 8 && ng > 8) kern = two ? k_gemv_stream<8, 2, 12> : k_gemv_stream<8, 1, 12>;
   else if (kpw == 8) kern = two ? k_gemv_stream<8, 2, 8> : k_gemv_stream<8, 1, 8>;
-  else if (kpw == 16 && wide && !two) kern = k_gemv_stream<16, 1, 12>;
-  else if (kpw == 16 && !wide) kern = two ? k_gemv_stream<16, 2, 8> : k_gemv_stream<16, 1, 8>;
-  else if (kpw == 24 && !two && !wide) kern = k_gemv_stream<24, 1, 8>;
-  else if (kpw == 32 && !two && !wide) kern = k_gemv_stream<32, 1, 8>;
+  else if (kpw == 16 && ng > 8 && !two) kern = k_gemv_stream<16, 1, 12>;
+  else if (kpw == 16 && ng <= 4) kern = two ? k_gemv_stream<16, 2, 4> : k_gemv_stream<16, 1, 4>;
+  else if (kpw == 16 && ng <= 8) kern = two ? k_gemv_stream<16, 2, 8> : k_gemv_stream<16, 1, 8>;
+  else if (kpw == 24 && !two) kern = ng <= 2 ? k_gemv_stream<24, 1, 2> : k_gemv_stream<24, 1, 4>;
+  else if (kpw == 32 && !two) kern = ng <= 2 ? k_gemv_stream<32, 1, 2> : k_gemv_stream<32, 1, 4>;
   if (!kern) return cudaErrorInvalidValue;
   const size_t sm = (size_t)kGsStages * kGsStageBytes + kGsTail;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);

@@ -215,7 +215,6 @@ struct GemvArgs {
   int nseg, n_total;
   int* err;           // error word (a cache append past its capacity, a wait that ran out), or null
   float norm_eps;     // > 0: x is RMS-normalised first (streamed kernel only)
-  int rows_per_stage; // streamed kernel: weight rows per ring stage (set by the launcher)
   uint64_t wait_ns;   // streamed kernel: limit of each ring wait
 };
 
@@ -276,9 +275,8 @@ cudaError_t launch_swiglu(const SwigluArgs& a, cudaStream_t s, bool pdl);
 
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t s, bool pdl);
 // The streamed GEMV (csrc/gemv.cu): whether it takes `a` on `grid` CTAs, and
-// its launch (rows_per_stage filled in by launch_gemv).
+// its launch.
 bool gemv_stream_fits(const GemvArgs& a, int grid);
-int gemv_rows_per_stage(int D);
 cudaError_t launch_gemv_stream(const GemvArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_attention_stream(const AttnStreamArgs& p, cudaStream_t s, bool pdl);
