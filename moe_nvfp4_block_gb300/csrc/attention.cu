@@ -229,10 +229,10 @@ cudaError_t launch_swiglu(const SwigluArgs& a, cudaStream_t s, bool pdl) {
 }
 
 // ------------------------------------------------------------------ rotary embedding
+// For shapes the streamed projection cannot rotate in its epilogue.
 // Grid (K, units / 4): CTA (r, j) serves row r.  Its threads first take the
-// rd/2 angles (pos0 + r) * freq[i] of that row and their sines and cosines
-// in double (positions reach the cache length, where an FP32 product would
-// lose the angle).  Then each warp takes one unit of the row: a q head, a k
+// rd/2 angles (pos0 + r) * freq[i] of that row and their cosines and sines
+// (rope_cs, as the projection's epilogue does).  Then each warp takes one unit of the row: a q head, a k
 // head or (with caches given) a v head.  For a q or k head, lane l rotates
 // the pairs (v[i], v[i + rd/2]) with i = l, l + 32 in FP32 and rounds to
 // bf16, in place; a k head's warp then writes its whole rotated head to
@@ -249,12 +249,7 @@ __global__ void __launch_bounds__(kRopeWarps * 32) k_rope(RopeArgs a) {
   const int half = a.rd / 2;
   const int pos0 = a.len ? *a.len : a.C;
   const int p = pos0 + r;
-  for (int i = threadIdx.x; i < half; i += blockDim.x) {
-    double sn, cs;
-    sincos((double)p * a.freq[i], &sn, &cs);
-    s_cos[i] = (float)cs;
-    s_sin[i] = (float)sn;
-  }
+  for (int i = threadIdx.x; i < half; i += blockDim.x) rope_cs(p, a.freq[i], s_cos[i], s_sin[i]);
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u = blockIdx.y * kRopeWarps + warp;

@@ -515,23 +515,41 @@ static moe_status attention_impl(const uint16_t* x, int K, int H, int nq, int nk
   g.wait_ns = g_wait_ns.load();
   const bool rope = pos && pos->rotary_dim > 0;
   g.seg[0] = {Wq, q, nullptr, nq * 128, nullptr, nullptr, 0};
-  // with a device length, the new keys and values also go into the caches
-  // in place, at positions *kv_len .. *kv_len + K - 1 (with a rotary
-  // embedding the rotation kernel appends the rotated keys instead)
-  const bool gemv_append = kv_len && !rope;
-  g.seg[1] = {Wk, kn, nullptr, nkv * 128, gemv_append ? kcache : nullptr, kv_len, C};
-  g.seg[2] = {Wv, vn, nullptr, nkv * 128, gemv_append ? vcache : nullptr, kv_len, C};
+  g.seg[1] = {Wk, kn, nullptr, nkv * 128, nullptr, kv_len, C};
+  g.seg[2] = {Wv, vn, nullptr, nkv * 128, nullptr, kv_len, C};
   g.nseg = 3;
   g.n_total = (nq + 2 * nkv) * 128;
   g.err = err;
+  // the rotary embedding in the streamed projection's epilogue where it
+  // takes the shape, else in a kernel of its own after the projection
+  double temp = 1.0;
+  bool rope_in_gemv = false;
+  if (rope) {
+    rope_freqs(*pos, g.rope_freq, &temp);
+    g.rope_rd = pos->rotary_dim;
+    g.rope_len = kv_len;
+    g.rope_C = C;
+    g.seg[0].rope = g.seg[1].rope = 1;
+    rope_in_gemv = gemv_stream_rope_fits(g, num_sms());
+    if (!rope_in_gemv) {
+      g.rope_rd = 0;
+      g.seg[0].rope = g.seg[1].rope = 0;
+    }
+  }
+  // with a device length, the new keys and values also go into the caches
+  // in place, at positions *kv_len .. *kv_len + K - 1 (a rotation kernel of
+  // its own appends the rotated keys instead)
+  if (kv_len && (!rope || rope_in_gemv)) {
+    g.seg[1].cache = kcache;
+    g.seg[2].cache = vcache;
+  }
   if (!gemv_stream_fits(g, num_sms())) {  // the row kernel takes normalised rows
     if (launch_rmsnorm(x, K, H, eps, xn, s, false) != cudaSuccess) return MOE_ERR_CUDA;
     g.x = xn;
     g.norm_eps = 0.f;
   }
   if (launch_gemv(g, s, true) != cudaSuccess) return MOE_ERR_CUDA;
-  double temp = 1.0;
-  if (rope) {
+  if (rope && !rope_in_gemv) {
     RopeArgs ra{};
     ra.q = q;
     ra.k = kn;
@@ -540,7 +558,7 @@ static moe_status attention_impl(const uint16_t* x, int K, int H, int nq, int nk
     ra.nq = nq;
     ra.nkv = nkv;
     ra.rd = pos->rotary_dim;
-    rope_freqs(*pos, ra.freq, &temp);
+    for (int i = 0; i < 64; ++i) ra.freq[i] = g.rope_freq[i];
     ra.len = kv_len;
     ra.C = C;
     ra.kc = kv_len ? kcache : nullptr;

@@ -71,6 +71,7 @@ struct GsTable {
   uint64_t full[kGsStages];
   uint64_t empty[kGsStages];
   int seg[kGsMaxGroups], row[kGsMaxGroups], n[kGsMaxGroups];
+  int pair[kGsMaxGroups];  // rotary embedding: 1 the first rows of a pair (the next group the second), 2 the second
   int ng;
   int abort;
   float inv[16];
@@ -108,9 +109,14 @@ __global__ void __launch_bounds__(kGsWarps * 32, 1) k_gemv_stream(const __grid_c
   };
 
   if (threadIdx.x == 0) {
-    // this CTA's output rows [r0, r1), cut into groups at matrix ends
-    const int r0 = (int)((long long)blockIdx.x * a.n_total / gridDim.x);
-    const int r1 = (int)((long long)(blockIdx.x + 1) * a.n_total / gridDim.x);
+    // this CTA's output rows [r0, r1), cut into groups at matrix ends.  With
+    // the rotary embedding the rows are split in units of 16 and a rope
+    // matrix's head is walked in the order 0-7, h-(h+7), 8-15, (h+8)-(h+15),
+    // ... (h = rope_rd / 2), then the rows past rope_rd: the two groups of a
+    // rotation pair are consecutive in one CTA.
+    const int unit = a.rope_rd ? 16 : 1, nu = a.n_total / unit;
+    const int r0 = (int)((long long)blockIdx.x * nu / gridDim.x) * unit;
+    const int r1 = (int)((long long)(blockIdx.x + 1) * nu / gridDim.x) * unit;
     int ng = 0, cur = r0, base = 0, sg = 0;
     T.abort = 0;
     while (cur < r1) {
@@ -120,9 +126,18 @@ __global__ void __launch_bounds__(kGsWarps * 32, 1) k_gemv_stream(const __grid_c
         break;
       }
       const int nr = min(kGsRows, min(r1, base + a.seg[sg].N) - cur);
+      int row = cur - base, pair = 0;
+      if (a.rope_rd && a.seg[sg].rope) {
+        const int v = row & 127;
+        if (v < a.rope_rd) {
+          pair = 1 + ((v >> 3) & 1);
+          row = row - v + (pair == 2 ? a.rope_rd / 2 : 0) + 8 * (v >> 4);
+        }
+      }
       T.seg[ng] = sg;
-      T.row[ng] = cur - base;
+      T.row[ng] = row;
       T.n[ng] = nr;
+      T.pair[ng] = pair;
       ++ng;
       cur += nr;
     }
@@ -281,28 +296,49 @@ __global__ void __launch_bounds__(kGsWarps * 32, 1) k_gemv_stream(const __grid_c
     p[(g + 8) * 8 + 2 * t + 1] = acc[gr][3];
   }
   __syncthreads();
+  // output (m, nl) of segment S: the row, and with a cache its in-place
+  // KV append at position *len + m
+  auto store = [&](const GemvSeg& S, int m, int nl, uint16_t b) {
+    S.out[(size_t)m * S.N + nl] = b;
+    if (S.cache) {
+      const int p = *S.len + m;
+      if (p < S.cap) S.cache[((size_t)(nl >> 7) * S.cap + p) * 128 + (nl & 127)] = b;
+      else if (a.err) atomicCAS(a.err, 0, (int)MOE_ERR_CAPACITY);
+    }
+  };
   for (int idx = threadIdx.x; idx < ng * 128; idx += blockDim.x) {
     const int gr = idx >> 7, m = (idx >> 3) & 15, n = idx & 7;
-    if (m >= K || n >= T.n[gr]) continue;
+    if (m >= K || n >= T.n[gr] || T.pair[gr] == 2) continue;
     float v = 0.f;
 #pragma unroll
     for (int w = 0; w < kGsWarps; ++w) v += red[((size_t)gr * kGsWarps + w) * 128 + m * 8 + n];
     const GemvSeg& S = a.seg[T.seg[gr]];
     const int nl = T.row[gr] + n;
-    if (S.res) v += bfl(S.res[(size_t)m * S.N + nl]);
-    const uint16_t b = float_to_bf16_bits(v);
-    S.out[(size_t)m * S.N + nl] = b;
-    if (S.cache) {  // in-place KV append at position *len + m
-      const int p = *S.len + m;
-      if (p < S.cap) S.cache[((size_t)(nl >> 7) * S.cap + p) * 128 + (nl & 127)] = b;
-      else if (a.err) atomicCAS(a.err, 0, (int)MOE_ERR_CAPACITY);
+    if (T.pair[gr] == 1) {
+      // rows i = nl % 128 and i + rope_rd/2 of the head: each rounded to
+      // bf16, rotated in FP32 by the row's angle, rounded again
+      float v1 = 0.f;
+#pragma unroll
+      for (int w = 0; w < kGsWarps; ++w) v1 += red[((size_t)(gr + 1) * kGsWarps + w) * 128 + m * 8 + n];
+      const float x0 = bfl(float_to_bf16_bits(v)), x1 = bfl(float_to_bf16_bits(v1));
+      float c, sn;
+      rope_cs((a.rope_len ? *a.rope_len : a.rope_C) + m, a.rope_freq[nl & 127], c, sn);
+      store(S, m, nl, float_to_bf16_bits(__fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, sn))));
+      store(S, m, T.row[gr + 1] + n, float_to_bf16_bits(__fadd_rn(__fmul_rn(x1, c), __fmul_rn(x0, sn))));
+      continue;
     }
+    if (S.res) v += bfl(S.res[(size_t)m * S.N + nl]);
+    store(S, m, nl, float_to_bf16_bits(v));
   }
 }
 
 // Row groups a CTA of the grid needs (at most): its rows in groups of 8,
 // plus one per matrix end inside its range.
 static int gemv_stream_groups(const GemvArgs& a, int grid) {
+  if (a.rope_rd) {  // units of 16 rows, matrix ends on unit boundaries
+    const int nu = a.n_total / 16;
+    return 2 * ((nu + grid - 1) / grid);
+  }
   const int rows_max = (a.n_total + grid - 1) / grid;
   return (rows_max + kGsRows - 1) / kGsRows + (a.nseg - 1);
 }
@@ -316,6 +352,15 @@ bool gemv_stream_fits(const GemvArgs& a, int grid) {
   if (kpw != 8 && kpw != 16 && kpw != 24 && kpw != 32) return false;
   if (a.K > 8 && kpw > 16) return false;
   return gemv_stream_groups(a, grid) <= gs_max_groups(kpw, a.K > 8 ? 2 : 1);
+}
+
+// Whether the streamed kernel can apply the rotary embedding in its
+// epilogue: rope_rd a multiple of 16 up to 128, every matrix whole heads.
+bool gemv_stream_rope_fits(const GemvArgs& a, int grid) {
+  if (a.rope_rd < 16 || a.rope_rd > 128 || a.rope_rd % 16 != 0) return false;
+  for (int i = 0; i < a.nseg; ++i)
+    if (a.seg[i].N % 128 != 0) return false;
+  return gemv_stream_fits(a, grid);
 }
 
 cudaError_t launch_gemv_stream(const GemvArgs& a, cudaStream_t s, bool pdl) {

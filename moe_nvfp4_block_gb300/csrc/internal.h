@@ -206,6 +206,7 @@ struct GemvSeg {
   uint16_t* cache;
   const int* len;
   int cap;
+  int rope;  // the rotary embedding applies to this matrix's heads (rope_rd > 0)
 };
 
 struct GemvArgs {
@@ -216,7 +217,16 @@ struct GemvArgs {
   int* err;           // error word (a cache append past its capacity, a wait that ran out), or null
   float norm_eps;     // > 0: x is RMS-normalised first (streamed kernel only)
   uint64_t wait_ns;   // streamed kernel: limit of each ring wait
+  // Streamed kernel: the rotary embedding of the rope segments' 128-row
+  // heads in the epilogue (0: none): rows i, i + rope_rd/2 (i < rope_rd/2)
+  // of a head rotated by the angle (pos0 + r) * rope_freq[i], pos0 =
+  // *rope_len or rope_C; rope_rd a multiple of 16.
+  int rope_rd;
+  const int* rope_len;
+  int rope_C;
+  double rope_freq[64];
 };
+bool gemv_stream_rope_fits(const GemvArgs& a, int grid);
 
 struct AttnArgs {
   const uint16_t* q;      // [K][nq*128]

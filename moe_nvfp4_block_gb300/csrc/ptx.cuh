@@ -224,6 +224,21 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) { return __uint_as_float(b16 << 16); }
 
+// Cosine and sine of the rotary angle p * f (p a position, f the pair's angle
+// per position).  The product and its reduction by 2 pi are taken in double
+// (Cody and Waite's two-constant reduction, "Software Manual for the
+// Elementary Functions", 1980: 2 pi = C1 + C2, C1 the double nearest 2 pi);
+// the sine and cosine of the reduced angle (|r| <= pi) in FP32.  Positions
+// reach the cache length, where an FP32 product would lose the angle; the
+// reduction keeps the FP64 work to five operations per angle.
+__device__ __forceinline__ void rope_cs(int p, double f, float& c, float& s) {
+  const double th = (double)p * f;
+  const double k = rint(th * 0.15915494309189535);  // 1 / (2 pi)
+  double r = fma(-k, 6.283185307179586, th);        // C1
+  r = fma(-k, 2.4492935982947064e-16, r);           // C2 = 2 pi - C1
+  sincosf((float)r, &s, &c);
+}
+
 // Router score of the sigmoid-scored router (MOE_SCORE_SIGMOID): the logistic
 // function as one fixed sequence of correctly rounded FP32 operations, so any
 // implementation of the same sequence selects the same experts.  exp(-l) by
