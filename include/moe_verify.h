@@ -441,6 +441,19 @@ moe_status moe_workspace_error(void* ws, int* code, void* stream);
 const char* moe_status_string(moe_status s);
 
 /*
+ * The address by which the device reaches page-locked host memory (pinned
+ * with cudaHostAlloc or cudaHostRegister and mapped, as every pinned buffer
+ * is under unified addressing).  The activations of a layer call -- x_norm,
+ * residual and y of moe_verify_layer -- may be such memory: the kernel then
+ * reads x and the residual and writes y across the host link itself, and a
+ * caller's host buffers take part in the call with no copy of their own.
+ * (Weights, caches and workspaces must be device memory.)  Returns
+ * MOE_ERR_INVALID_ARG, with *dev untouched, when `host` is not mapped
+ * page-locked memory.
+ */
+moe_status moe_host_pointer(const void* host, void** dev);
+
+/*
  * Test hook: upper bound, in nanoseconds, of every device-side wait in
  * kernels launched after this call (default 2e9).  0 makes every wait give
  * up at once, which exercises the timeout path without hanging a GPU.

@@ -33,7 +33,7 @@ EXPORTS = ("moe_verify_layer_workspace_size", "moe_router_topk", "moe_group_ints
            "moe_verify_layer_profiled", "verify_accept_prefix", "moe_rmsnorm", "moe_lm_head_workspace_size",
            "moe_lm_head_argmax", "moe_verify_stack_workspace_size", "moe_verify_stack",
            "moe_attention_workspace_size", "moe_attention_block", "moe_verify_layer_static",
-           "moe_verify_step_workspace_size", "moe_verify_step", "moe_workspace_error", "moe_status_string",
+           "moe_verify_step_workspace_size", "moe_verify_step", "moe_workspace_error", "moe_status_string", "moe_host_pointer",
            "moe_debug_set_wait_limit_ns", "moe_debug_set_trace", "moe_debug_partials_offset", "moe_kv_commit",
            "moe_synthetic_drafts", "moe_verify_rounds", "moe_dense_mlp_workspace_size", "moe_dense_mlp_block")
 
@@ -134,6 +134,8 @@ def _load():
     L.moe_workspace_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int), vp]
     L.moe_status_string.restype = ctypes.c_char_p
     L.moe_status_string.argtypes = [ci]
+    L.moe_host_pointer.restype = ci
+    L.moe_host_pointer.argtypes = [vp, ctypes.POINTER(vp)]
     L.moe_debug_set_wait_limit_ns.restype = None
     L.moe_debug_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     L.moe_debug_set_trace.restype = None
@@ -152,6 +154,23 @@ def status_string(s: int) -> str:
 
 def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def host_pointer(t) -> int:
+    """The device address of a pinned host tensor (moe_host_pointer)."""
+    d = ctypes.c_void_p()
+    _check(lib.moe_host_pointer(ctypes.c_void_p(t.data_ptr()), ctypes.byref(d)), "moe_host_pointer")
+    return d.value
+
+
+def _act_ptr(t):
+    """A layer call's activation: a CUDA tensor, or a pinned host tensor
+    that the kernel reads or writes across the host link."""
+    if t is None or t.is_cuda:
+        return _ptr(t)
+    if not t.is_pinned():
+        raise ValueError("a host activation must be pinned memory")
+    return ctypes.c_void_p(host_pointer(t))
 
 
 def _stream(stream):
@@ -232,7 +251,7 @@ def moe_router_topk(layer: Layer, x_norm, idx, w, group, ws, stream=None):
 def moe_verify_layer(layer: Layer, x_norm, residual, y, ws, idx_out=None, w_out=None, group_out=None,
                      stream=None, c_layer: moe_layer | None = None):
     c = layer.c() if c_layer is None else c_layer
-    _check(lib.moe_verify_layer(ctypes.byref(c), _ptr(x_norm), x_norm.shape[0], _ptr(residual), _ptr(y),
+    _check(lib.moe_verify_layer(ctypes.byref(c), _act_ptr(x_norm), x_norm.shape[0], _act_ptr(residual), _act_ptr(y),
                                 _ptr(idx_out), _ptr(w_out), _ptr(group_out), _ptr(ws), ws.numel(),
                                 _stream(stream)), "moe_verify_layer")
 

@@ -873,6 +873,17 @@ moe_status moe_workspace_error(void* ws, int* code, void* stream) {
   return MOE_OK;
 }
 
+moe_status moe_host_pointer(const void* host, void** dev) {
+  if (!host || !dev) return MOE_ERR_INVALID_ARG;
+  void* d = nullptr;
+  if (cudaHostGetDevicePointer(&d, const_cast<void*>(host), 0) != cudaSuccess || !d) {
+    cudaGetLastError();  // the failed query is not an error of the caller's stream
+    return MOE_ERR_INVALID_ARG;
+  }
+  *dev = d;
+  return MOE_OK;
+}
+
 const char* moe_status_string(moe_status s) {
   switch (s) {
     case MOE_OK: return "ok";

@@ -85,3 +85,14 @@ def test_bad_call_arguments_rejected_on_host(M):
     assert M.lib.moe_attention_workspace_size(4, 2048, 32, 8, 128) > 0
     for s in range(-6, 1):
         assert M.status_string(s) not in ("", "unknown status")
+
+
+def test_host_pointer_refuses_unpinned_memory(M):
+    # ordinary (pageable) host memory is not mapped into the device's
+    # address space: refused with MOE_ERR_INVALID_ARG, the output untouched
+    buf = ctypes.create_string_buffer(4096)
+    dev = ctypes.c_void_p(12345)
+    rc = M.lib.moe_host_pointer(ctypes.cast(buf, ctypes.c_void_p), ctypes.byref(dev))
+    assert rc == M.MOE_ERR_INVALID_ARG
+    assert dev.value == 12345
+    assert M.lib.moe_host_pointer(None, ctypes.byref(dev)) == M.MOE_ERR_INVALID_ARG

@@ -155,6 +155,31 @@ def test_deterministic_and_workspace_reuse(M):
         assert np.array_equal(u, v)
 
 
+def test_host_activations_match_device_activations(M):
+    # x, the residual and y in pinned host memory (the kernel reads and
+    # writes them across the host link) give the device-buffer call's
+    # routing and output bit for bit
+    w = synthgen.WORKLOADS["k2_layer"]
+    L, x, res = _case(w, res_inst=1)
+    dl = upload(L, w)
+    ws = M.workspace(dl, w.K)
+    want = run_layer(M, dl, x, res, ws=ws)
+    hx = torch.from_numpy(x).view(torch.bfloat16).pin_memory()
+    hr = torch.from_numpy(res).view(torch.bfloat16).pin_memory()
+    hy = torch.zeros_like(hx).pin_memory()
+    idx = torch.full((w.K, dl.top_k), -7, dtype=torch.int32, device="cuda")
+    wt = torch.empty((w.K, dl.top_k), dtype=torch.float32, device="cuda")
+    grp = torch.full((M.moe_group_ints(w.K, dl.n_experts, dl.top_k),), -7, dtype=torch.int32, device="cuda")
+    M.moe_verify_layer(dl, hx, hr, hy, ws, idx, wt, grp)
+    torch.cuda.synchronize()
+    assert M.moe_workspace_error(ws) == 0
+    got = (hy.view(torch.int16).numpy().view(np.uint16), idx.cpu().numpy(), wt.cpu().numpy(), grp.cpu().numpy())
+    for u, v in zip(want, got):
+        assert np.array_equal(u, v)
+    with pytest.raises(ValueError):
+        M.moe_verify_layer(dl, torch.from_numpy(x).view(torch.bfloat16), None, hy, ws)  # not pinned
+
+
 def test_one_workspace_across_shapes(M):
     # The workspace's counters sit at fixed offsets and the words the CTAs
     # exchange carry the call's tag, so one zero-filled workspace serves calls
