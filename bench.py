@@ -449,6 +449,7 @@ def run_gpu(args):
     stream.synchronize()
     with torch.cuda.stream(stream):
         e0.record(stream)
+        t_enq = time.perf_counter()
         for i in range(n_e2e):
             j = i % R
             if e2e_mode == "host buffers passed to the call":
@@ -457,6 +458,7 @@ def run_gpu(args):
                 xs[j].copy_(hx[j], non_blocking=True)
                 M.moe_verify_layer(layers[j], xs[j], None, ys[j], ws, stream=stream, c_layer=cl[j])
                 hy[j].copy_(ys[j], non_blocking=True)
+        t_enq = time.perf_counter() - t_enq
         e1.record(stream)
     stream.synchronize()
     e2e_ms = e0.elapsed_time(e1)
@@ -483,7 +485,7 @@ def run_gpu(args):
         "distinct_experts_mean": float(np.mean(n_u)),
         "clocks": clk,
         "e2e": {"value": round(e2e_gbs, 1), "unit": "GB/s", "h2d_bytes_per_step": act, "d2h_bytes_per_step": act,
-                "steps": n_e2e, "mode": e2e_mode},
+                "steps": n_e2e, "mode": e2e_mode, "host_enqueue_us_per_step": round(t_enq * 1e6 / n_e2e, 2)},
         "gpu_launches": steps,
         "kernel_ms": {k: round(v, 5) for k, v in mean_ms.items()},
         "kernel_ms_dist": {k: {kk: (round(vv, 5) if isinstance(vv, float) else vv) for kk, vv in pctl(v).items()}
