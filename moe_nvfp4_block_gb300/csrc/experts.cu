@@ -89,10 +89,6 @@ __device__ __forceinline__ void xchg_tagged(unsigned long long* p, unsigned long
   (void)prev;
 }
 
-// Between two attempts of a poll (measured: a short sleep beats spinning on
-// loads, for the waiting warp and for the L2 lines every CTA polls).
-__device__ __forceinline__ void poll_pause() { __nanosleep(128); }
-
 __device__ __forceinline__ unsigned long long ld_tagged(const unsigned long long* p) {
   unsigned long long v;
   asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
@@ -227,7 +223,6 @@ __device__ __noinline__ bool topk_general(const unsigned long long* row, unsigne
     }
     if (__all_sync(0xffffffffu, mine)) break;
     if (warp_gives_up(t0, wait_ns, abort_flag, lane)) return false;
-    poll_pause();
   }
   for (int s = 0; s < k; ++s) {
     float bv = -INFINITY;
@@ -309,7 +304,6 @@ __device__ __noinline__ bool route_row_fast(const unsigned long long* row, unsig
       got = false;
       break;
     }
-    poll_pause();
   }
   unsigned long long sel, first;  // lane s < k takes selection s
   warp_top8(v, lane, sel, first);
@@ -1310,11 +1304,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_experts(const __grid_consta
                     ok = false;
                     break;
                   }
-                  poll_pause();
                 }
                 if (!ok) break;
-              } else {
-                poll_pause();
               }
             }
           }
@@ -1463,7 +1454,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_moe_experts(const __grid_consta
               good = false;
               break;
             }
-            poll_pause();
           }
 #pragma unroll
           for (int u = 0; u < kChunk; ++u) {
