@@ -3,6 +3,7 @@
 // mlxfast Laguna XS 2.1 (DFlash), opening section: decode advances by the
 // longest correct prefix).  One warp scans 32 rows per step with a ballot.
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace moe {
 
@@ -69,6 +70,46 @@ cudaError_t launch_synthetic_drafts(const int32_t* target, const uint8_t* coin, 
   max_carveout(k_synthetic_drafts);
   k_synthetic_drafts<<<1, 32, 0, s>>>(target, coin, alt, K, vocab, draft);
   return cudaGetLastError();
+}
+
+// A layer call's rows in page-locked host memory, staged into the workspace
+// once, so that the layer kernel's CTAs read them from L2 rather than each
+// across the host link.  The loads do not depend on the previous kernel and
+// are issued before the dependency wait; the stores, into memory that the
+// previous call may still use, after it.
+constexpr int kStageThreads = 512;
+constexpr int kStageVecs = 8;  // 16-byte pieces per thread: K * H * 2 <= 64 KB
+
+__global__ void __launch_bounds__(kStageThreads) k_stage_rows(const uint4* src, uint4* dst, int n16) {
+  pdl_launch_dependents();
+  uint4 v[kStageVecs];
+#pragma unroll
+  for (int u = 0; u < kStageVecs; ++u) {
+    const int i = threadIdx.x + u * kStageThreads;
+    if (i < n16) v[u] = src[i];
+  }
+  pdl_wait();
+#pragma unroll
+  for (int u = 0; u < kStageVecs; ++u) {
+    const int i = threadIdx.x + u * kStageThreads;
+    if (i < n16) dst[i] = v[u];
+  }
+}
+
+cudaError_t launch_stage_rows(const void* src, void* dst, size_t bytes, cudaStream_t s) {
+  const size_t n16 = bytes / 16;
+  if (bytes % 16 != 0 || n16 > (size_t)kStageThreads * kStageVecs) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(kStageThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  max_carveout(k_stage_rows);
+  return cudaLaunchKernelEx(&cfg, k_stage_rows, static_cast<const uint4*>(src), static_cast<uint4*>(dst), (int)n16);
 }
 
 }  // namespace moe

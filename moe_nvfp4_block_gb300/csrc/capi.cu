@@ -318,6 +318,17 @@ __attribute__((visibility("hidden"))) moe_status run_layer(const moe_layer* laye
   // one launch: the experts kernel computes the router logits itself
   // (events 0 and 1 bracket no work)
   if (!mark(0) || !mark(1)) return MOE_ERR_CUDA;
+  // rows in page-locked host memory: staged into the workspace by one CTA
+  // (every CTA of the layer kernel reads all of them)
+  cudaPointerAttributes pa{};
+  if (cudaPointerGetAttributes(&pa, x_norm) != cudaSuccess) {
+    cudaGetLastError();  // an unknown pointer: not an error of the caller's stream
+  } else if (pa.type == cudaMemoryTypeHost) {
+    uint16_t* xs = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + lay.xs);
+    if (launch_stage_rows(x_norm, xs, sizeof(uint16_t) * (size_t)K * layer->hidden, st) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    x_norm = xs;
+  }
   s = launch_layer(layer, x_norm, K, residual, y, idx_out, w_out, group_out, wp, st, pdl, norm_eps, pf);
   if (s != MOE_OK) return s;
   if (!mark(2) || !mark(3)) return MOE_ERR_CUDA;

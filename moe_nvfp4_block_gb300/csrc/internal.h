@@ -43,6 +43,7 @@ struct WsLayout {
   size_t flags;    // tagged [G+1][I/16][4]: gate/up item done, per duty warp
   size_t h;        // tagged [G+1][K][I/2]: h, two bf16 per word
   size_t dpart;    // tagged [K][k+1][H]: FP32 down partials per (row, slot)
+  size_t xs;       // bf16 [K][H]: the rows, staged when the caller's are host memory
   size_t total;
 };
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -69,6 +70,7 @@ inline WsLayout ws_layout(int K, int E, int k, int H, int I) {
   L.flags = take(sizeof(uint64_t) * (size_t)(G + 1) * (I / 16) * 4);
   L.h = take(sizeof(uint64_t) * (size_t)(G + 1) * K * (I / 2));
   L.dpart = take(sizeof(uint64_t) * (size_t)K * (k + 1) * H);
+  L.xs = take(sizeof(uint16_t) * (size_t)K * H);
   L.total = o;
   return L;
 }
@@ -309,6 +311,10 @@ cudaError_t launch_experts(const ExpertsCommon& c, const CUtensorMap* maps, cons
 size_t experts_smem_bytes(int K, int H, int I, int E, int k, int G, int* stages, int* nred);
 cudaError_t launch_accept(const int32_t* draft, const int32_t* target, int K, int32_t* out, cudaStream_t s);
 cudaError_t launch_kv_commit(int32_t* len, const int32_t* n_accepted, int K, int cap, int* err, cudaStream_t s);
+// bytes (a multiple of 16, at most 64 KB) from src to dst in one CTA, with
+// programmatic dependent launch: loads before the dependency wait, stores
+// after it (accept.cu)
+cudaError_t launch_stage_rows(const void* src, void* dst, size_t bytes, cudaStream_t s);
 cudaError_t launch_synthetic_drafts(const int32_t* target, const uint8_t* coin, const int32_t* alt, int K, int vocab,
                                     int32_t* draft, cudaStream_t s);
 
