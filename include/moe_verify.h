@@ -444,9 +444,11 @@ const char* moe_status_string(moe_status s);
  * The address by which the device reaches page-locked host memory (pinned
  * with cudaHostAlloc or cudaHostRegister and mapped, as every pinned buffer
  * is under unified addressing).  The activations of a layer call -- x_norm,
- * residual and y of moe_verify_layer -- may be such memory: the kernel then
- * reads x and the residual and writes y across the host link itself, and a
- * caller's host buffers take part in the call with no copy of their own.
+ * residual and y of moe_verify_layer -- may be such memory, and a caller's
+ * host buffers then take part in the call with no copy of their own: rows in
+ * host memory are staged once into the workspace by the call's first kernel
+ * (their loads overlap the previous kernel on the stream), the residual is
+ * read and y written across the host link directly.
  * (Weights, caches and workspaces must be device memory.)  Returns
  * MOE_ERR_INVALID_ARG, with *dev untouched, when `host` is not mapped
  * page-locked memory.
