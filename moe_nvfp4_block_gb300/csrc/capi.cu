@@ -675,9 +675,27 @@ static moe_status dense_mlp_impl(const uint16_t* x, int K, int H, int I, const u
                                  int* err, cudaStream_t s) {
   uint16_t* xn = reinterpret_cast<uint16_t*>(b + L.xn);
   uint16_t* h = reinterpret_cast<uint16_t*>(b + L.h);
-  if (launch_rmsnorm(x, K, H, eps, xn, s, false) != cudaSuccess) return MOE_ERR_CUDA;
-  SwigluArgs sa{xn, Wg, Wu, h, K, H, I};
-  if (launch_swiglu(sa, s, true) != cudaSuccess) return MOE_ERR_CUDA;
+  // gate and up in the streamed projection (RMSNorm folded in, SwiGLU in its
+  // epilogue) where it takes the shape, else the row kernel on normalised rows
+  GemvArgs gu{};
+  gu.x = x;
+  gu.K = K;
+  gu.D = H;
+  gu.norm_eps = eps;
+  gu.seg[0] = {Wg, h, nullptr, I, nullptr, nullptr, 0};
+  gu.seg[1] = {Wu, h, nullptr, I, nullptr, nullptr, 0};
+  gu.nseg = 2;
+  gu.n_total = 2 * I;
+  gu.glu = 1;
+  gu.err = err;
+  gu.wait_ns = g_wait_ns.load();
+  if (gemv_stream_fits(gu, num_sms())) {
+    if (launch_gemv_stream(gu, s, true) != cudaSuccess) return MOE_ERR_CUDA;
+  } else {
+    if (launch_rmsnorm(x, K, H, eps, xn, s, false) != cudaSuccess) return MOE_ERR_CUDA;
+    SwigluArgs sa{xn, Wg, Wu, h, K, H, I};
+    if (launch_swiglu(sa, s, true) != cudaSuccess) return MOE_ERR_CUDA;
+  }
   GemvArgs gd{};
   gd.x = h;
   gd.K = K;

@@ -39,14 +39,16 @@ constexpr int kGsRows = 8;                 // rows per group (the mma's n dimens
 constexpr int kGsCols = 2048;              // columns per block: 4 KB of a row
 constexpr int kGsPitch = kGsCols * 2 + 64; // bytes between a stage's rows
 constexpr int kGsStageBytes = kGsRows * kGsPitch;
-constexpr int kGsMaxGroups = 12;  // row groups per CTA (one accumulator set each), at most
+constexpr int kGsMaxGroups = 16;  // row groups per CTA (one accumulator set each), at most
 constexpr int kGsTail = 1024;     // barriers and the group table after the ring
 // Bound on waiting for the CTA's own copies before it exits (independent of
 // the caller's wait limit, which may be 0 in a test of the give-up path).
 constexpr uint64_t kGsDrainNs = 2000000000ull;
 // Accumulator sets (row groups) of an instantiation: x's fragments take
 // KPW * 2 * KH registers, so the narrow ones have room for more sets.
-constexpr int gs_max_groups(int kpw, int kh) { return kpw * kh <= 16 ? 12 : (kpw <= 16 ? 8 : 4); }
+constexpr int gs_max_groups(int kpw, int kh) {
+  return kpw * kh <= 8 ? 16 : (kpw * kh <= 16 ? 12 : (kpw <= 16 ? 8 : 4));
+}
 
 __device__ __forceinline__ float bfl(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bfh(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -114,17 +116,27 @@ __global__ void __launch_bounds__(kGsWarps * 32, 1) k_gemv_stream(const __grid_c
     // matrix's head is walked in the order 0-7, h-(h+7), 8-15, (h+8)-(h+15),
     // ... (h = rope_rd / 2), then the rows past rope_rd: the two groups of a
     // rotation pair are consecutive in one CTA.
-    const int unit = a.rope_rd ? 16 : 1, nu = a.n_total / unit;
+    const int unit = (a.rope_rd || a.glu) ? 16 : 1, nu = a.n_total / unit;
     const int r0 = (int)((long long)blockIdx.x * nu / gridDim.x) * unit;
     const int r1 = (int)((long long)(blockIdx.x + 1) * nu / gridDim.x) * unit;
     int ng = 0, cur = r0, base = 0, sg = 0;
     T.abort = 0;
     while (cur < r1) {
-      while (cur >= base + a.seg[sg].N) base += a.seg[sg++].N;
       if (ng == NG) {  // more groups than accumulator sets: refused by the launcher
         T.abort = 1;
         break;
       }
+      if (a.glu) {  // unit u: gate rows 8u .. 8u + 7, then the same up rows
+        const int up = (cur >> 3) & 1;
+        T.seg[ng] = up;
+        T.row[ng] = (cur >> 4) * 8;
+        T.n[ng] = kGsRows;
+        T.pair[ng] = 1 + up;
+        ++ng;
+        cur += kGsRows;
+        continue;
+      }
+      while (cur >= base + a.seg[sg].N) base += a.seg[sg++].N;
       const int nr = min(kGsRows, min(r1, base + a.seg[sg].N) - cur);
       int row = cur - base, pair = 0;
       if (a.rope_rd && a.seg[sg].rope) {
@@ -314,6 +326,14 @@ __global__ void __launch_bounds__(kGsWarps * 32, 1) k_gemv_stream(const __grid_c
     for (int w = 0; w < kGsWarps; ++w) v += red[((size_t)gr * kGsWarps + w) * 128 + m * 8 + n];
     const GemvSeg& S = a.seg[T.seg[gr]];
     const int nl = T.row[gr] + n;
+    if (T.pair[gr] == 1 && a.glu) {
+      // gate row nl and up row nl: h = bf16(silu(g) * u), the FP32 sums unrounded
+      float u = 0.f;
+#pragma unroll
+      for (int w = 0; w < kGsWarps; ++w) u += red[((size_t)(gr + 1) * kGsWarps + w) * 128 + m * 8 + n];
+      store(S, m, nl, float_to_bf16_bits(v * __frcp_rn(1.f + expf(-v)) * u));
+      continue;
+    }
     if (T.pair[gr] == 1) {
       // rows i = nl % 128 and i + rope_rd/2 of the head: each rounded to
       // bf16, rotated in FP32 by the row's angle, rounded again
@@ -335,7 +355,7 @@ __global__ void __launch_bounds__(kGsWarps * 32, 1) k_gemv_stream(const __grid_c
 // Row groups a CTA of the grid needs (at most): its rows in groups of 8,
 // plus one per matrix end inside its range.
 static int gemv_stream_groups(const GemvArgs& a, int grid) {
-  if (a.rope_rd) {  // units of 16 rows, matrix ends on unit boundaries
+  if (a.rope_rd || a.glu) {  // units of 16 rows, matrix ends on unit boundaries
     const int nu = a.n_total / 16;
     return 2 * ((nu + grid - 1) / grid);
   }
@@ -369,7 +389,8 @@ cudaError_t launch_gemv_stream(const GemvArgs& a, cudaStream_t s, bool pdl) {
   const int ng = gemv_stream_groups(a, num_sms());
   void (*kern)(GemvArgs) = nullptr;
   // the smallest set count that suffices (fewer accumulator registers)
-  if (kpw == 8 && ng > 8) kern = two ? k_gemv_stream<8, 2, 12> : k_gemv_stream<8, 1, 12>;
+  if (kpw == 8 && ng > 12 && !two) kern = k_gemv_stream<8, 1, 16>;
+  else if (kpw == 8 && ng > 8) kern = two ? k_gemv_stream<8, 2, 12> : k_gemv_stream<8, 1, 12>;
   else if (kpw == 8) kern = two ? k_gemv_stream<8, 2, 8> : k_gemv_stream<8, 1, 8>;
   else if (kpw == 16 && ng > 8 && !two) kern = k_gemv_stream<16, 1, 12>;
   else if (kpw == 16 && ng <= 4) kern = two ? k_gemv_stream<16, 2, 4> : k_gemv_stream<16, 1, 4>;

@@ -227,6 +227,10 @@ struct GemvArgs {
   const int* rope_len;
   int rope_C;
   double rope_freq[64];
+  // Streamed kernel, SwiGLU: seg[0] the gate and seg[1] the up matrix (N
+  // rows each, N a multiple of 8, n_total = 2N); the output is
+  // h = bf16(silu(gate) * up) into seg[0].out.
+  int glu;
 };
 bool gemv_stream_rope_fits(const GemvArgs& a, int grid);
 

@@ -86,10 +86,14 @@ def test_laguna_attention_inplace_append(cuda_ok):
     assert not np.any(kc[:, C0 + K:])
 
 
-def test_dense_mlp_block(cuda_ok):
+@pytest.mark.parametrize("K,inter", [(4, 8192), (16, 2048), (1, 256), (12, 8192)])
+def test_dense_mlp_block(cuda_ok, K, inter):
+    # gate/up in the streamed projection with the SwiGLU in its epilogue
+    # (K = 4 at intermediate 8192: 14 row groups per CTA; K = 16: two m-halves;
+    # K = 1 at 256), and the row kernels where it does not fit (K = 12 at 8192)
     import moe_nvfp4_block_gb300 as M
-    w = synthgen.WORKLOADS["k4_full_step"]
-    mlp = synthgen.make_dense_mlp(w, 0)
+    w = dataclasses.replace(synthgen.WORKLOADS["k4_full_step"], K=K)
+    mlp = synthgen.make_dense_mlp(w, 0, inter)
     x = synthgen.make_x(w, 12)
     ref = oracle.dense_mlp(oracle.rmsnorm(x), x, mlp["Wg"], mlp["Wu"], mlp["Wd"])
     xd = to_dev_bf16(x)

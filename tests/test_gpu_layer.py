@@ -155,11 +155,13 @@ def test_deterministic_and_workspace_reuse(M):
         assert np.array_equal(u, v)
 
 
-def test_host_activations_match_device_activations(M):
-    # x, the residual and y in pinned host memory (the kernel reads and
-    # writes them across the host link) give the device-buffer call's
-    # routing and output bit for bit
-    w = synthgen.WORKLOADS["k2_layer"]
+@pytest.mark.parametrize("name", ["k2_layer", "k16_zipf_stack40"])
+def test_host_activations_match_device_activations(M, name):
+    # x, the residual and y in pinned host memory (x staged into the
+    # workspace by one CTA -- 64 KB at K = 16, the most it takes -- the
+    # residual read and y written across the host link) give the
+    # device-buffer call's routing and output bit for bit
+    w = synthgen.WORKLOADS[name]
     L, x, res = _case(w, res_inst=1)
     dl = upload(L, w)
     ws = M.workspace(dl, w.K)
