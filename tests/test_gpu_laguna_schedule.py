@@ -58,6 +58,32 @@ def test_laguna_attention(cuda_ok, layer, K, C):
     assert_parity(bf16_bits(out), ref["x"], "block output")
 
 
+@pytest.mark.parametrize("K,nq,rd,window,C", [(3, 16, 8, 0, 256), (16, 32, 128, 0, 272), (16, 32, 32, 96, 400),
+                                               (8, 64, 128, 512, 1040)])
+def test_rotary_paths(cuda_ok, K, nq, rd, window, C):
+    # the rotary embedding in the projection's epilogue (rotary widths that
+    # are multiples of 16; K = 16: x fragments of two 8-row halves) and in a
+    # kernel of its own (width 8), against the oracle
+    import moe_nvfp4_block_gb300 as M
+    H, nkv = 2048, 8
+    a = _att(K, H, nq, nkv, C, 70 + K + rd)
+    ref = oracle.attention_ex(a["x"], a["Wq"], a["Wk"], a["Wv"], a["Wo"], a["kc"], a["vc"], nq, nkv, 128,
+                              window=window, rotary_dim=rd, theta=10000.0)
+    d = {k: to_dev_bf16(v) for k, v in a.items()}
+    out = torch.empty_like(d["x"])
+    kn = torch.empty(K, nkv * 128, dtype=torch.bfloat16, device="cuda")
+    vn = torch.empty_like(kn)
+    o = torch.empty(K, nq * 128, dtype=torch.bfloat16, device="cuda")
+    ws = M.attention_workspace(K, H, nq, nkv)
+    M.moe_attention_block(d["x"], d["Wq"], d["Wk"], d["Wv"], d["Wo"], d["kc"], d["vc"], out, ws, nq, nkv,
+                          k_new=kn, v_new=vn, o_out=o, pos=M.attn_pos(window, rd, 10000.0))
+    torch.cuda.synchronize()
+    assert M.moe_workspace_error(ws) == 0
+    assert_parity(bf16_bits(kn), ref["k_new"], f"rotated new keys (rd {rd}, K {K})")
+    assert_parity(bf16_bits(o), ref["o"], f"attention output o (rd {rd}, K {K})")
+    assert_parity(bf16_bits(out), ref["x"], f"block output (rd {rd}, K {K})")
+
+
 def test_laguna_attention_inplace_append(cuda_ok):
     # the sliding layer with a device length: the rotated keys and the values
     # go into the caches at positions len .. len + K - 1
