@@ -2,6 +2,8 @@
 // whose draft token differs from the target's greedy token, or K (README of
 // mlxfast Laguna XS 2.1 (DFlash), opening section: decode advances by the
 // longest correct prefix).  One warp scans 32 rows per step with a ballot.
+// Also the small kernels around it: the cache-length commit of the verify
+// loop, the synthetic drafter, and the staging of a layer call's host rows.
 #include "internal.h"
 #include "ptx.cuh"
 

@@ -26,6 +26,11 @@
 // those of the odd step.  x and W use the same order, so every product is
 // x[r][c] * W[n][c]; only the order of the FP32 sum differs from a plain
 // dot product.
+//
+// Two epilogues pair rows that the walk keeps in one CTA (rows split in
+// units of 16, two 8-row groups each): the rotary embedding of the q and k
+// heads (rows i and i + rd/2 of a head) and SwiGLU (gate row n and up row
+// n), both formed from the two groups' outputs before anything is stored.
 #include "internal.h"
 #include "ptx.cuh"
 
