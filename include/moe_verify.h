@@ -451,7 +451,9 @@ const char* moe_status_string(moe_status s);
  * read and y written across the host link directly.
  * (Weights, caches and workspaces must be device memory.)  Returns
  * MOE_ERR_INVALID_ARG, with *dev untouched, when `host` is not mapped
- * page-locked memory.
+ * page-locked memory -- also for pageable memory on a system whose device
+ * could reach it; a layer call refuses activations in pageable memory with
+ * MOE_ERR_INVALID_ARG.
  */
 moe_status moe_host_pointer(const void* host, void** dev);
 

@@ -168,9 +168,10 @@ def _act_ptr(t):
     that the kernel reads or writes across the host link."""
     if t is None or t.is_cuda:
         return _ptr(t)
-    if not t.is_pinned():
+    d = ctypes.c_void_p()  # moe_host_pointer refuses memory that is not pinned
+    if lib.moe_host_pointer(ctypes.c_void_p(t.data_ptr()), ctypes.byref(d)) != MOE_OK:
         raise ValueError("a host activation must be pinned memory")
-    return ctypes.c_void_p(host_pointer(t))
+    return d
 
 
 def _stream(stream):

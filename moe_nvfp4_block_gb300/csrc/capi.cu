@@ -318,11 +318,21 @@ __attribute__((visibility("hidden"))) moe_status run_layer(const moe_layer* laye
   // one launch: the experts kernel computes the router logits itself
   // (events 0 and 1 bracket no work)
   if (!mark(0) || !mark(1)) return MOE_ERR_CUDA;
-  // rows in page-locked host memory: staged into the workspace by one CTA
-  // (every CTA of the layer kernel reads all of them)
+  // activations in pageable host memory are refused (the device cannot reach
+  // it everywhere); rows in page-locked host memory are staged into the
+  // workspace by one CTA (every CTA of the layer kernel reads all of them)
+  const void* acts[3] = {x_norm, residual, y};
   cudaPointerAttributes pa{};
+  for (const void* p : acts) {
+    if (!p) continue;
+    if (cudaPointerGetAttributes(&pa, p) != cudaSuccess) {
+      cudaGetLastError();  // an unknown pointer: not an error of the caller's stream
+      continue;
+    }
+    if (pa.type == cudaMemoryTypeUnregistered) return MOE_ERR_INVALID_ARG;
+  }
   if (cudaPointerGetAttributes(&pa, x_norm) != cudaSuccess) {
-    cudaGetLastError();  // an unknown pointer: not an error of the caller's stream
+    cudaGetLastError();
   } else if (pa.type == cudaMemoryTypeHost) {
     uint16_t* xs = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + lay.xs);
     if (launch_stage_rows(x_norm, xs, sizeof(uint16_t) * (size_t)K * layer->hidden, st) != cudaSuccess)
@@ -905,12 +915,15 @@ moe_status moe_workspace_error(void* ws, int* code, void* stream) {
 
 moe_status moe_host_pointer(const void* host, void** dev) {
   if (!host || !dev) return MOE_ERR_INVALID_ARG;
-  void* d = nullptr;
-  if (cudaHostGetDevicePointer(&d, const_cast<void*>(host), 0) != cudaSuccess || !d) {
+  // page-locked host memory only: where the device can also reach pageable
+  // memory (address translation on a coherent host link), the mapping query
+  // succeeds for it as well, so the memory type decides
+  cudaPointerAttributes pa{};
+  if (cudaPointerGetAttributes(&pa, host) != cudaSuccess || pa.type != cudaMemoryTypeHost || !pa.devicePointer) {
     cudaGetLastError();  // the failed query is not an error of the caller's stream
     return MOE_ERR_INVALID_ARG;
   }
-  *dev = d;
+  *dev = pa.devicePointer;
   return MOE_OK;
 }
 

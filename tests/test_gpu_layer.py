@@ -180,6 +180,14 @@ def test_host_activations_match_device_activations(M, name):
         assert np.array_equal(u, v)
     with pytest.raises(ValueError):
         M.moe_verify_layer(dl, torch.from_numpy(x).view(torch.bfloat16), None, hy, ws)  # not pinned
+    # the C ABI itself refuses pageable activations before launching anything
+    import ctypes
+    xp = np.ascontiguousarray(x)
+    c = dl.c()
+    rc = M.lib.moe_verify_layer(ctypes.byref(c), ctypes.c_void_p(xp.ctypes.data), w.K, None,
+                                ctypes.c_void_p(hy.data_ptr()), None, None, None, ctypes.c_void_p(ws.data_ptr()),
+                                ws.numel(), None)
+    assert rc == M.MOE_ERR_INVALID_ARG
 
 
 def test_one_workspace_across_shapes(M):
