@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(kGsWarps * 32, 1) k_gemv_stream(const __grid_c
       const int slot = s % kGsStages;
       const uint32_t par = (uint32_t)(s / kGsStages) & 1u;
       bool ok = !*abort && mbar_wait_bounded(&T.full[slot], par, a.wait_ns, abort);
-      ok = __all_sync(0xffffffffu, ok);  // converged for mma.sync; one verdict per warp
+      ok = __all_sync(0xffffffffu, ok);  // converged for mma.sync; one outcome per warp
       if (!ok) {
         *abort = 1;
       } else {
